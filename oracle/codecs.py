@@ -1,0 +1,88 @@
+"""Number formats used at the layer's storage points, written from their definitions.
+
+TEST INFRASTRUCTURE (see oracle/__init__.py): never imported by the product path.
+
+bfloat16: the upper 16 bits of an IEEE-754 binary32 value (1 sign, 8 exponent, 7 fraction
+bits); a binary32 value is rounded to it to nearest, ties to even.
+
+FP8 e4m3 ("fn" variant of the OCP 8-bit floating point specification): 1 sign bit, 4 exponent
+bits with bias 7, 3 fraction bits; exponent field 0 encodes subnormals m/8 * 2^-6; no
+infinities; S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+Encoding here is round-to-nearest-even with saturation to +-448 ("satfinite"), the rule the
+Beam page's FP8 KV cache needs (vLLM page, "--kv-cache-dtype fp8"; the quantisation rule
+itself is not printed, so saturation is the stated reading).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+
+
+def f32(x) -> np.ndarray:
+    """Round to binary32 (numpy's float64 -> float32 cast rounds to nearest even)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+def bf16_bits(x) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) of x, rounding x to binary32 first, then to nearest-even."""
+    f = np.ascontiguousarray(f32(x))
+    u = f.view(np.uint32).astype(np.uint64)
+    nan = np.isnan(f)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+    # a NaN keeps its sign and becomes the quiet NaN pattern
+    r = np.where(nan, (u >> np.uint64(16)).astype(np.uint16) | np.uint16(0x0040), r)
+    return r
+
+
+def bf16_from_bits(b) -> np.ndarray:
+    u = (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16))
+    with np.errstate(invalid="ignore"):
+        return np.ascontiguousarray(u).view(np.float32).astype(np.float64)
+
+
+def bf16_round(x) -> np.ndarray:
+    """x rounded to bfloat16, returned as float64 (exactly representable)."""
+    return bf16_from_bits(bf16_bits(x))
+
+
+def e4m3_table() -> np.ndarray:
+    """Value of each of the 256 e4m3 codes (float64; NaN for the two NaN codes)."""
+    vals = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = sign * (m / 8.0) * 2.0 ** -6
+        else:
+            vals[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+_E4M3 = e4m3_table()
+# positive finite magnitudes, in code order 0x00..0x7E (increasing)
+_E4M3_POS = _E4M3[:0x7F]
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    return _E4M3[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Codes (uint8) of x rounded to nearest-even on the e4m3 grid, saturated to +-448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)                 # subnormal binade shares the 2^-6 exponent
+    quantum = 2.0 ** (e - 3.0)              # 3 fraction bits
+    q = np.rint(a / quantum) * quantum      # rint: ties to even on the integer multiple
+    q = np.minimum(q, E4M3_MAX)
+    code = np.searchsorted(_E4M3_POS, q).astype(np.uint8)
+    code = np.where(np.signbit(x), code | np.uint8(0x80), code)
+    code = np.where(np.isnan(x), np.uint8(0x7F), code)
+    return code.astype(np.uint8)

@@ -1,0 +1,9 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the bench and the oracle's tests.
+
+This package draws random numbers and names layer shapes. It holds none of the layer's
+arithmetic, so that both sides of every parity test can be fed from it.
+"""
+from .beam_inputs import (  # noqa: F401
+    BeamShape, TINY, BEAM, derived_seed, normal, layer_weights, expert_weights,
+    activations, kv_cache, decode_positions, prefill_positions,
+)
