@@ -1,0 +1,542 @@
+"""Benchmark of the Beam decoder-layer forward on GB300 (one JSON line on rank 0).
+
+Workloads (seeded synthetic inputs, random-init weights; shapes of the Beam layer):
+  swa_decode   (default) one full-width sliding-window MoE layer, batch-1 decode, context 4096,
+               BF16 KV cache
+  nope_decode  one full-width NoPE MoE layer with SSMax, decode at context 100,000 per
+               sequence (--batch 1/2/4/8, --kv bf16/fp8)
+  stack_decode the 6-layer truncated stack (layers 0-2 dense, 3-5 MoE, layer 5 NoPE), decode
+               (--batch, --context, --kv; the 8-K / batch-128 / FP8 case is
+               --batch 128 --context 8192 --kv fp8; batch 1 / 100K / BF16 by default)
+
+A step is one pass of the whole layer (or stack) over one batch of new tokens. Inputs are
+resident in HBM when the timed region starts; each step streams far more than the 129 MB L2
+(the layer's weights), so no flush is needed. Steps run as per-call CUDA graphs (one per
+library call) with CUDA events between them, which gives the step time and each call's
+time from the same timed region.
+
+--impl reference times the CPU oracle on the same workload instead (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import BEAM  # noqa: E402
+
+METRIC = "Beam-layer decode µs/token & HBM GB/s % of peak; prefill tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------- helpers ----
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def is_nope(l, L):
+    return (l + 1) % 6 == 0 or l == L - 1
+
+
+def layer_bytes(shape, dense, n_experts_touched, kv_bytes):
+    """Algorithmic HBM bytes of one layer step: every weight byte the step must read once,
+    the KV bytes it must read, the gains; activations are negligible (<0.1%)."""
+    H, D = shape.hidden, shape.head_dim
+    b = shape.qkvg_rows * H * 2 + H * shape.q_rows * 2           # packed QKVG, o_proj
+    b += 4 * H * 2 + 2 * D * 2 + shape.n_q * 2                   # gains, gate bias
+    if dense:
+        b += 3 * H * shape.d_ff_dense * 2
+    else:
+        b += shape.n_experts * H * 4 + shape.n_experts * 4       # FP32 router
+        b += n_experts_touched * 3 * H * shape.d_ff_expert * 2
+    return b + kv_bytes
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            time.sleep(0.15)
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = []
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            try:
+                rows.append((float(f[0]), float(f[1]), float(f[2]), f[3:7]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        loaded = [r[0] for r in rows if r[2] > 200.0] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if it was taken on the
+    current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    if d.get("source_hash") != source_hash(d["sources"]):
+        return None
+    return d["bytes_per_launch"]
+
+
+# --------------------------------------------------------------------------- workloads ----
+
+class Workload:
+    """Holds weights, caches and inputs of one benchmark case on the device."""
+
+    def __init__(self, args, device):
+        from hybrid_attention_moe_gb300 import beam as B
+        from hybrid_attention_moe_gb300.stack import BeamStack
+        self.B = B
+        self.args = args
+        self.device = device
+        shape = BEAM
+        kind = args.workload
+        fp8 = args.kv == "fp8"
+        if kind == "swa_decode":
+            layers, ctx, batch = [3], 4096, 1
+        elif kind == "nope_decode":
+            layers, ctx, batch = [5], 100_000, args.batch
+        else:
+            layers, ctx, batch = list(range(6)), args.context, args.batch
+        self.layers, self.ctx, self.batch, self.fp8 = layers, ctx, batch, fp8
+        scale = 1.0
+        W, caches = [], []
+        for l in layers:
+            W.append(synth.layer_weights(shape, l, args.seed, device=device))
+            nope = is_nope(l, shape.n_layers)
+            cap, win = (ctx + 8, 0) if nope else (shape.window, shape.window)
+            c = synth.kv_cache(shape, batch, cap, args.seed, l, fp8=fp8, k_scale=scale,
+                               v_scale=scale, device=device)
+            caches.append(B.KVCache(c["k"], c["v"], win, scale, scale))
+        self.shape = shape
+        self.stack = BeamStack(shape, W, caches, first_layer=layers[0], device=device)
+        self.seq = torch.arange(batch, dtype=torch.int32, device=device)
+        self.pos = torch.full((batch,), ctx + 1, dtype=torch.int32, device=device)
+        self.max_pos = ctx + 1
+        self.e = synth.activations(batch, shape.hidden, args.seed, "h", device)
+        self.W = W
+        self.caches = caches
+
+    def step_calls(self):
+        """The library calls of one step as (name, fn) closures over fixed buffers."""
+        B, st = self.B, self.stack
+        T = self.batch
+        b = st.buffers(T)
+        ws = st.ws.get(B.workspace_bytes(st.cfgs[0], T, self.max_pos))
+        calls = [("input", lambda: b["h"].copy_(self.e)),
+                 ("pre_norm", lambda: B.beam_boundary_norm(None, b["h"], b["u"], None,
+                                                           st.W[0]["attn_pre"], 1,
+                                                           st.cfgs[0].eps))]
+        for i in range(st.L):
+            W, cfg, kc, l = st.W[i], st.cfgs[i], st.caches[i], st.ids[i]
+            nxt = st.W[i + 1]["attn_pre"] if i + 1 < st.L else None
+            calls += [
+                (f"L{l}.qkv_gate", lambda W=W, cfg=cfg, kc=kc: B.beam_qkv_gate(
+                    cfg, b["u"], W["w_qkvg"], W["q_norm"], W["k_norm"], self.seq, self.pos,
+                    b["q"], b["g"], kc, ws)),
+                (f"L{l}.attn", lambda W=W, cfg=cfg, kc=kc: B.beam_attn(
+                    cfg, b["q"], b["g"], W["gate_bias"], kc, self.seq, self.pos, self.max_pos,
+                    W["w_o"], b["a"], ws)),
+                (f"L{l}.norm_attn", lambda W=W, cfg=cfg, l=l: B.beam_boundary_norm(
+                    b["a"], b["h"], b["u"], W["attn_post"], W["mlp_pre"], 2 * l + 2, cfg.eps)),
+            ]
+            if st.dense[i]:
+                calls.append((f"L{l}.dense_mlp", lambda W=W, cfg=cfg: B.beam_dense_mlp(
+                    cfg, b["u"], W["w_gate_up"], W["w_down"], b["m"], ws)))
+            else:
+                calls += [
+                    (f"L{l}.route", lambda W=W, cfg=cfg: B.beam_route(
+                        cfg, b["u"], W["router"], W["corr_bias"], b["logits"], b["idx"], b["w"],
+                        ws)),
+                    (f"L{l}.moe", lambda W=W, cfg=cfg: B.beam_moe(
+                        cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"], ws)),
+                ]
+            calls.append((f"L{l}.norm_mlp", lambda W=W, cfg=cfg, l=l, nxt=nxt:
+                          B.beam_boundary_norm(b["m"], b["h"], b["u"] if nxt is not None else None,
+                                               W["mlp_post"], nxt, 2 * l + 3, cfg.eps)))
+        return calls, b
+
+    def touched_experts(self, b):
+        """Distinct experts each MoE layer's routing selected in the last step."""
+        return len(set(b["idx"].cpu().numpy().ravel().tolist()))
+
+    def algorithmic_bytes(self, touched):
+        shape = self.shape
+        tot = 0
+        per = {}
+        for i, l in enumerate(self.layers):
+            nope = is_nope(l, shape.n_layers)
+            keys = self.ctx + 1 if nope else min(shape.window, self.ctx + 1)
+            elem = 1 if self.fp8 else 2
+            kv = self.batch * keys * shape.n_kv * shape.head_dim * 2 * elem
+            dense = l in shape.dense_layers
+            per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv)
+            tot += per[l]
+        return tot, per
+
+
+# --------------------------------------------------------------------------- our arm ----
+
+def run_ours(args, rank, world, device):
+    B_mod = __import__("hybrid_attention_moe_gb300.beam", fromlist=["beam"])
+    import __graft_entry__ as ge
+    ge.build()
+    wl = Workload(args, device)
+    calls, b = wl.step_calls()
+    names = [n for n, _ in calls]
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    # eager warm-up: sets kernel attributes and sizes the workspace before any capture
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for _, fn in calls:
+                fn()
+    torch.cuda.synchronize()
+    c0 = B_mod.beam_launch_count()
+    with torch.cuda.stream(stream):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    launches_step = B_mod.beam_launch_count() - c0
+
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph, stream=stream):
+        for _, fn in calls:
+            fn()
+    # the timed region: K steps in one graph, a timing event before every call
+    try:
+        events = [[torch.cuda.Event(enable_timing=True, external=True)
+                   for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+        timed = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(timed, stream=stream):
+            for s in range(args.steps):
+                for i, (_, fn) in enumerate(calls):
+                    events[s][i].record(stream)
+                    fn()
+                events[s][-1].record(stream)
+        mode = "one graph of all timed steps, external timing events between calls"
+    except (TypeError, RuntimeError):
+        timed, events, mode = None, None, "per-step graphs"
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step_graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(torch.cuda.current_device()) as clk, torch.cuda.stream(stream):
+        t0.record(stream)
+        if timed is not None:
+            timed.replay()
+        else:
+            for _ in range(args.steps):
+                step_graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step = t0.elapsed_time(t1) / args.steps
+    per_call_us = {}
+    if events is not None:
+        for i, name in enumerate(names):
+            per_call_us[name] = 1000.0 * float(np.mean(
+                [events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps)]))
+    if world > 1:
+        t = torch.tensor([ms_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # experts touched by the routing of the last step (the idx buffer holds the last MoE
+    # layer's selection; the others are taken to touch as many)
+    touched = {}
+    moe_layers = [l for i, l in enumerate(wl.layers) if not wl.stack.dense[i]]
+    if moe_layers:
+        n = wl.touched_experts(b)
+        for l in moe_layers:
+            touched[l] = n
+    algo_bytes, per_layer = wl.algorithmic_bytes(touched)
+    us_per_token_layer = ms_step * 1000.0 / (wl.batch * world) / len(wl.layers)
+    hbm, hbm_kind = peaks()
+    layer_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
+
+    roof = None
+    if per_call_us:
+        dom = max(per_call_us, key=per_call_us.get)
+        dom_bytes, dom_key = dominant_bytes(wl, dom, touched)
+        dom_gbs = dom_bytes / (per_call_us[dom] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(dom_gbs / hbm, 4),
+                "traffic": ncu_traffic(dom_key), "bytes_per_launch": dom_bytes,
+                "duration_us": round(per_call_us[dom], 2), "peak_kind": hbm_kind}
+
+    e2e = run_e2e(args, wl, step_graph, stream, world)
+    res = {
+        "metric": METRIC,
+        "value": round(us_per_token_layer, 3),
+        "unit": "us/token/layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) activations and KV cache, random-init N(0,0.02) weights",
+        "config": {
+            "workload": args.workload, "layers": wl.layers, "batch": wl.batch,
+            "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
+            "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
+            "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": f"no flush: each step streams {algo_bytes / 1e6:.0f} MB (> 129 MB L2)",
+            "timing": mode,
+        },
+        "layer_hbm": {"algorithmic_bytes_per_step": algo_bytes,
+                      "achieved_gbs": round(layer_gbs, 1), "peak_gbs": hbm,
+                      "frac": round(layer_gbs / hbm, 4), "peak_kind": hbm_kind},
+        "roofline": roof,
+        "per_call_us": {k: round(v, 2) for k, v in per_call_us.items()},
+        "e2e": e2e,
+        "gpu_launches": launches_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args, wl, budget_s=args.cpu_budget)
+    return res
+
+
+def dominant_bytes(wl, name, touched):
+    """Algorithmic bytes of one call of the step (weights and cache it must read once)."""
+    l = int(name.split(".")[0][1:])
+    if name.endswith(".moe"):
+        return touched[l] * 3 * BEAM.hidden * BEAM.d_ff_expert * 2, "moe_decode"
+    if name.endswith(".attn"):
+        keys = wl.ctx + 1 if is_nope(l, BEAM.n_layers) else min(BEAM.window, wl.ctx + 1)
+        elem = 1 if wl.fp8 else 2
+        kv = wl.batch * keys * BEAM.n_kv * BEAM.head_dim * 2 * elem
+        return kv + BEAM.hidden * BEAM.q_rows * 2, "attn_decode"
+    if name.endswith(".dense_mlp"):
+        return 3 * BEAM.hidden * BEAM.d_ff_dense * 2, "dense_decode"
+    if name.endswith(".route"):
+        return BEAM.n_experts * BEAM.hidden * 4, "route_decode"
+    if name.endswith(".qkv_gate"):
+        return BEAM.qkvg_rows * BEAM.hidden * 2, "qkv_decode"
+    return 2 * wl.batch * BEAM.hidden * 2, "norm"
+
+
+def run_e2e(args, wl, step_graph, stream, world):
+    """Same step with the tokens' hidden state copied in from pinned host memory and the
+    output h copied back, both inside the timed region."""
+    b = wl.stack.buffers(wl.batch)
+    h_host = wl.e.cpu().pin_memory()
+    out_host = torch.empty_like(h_host).pin_memory()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            wl.e.copy_(h_host, non_blocking=True)
+            step_graph.replay()
+            out_host.copy_(b["h"], non_blocking=True)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    nbytes = h_host.numel() * h_host.element_size()
+    return {"value": round(ms * 1000.0 / (wl.batch * world) / len(wl.layers), 3),
+            "unit": "us/token/layer", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+
+# ------------------------------------------------------------------------ oracle arm ----
+
+def oracle_sample(args, wl):
+    """A bounded oracle workload: the first sequence's new token through the held layers."""
+    import oracle as O
+    shape = wl.shape
+
+    def np64(t):
+        return t.float().cpu().numpy()
+
+    class Lazy:
+        def __init__(self, t):
+            self.t, self.c = t, {}
+
+        def __getitem__(self, e):
+            if e not in self.c:
+                self.c[e] = np64(self.t[e])
+            return self.c[e]
+
+    Wo = []
+    for W in wl.W:
+        d = {}
+        for k, v in W.items():
+            d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else np64(v)
+        Wo.append(d)
+    caches = []
+    for kc in wl.caches:
+        if kc.fp8:
+            caches.append(O.KVCache(kc.k[:1].cpu().numpy(), kc.v[:1].cpu().numpy(), "fp8",
+                                    kc.k_scale, kc.v_scale, window=kc.window))
+        else:
+            caches.append(O.KVCache(np64(kc.k[:1]), np64(kc.v[:1]), "bf16", window=kc.window))
+    h0 = np64(wl.e[:1]).astype(np.float64)
+    pos = [wl.ctx + 1]
+
+    def run():
+        h, u = O.boundary_norm(None, h0, None, Wo[0]["attn_pre"], 1, shape.eps)
+        for i, l in enumerate(wl.layers):
+            nxt = Wo[i + 1]["attn_pre"] if i + 1 < len(wl.layers) else None
+            h, u = O.layer_forward(shape, l, Wo[i], h, u, caches[i], [0], pos, nxt)
+        return h
+
+    run()   # untimed: fetches the experts the oracle's own routing picks
+    return run
+
+
+def cpu_baseline(args, wl, budget_s=15.0):
+    run = oracle_sample(args, wl)
+    n, t_total = 0, 0.0
+    while t_total < budget_s and n < 50:
+        t = time.perf_counter()
+        run()
+        t_total += time.perf_counter() - t
+        n += 1
+    us = t_total / n * 1e6 / len(wl.layers)
+    return {"value": round(us, 1), "unit": "us/token/layer", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{n} x one token of sequence 0 through layers {wl.layers} "
+                      f"(context {wl.ctx}); float64 NumPy oracle, {t_total:.1f} s"}
+
+
+def run_reference(args, rank, world, device):
+    if rank != 0:
+        return None
+    wl = Workload(args, device)
+    run = oracle_sample(args, wl)
+    for _ in range(args.warmup):
+        run()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t) / args.steps
+    us = dt * 1e6 / len(wl.layers)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/token/layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1000, 2), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the CUDA arm)",
+        "config": {"workload": args.workload, "layers": wl.layers, "batch": 1,
+                   "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
+                   "sample": "one token of sequence 0 per step"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/token/layer",
+                         "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "one token of sequence 0 through the held layers per step"},
+        "e2e": {"value": round(us, 1), "unit": "us/token/layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------------------ main ----
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="swa_decode",
+                    choices=["swa_decode", "nope_decode", "stack_decode"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--context", type=int, default=100_000)
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        args.warmup = 3
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(device))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, device)
+    else:
+        res = run_ours(args, rank, world, device)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,665 @@
+// GQA attention over the KV cache, sigmoid output gate, o_proj.
+// Beam page, Attention section: 48 query heads share 8 KV heads (dim 128); sliding-window
+// layers attend to the last 512 keys, NoPE layers to the whole context; each head's output is
+// multiplied by sigmoid(gate + per-head bias) before o_proj. Change 2 of the optimisation list
+// keeps the gate as its own step; here it is fused into the attention epilogue.
+//
+// Decode (few tokens): split-K flash decoding. A CTA takes one (token, KV head, key range);
+// the G query heads of the KV group form the rows of a 16-row tensor-core tile, so every K/V
+// byte read from HBM serves all G heads. Each of the 4 warps streams its own 32-key tiles
+// through a 2-stage cp.async pipeline; partial (max, sum, P.V) go to the workspace and a merge
+// kernel combines the splits, normalises, gates and writes o.
+// Prefill (many tokens): a CTA takes 16 consecutive tokens and one KV group; warp w computes
+// query head w of the group for those 16 tokens, all warps sharing each staged K/V tile.
+//
+// P is split into bf16 hi + lo parts for the P.V product, so P carries ~16 significant bits;
+// the logits Q.K^T are exact products of bf16 inputs accumulated in FP32.
+#include <math.h>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "gemv.cuh"
+#include "mma.cuh"
+
+namespace beam {
+namespace {
+
+constexpr float kNegInf = -INFINITY;
+constexpr int kDecWarps = 4;
+constexpr int kDecKT = 32;   // keys per warp tile (decode)
+constexpr int kPreKT = 64;   // keys per CTA tile (prefill)
+constexpr int kRows = 16;    // tensor-core tile rows
+
+template <int D, bool FP8, int KT>
+struct TileGeom {
+  static constexpr int ROWB = D * 2;          // bf16 row bytes
+  static constexpr int CH = D / 8;            // 16-byte chunks per bf16 row
+  static constexpr int RAWROW = FP8 ? D : D * 2;
+  static constexpr int RAWCH = RAWROW / 16;   // 16-byte chunks per stored row
+  static constexpr int TILEB = KT * ROWB;     // one bf16 tile
+  static constexpr int RAWB = KT * RAWROW;    // one stored tile
+  // 2 stages of raw K and V, plus (fp8 only) one converted K and V tile
+  static constexpr int BYTES = 4 * RAWB + (FP8 ? 2 * TILEB : 0);
+};
+
+// Issue the copies of `rows` keys starting at cache slot chain s0 (slot of row r is
+// (s0 + r) mod cap) into raw tile `dst`; rows >= nvalid are zero-filled. Threads
+// [tid0, tid0 + nthr) share the work. bf16 tiles are stored swizzled, fp8 tiles plainly.
+template <int D, bool FP8, int KT>
+__device__ __forceinline__ void issue_tile(uint8_t* dst, const uint8_t* src_base, int s0, int cap,
+                                           int nvalid, int tid, int nthr) {
+  using Gm = TileGeom<D, FP8, KT>;
+  const uint32_t d0 = smem_u32(dst);
+  for (int q = tid; q < KT * Gm::RAWCH; q += nthr) {
+    const int r = q / Gm::RAWCH, ch = q - r * Gm::RAWCH;
+    int sl = s0 + r;
+    while (sl >= cap) sl -= cap;
+    const bool ok = r < nvalid;
+    const uint8_t* src = src_base + (ok ? size_t(sl) * Gm::RAWROW + ch * 16 : 0);
+    const uint32_t off = FP8 ? uint32_t(r * Gm::RAWROW + ch * 16) : swz(r, ch, Gm::ROWB);
+    cp_async16(d0 + off, src, ok ? 16 : 0);
+  }
+}
+
+// fp8 raw tile -> swizzled bf16 tile (exact conversion).
+template <int D, int KT>
+__device__ __forceinline__ void convert_tile(const uint8_t* raw, uint8_t* out, int tid, int nthr) {
+  using Gm = TileGeom<D, true, KT>;
+  for (int q = tid; q < KT * Gm::RAWCH; q += nthr) {
+    const int r = q / Gm::RAWCH, c16 = q - r * Gm::RAWCH;
+    const uint4 v = *reinterpret_cast<const uint4*>(raw + r * Gm::RAWROW + c16 * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = e4m3x2_to_bf16x2(uint16_t(w[i] & 0xFFFF));
+      o[2 * i + 1] = e4m3x2_to_bf16x2(uint16_t(w[i] >> 16));
+    }
+    *reinterpret_cast<uint4*>(out + swz(r, 2 * c16, Gm::ROWB)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(out + swz(r, 2 * c16 + 1, Gm::ROWB)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+// S[16 x KT] = Q (fragments qa) . K_tile^T
+template <int D, int KT>
+__device__ __forceinline__ void qk_tile(const uint32_t (&qa)[D / 16][4], const uint8_t* ktile,
+                                        float (&s)[KT / 8][4]) {
+  constexpr int ROWB = D * 2;
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3, rr = lane & 7;
+  const uint32_t base = smem_u32(ktile);
+#pragma unroll
+  for (int j = 0; j < KT / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+    for (int nb = 0; nb < KT / 16; ++nb) {
+      const int row = nb * 16 + ((mi >> 1) << 3) + rr;
+      const int ch = 2 * kk + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(base + swz(row, ch, ROWB), b0, b1, b2, b3);
+      mma_bf16(s[2 * nb], qa[kk], b0, b1);
+      mma_bf16(s[2 * nb + 1], qa[kk], b2, b3);
+    }
+  }
+}
+
+// acc[16 x D] += P[16 x KT] . V_tile; P given as C fragments p (already exponentiated).
+template <int D, int KT, bool SPLITP>
+__device__ __forceinline__ void pv_tile(const float (&p)[KT / 8][4], const uint8_t* vtile,
+                                        float (&acc)[D / 8][4]) {
+  constexpr int ROWB = D * 2;
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3, rr = lane & 7;
+  const uint32_t base = smem_u32(vtile);
+#pragma unroll
+  for (int ks = 0; ks < KT / 16; ++ks) {
+    uint32_t hi[4], lo[4];
+    const float* p0 = p[2 * ks];
+    const float* p1 = p[2 * ks + 1];
+    hi[0] = pack_bf16x2(p0[0], p0[1]);
+    hi[1] = pack_bf16x2(p0[2], p0[3]);
+    hi[2] = pack_bf16x2(p1[0], p1[1]);
+    hi[3] = pack_bf16x2(p1[2], p1[3]);
+    if (SPLITP) {
+      lo[0] = pack_bf16x2(p0[0] - bf_lo(hi[0]), p0[1] - bf_hi(hi[0]));
+      lo[1] = pack_bf16x2(p0[2] - bf_lo(hi[1]), p0[3] - bf_hi(hi[1]));
+      lo[2] = pack_bf16x2(p1[0] - bf_lo(hi[2]), p1[1] - bf_hi(hi[2]));
+      lo[3] = pack_bf16x2(p1[2] - bf_lo(hi[3]), p1[3] - bf_hi(hi[3]));
+    }
+#pragma unroll
+    for (int db = 0; db < D / 16; ++db) {
+      const int row = ks * 16 + ((mi & 1) << 3) + rr;
+      const int ch = 2 * db + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(base + swz(row, ch, ROWB), b0, b1, b2, b3);
+      mma_bf16(acc[2 * db], hi, b0, b1);
+      mma_bf16(acc[2 * db + 1], hi, b2, b3);
+      if (SPLITP) {
+        mma_bf16(acc[2 * db], lo, b0, b1);
+        mma_bf16(acc[2 * db + 1], lo, b2, b3);
+      }
+    }
+  }
+}
+
+// Online-softmax update of one tile. s holds raw logits; keys whose `valid` bit is clear
+// are masked. On return s holds P = exp2(s * sl2 - m).
+template <int KT, int DN>
+__device__ __forceinline__ void softmax_update(float (&s)[KT / 8][4], const bool (&valid)[KT / 8][4],
+                                               float sl2, float (&m)[2], float (&l)[2],
+                                               float (&acc)[DN][4]) {
+  float mx[2] = {kNegInf, kNegInf};
+#pragma unroll
+  for (int j = 0; j < KT / 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = valid[j][e] ? s[j][e] * sl2 : kNegInf;
+      s[j][e] = x;
+      mx[e >> 1] = fmaxf(mx[e >> 1], x);
+    }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+    const float mnew = fmaxf(m[h], mx[h]);
+    const float corr = (mnew == kNegInf) ? 1.f : exp2f(m[h] - mnew);
+    m[h] = mnew;
+    l[h] *= corr;
+#pragma unroll
+    for (int n = 0; n < DN; ++n) {
+      acc[n][2 * h] *= corr;
+      acc[n][2 * h + 1] *= corr;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KT / 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float mm = m[e >> 1];
+      const float pv = (s[j][e] == kNegInf) ? 0.f : exp2f(s[j][e] - mm);
+      s[j][e] = pv;
+      l[e >> 1] += pv;
+    }
+}
+
+// Query fragments of 16 rows; row r is query head (head0 + r*hstride) of token (tok0 + r*tstride),
+// rows with r >= nrows are zero.
+template <int D>
+__device__ __forceinline__ void load_q(const uint16_t* q, uint32_t (&qa)[D / 16][4],
+                                       const int (&rowoff)[2], const bool (&rowok)[2]) {
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 3;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(q + rowoff[h] + kk * 16 + 2 * c);
+      qa[kk][h] = rowok[h] ? src[0] : 0u;       // a0 / a1: cols 2c..2c+1
+      qa[kk][h + 2] = rowok[h] ? src[4] : 0u;   // a2 / a3: cols 2c+8..
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Decode: split-K partials
+// ------------------------------------------------------------------------------------------
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
+    const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_id,
+    const int32_t* __restrict__ pos, int n_q, int n_kv, beam_kv_cache kc, int kps, int n_splits,
+    float sl2, float* __restrict__ part_acc, float* __restrict__ part_ml) {
+  using Gm = TileGeom<D, FP8, kDecKT>;
+  constexpr int KT = kDecKT;
+  constexpr int DN = D / 8;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int split = blockIdx.x, hk = blockIdx.y, t = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = n_q / n_kv;
+  const int p = pos[t], s = seq_id[t];
+  bool ok = p >= 1 && s >= 0 && s < kc.num_seqs && !(kc.window == 0 && p > kc.capacity);
+  if (!ok && split == 0 && hk == 0 && threadIdx.x == 0)
+    flag((p < 1 || (kc.window == 0 && p > kc.capacity)) ? BEAM_DEV_BAD_POSITION : BEAM_DEV_BAD_SEQ);
+  const int lo = kc.window > 0 ? max(1, p - kc.window + 1) : 1;
+  const int nkeys = ok ? p - lo + 1 : 0;
+  const int k_begin = split * kps;
+  const int k_end = min(nkeys, k_begin + kps);
+  const int ntiles = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
+  const int my_tiles = ntiles > warp ? (ntiles - warp + kDecWarps - 1) / kDecWarps : 0;
+
+  uint32_t qa[D / 16][4];
+  {
+    const int rows[2] = {g, g + 8};
+    int off[2];
+    bool rok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      rok[h] = rows[h] < G;
+      off[h] = (t * n_q + hk * G + (rok[h] ? rows[h] : 0)) * D;
+    }
+    load_q<D>(q, qa, off, rok);
+  }
+
+  float acc[DN][4];
+#pragma unroll
+  for (int n = 0; n < DN; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+
+  uint8_t* wbase = smem + warp * Gm::BYTES;
+  const size_t head_off = (size_t(ok ? s : 0) * n_kv + hk) * kc.capacity;
+  const uint8_t* kbase = static_cast<const uint8_t*>(kc.k) + head_off * Gm::RAWROW;
+  const uint8_t* vbase = static_cast<const uint8_t*>(kc.v) + head_off * Gm::RAWROW;
+  const int slot_lo = ok ? (lo - 1) % kc.capacity : 0;
+
+  auto issue = [&](int i, int stage) {
+    const int key0 = k_begin + (warp + i * kDecWarps) * KT;
+    const int s0 = (slot_lo + key0) % kc.capacity;
+    uint8_t* kd = wbase + stage * 2 * Gm::RAWB;
+    issue_tile<D, FP8, KT>(kd, kbase, s0, kc.capacity, k_end - key0, lane, 32);
+    issue_tile<D, FP8, KT>(kd + Gm::RAWB, vbase, s0, kc.capacity, k_end - key0, lane, 32);
+  };
+  if (my_tiles > 0) issue(0, 0);
+  cp_async_commit();
+  for (int i = 0; i < my_tiles; ++i) {
+    if (i + 1 < my_tiles) issue(i + 1, (i + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncwarp();
+    const uint8_t* kt = wbase + (i & 1) * 2 * Gm::RAWB;
+    const uint8_t* vt = kt + Gm::RAWB;
+    if (FP8) {
+      uint8_t* cvt = wbase + 4 * Gm::RAWB;
+      convert_tile<D, KT>(kt, cvt, lane, 32);
+      convert_tile<D, KT>(vt, cvt + Gm::TILEB, lane, 32);
+      __syncwarp();
+      kt = cvt;
+      vt = cvt + Gm::TILEB;
+    }
+    float sacc[KT / 8][4];
+    qk_tile<D, KT>(qa, kt, sacc);
+    const int key0 = k_begin + (warp + i * kDecWarps) * KT;
+    bool valid[KT / 8][4];
+#pragma unroll
+    for (int j = 0; j < KT / 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) valid[j][e] = key0 + 8 * j + 2 * c + (e & 1) < k_end;
+    softmax_update<KT, DN>(sacc, valid, sl2, m, l, acc);
+    pv_tile<D, KT, true>(sacc, vt, acc);
+    __syncwarp();
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+  }
+
+  // combine the 4 warps of the CTA through shared memory
+  cp_async_wait<0>();
+  __syncthreads();
+  constexpr int ACC_LD = D + 4;
+  float* sacc_all = reinterpret_cast<float*>(smem);                       // [warps][16][ACC_LD]
+  float* sml = sacc_all + kDecWarps * kRows * ACC_LD;                     // [warps][16][2]
+  {
+    float* a = sacc_all + warp * kRows * ACC_LD;
+#pragma unroll
+    for (int n = 0; n < DN; ++n) {
+      a[g * ACC_LD + 8 * n + 2 * c] = acc[n][0];
+      a[g * ACC_LD + 8 * n + 2 * c + 1] = acc[n][1];
+      a[(g + 8) * ACC_LD + 8 * n + 2 * c] = acc[n][2];
+      a[(g + 8) * ACC_LD + 8 * n + 2 * c + 1] = acc[n][3];
+    }
+    if (c == 0) {
+      sml[(warp * kRows + g) * 2] = m[0];
+      sml[(warp * kRows + g) * 2 + 1] = l[0];
+      sml[(warp * kRows + g + 8) * 2] = m[1];
+      sml[(warp * kRows + g + 8) * 2 + 1] = l[1];
+    }
+  }
+  __syncthreads();
+  const size_t pbase = (size_t(t) * n_kv + hk) * n_splits + split;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int row = idx / D, d = idx - row * D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sml[(w * kRows + row) * 2]);
+    float O = 0.f, L = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float f = exp2f(sml[(w * kRows + row) * 2] - M);
+        O += f * sacc_all[(w * kRows + row) * ACC_LD + d];
+        L += f * sml[(w * kRows + row) * 2 + 1];
+      }
+    }
+    part_acc[(pbase * kRows + row) * D + d] = O;
+    if (d == 0) {
+      part_ml[(pbase * kRows + row) * 2] = M;
+      part_ml[(pbase * kRows + row) * 2 + 1] = L;
+    }
+  }
+}
+
+// Merge the splits of one (token, KV head), normalise, round, gate, round.
+__global__ void __launch_bounds__(256) attn_merge_gate_kernel(
+    const float* __restrict__ part_acc, const float* __restrict__ part_ml, int n_splits, int n_q,
+    int n_kv, int D, float v_scale, const uint16_t* __restrict__ gpre,
+    const uint16_t* __restrict__ gate_bias, uint16_t* __restrict__ og) {
+  const int hk = blockIdx.x, t = blockIdx.y;
+  const int G = n_q / n_kv;
+  const size_t pbase = (size_t(t) * n_kv + hk) * n_splits;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int row = idx / D, d = idx - row * D;
+    float M = kNegInf;
+    for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, part_ml[((pbase + sp) * kRows + row) * 2]);
+    float O = 0.f, L = 0.f;
+    if (M != kNegInf) {
+      for (int sp = 0; sp < n_splits; ++sp) {
+        const float f = exp2f(part_ml[((pbase + sp) * kRows + row) * 2] - M);
+        O += f * part_acc[((pbase + sp) * kRows + row) * D + d];
+        L += f * part_ml[((pbase + sp) * kRows + row) * 2 + 1];
+      }
+    }
+    const float o = L > 0.f ? round_bf(O / L * v_scale) : 0.f;
+    const int hq = hk * G + row;
+    const size_t oi = (size_t(t) * n_q + hq) * D + d;
+    const float gate = sigmoidf_(bf2f(gpre[oi]) + bf2f(gate_bias[hq]));
+    og[oi] = f2bf(o * gate);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Prefill: query tiles of 16 tokens x one KV group
+// ------------------------------------------------------------------------------------------
+template <int D, bool FP8>
+__global__ void __launch_bounds__(256) attn_prefill_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ gpre,
+    const uint16_t* __restrict__ gate_bias, const int32_t* __restrict__ seq_id,
+    const int32_t* __restrict__ pos, int T, int n_q, int n_kv, beam_kv_cache kc, float sl2,
+    uint16_t* __restrict__ og) {
+  using Gm = TileGeom<D, FP8, kPreKT>;
+  constexpr int KT = kPreKT;
+  constexpr int DN = D / 8;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_seq[kRows], s_lo[kRows], s_hi[kRows];
+  const int t0 = blockIdx.x * kRows, hk = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = n_q / n_kv;
+  const int hq = hk * G + warp;
+
+  if (threadIdx.x < kRows) {
+    const int t = t0 + threadIdx.x;
+    int sq = -1, lo = 1, hi = 0;
+    if (t < T) {
+      const int p = pos[t], s = seq_id[t];
+      const bool badp = p < 1 || (kc.window == 0 && p > kc.capacity);
+      const bool bads = s < 0 || s >= kc.num_seqs;
+      if (badp) flag(BEAM_DEV_BAD_POSITION);
+      if (bads) flag(BEAM_DEV_BAD_SEQ);
+      if (!badp && !bads) {
+        sq = s;
+        hi = p;
+        lo = kc.window > 0 ? max(1, p - kc.window + 1) : 1;
+      }
+    }
+    s_seq[threadIdx.x] = sq;
+    s_lo[threadIdx.x] = lo;
+    s_hi[threadIdx.x] = hi;
+  }
+  __syncthreads();
+
+  uint32_t qa[D / 16][4];
+  {
+    int off[2];
+    bool rok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + g + 8 * h;
+      rok[h] = t < T && s_seq[g + 8 * h] >= 0;
+      off[h] = ((rok[h] ? t : 0) * n_q + hq) * D;
+    }
+    load_q<D>(q, qa, off, rok);
+  }
+  const int rseq[2] = {s_seq[g], s_seq[g + 8]};
+  const int rlo[2] = {s_lo[g], s_lo[g + 8]};
+  const int rhi[2] = {s_hi[g], s_hi[g + 8]};
+
+  float acc[DN][4];
+#pragma unroll
+  for (int n = 0; n < DN; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+
+  int cur = -1;
+  while (true) {
+    // next sequence present in the tile
+    int nxt = 0x7fffffff;
+    for (int r = 0; r < kRows; ++r)
+      if (s_seq[r] > cur) nxt = min(nxt, s_seq[r]);
+    if (nxt == 0x7fffffff) break;
+    cur = nxt;
+    int kmin = 0x7fffffff, kmax = 0;
+    for (int r = 0; r < kRows; ++r)
+      if (s_seq[r] == cur) { kmin = min(kmin, s_lo[r]); kmax = max(kmax, s_hi[r]); }
+    const int nkeys = kmax - kmin + 1;
+    const int ntiles = (nkeys + KT - 1) / KT;
+    const size_t head_off = (size_t(cur) * n_kv + hk) * kc.capacity;
+    const uint8_t* kbase = static_cast<const uint8_t*>(kc.k) + head_off * Gm::RAWROW;
+    const uint8_t* vbase = static_cast<const uint8_t*>(kc.v) + head_off * Gm::RAWROW;
+    const int slot_lo = (kmin - 1) % kc.capacity;
+    auto issue = [&](int i, int stage) {
+      const int key0 = i * KT;
+      const int s0 = (slot_lo + key0) % kc.capacity;
+      uint8_t* kd = smem + stage * 2 * Gm::RAWB;
+      issue_tile<D, FP8, KT>(kd, kbase, s0, kc.capacity, nkeys - key0, threadIdx.x, blockDim.x);
+      issue_tile<D, FP8, KT>(kd + Gm::RAWB, vbase, s0, kc.capacity, nkeys - key0, threadIdx.x,
+                             blockDim.x);
+    };
+    issue(0, 0);
+    cp_async_commit();
+    for (int i = 0; i < ntiles; ++i) {
+      if (i + 1 < ntiles) issue(i + 1, (i + 1) & 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+      __syncthreads();
+      const uint8_t* kt = smem + (i & 1) * 2 * Gm::RAWB;
+      const uint8_t* vt = kt + Gm::RAWB;
+      if (FP8) {
+        uint8_t* cvt = smem + 4 * Gm::RAWB;
+        convert_tile<D, KT>(kt, cvt, threadIdx.x, blockDim.x);
+        convert_tile<D, KT>(vt, cvt + Gm::TILEB, threadIdx.x, blockDim.x);
+        __syncthreads();
+        kt = cvt;
+        vt = cvt + Gm::TILEB;
+      }
+      const int kp0 = kmin + i * KT;   // position of the tile's first key
+      bool any = false;
+      bool valid[KT / 8][4];
+#pragma unroll
+      for (int j = 0; j < KT / 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = e >> 1;
+          const int kp = kp0 + 8 * j + 2 * c + (e & 1);
+          valid[j][e] = rseq[h] == cur && kp >= rlo[h] && kp <= rhi[h];
+          any |= valid[j][e];
+        }
+      if (__any_sync(0xffffffffu, any)) {
+        float sacc[KT / 8][4];
+        qk_tile<D, KT>(qa, kt, sacc);
+        softmax_update<KT, DN>(sacc, valid, sl2, m, l, acc);
+        pv_tile<D, KT, true>(sacc, vt, acc);
+      }
+      __syncthreads();
+    }
+    cp_async_wait<0>();
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+  }
+  const float vs = FP8 ? kc.v_scale : 1.f;
+  const float gb = bf2f(gate_bias[hq]);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = t0 + g + 8 * h;
+    if (t >= T) continue;
+    const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+    const size_t ob = (size_t(t) * n_q + hq) * D;
+#pragma unroll
+    for (int n = 0; n < DN; ++n) {
+      const int d = 8 * n + 2 * c;
+      const float o0 = round_bf(acc[n][2 * h] * inv * vs);
+      const float o1 = round_bf(acc[n][2 * h + 1] * inv * vs);
+      const uint32_t gg = *reinterpret_cast<const uint32_t*>(gpre + ob + d);
+      const float r0 = o0 * sigmoidf_(bf_lo(gg) + gb);
+      const float r1 = o1 * sigmoidf_(bf_hi(gg) + gb);
+      *reinterpret_cast<uint32_t*>(og + ob + d) = pack_bf16x2(r0, r1);
+    }
+  }
+}
+
+int g_num_sms = 0;
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 152;
+  }
+  return g_num_sms;
+}
+
+constexpr int kDecodeMaxT = 32;
+
+struct DecodePlan {
+  int kps, n_splits;
+};
+
+DecodePlan decode_plan(int T, int n_kv, int max_keys) {
+  const int per = T * n_kv;
+  int splits = (2 * num_sms() + per - 1) / per;
+  const int max_splits = (max_keys + 127) / 128;
+  splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
+  int kps = (max_keys + splits - 1) / splits;
+  kps = (kps + 127) / 128 * 128;
+  splits = (max_keys + kps - 1) / kps;
+  if (splits < 1) splits = 1;
+  return {kps, splits};
+}
+
+int max_keys_of(int window, int max_pos) {
+  return window > 0 ? (max_pos < window ? max_pos : window) : max_pos;
+}
+
+template <class K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, bool FP8>
+cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_t* pos, int T,
+                          int n_q, int n_kv, const beam_kv_cache& kc, DecodePlan pl, float sl2,
+                          float* pacc, float* pml, cudaStream_t st) {
+  using Gm = TileGeom<D, FP8, kDecKT>;
+  int bytes = kDecWarps * Gm::BYTES;
+  const int comb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
+  if (comb > bytes) bytes = comb;
+  auto kern = attn_decode_split_kernel<D, FP8>;
+  cudaError_t e = set_smem(kern, bytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(pl.n_splits, n_kv, T);
+  kern<<<grid, kDecWarps * 32, bytes, st>>>(q, seq_id, pos, n_q, n_kv, kc, pl.kps, pl.n_splits,
+                                            sl2, pacc, pml);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <int D, bool FP8>
+cudaError_t launch_prefill(const uint16_t* q, const uint16_t* g, const uint16_t* gb,
+                           const int32_t* seq_id, const int32_t* pos, int T, int n_q, int n_kv,
+                           const beam_kv_cache& kc, float sl2, uint16_t* og, cudaStream_t st) {
+  using Gm = TileGeom<D, FP8, kPreKT>;
+  const int bytes = Gm::BYTES;
+  auto kern = attn_prefill_kernel<D, FP8>;
+  cudaError_t e = set_smem(kern, bytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((T + kRows - 1) / kRows, n_kv);
+  kern<<<grid, 32 * (n_q / n_kv), bytes, st>>>(q, g, gb, seq_id, pos, T, n_q, n_kv, kc, sl2, og);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
+  size_t b = align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
+  if (T <= kDecodeMaxT) {
+    const DecodePlan pl = decode_plan(T, c->n_kv, max_keys_of(window, max_pos > 0 ? max_pos : 1));
+    const size_t parts = size_t(T) * c->n_kv * pl.n_splits * kRows;
+    b += align_up(parts * c->head_dim * 4, 256) + align_up(parts * 2 * 4, 256);
+  }
+  return b;
+}
+
+}  // namespace beam
+
+extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
+                                 const beam_bf16* g, const beam_bf16* gate_bias,
+                                 const beam_kv_cache* cache, const int32_t* seq_id,
+                                 const int32_t* pos, int T, int max_pos, const beam_bf16* w_o,
+                                 beam_bf16* out, void* ws, size_t ws_bytes,
+                                 beam_stream_t stream) {
+  using namespace beam;
+  beam_status stt = check_cfg_attn(cfg);
+  if (stt != BEAM_OK) return stt;
+  if ((stt = check_cache(cache, cfg)) != BEAM_OK) return stt;
+  if (T < 0 || max_pos < 1 || !q || !g || !gate_bias || !seq_id || !pos || !w_o || !out)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(g) || !aligned16(w_o) || !aligned16(out) || !aligned16(ws))
+    return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  const int D = cfg->head_dim, H = cfg->hidden, HD = cfg->n_q * D;
+  const bool fp8 = cache->dtype == BEAM_KV_FP8_E4M3;
+  const float sl2 = float(1.4426950408889634 / sqrt(double(D))) * (fp8 ? cache->k_scale : 1.f);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  uint16_t* og = cv.take<uint16_t>(size_t(T) * HD);
+  cudaError_t e;
+  if (T <= kDecodeMaxT) {
+    const DecodePlan pl = decode_plan(T, cfg->n_kv, max_keys_of(cache->window, max_pos));
+    const size_t parts = size_t(T) * cfg->n_kv * pl.n_splits * kRows;
+    float* pacc = cv.take<float>(parts * D);
+    float* pml = cv.take<float>(parts * 2);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    if (D == 128)
+      e = fp8 ? launch_decode<128, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st)
+              : launch_decode<128, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st);
+    else
+      e = fp8 ? launch_decode<64, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st)
+              : launch_decode<64, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    attn_merge_gate_kernel<<<dim3(cfg->n_kv, T), 256, 0, st>>>(
+        pacc, pml, pl.n_splits, cfg->n_q, cfg->n_kv, D, fp8 ? cache->v_scale : 1.f, g, gate_bias,
+        og);
+    note_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+  } else {
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    if (cfg->n_q / cfg->n_kv * 32 > 256) return BEAM_ERR_UNSUPPORTED;
+    if (D == 128)
+      e = fp8 ? launch_prefill<128, true>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st)
+              : launch_prefill<128, false>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st);
+    else
+      e = fp8 ? launch_prefill<64, true>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st)
+              : launch_prefill<64, false>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  }
+  const cudaError_t ge =
+      T >= kGemmMinT && tc::gemm_supported(og, HD, w_o, HD, HD)
+          ? tc::gemm_bf16(og, T, HD, HD, w_o, H, HD, out, H, true, st)
+          : launch_gemv<kOutBF16>(w_o, H, HD, og, T, nullptr, out, H, st);
+  if (ge != cudaSuccess) return BEAM_ERR_CUDA;
+  return BEAM_OK;
+}

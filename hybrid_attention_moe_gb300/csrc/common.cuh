@@ -1,0 +1,145 @@
+// Shared device helpers for the Beam layer kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/beam.h"
+
+namespace beam {
+
+// Status word of the device (BEAM_DEV_* bits). Defined once in misc.cu.
+extern __device__ unsigned int g_dev_status;
+
+__device__ __forceinline__ void flag(unsigned int bit) { atomicOr(&g_dev_status, bit); }
+
+// ---- bf16 <-> fp32 ------------------------------------------------------------------
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+__device__ __forceinline__ float bflo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bfhi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float round_bf(float f) { return bf2f(f2bf(f)); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  return uint32_t(f2bf(lo)) | (uint32_t(f2bf(hi)) << 16);
+}
+
+// 8 bf16 held in a uint4 -> 8 floats
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  f[0] = bflo(v.x); f[1] = bfhi(v.x); f[2] = bflo(v.y); f[3] = bfhi(v.y);
+  f[4] = bflo(v.z); f[5] = bfhi(v.z); f[6] = bflo(v.w); f[7] = bfhi(v.w);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (weights are read once per call).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float4 ld_stream_f4(const void* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---- reductions -----------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over the block; every thread gets the result. `red` holds >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float s = lane < nw ? red[lane] : 0.f;
+  s = warp_sum(s);
+  return s;
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float siluf_(float z) { return z / (1.0f + __expf(-z)); }
+
+// ---- host-side argument checks ------------------------------------------------------------
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(p); }
+
+// Host-side count of kernel launches (misc.cu).
+void note_launches(int n);
+
+inline beam_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Carves 256-byte aligned regions out of the caller's workspace.
+struct Carver {
+  char* base;
+  size_t cap;
+  size_t off = 0;
+  bool ok = true;
+  template <class T>
+  T* take(size_t count) {
+    size_t o = align_up(off, 256);
+    size_t bytes = count * sizeof(T);
+    if (o + bytes > cap) { ok = false; return nullptr; }
+    off = o + bytes;
+    return reinterpret_cast<T*>(base + o);
+  }
+};
+
+}  // namespace beam
+
+namespace beam {
+
+// Token count from which the projections run on the tensor-core GEMM instead of the
+// weight-streaming GEMV (below it the weights' HBM read dominates and the GEMV is at roofline).
+constexpr int kGemmMinT = 64;
+
+// Attention widths this build compiles for.
+inline bool head_dim_ok(int D) { return D == 64 || D == 128; }
+
+inline beam_status check_cfg_attn(const beam_layer_cfg* c) {
+  if (c == nullptr) return BEAM_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || (c->hidden & 7) || c->n_q <= 0 || c->n_kv <= 0 ||
+      c->n_q % c->n_kv != 0 || c->head_dim <= 0 ||
+      (c->kind != BEAM_ATTN_SWA_ROPE && c->kind != BEAM_ATTN_NOPE_SSMAX) || !(c->eps >= 0.f))
+    return BEAM_ERR_INVALID_ARG;
+  if (!head_dim_ok(c->head_dim)) return BEAM_ERR_UNSUPPORTED;
+  if (c->n_q / c->n_kv > 16) return BEAM_ERR_UNSUPPORTED;
+  return BEAM_OK;
+}
+
+inline beam_status check_cache(const beam_kv_cache* kc, const beam_layer_cfg* c) {
+  if (kc == nullptr || kc->k == nullptr || kc->v == nullptr || kc->num_seqs <= 0 ||
+      kc->capacity <= 0 || kc->window < 0)
+    return BEAM_ERR_INVALID_ARG;
+  if (kc->dtype != BEAM_KV_BF16 && kc->dtype != BEAM_KV_FP8_E4M3) return BEAM_ERR_INVALID_ARG;
+  if (kc->dtype == BEAM_KV_FP8_E4M3 && !(kc->k_scale > 0.f && kc->v_scale > 0.f))
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(kc->k) || !aligned16(kc->v)) return BEAM_ERR_INVALID_ARG;
+  if (kc->window > 0 && kc->capacity < kc->window) return BEAM_ERR_INVALID_ARG;
+  (void)c;
+  return BEAM_OK;
+}
+
+}  // namespace beam

@@ -1,0 +1,391 @@
+// BF16 tensor-core GEMM for the prefill projections: C[M][N] = A[M][K] . B[N][K]^T, FP32
+// accumulation in tensor memory, written as FP32 or BF16.
+//
+// Blackwell (sm_103a) structure: one CTA per 128 x 256 output tile; a 4-stage shared-memory
+// ring of 64-wide K slices filled by TMA (128-byte swizzle, no multicast), consumed by
+// tcgen05.mma issued from one thread into a 128 x 256 FP32 accumulator in TMEM; four
+// epilogue warps read the accumulator back with tcgen05.ld and store it. Warp roles:
+//   warp 0 : TMA producer (one elected lane)
+//   warp 1 : TMEM allocation owner and MMA issuer (one elected lane)
+//   warps 2-5 : epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. output rows)
+// Every mbarrier wait is bounded; on expiry the CTA records BEAM_DEV_TIMEOUT in the status
+// word, lets its in-flight copies land, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "mma.cuh"
+
+namespace beam {
+namespace tc {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int THREADS = 192;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kWaitLimit polls (each poll may suspend the thread briefly).
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try(a, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups of 128 B
+// stacked at 1024 B (stride byte offset); the leading byte offset is unused for this layout.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(1) << 16;             // leading byte offset (ignored), 16 B units
+  d |= uint64_t(1024 >> 4) << 32;     // stride byte offset, 16 B units
+  d |= uint64_t(1) << 46;             // descriptor version for tcgen05
+  d |= uint64_t(2) << 61;             // swizzle: 128 B
+  return d;
+}
+
+// Instruction descriptor of kind::f16: BF16 A and B (K-major), FP32 D, M = 128, N = BN.
+constexpr uint32_t kIdesc = (1u << 4)            // D format F32
+                            | (1u << 7)          // A format BF16
+                            | (1u << 10)         // B format BF16
+                            | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// One CTA computes output columns [n0, n0 + BN) (kSwiGLU: units [n0, n0 + BN/2)) for A rows
+// [a_row0, a_row0 + rows). Dense GEMMs take a_row0 = 128 * blockIdx.y, b_row0 = 0; grouped
+// GEMMs read (b_row0, a_row0, rows) from a device-side job list (one job per expert row tile).
+struct GemmParams {
+  int M, N, K;           // A rows (bound), output columns (units for kSwiGLU), reduction
+  void* C;
+  int ldc;
+  const int4* jobs;      // grouped: {group, a_row0, rows, -}; nullptr for a dense GEMM
+  const int* n_jobs;     // grouped: number of valid jobs (device)
+  int b_stride;          // grouped: B rows per group (b_row0 = group * b_stride)
+  int up_off;            // kSwiGLU: B row offset of the up half from the gate half
+  const int* row_map;    // optional: C row of A row r is row_map[r]
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                   GemmParams p) {
+  int b_row0 = 0, a_row0 = blockIdx.y * BM, rows = BM;
+  if (p.jobs != nullptr) {
+    if (int(blockIdx.y) >= *p.n_jobs) return;   // uniform for the CTA, before any setup
+    const int4 j = p.jobs[blockIdx.y];
+    b_row0 = j.x * p.b_stride;
+    a_row0 = j.y;
+    rows = j.z;
+  }
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t accb = smem_u32(bars + 2 * STAGES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per CTA
+  const int n0 = blockIdx.x * NT;
+  const int KB = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*abort_flag || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_expect_tx(full0 + 8 * s, STAGE_BYTES);
+        const uint32_t sa = s_base + s * STAGE_BYTES;
+        tma_load_2d(sa, &ta, kb * BK, a_row0, full0 + 8 * s);
+        if (MODE == kSwiGLU) {
+          tma_load_2d(sa + A_BYTES, &tb, kb * BK, b_row0 + n0, full0 + 8 * s);
+          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tb, kb * BK, b_row0 + p.up_off + n0,
+                      full0 + 8 * s);
+        } else {
+          tma_load_2d(sa + A_BYTES, &tb, kb * BK, b_row0 + n0, full0 + 8 * s);
+        }
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
+          mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*abort_flag || !mbar_wait(full0 + 8 * s, ph)) {
+          *abort_flag = 1;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t sa = s_base + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          umma(tmem, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), (kb | k) != 0);
+        umma_commit(empty0 + 8 * s);
+      }
+      umma_commit(accb);   // arrives once every MMA issued above has completed
+    }
+  } else {
+    const int quad = warp & 3;
+    const bool ok = mbar_wait(accb, 0);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!ok) *abort_flag = 1;
+    const int r = quad * 32 + lane;
+    const int arow = a_row0 + r;
+    const bool row_ok = r < rows && arow < p.M;
+    const int crow = row_ok ? (p.row_map ? p.row_map[arow] : arow) : 0;
+    const uint32_t tbase = tmem + (uint32_t(quad * 32) << 16);
+    // tcgen05.ld is warp-collective: take the decision once for the whole warp
+    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+#pragma unroll 1
+      for (int c = 0; c < NT / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(tbase + uint32_t(c * 16), v);
+        const int col = n0 + c * 16;
+        if (MODE == kSwiGLU) {
+          uint32_t up[16];
+          tmem_ld16(tbase + uint32_t(BN / 2 + c * 16), up);
+          if (row_ok && col < p.N) {
+            uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              a[i] = siluf_(__uint_as_float(v[i])) * __uint_as_float(up[i]);
+            if (col + 16 <= p.N && (p.ldc & 7) == 0) {
+              uint32_t q[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) q[i] = pack_bf2(a[2 * i], a[2 * i + 1]);
+              reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+              reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            } else {
+              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = f2bf(a[i]);
+            }
+          }
+        } else if (row_ok && col < p.N) {
+          if (MODE == kF32) {
+            float* dst = static_cast<float*>(p.C) + size_t(crow) * p.ldc + col;
+            if (col + 16 <= p.N && (p.ldc & 3) == 0) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<float4*>(dst)[i] =
+                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            } else {
+              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = __uint_as_float(v[i]);
+            }
+          } else {
+            uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
+            if (col + 16 <= p.N && (p.ldc & 7) == 0) {
+              uint32_t q[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                q[i] = pack_bf2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+              reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+              reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            } else {
+              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = f2bf(__uint_as_float(v[i]));
+            }
+          }
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag(BEAM_DEV_TIMEOUT);
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool encoder() {
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return true;
+}
+
+// 2-D bf16 map over rows x inner (row stride ld elements), box box_rows x 64, 128 B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int box_rows) {
+  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_supported(const void* A, int lda, const void* B, int ldb, int K) {
+  return aligned16(A) && aligned16(B) && (lda % 8) == 0 && (ldb % 8) == 0 && (K % 8) == 0 &&
+         K > 0;
+}
+
+namespace {
+
+template <int MODE>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, dim3 grid,
+                   cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N, int ldb,
+                      void* C, int ldc, bool out_bf16, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
+  if (!encoder()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
+    return cudaErrorInvalidValue;
+  GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
+  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  return out_bf16 ? launch<kBF16>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
+}
+
+cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,
+                        int ldb, uint16_t* C, int ldc, cudaStream_t st) {
+  if (M <= 0 || F <= 0) return cudaSuccess;
+  if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
+  if (!encoder()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, 2 * F, ldb, BN / 2))
+    return cudaErrorInvalidValue;
+  GemmParams p{M, F, K, C, ldc, nullptr, nullptr, 0, F, nullptr};
+  dim3 grid((F + BN / 2 - 1) / (BN / 2), (M + BM - 1) / BM);
+  return launch<kSwiGLU>(ta, tb, p, grid, st);
+}
+
+cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
+                         int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
+                         int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
+                         cudaStream_t st) {
+  if (M <= 0 || N <= 0 || max_jobs <= 0) return cudaSuccess;
+  if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
+  if (!encoder()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  const int bbox = mode == kSwiGLU ? BN / 2 : BN;
+  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, b_rows, ldb, bbox))
+    return cudaErrorInvalidValue;
+  GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map};
+  const int nt = mode == kSwiGLU ? BN / 2 : BN;
+  dim3 grid((N + nt - 1) / nt, max_jobs);
+  if (mode == kSwiGLU) return launch<kSwiGLU>(ta, tb, p, grid, st);
+  if (mode == kBF16) return launch<kBF16>(ta, tb, p, grid, st);
+  return launch<kF32>(ta, tb, p, grid, st);
+}
+
+}  // namespace tc
+}  // namespace beam
+
+extern "C" beam_status beam_gemm_bf16(const beam_bf16* A, int M, int K, int lda,
+                                      const beam_bf16* B, int N, int ldb, void* C, int ldc,
+                                      int out_bf16, beam_stream_t stream) {
+  using namespace beam;
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || ldc < N || lda < K || ldb < K)
+    return BEAM_ERR_INVALID_ARG;
+  if (!tc::gemm_supported(A, lda, B, ldb, K)) return BEAM_ERR_INVALID_ARG;
+  const cudaError_t e = tc::gemm_bf16(A, M, K, lda, B, N, ldb, C, ldc, out_bf16 != 0,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA;
+}

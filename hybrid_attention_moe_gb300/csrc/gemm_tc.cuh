@@ -1,0 +1,36 @@
+// Tensor-core (tcgen05 + TMA) BF16 GEMM used by the prefill paths: C = A . B^T.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace beam {
+namespace tc {
+
+// A [M][K] (row stride lda), B [N][K] (row stride ldb), both bf16 and 16-byte aligned with
+// lda, ldb, K multiples of 8. C [M][N] (row stride ldc) is FP32, or BF16 if out_bf16.
+cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N, int ldb,
+                      void* C, int ldc, bool out_bf16, cudaStream_t st);
+
+bool gemm_supported(const void* A, int lda, const void* B, int ldb, int K);
+
+// Epilogue modes of the grouped GEMM.
+enum GemmMode { kF32 = 0, kBF16 = 1, kSwiGLU = 2 };
+
+// C[M][F] = bf16(silu(A . Bg^T) * (A . Bu^T)), B = [gate rows F; up rows F] x K.
+cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,
+                        int ldb, uint16_t* C, int ldc, cudaStream_t st);
+
+// Grouped GEMM over a device job list: job j = {g, a_row0, rows, -} multiplies A rows
+// [a_row0, a_row0 + rows) (at most 128) by the B rows of group g, which start at row
+// g * b_stride of B (a 2-D matrix of b_rows rows: all experts stacked). Output column count N
+// (units for kSwiGLU, whose up half starts up_off rows after the gate half). The output row
+// of A row r is row_map[r] if given. The grid covers max_jobs jobs; jobs at index >= *n_jobs
+// return at once.
+cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
+                         int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
+                         int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
+                         cudaStream_t st);
+
+}  // namespace tc
+}  // namespace beam

@@ -1,0 +1,347 @@
+// Routed SwiGLU experts with the weighted top-k combine, and the dense SwiGLU MLP.
+// Beam page, MoE section (256 experts of d_ff 2560, no shared expert; layers 0-2 dense SwiGLU
+// with d_ff 20480) and changes 3 and 7 of the optimisation list (the top-8 combine fused into
+// a neighbouring kernel; the dense activation in one kernel). The Flint page's small-batch MoE
+// kernels ("router and expert GEMV read only the selected experts") motivate reading only
+// the experts some token selected.
+//
+// beam_moe runs three kernels:
+//   plan      : one CTA buckets the T*k (token, slot) pairs by expert -> active expert list
+//   gate_up   : warp per (active expert, f): rows f (gate) and F+f (up) of that expert, dotted
+//               with every pair's token; a[pair][f] = bf16(silu(gate) * up)
+//   down      : warp per output row h: row h of every active expert's W_down dotted with its
+//               pairs' activations (FP32 y in shared memory), then out[t][h] =
+//               bf16(sum_j w[t][j] y[t*k+j]) in slot order -- the combine needs no extra pass.
+// Each weight byte of a selected expert is read from HBM once per call.
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "gemv.cuh"
+
+namespace beam {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPairTile = 4;        // pairs per weight pass in the gate_up / down warps
+constexpr int kFusedMaxPairs = 1024;  // down+combine in shared memory up to this many pairs
+
+constexpr int kMoeGemmMinT = 32;   // from here the experts run as grouped tensor-core GEMMs
+
+struct MoePlan {
+  int* n_active;   // [1]
+  int* active;     // [E] expert ids, increasing
+  int* act_off;    // [E+1] offsets into pairs
+  int* pairs;      // [P] pair ids t*k + j grouped by expert
+  int4* jobs;      // grouped GEMM only: {expert, first sorted row, rows <= 128, 0}
+  int* n_jobs;     // [1]
+};
+
+__global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* __restrict__ idx,
+                                                                int P, int E, MoePlan pl) {
+  extern __shared__ int sh[];
+  int* cnt = sh;            // [E]
+  int* off = sh + E;        // [E+1]
+  int* fill = sh + 2 * E + 1;  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; fill[e] = 0; }
+  __syncthreads();
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const int e = idx[i];
+    if (e < 0 || e >= E) { flag(BEAM_DEV_BAD_EXPERT); continue; }
+    atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, na = 0;
+    for (int e = 0; e < E; ++e) {
+      off[e] = o;
+      if (cnt[e] > 0) {
+        pl.active[na] = e;
+        pl.act_off[na] = o;
+        ++na;
+      }
+      o += cnt[e];
+    }
+    off[E] = o;
+    pl.act_off[na] = o;
+    *pl.n_active = na;
+    if (pl.jobs != nullptr) {
+      int nj = 0;
+      for (int a = 0; a < na; ++a) {
+        const int e = pl.active[a], o0 = pl.act_off[a], c = pl.act_off[a + 1] - o0;
+        for (int r = 0; r < c; r += 128) pl.jobs[nj++] = make_int4(e, o0 + r, min(128, c - r), 0);
+      }
+      *pl.n_jobs = nj;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const int e = idx[i];
+    if (e < 0 || e >= E) continue;
+    const int slot = atomicAdd(&fill[e], 1);
+    pl.pairs[off[e] + slot] = i;
+  }
+}
+
+// grid (ceil(F / (8 * FPW)), max active experts); warp handles FPW consecutive f units.
+template <int U>
+__global__ void __launch_bounds__(256) moe_gate_up_kernel(
+    const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
+    MoePlan pl, uint16_t* __restrict__ a) {
+  const int ai = blockIdx.y;
+  if (ai >= *pl.n_active) return;
+  const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (f >= F) return;
+  const int lane = threadIdx.x & 31;
+  const int e = pl.active[ai];
+  const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
+  const uint16_t* base = w_gu + size_t(e) * 2 * F * H;
+  const uint16_t* w[2] = {base + size_t(f) * H, base + size_t(F + f) * H};
+  for (int pp = p0; pp < p1; pp += kPairTile) {
+    const int nt = min(kPairTile, p1 - pp);
+    int pid[kPairTile];
+    const uint16_t* x[kPairTile];
+#pragma unroll
+    for (int i = 0; i < kPairTile; ++i) {
+      pid[i] = pl.pairs[pp + min(i, nt - 1)];
+      x[i] = u + size_t(pid[i] / k) * H;
+    }
+    float acc[2][kPairTile];
+    warp_dot<2, kPairTile, U>(w, x, nt, H, acc);
+#pragma unroll
+    for (int i = 0; i < kPairTile; ++i)
+      if (i < nt && lane == i) a[size_t(pid[i]) * F + f] = f2bf(siluf_(acc[0][i]) * acc[1][i]);
+  }
+}
+
+// Fused down projection + combine. grid ceil(H / 8); warp per output row h.
+// dynamic smem: 8 warps x P floats.
+template <int U>
+__global__ void __launch_bounds__(256) moe_down_combine_kernel(
+    const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn,
+    const float* __restrict__ topk_w, int T, int H, int F, int k, MoePlan pl,
+    uint16_t* __restrict__ out) {
+  extern __shared__ float ysh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + warp;
+  if (h >= H) return;
+  const int P = T * k;
+  float* y = ysh + size_t(warp) * P;
+  for (int i = lane; i < P; i += 32) y[i] = 0.f;
+  __syncwarp();
+  const int na = *pl.n_active;
+  for (int ai = 0; ai < na; ++ai) {
+    const int e = pl.active[ai];
+    const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
+    const uint16_t* w[1] = {w_dn + (size_t(e) * H + h) * F};
+    for (int pp = p0; pp < p1; pp += kPairTile) {
+      const int nt = min(kPairTile, p1 - pp);
+      int pid[kPairTile];
+      const uint16_t* x[kPairTile];
+#pragma unroll
+      for (int i = 0; i < kPairTile; ++i) {
+        pid[i] = pl.pairs[pp + min(i, nt - 1)];
+        x[i] = a + size_t(pid[i]) * F;
+      }
+      float acc[1][kPairTile];
+      warp_dot<1, kPairTile, U>(w, x, nt, F, acc);
+#pragma unroll
+      for (int i = 0; i < kPairTile; ++i)
+        if (i < nt && lane == i) y[pid[i]] = acc[0][i];
+    }
+  }
+  __syncwarp();
+  for (int t = lane; t < T; t += 32) {
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) s = fmaf(topk_w[size_t(t) * k + j], y[t * k + j], s);
+    out[size_t(t) * H + h] = f2bf(s);
+  }
+}
+
+// Unfused form for many pairs: y[pair][h] (FP32) to the workspace, then a combine pass.
+template <int U>
+__global__ void __launch_bounds__(256) moe_down_kernel(const uint16_t* __restrict__ a,
+                                                       const uint16_t* __restrict__ w_dn, int H,
+                                                       int F, MoePlan pl, float* __restrict__ y) {
+  const int ai = blockIdx.y;
+  if (ai >= *pl.n_active) return;
+  const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (h >= H) return;
+  const int lane = threadIdx.x & 31;
+  const int e = pl.active[ai];
+  const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
+  const uint16_t* w[1] = {w_dn + (size_t(e) * H + h) * F};
+  for (int pp = p0; pp < p1; pp += kPairTile) {
+    const int nt = min(kPairTile, p1 - pp);
+    int pid[kPairTile];
+    const uint16_t* x[kPairTile];
+#pragma unroll
+    for (int i = 0; i < kPairTile; ++i) {
+      pid[i] = pl.pairs[pp + min(i, nt - 1)];
+      x[i] = a + size_t(pid[i]) * F;
+    }
+    float acc[1][kPairTile];
+    warp_dot<1, kPairTile, U>(w, x, nt, F, acc);
+#pragma unroll
+    for (int i = 0; i < kPairTile; ++i)
+      if (i < nt && lane == i) y[size_t(pid[i]) * H + h] = acc[0][i];
+  }
+}
+
+__global__ void moe_combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
+                                   const int32_t* __restrict__ idx, int T, int H, int k, int E,
+                                   uint16_t* __restrict__ out) {
+  const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= size_t(T) * H) return;
+  const int t = int(i / H), h = int(i - size_t(t) * H);
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[size_t(t) * k + j];
+    if (e < 0 || e >= E) continue;
+    s = fmaf(topk_w[size_t(t) * k + j], y[(size_t(t) * k + j) * H + h], s);
+  }
+  out[i] = f2bf(s);
+}
+
+// Rows of u in expert-sorted pair order: us[i] = u[pairs[i] / k].
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ u, int H, int k, MoePlan pl,
+                                   int P, uint16_t* __restrict__ us) {
+  const int nv = H / 8;
+  const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= size_t(P) * nv) return;
+  const int r = int(i / nv), c = int(i - size_t(r) * nv);
+  const int tok = pl.pairs[r] / k;
+  reinterpret_cast<uint4*>(us + size_t(r) * H)[c] =
+      reinterpret_cast<const uint4*>(u + size_t(tok) * H)[c];
+}
+
+int max_jobs(int P, int E) { return (P + 127) / 128 + (P < E ? P : E); }
+
+MoePlan carve_plan(Carver& cv, int E, int P, bool grouped) {
+  MoePlan pl;
+  pl.n_active = cv.take<int>(1);
+  pl.active = cv.take<int>(E);
+  pl.act_off = cv.take<int>(E + 1);
+  pl.pairs = cv.take<int>(P);
+  pl.jobs = grouped ? cv.take<int4>(max_jobs(P, E)) : nullptr;
+  pl.n_jobs = grouped ? cv.take<int>(1) : nullptr;
+  return pl;
+}
+
+}  // namespace
+
+size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
+  const size_t P = size_t(T) * c->topk, E = c->n_experts;
+  size_t b = 256 + align_up(E * 4, 256) + align_up((E + 1) * 4, 256) + align_up(P * 4, 256);
+  b += align_up(P * c->d_ff_expert * 2, 256);
+  const bool grouped = T >= kMoeGemmMinT;
+  if (grouped) {
+    b += align_up(size_t(max_jobs(int(P), int(E))) * 16, 256) + 256;
+    b += align_up(P * c->hidden * 2, 256);                       // gathered inputs
+  }
+  if (grouped || P > size_t(kFusedMaxPairs)) b += align_up(P * c->hidden * 4, 256);
+  return b;
+}
+
+size_t dense_ws_bytes(const beam_layer_cfg* c, int T) {
+  return align_up(size_t(T) * c->d_ff_dense * 2, 256);
+}
+
+}  // namespace beam
+
+extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                const int32_t* topk_idx, const float* topk_w,
+                                const beam_bf16* w_gate_up, const beam_bf16* w_down, int T,
+                                beam_bf16* out, void* ws, size_t ws_bytes, beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !topk_idx || !topk_w || !w_gate_up || !w_down || !out)
+    return BEAM_ERR_INVALID_ARG;
+  const int H = cfg->hidden, F = cfg->d_ff_expert, E = cfg->n_experts, k = cfg->topk;
+  if (H <= 0 || (H & 7) || F <= 0 || (F & 7) || E <= 0 || k <= 0) return BEAM_ERR_INVALID_ARG;
+  if (E > 4096) return BEAM_ERR_UNSUPPORTED;
+  if (!aligned16(u) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(ws))
+    return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  const int P = T * k;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  const bool grouped = T >= kMoeGemmMinT && tc::gemm_supported(u, H, w_gate_up, H, H) &&
+                       tc::gemm_supported(u, F, w_down, F, F);
+  MoePlan pl = carve_plan(cv, E, P, grouped);
+  uint16_t* act = cv.take<uint16_t>(size_t(P) * F);
+  uint16_t* us = grouped ? cv.take<uint16_t>(size_t(P) * H) : nullptr;
+  float* y = (grouped || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  const int max_active = P < E ? P : E;
+  moe_plan_kernel<<<1, kPlanThreads, (3 * E + 1) * sizeof(int), st>>>(topk_idx, P, E, pl);
+  note_launches(1);
+  if (grouped) {
+    // gather -> grouped gate/up GEMM with the SwiGLU epilogue (sorted rows) -> grouped down
+    // GEMM writing each row back to its (token, slot) pair -> weighted combine
+    const size_t nv = size_t(P) * (H / 8);
+    gather_rows_kernel<<<unsigned((nv + 255) / 256), 256, 0, st>>>(u, H, k, pl, P, us);
+    note_launches(1);
+    const int mj = max_jobs(P, E);
+    if (tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, w_gate_up, E * 2 * F, 2 * F, H, pl.jobs,
+                         pl.n_jobs, mj, F, F, nullptr, act, F, st) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    if (tc::gemm_grouped(tc::kF32, act, P, F, F, w_down, E * H, H, F, pl.jobs, pl.n_jobs, mj, H,
+                         0, pl.pairs, y, H, st) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    const size_t n = size_t(T) * H;
+    moe_combine_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(y, topk_w, topk_idx, T, H, k,
+                                                                  E, out);
+    note_launches(1);
+    return launch_status();
+  }
+  moe_gate_up_kernel<4><<<dim3((F + 7) / 8, max_active), 256, 0, st>>>(u, w_gate_up, H, F, k, pl,
+                                                                      act);
+  note_launches(1);
+  if (P <= kFusedMaxPairs) {
+    const int smem = 8 * P * int(sizeof(float));
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(moe_down_combine_kernel<8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    moe_down_combine_kernel<8><<<(H + 7) / 8, 256, smem, st>>>(act, w_down, topk_w, T, H, F, k,
+                                                              pl, out);
+    note_launches(1);
+  } else {
+    moe_down_kernel<8><<<dim3((H + 7) / 8, max_active), 256, 0, st>>>(act, w_down, H, F, pl, y);
+    const size_t n = size_t(T) * H;
+    moe_combine_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(y, topk_w, topk_idx, T, H, k,
+                                                                  E, out);
+    note_launches(2);
+  }
+  return launch_status();
+}
+
+extern "C" beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                      const beam_bf16* w_gate_up, const beam_bf16* w_down, int T,
+                                      beam_bf16* out, void* ws, size_t ws_bytes,
+                                      beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !w_gate_up || !w_down || !out) return BEAM_ERR_INVALID_ARG;
+  const int H = cfg->hidden, Fd = cfg->d_ff_dense;
+  if (H <= 0 || (H & 7) || Fd <= 0 || (Fd & 7)) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out) ||
+      !aligned16(ws))
+    return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  uint16_t* act = cv.take<uint16_t>(size_t(T) * Fd);
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  const bool tcore = T >= kGemmMinT && tc::gemm_supported(u, H, w_gate_up, H, H) &&
+                     tc::gemm_supported(act, Fd, w_down, Fd, Fd);
+  if (tcore) {
+    if (tc::gemm_swiglu(u, T, H, H, w_gate_up, Fd, H, act, Fd, st) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    if (tc::gemm_bf16(act, T, Fd, Fd, w_down, H, Fd, out, H, true, st) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    return BEAM_OK;
+  }
+  if (launch_gemv<kOutSwiGLU>(w_gate_up, Fd, H, u, T, nullptr, act, Fd, st) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  if (launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st) != cudaSuccess)
+    return BEAM_ERR_CUDA;
+  return BEAM_OK;
+}

@@ -1,0 +1,164 @@
+// Packed QKV + gate projection, per-head Q/K RMSNorm, RoPE or SSMax, KV-cache write.
+// Beam page, Attention section (48 query / 8 KV heads of 128, Q and K RMS-normalised per head
+// before RoPE or SSMax (1 + p/2048)^0.1) and changes 2, 5 and 6 of the optimisation list
+// (one packed projection; norm, rotation and cache write in one kernel).
+#include <math.h>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "gemv.cuh"
+
+namespace beam {
+namespace {
+
+constexpr int kMaxHalf = 64;  // D/2 for D = 128
+
+// One CTA per token. z holds the projection (fp32) of the token: rows Q | K | V | gate.
+// Warps take (kind, head) slots: n_q query heads, n_kv key heads, n_kv value heads and n_q
+// gate heads. Lane l holds elements l, l+32, ... of the head (VPL = D/32 values), so the
+// RoPE partner i + D/2 of element l + 32j is element j + VPL/2 of the same lane.
+template <int VPL>
+__global__ void __launch_bounds__(256) qkv_epilogue_kernel(
+    const float* __restrict__ z, int rows, const uint16_t* __restrict__ qnw,
+    const uint16_t* __restrict__ knw, const int32_t* __restrict__ seq_id,
+    const int32_t* __restrict__ pos, int n_q, int n_kv, int nope, float theta, float ss_base,
+    float ss_exp, float eps, uint16_t* __restrict__ q_out, uint16_t* __restrict__ g_out,
+    beam_kv_cache kc) {
+  constexpr int D = VPL * 32;
+  constexpr int HALF = D / 2;
+  __shared__ float cs[kMaxHalf], sn[kMaxHalf];
+  __shared__ float s_ssmax;
+  const int t = blockIdx.x;
+  const int p = pos[t];
+  const int s = seq_id[t];
+  bool ok_kv = true;
+  if (p < 1) { if (threadIdx.x == 0) flag(BEAM_DEV_BAD_POSITION); ok_kv = false; }
+  if (s < 0 || s >= kc.num_seqs) { if (threadIdx.x == 0) flag(BEAM_DEV_BAD_SEQ); ok_kv = false; }
+  if (kc.window == 0 && p > kc.capacity) {
+    if (threadIdx.x == 0) flag(BEAM_DEV_BAD_POSITION);
+    ok_kv = false;
+  }
+  if (!nope) {
+    // angle (p-1) * theta^(-2i/D), formed and reduced modulo 2*pi in double precision so
+    // that positions around 1e5 keep full single-precision accuracy in cos/sin
+    for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+      const double inv = exp2(-(2.0 * i / D) * log2((double)theta));
+      double ang = double(p - 1) * inv;
+      const double two_pi = 6.283185307179586476925;
+      ang -= two_pi * rint(ang / two_pi);
+      float sv, cv;
+      sincosf(float(ang), &sv, &cv);
+      cs[i] = cv;
+      sn[i] = sv;
+    }
+  } else if (threadIdx.x == 0) {
+    s_ssmax = float(pow(1.0 + double(p) / double(ss_base), double(ss_exp)));
+  }
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int nslots = 2 * n_q + 2 * n_kv;
+  const float* zt = z + size_t(t) * rows;
+  for (int slot = threadIdx.x >> 5; slot < nslots; slot += blockDim.x >> 5) {
+    int kind, head, row0;
+    if (slot < n_q) { kind = 0; head = slot; row0 = head * D; }
+    else if (slot < n_q + n_kv) { kind = 1; head = slot - n_q; row0 = (n_q + head) * D; }
+    else if (slot < n_q + 2 * n_kv) { kind = 2; head = slot - n_q - n_kv; row0 = (n_q + n_kv + head) * D; }
+    else { kind = 3; head = slot - n_q - 2 * n_kv; row0 = (n_q + 2 * n_kv + head) * D; }
+    float v[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) v[j] = round_bf(zt[row0 + lane + 32 * j]);  // projection out
+    if (kind == 3) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) g_out[size_t(t) * n_q * D + head * D + lane + 32 * j] = f2bf(v[j]);
+      continue;
+    }
+    if (kind <= 1) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) ss = fmaf(v[j], v[j], ss);
+      const float r = rsqrtf(warp_sum(ss) / float(D) + eps);
+      const uint16_t* gw = kind == 0 ? qnw : knw;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) v[j] = v[j] * r * bf2f(gw[lane + 32 * j]);
+      if (!nope) {
+#pragma unroll
+        for (int j = 0; j < VPL / 2; ++j) {
+          const int i = lane + 32 * j;  // < HALF
+          const float a = v[j], b = v[j + VPL / 2];
+          v[j] = a * cs[i] - b * sn[i];
+          v[j + VPL / 2] = b * cs[i] + a * sn[i];
+        }
+      } else if (kind == 0) {
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) v[j] *= s_ssmax;
+      }
+    }
+    if (kind == 0) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) q_out[(size_t(t) * n_q + head) * D + lane + 32 * j] = f2bf(v[j]);
+      continue;
+    }
+    if (!ok_kv) continue;
+    const int slotk = (p - 1) % kc.capacity;
+    const size_t base = ((size_t(s) * n_kv + head) * kc.capacity + slotk) * D;
+    if (kc.dtype == BEAM_KV_BF16) {
+      uint16_t* dst = static_cast<uint16_t*>(kind == 1 ? kc.k : kc.v) + base;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) dst[lane + 32 * j] = f2bf(v[j]);
+    } else {
+      uint8_t* dst = static_cast<uint8_t*>(kind == 1 ? kc.k : kc.v) + base;
+      const float sc = kind == 1 ? kc.k_scale : kc.v_scale;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j)
+        dst[lane + 32 * j] = __nv_cvt_float_to_fp8(__fdiv_rn(v[j], sc), __NV_SATFINITE, __NV_E4M3);
+    }
+  }
+}
+
+}  // namespace
+
+size_t qkv_ws_bytes(const beam_layer_cfg* c, int T) {
+  const size_t rows = size_t(2 * c->n_q + 2 * c->n_kv) * c->head_dim;
+  return align_up(size_t(T) * rows * sizeof(float), 256);
+}
+
+}  // namespace beam
+
+extern "C" beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                     const beam_bf16* w_qkvg, const beam_bf16* q_norm_w,
+                                     const beam_bf16* k_norm_w, const int32_t* seq_id,
+                                     const int32_t* pos, int T, beam_bf16* q_out,
+                                     beam_bf16* g_out, const beam_kv_cache* cache, void* ws,
+                                     size_t ws_bytes, beam_stream_t stream) {
+  using namespace beam;
+  beam_status st = check_cfg_attn(cfg);
+  if (st != BEAM_OK) return st;
+  if ((st = check_cache(cache, cfg)) != BEAM_OK) return st;
+  if (T < 0 || !u || !w_qkvg || !q_norm_w || !k_norm_w || !seq_id || !pos || !q_out || !g_out)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_qkvg) || !aligned16(ws)) return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  const int D = cfg->head_dim, H = cfg->hidden;
+  const int rows = (2 * cfg->n_q + 2 * cfg->n_kv) * D;
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  float* z = cv.take<float>(size_t(T) * rows);
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t ge =
+      T >= kGemmMinT && tc::gemm_supported(u, H, w_qkvg, H, H)
+          ? tc::gemm_bf16(u, T, H, H, w_qkvg, rows, H, z, rows, false, s)
+          : launch_gemv<kOutF32>(w_qkvg, rows, H, u, T, z, nullptr, rows, s);
+  if (ge != cudaSuccess) return BEAM_ERR_CUDA;
+  const int nope = cfg->kind == BEAM_ATTN_NOPE_SSMAX;
+  if (D == 128)
+    qkv_epilogue_kernel<4><<<T, 256, 0, s>>>(z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
+                                             cfg->n_kv, nope, cfg->rope_theta, cfg->ssmax_base,
+                                             cfg->ssmax_exp, cfg->eps, q_out, g_out, *cache);
+  else
+    qkv_epilogue_kernel<2><<<T, 256, 0, s>>>(z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
+                                             cfg->n_kv, nope, cfg->rope_theta, cfg->ssmax_base,
+                                             cfg->ssmax_exp, cfg->eps, q_out, g_out, *cache);
+  note_launches(1);
+  return launch_status();
+}

@@ -1,0 +1,220 @@
+// FP32 router, DeepSeek-V3 style group-limited top-k.
+// Beam page, MoE section (sigmoid scores plus a correction bias pick the best 4 of 8 expert
+// groups, then the top-8 experts; the renormalised weights are scaled by 2.5; the 5120 x 256
+// router weights, accumulation and logits are FP32) and change 4 of the optimisation list
+// (a dedicated small-batch FP32 router kernel).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace beam {
+namespace {
+
+constexpr int kRouteMaxT = 8;  // tokens per CTA pass in the GEMV form
+
+// Small T: one CTA per expert row; its warps split the hidden axis; every token of a pass
+// reuses the row held in registers/L1.
+__global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __restrict__ u,
+                                                          const float* __restrict__ wr, int T,
+                                                          int H, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ float red[8][kRouteMaxT];
+  const int e = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* row = wr + size_t(e) * H;
+  for (int t0 = 0; t0 < T; t0 += kRouteMaxT) {
+    const int nt = min(kRouteMaxT, T - t0);
+    float acc[kRouteMaxT];
+#pragma unroll
+    for (int t = 0; t < kRouteMaxT; ++t) acc[t] = 0.f;
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
+      const float4 w0 = ld_stream_f4(row + i * 8);
+      const float4 w1 = ld_stream_f4(row + i * 8 + 4);
+#pragma unroll
+      for (int t = 0; t < kRouteMaxT; ++t) {
+        if (t < nt) {
+          float x[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(u + size_t(t0 + t) * H + i * 8)), x);
+          acc[t] = fmaf(w0.x, x[0], acc[t]); acc[t] = fmaf(w0.y, x[1], acc[t]);
+          acc[t] = fmaf(w0.z, x[2], acc[t]); acc[t] = fmaf(w0.w, x[3], acc[t]);
+          acc[t] = fmaf(w1.x, x[4], acc[t]); acc[t] = fmaf(w1.y, x[5], acc[t]);
+          acc[t] = fmaf(w1.z, x[6], acc[t]); acc[t] = fmaf(w1.w, x[7], acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouteMaxT; ++t) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) red[warp][t] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < nt) {
+      float s = 0.f;
+      for (int w = 0; w < int(blockDim.x >> 5); ++w) s += red[w][threadIdx.x];
+      logits[size_t(t0 + threadIdx.x) * E + e] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// Large T: 64 x 64 output tiles, FP32 SIMT, bf16 activations widened on the fly.
+constexpr int kTM = 64, kTN = 64, kTK = 32;
+__global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __restrict__ u,
+                                                          const float* __restrict__ wr, int T,
+                                                          int H, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ float As[kTK][kTM + 4];
+  __shared__ float Bs[kTK][kTN + 4];
+  const int tm = blockIdx.y * kTM, tn = blockIdx.x * kTN;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += kTK) {
+    for (int i = threadIdx.x; i < kTM * kTK; i += 256) {
+      const int r = i / kTK, k = i - r * kTK;
+      const int t = tm + r;
+      As[k][r] = (t < T && k0 + k < H) ? bf2f(u[size_t(t) * H + k0 + k]) : 0.f;
+      const int e = tn + r;
+      Bs[k][r] = (e < E && k0 + k < H) ? wr[size_t(e) * H + k0 + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < kTK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[k][ty * 4 + i]; b[i] = Bs[k][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = tm + ty * 4 + i, e = tn + tx * 4 + j;
+      if (t < T && e < E) logits[size_t(t) * E + e] = acc[i][j];
+    }
+}
+
+// Warp-wide argmax of (value, index), ties to the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    if (v2 > v || (v2 == v && i2 < i)) { v = v2; i = i2; }
+  }
+}
+
+constexpr int kMaxE = 1024, kMaxG = 32, kMaxK = 32;
+
+// One warp per token. s = sigmoid(logit), b = s + bias (FP32); group score = top-2 sum of b.
+__global__ void __launch_bounds__(128) router_topk_kernel(
+    const float* __restrict__ logits, const float* __restrict__ corr_bias, int T, int E, int G,
+    int kG, int k, float scale, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  __shared__ float sb[4][kMaxE];
+  __shared__ float ss[4][kMaxE];
+  __shared__ float sg[4][kMaxG];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + warp;
+  if (t >= T) return;
+  float* b = sb[warp];
+  float* s = ss[warp];
+  for (int e = lane; e < E; e += 32) {
+    const float z = logits[size_t(t) * E + e];
+    const float sv = 1.0f / (1.0f + expf(-z));
+    s[e] = sv;
+    b[e] = sv + corr_bias[e];
+  }
+  __syncwarp();
+  const int per = E / G;
+  if (lane < G) {
+    float m1 = -INFINITY, m2 = -INFINITY;
+    for (int j = 0; j < per; ++j) {
+      const float v = b[lane * per + j];
+      if (v > m1) { m2 = m1; m1 = v; } else if (v > m2) { m2 = v; }
+    }
+    sg[warp][lane] = m1 + m2;
+  }
+  __syncwarp();
+  // keep the kG best groups
+  unsigned keep = 0u;
+  for (int r = 0; r < kG; ++r) {
+    float v = (lane < G && !((keep >> lane) & 1u)) ? sg[warp][lane] : -INFINITY;
+    int i = lane < G ? lane : 0x7fffffff;
+    warp_argmax(v, i);
+    keep |= 1u << i;
+  }
+  // top-k experts of the kept groups, by b, ties to the lower index
+  float ssum = 0.f;
+  int sel_i[kMaxK];
+  float sel_s[kMaxK];
+  for (int r = 0; r < k; ++r) {
+    float v = -INFINITY;
+    int i = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      if (!((keep >> (e / per)) & 1u)) continue;
+      const float be = b[e];
+      if (be > v || (be == v && e < i)) { v = be; i = e; }
+    }
+    warp_argmax(v, i);
+    sel_i[r] = i;
+    sel_s[r] = s[i];
+    ssum += s[i];
+    __syncwarp();
+    if (lane == 0) b[i] = -INFINITY;  // taken
+    __syncwarp();
+  }
+  if (lane == 0) {
+    for (int r = 0; r < k; ++r) {
+      topk_idx[size_t(t) * k + r] = sel_i[r];
+      topk_w[size_t(t) * k + r] = sel_s[r] / ssum * scale;
+    }
+  }
+}
+
+}  // namespace
+
+size_t route_ws_bytes(const beam_layer_cfg* c, int T) {
+  return align_up(size_t(T) * c->n_experts * sizeof(float), 256);
+}
+
+}  // namespace beam
+
+extern "C" beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                  const float* w_router, const float* corr_bias, int T,
+                                  float* logits, int32_t* topk_idx, float* topk_w, void* ws,
+                                  size_t ws_bytes, beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !w_router || !corr_bias || !topk_idx || !topk_w)
+    return BEAM_ERR_INVALID_ARG;
+  const int E = cfg->n_experts, G = cfg->n_groups, H = cfg->hidden;
+  if (H <= 0 || (H & 7) || E <= 0 || G <= 0 || E % G != 0 || cfg->topk_groups < 1 ||
+      cfg->topk_groups > G || cfg->topk < 1 || cfg->topk > cfg->topk_groups * (E / G) ||
+      E / G < 2)
+    return BEAM_ERR_INVALID_ARG;
+  if (E > kMaxE || G > kMaxG || cfg->topk > kMaxK) return BEAM_ERR_UNSUPPORTED;
+  if (!aligned16(u) || !aligned16(w_router) || !aligned16_or_null(logits) || !aligned16(ws))
+    return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* lg = logits;
+  if (lg == nullptr) {
+    Carver cv{static_cast<char*>(ws), ws_bytes};
+    lg = cv.take<float>(size_t(T) * E);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  }
+  if (T <= 32)
+    router_gemv_kernel<<<E, 256, 0, st>>>(u, w_router, T, H, E, lg);
+  else
+    router_gemm_kernel<<<dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), 256, 0, st>>>(
+        u, w_router, T, H, E, lg);
+  note_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+  router_topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
+                                                  cfg->topk, cfg->route_scale, topk_idx, topk_w);
+  note_launches(1);
+  return launch_status();
+}

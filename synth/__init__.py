@@ -5,5 +5,6 @@ arithmetic, so that both sides of every parity test can be fed from it.
 """
 from .beam_inputs import (  # noqa: F401
     BeamShape, TINY, BEAM, derived_seed, normal, layer_weights, expert_weights,
+    attention_weights, router_weights, dense_weights,
     activations, kv_cache, decode_positions, prefill_positions,
 )

@@ -104,13 +104,10 @@ def expert_weights(shape: BeamShape, layer: int, seed: int, device="cpu", expert
     return w_gu, w_dn
 
 
-def layer_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu",
-                  dense: bool | None = None, with_experts: bool = True):
-    """All weights of one layer as a dict of tensors (row-major [out][in])."""
+def attention_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
+    """Norm gains and the attention sublayer's weights of one layer."""
     H, D = shape.hidden, shape.head_dim
-    if dense is None:
-        dense = layer in shape.dense_layers
-    w = {
+    return {
         "attn_pre": normal((H,), 0.1, 1.0, seed, (layer, "attn_pre"), device),
         "attn_post": normal((H,), 0.1, 1.0, seed, (layer, "attn_post"), device),
         "mlp_pre": normal((H,), 0.1, 1.0, seed, (layer, "mlp_pre"), device),
@@ -121,15 +118,34 @@ def layer_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu",
         "gate_bias": normal((shape.n_q,), 1.0, 0.0, seed, (layer, "gate_bias"), device),
         "w_o": normal((H, shape.q_rows), 0.02, 0.0, seed, (layer, "w_o"), device),
     }
+
+
+def router_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
+    E, H = shape.n_experts, shape.hidden
+    return {
+        "router": normal((E, H), 0.02, 0.0, seed, (layer, "router"), device, torch.float32),
+        "corr_bias": normal((E,), 0.01, 0.0, seed, (layer, "corr_bias"), device, torch.float32),
+    }
+
+
+def dense_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
+    H, Fd = shape.hidden, shape.d_ff_dense
+    return {
+        "w_gate_up": normal((2 * Fd, H), 0.02, 0.0, seed, (layer, "dense_gate_up"), device),
+        "w_down": normal((H, Fd), 0.02, 0.0, seed, (layer, "dense_down"), device),
+    }
+
+
+def layer_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu",
+                  dense: bool | None = None, with_experts: bool = True):
+    """All weights of one layer as a dict of tensors (row-major [out][in])."""
+    if dense is None:
+        dense = layer in shape.dense_layers
+    w = attention_weights(shape, layer, seed, device)
     if dense:
-        Fd = shape.d_ff_dense
-        w["w_gate_up"] = normal((2 * Fd, H), 0.02, 0.0, seed, (layer, "dense_gate_up"), device)
-        w["w_down"] = normal((H, Fd), 0.02, 0.0, seed, (layer, "dense_down"), device)
+        w.update(dense_weights(shape, layer, seed, device))
     else:
-        E = shape.n_experts
-        w["router"] = normal((E, H), 0.02, 0.0, seed, (layer, "router"), device, torch.float32)
-        w["corr_bias"] = normal((E,), 0.01, 0.0, seed, (layer, "corr_bias"), device,
-                                torch.float32)
+        w.update(router_weights(shape, layer, seed, device))
         if with_experts:
             w["w_gate_up"], w["w_down"] = expert_weights(shape, layer, seed, device)
     return w

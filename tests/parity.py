@@ -1,0 +1,81 @@
+"""Shared helpers of the parity tests: tolerance metrics and torch <-> oracle conversions.
+
+Tolerances (stated for the layer): bf16 outputs within 2e-2 max-abs-relative and 1e-3
+mean-relative of the oracle; outputs that read an FP8-e4m3 KV cache within 5e-2
+max-abs-relative (mean-relative 2e-3, derived: the two sides quantise with the same rule and
+differ only where an FP32 rounding difference flips an e4m3 code); router logits within 1e-5
+relative, with the row's RMS as the floor of the denominator; selected expert indices
+bit-exact (as sets; the order is by score).
+"""
+import numpy as np
+import torch
+
+import oracle as O
+
+BF16_MAX_REL, BF16_MEAN_REL = 2e-2, 1e-3
+FP8_MAX_REL, FP8_MEAN_REL = 5e-2, 2e-3
+LOGIT_REL = 1e-5
+
+
+def np64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def max_abs_rel(a, r):
+    a, r = np.asarray(a, np.float64), np.asarray(r, np.float64)
+    return float(np.max(np.abs(a - r)) / max(np.max(np.abs(r)), 1e-30))
+
+
+def mean_rel(a, r):
+    a, r = np.asarray(a, np.float64), np.asarray(r, np.float64)
+    return float(np.mean(np.abs(a - r)) / max(np.mean(np.abs(r)), 1e-30))
+
+
+def assert_close(a, r, what, fp8=False):
+    mx, mn = max_abs_rel(a, r), mean_rel(a, r)
+    lim_mx, lim_mn = (FP8_MAX_REL, FP8_MEAN_REL) if fp8 else (BF16_MAX_REL, BF16_MEAN_REL)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite output"
+    assert mx <= lim_mx and mn <= lim_mn, \
+        f"{what}: max-abs-rel {mx:.3e} (<= {lim_mx}), mean-rel {mn:.3e} (<= {lim_mn})"
+    return mx, mn
+
+
+def assert_logits_close(a, r, what="router logits"):
+    a, r = np.asarray(a, np.float64), np.asarray(r, np.float64)
+    rms = np.sqrt(np.mean(r * r, axis=-1, keepdims=True))
+    den = np.maximum(np.abs(r), rms)
+    worst = float(np.max(np.abs(a - r) / den))
+    assert worst <= LOGIT_REL, f"{what}: relative error {worst:.3e} > {LOGIT_REL}"
+    return worst
+
+
+def oracle_cache(kc):
+    """Oracle copy of a binding KVCache (values for bf16, codes for fp8)."""
+    if kc.fp8:
+        k, v = kc.k.cpu().numpy(), kc.v.cpu().numpy()
+        return O.KVCache(k, v, "fp8", kc.k_scale, kc.v_scale, window=kc.window)
+    # bf16 values are exact in float32, which halves the host copy of a long cache
+    return O.KVCache(kc.k.float().cpu().numpy(), kc.v.float().cpu().numpy(), "bf16",
+                     window=kc.window)
+
+
+def route_margins(cfg, u, w_router, corr_bias):
+    """Smallest gap, over tokens, between the kept/dropped group scores and between the k-th
+    and (k+1)-th expert scores inside the kept groups (oracle FP32 scores)."""
+    _, _, b = O.route_scores(cfg, u, w_router, corr_bias)
+    per = cfg.n_experts // cfg.n_groups
+    gmin = emin = np.inf
+    for t in range(b.shape[0]):
+        bt = b[t].astype(np.float64)
+        gsc = np.sort(bt.reshape(cfg.n_groups, per), axis=1)[:, -2:].sum(axis=1)
+        order = np.lexsort((np.arange(cfg.n_groups), -gsc))
+        gs = gsc[order]
+        gmin = min(gmin, gs[cfg.topk_groups - 1] - gs[cfg.topk_groups])
+        keep = order[: cfg.topk_groups]
+        cand = np.sort(np.concatenate([bt[g * per:(g + 1) * per] for g in keep]))[::-1]
+        emin = min(emin, cand[cfg.topk - 1] - cand[cfg.topk])
+    return gmin, emin
+
+
+def device_tensor(x, device="cuda"):
+    return x.to(device) if isinstance(x, torch.Tensor) else torch.as_tensor(x, device=device)

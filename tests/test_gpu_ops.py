@@ -1,0 +1,306 @@
+"""GPU parity, one C-ABI entry point at a time, against the oracle on the same seeded inputs.
+
+Sizes: the tiny Beam-shaped widths (several tiles and ragged tails at small cost) and the
+full Beam widths (hidden 5120, 48/8 heads of 128, 256 experts) at decode and prefill token
+counts. Both sides get the same tensors; nothing the kernels produce is fed to the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from synth import BEAM, TINY
+from hybrid_attention_moe_gb300 import beam as B
+from parity import (assert_close, assert_logits_close, np64, oracle_cache, route_margins)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def ws_for(cfg, T, max_pos=1):
+    return torch.empty(B.workspace_bytes(cfg, T, max_pos), dtype=torch.uint8, device=DEV)
+
+
+def cfg_of(shape, nope=False):
+    return B.LayerCfg.from_shape(shape, B.BEAM_ATTN_NOPE_SSMAX if nope else B.BEAM_ATTN_SWA_ROPE)
+
+
+def check_status():
+    bits = B.beam_get_device_status()
+    assert bits == 0, f"device status bits {bits:#x}"
+
+
+# ------------------------------------------------------------------ boundary norm ----
+
+@pytest.mark.parametrize("H,T", [(256, 1), (256, 37), (5120, 1), (5120, 8), (5120, 130)])
+@pytest.mark.parametrize("n", [1, 2, 9, 104])
+def test_boundary_norm(H, T, n):
+    seed = 100 + n
+    h = synth.activations(T, H, seed, "h")
+    x = None if n == 1 else synth.activations(T, H, seed, "x")
+    wpost = synth.normal((H,), 0.1, 1.0, seed, ("wpost",))
+    wpre = synth.normal((H,), 0.1, 1.0, seed, ("wpre",))
+    hd, ud = h.to(DEV), torch.empty_like(h, device=DEV)
+    B.beam_boundary_norm(None if x is None else x.to(DEV), hd, ud,
+                         None if x is None else wpost.to(DEV), wpre.to(DEV), n, 1e-6)
+    h_ref, u_ref = O.boundary_norm(None if x is None else np64(x), np64(h), np64(wpost),
+                                   np64(wpre), n, 1e-6)
+    assert_close(np64(hd), h_ref, "h")
+    assert_close(np64(ud), u_ref, "u")
+    # last boundary: no next pre-norm
+    if x is not None:
+        hd2 = h.to(DEV)
+        B.beam_boundary_norm(x.to(DEV), hd2, None, wpost.to(DEV), None, n, 1e-6)
+        assert torch.equal(hd2, hd)
+
+
+# ------------------------------------------------------------------ qkv + gate ----
+
+def _qkv_inputs(shape, T, seed, positions, seqs, fp8, nope, scale=(1.0, 1.0)):
+    W = synth.attention_weights(shape, 0, seed, device=DEV)
+    u = synth.activations(T, shape.hidden, seed, "u", device=DEV)
+    n_seqs = max(seqs) + 1
+    if nope:
+        cap = max(positions) + 8
+        window = 0
+    else:
+        cap = shape.window + T + 3
+        window = shape.window
+    c = synth.kv_cache(shape, n_seqs, cap, seed, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
+                       device=DEV)
+    kc = B.KVCache(c["k"], c["v"], window, scale[0], scale[1])
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    return W, u, kc, seq, pos
+
+
+QKV_CASES = [
+    # shape, T, positions, seqs
+    (TINY, 1, [1], [0]),
+    (TINY, 5, [3, 4, 5, 6, 7], [0, 0, 0, 0, 0]),
+    (TINY, 40, list(range(90, 130)), [0] * 40),
+    (BEAM, 1, [4097], [0]),
+    (BEAM, 8, [100_001 + 977 * i for i in range(8)], list(range(8))),
+    (BEAM, 48, list(range(2001, 2025)) + list(range(99_990, 100_014)), [0] * 24 + [1] * 24),
+    (BEAM, 130, list(range(50_001, 50_131)), [0] * 130),          # tensor-core projection
+]
+
+
+@pytest.mark.parametrize("case", range(len(QKV_CASES)))
+@pytest.mark.parametrize("nope", [False, True])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_qkv_gate(case, nope, fp8):
+    shape, T, positions, seqs = QKV_CASES[case]
+    if nope:   # keep the whole-context cache small; RoPE keeps the large positions
+        positions = [1 + p % 6000 for p in positions]
+    scale = (0.0371, 0.5) if fp8 else (1.0, 1.0)
+    W, u, kc, seq, pos = _qkv_inputs(shape, T, 7 + case, positions, seqs, fp8, nope, scale)
+    cfg = cfg_of(shape, nope)
+    oc = oracle_cache(kc)
+    q = torch.empty((T, shape.n_q, shape.head_dim), dtype=torch.bfloat16, device=DEV)
+    g = torch.empty((T, shape.q_rows), dtype=torch.bfloat16, device=DEV)
+    B.beam_qkv_gate(cfg, u, W["w_qkvg"], W["q_norm"], W["k_norm"], seq, pos, q, g, kc,
+                    ws_for(cfg, T))
+    check_status()
+    q_ref, g_ref = O.qkv_gate(shape, np64(u), np64(W["w_qkvg"]), np64(W["q_norm"]),
+                              np64(W["k_norm"]), seqs, positions, oc, nope)
+    assert_close(np64(q), q_ref, "q'")
+    assert_close(np64(g), g_ref, "g")
+    oc_gpu = oracle_cache(kc)
+    for s, p in zip(seqs, positions):
+        kg, vg = oc_gpu.load(s, np.array([p]))
+        kr, vr = oc.load(s, np.array([p]))
+        assert_close(kg, kr, "cached k", fp8=fp8)
+        assert_close(vg, vr, "cached v", fp8=fp8)
+
+
+# ------------------------------------------------------------------ attention ----
+
+ATTN_CASES = [
+    # shape, contexts (cached keys per sequence before the call), tokens per sequence
+    (TINY, [0], 1),
+    (TINY, [5, 40, 16, 3], 1),
+    (TINY, [10], 64),            # prefill kernel, window boundary crossed mid-chunk
+    (TINY, [30, 0], 40),         # two sequences in one prefill call
+    (BEAM, [4096], 1),
+    (BEAM, [300, 5000, 777, 12_345], 1),
+    (BEAM, [2500], 48),
+    (BEAM, [100, 700], 33),      # ragged prefill tile, two sequences
+    (BEAM, [1000], 96),          # prefill kernel + tensor-core o_proj
+]
+
+
+@pytest.mark.parametrize("case", range(len(ATTN_CASES)))
+@pytest.mark.parametrize("nope", [False, True])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_attn(case, nope, fp8):
+    shape, ctxs, per = ATTN_CASES[case]
+    seed = 31 + case
+    S = len(ctxs)
+    T = S * per
+    seqs = [s for s in range(S) for _ in range(per)]
+    positions = [ctxs[s] + 1 + i for s in range(S) for i in range(per)]
+    max_pos = max(positions)
+    if nope:
+        cap, window = max_pos + 5, 0
+    else:
+        cap, window = shape.window + per + 2, shape.window
+    scale = (0.0371, 0.5) if fp8 else (1.0, 1.0)
+    c = synth.kv_cache(shape, S, cap, seed, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
+                       device=DEV)
+    kc = B.KVCache(c["k"], c["v"], window, *scale)
+    q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, seed, ("q",), DEV)
+    g = synth.activations(T, shape.q_rows, seed, "g", DEV)
+    W = synth.attention_weights(shape, 0, seed, device=DEV)
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    cfg = cfg_of(shape, nope)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
+                ws_for(cfg, T, max_pos))
+    check_status()
+    ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
+                      positions, np64(W["w_o"]))
+    assert_close(np64(out), ref, "attn out", fp8=fp8)
+
+
+# ------------------------------------------------------------------ router ----
+
+@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 77), (BEAM, 1), (BEAM, 8), (BEAM, 300)])
+def test_route(shape, T):
+    cfg = cfg_of(shape)
+    for attempt in range(20):
+        seed = 1000 * attempt + T
+        u = synth.activations(T, shape.hidden, seed, "u")
+        R = synth.router_weights(shape, 0, seed)
+        gmin, emin = route_margins(shape, np64(u), np64(R["router"]), np64(R["corr_bias"]))
+        if min(gmin, emin) >= 1e-6:
+            break
+    else:
+        pytest.fail("no tie-free draw")
+    logits = torch.empty((T, shape.n_experts), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, shape.topk), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, shape.topk), dtype=torch.float32, device=DEV)
+    B.beam_route(cfg, u.to(DEV), R["router"].to(DEV), R["corr_bias"].to(DEV), logits, idx, w,
+                 ws_for(cfg, T))
+    lg_ref, idx_ref, w_ref = O.route(shape, np64(u), np64(R["router"]), np64(R["corr_bias"]))
+    assert_logits_close(logits.cpu().double().numpy(), lg_ref)
+    gi, gw = idx.cpu().numpy(), w.cpu().double().numpy()
+    for t in range(T):
+        assert sorted(gi[t].tolist()) == sorted(idx_ref[t].tolist()), f"token {t}"
+        assert gi[t].tolist() == idx_ref[t].tolist()     # gaps >= 1e-6 fix the order too
+    assert np.max(np.abs(gw - w_ref) / np.abs(w_ref)) < 1e-5
+    # no logits buffer: selection identical
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(w)
+    B.beam_route(cfg, u.to(DEV), R["router"].to(DEV), R["corr_bias"].to(DEV), None, idx2, w2,
+                 ws_for(cfg, T))
+    assert torch.equal(idx2, idx) and torch.equal(w2, w)
+
+
+# ------------------------------------------------------------------ experts ----
+
+def _random_routing(shape, T, seed, n_used=None):
+    rng = np.random.default_rng(seed)
+    pool = np.arange(shape.n_experts) if n_used is None else \
+        rng.choice(shape.n_experts, n_used, replace=False)
+    idx = np.stack([rng.choice(pool, shape.topk, replace=False) for _ in range(T)])
+    w = rng.uniform(0.05, 0.6, size=(T, shape.topk)).astype(np.float32)
+    return idx.astype(np.int32), w
+
+
+@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 9, None), (TINY, 31, None),
+                                            (TINY, 32, None), (TINY, 300, None), (BEAM, 1, None),
+                                            (BEAM, 4, None), (BEAM, 40, 12), (BEAM, 200, 10)])
+def test_moe(shape, T, n_used):
+    """GEMV form below 32 tokens (fused down+combine up to 1024 pairs), grouped tensor-core
+    GEMMs from 32 tokens (n_used limits the distinct experts so several 128-row tiles and
+    ragged tails occur per expert)."""
+    seed = 55 + T
+    cfg = cfg_of(shape)
+    idx, w = _random_routing(shape, T, seed, n_used)
+    if shape is TINY:
+        wgu, wdn = synth.expert_weights(shape, 0, seed, device=DEV)
+    else:   # only the experts used, placed at their indices of a full-size tensor
+        E, F, H = shape.n_experts, shape.d_ff_expert, shape.hidden
+        wgu = torch.zeros((E, 2 * F, H), dtype=torch.bfloat16, device=DEV)
+        wdn = torch.zeros((E, H, F), dtype=torch.bfloat16, device=DEV)
+        used = sorted(set(idx.ravel().tolist()))
+        gu, dn = synth.expert_weights(shape, 0, seed, device=DEV, experts=used)
+        for i, e in enumerate(used):
+            wgu[e], wdn[e] = gu[i], dn[i]
+    u = synth.activations(T, shape.hidden, seed, "u", DEV)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_moe(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), wgu, wdn,
+               out, ws_for(cfg, T))
+    check_status()
+    used = sorted(set(idx.ravel().tolist()))
+    ogu = {e: np64(wgu[e]) for e in used}
+    odn = {e: np64(wdn[e]) for e in used}
+    ref = O.moe(shape, np64(u), idx, w.astype(np.float64), ogu, odn)
+    assert_close(np64(out), ref, "moe out")
+
+
+@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 13), (TINY, 64), (TINY, 200), (BEAM, 1),
+                                     (BEAM, 8), (BEAM, 40), (BEAM, 130)])
+def test_dense_mlp(shape, T):
+    seed = 77 + T
+    cfg = cfg_of(shape)
+    Wd = synth.dense_weights(shape, 0, seed, device=DEV)
+    u = synth.activations(T, shape.hidden, seed, "u", DEV)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_dense_mlp(cfg, u, Wd["w_gate_up"], Wd["w_down"], out, ws_for(cfg, T))
+    ref = O.dense_mlp(shape, np64(u), np64(Wd["w_gate_up"]), np64(Wd["w_down"]))
+    assert_close(np64(out), ref, "dense out")
+
+
+# ------------------------------------------------------------------ device-side checks ----
+
+def test_bad_positions_are_flagged_and_skipped():
+    shape = TINY
+    cfg = cfg_of(shape, nope=True)
+    W, u, kc, seq, pos = _qkv_inputs(shape, 2, 3, [5, 9], [0, 0], False, True)
+    before = kc.k.clone()
+    bad = torch.tensor([0, 10_000], dtype=torch.int32, device=DEV)   # p < 1; p > capacity
+    q = torch.empty((2, shape.n_q, shape.head_dim), dtype=torch.bfloat16, device=DEV)
+    g = torch.empty((2, shape.q_rows), dtype=torch.bfloat16, device=DEV)
+    B.beam_get_device_status()
+    B.beam_qkv_gate(cfg, u, W["w_qkvg"], W["q_norm"], W["k_norm"], seq, bad, q, g, kc,
+                    ws_for(cfg, 2))
+    assert B.beam_get_device_status() & B.DEV_BAD_POSITION
+    assert torch.equal(kc.k, before)
+    bad_seq = torch.tensor([0, 7], dtype=torch.int32, device=DEV)
+    B.beam_qkv_gate(cfg, u, W["w_qkvg"], W["q_norm"], W["k_norm"], bad_seq, pos, q, g, kc,
+                    ws_for(cfg, 2))
+    assert B.beam_get_device_status() & B.DEV_BAD_SEQ
+    idx = torch.tensor([[0, 1, 99, 2]], dtype=torch.int32, device=DEV)
+    w = torch.full((1, 4), 0.5, dtype=torch.float32, device=DEV)
+    wgu, wdn = synth.expert_weights(shape, 0, 1, device=DEV)
+    out = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_moe(cfg_of(shape), u[:1], idx, w, wgu, wdn, out, ws_for(cfg, 1))
+    assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+
+
+def test_invalid_arguments_return_errors():
+    shape = TINY
+    cfg = cfg_of(shape)
+    h = torch.zeros((2, 100), dtype=torch.bfloat16, device=DEV)     # H not a multiple of 8
+    with pytest.raises(B.BeamError, match="invalid argument"):
+        B.beam_boundary_norm(None, h, h, None, h[0], 1, 1e-6)
+    x = torch.zeros((2, 256), dtype=torch.bfloat16, device=DEV)
+    tiny_ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(B.BeamError, match="invalid argument"):
+        Wd = synth.dense_weights(shape, 0, 1, device=DEV)
+        B.beam_dense_mlp(cfg, x, Wd["w_gate_up"], Wd["w_down"], x, tiny_ws)
+    bad = B.LayerCfg.from_shape(shape, B.BEAM_ATTN_SWA_ROPE)
+    bad.head_dim = 96
+    W = synth.attention_weights(shape, 0, 1, device=DEV)
+    c = synth.kv_cache(shape, 1, 32, 1, device=DEV)
+    kc = B.KVCache(c["k"], c["v"], 16)
+    s = torch.zeros(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(B.BeamError, match="unsupported"):
+        B.beam_qkv_gate(bad, x, W["w_qkvg"], W["q_norm"], W["k_norm"], s, s + 1,
+                        torch.empty((2, 4, 96), dtype=torch.bfloat16, device=DEV),
+                        torch.empty((2, 384), dtype=torch.bfloat16, device=DEV), kc,
+                        ws_for(cfg, 2))
