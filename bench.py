@@ -153,39 +153,44 @@ class Workload:
         shape = BEAM
         kind = args.workload
         fp8 = args.kv == "fp8"
+        chunk = 1
         if kind == "swa_decode":
             layers, ctx, batch = [3], 4096, 1
         elif kind == "nope_decode":
             layers, ctx, batch = [5], 100_000, args.batch
+        elif kind == "stack_prefill":
+            layers, ctx, batch, chunk = list(range(6)), args.context, args.seqs, args.chunk
         else:
             layers, ctx, batch = list(range(6)), args.context, args.batch
         self.layers, self.ctx, self.batch, self.fp8 = layers, ctx, batch, fp8
+        self.chunk = chunk
+        self.prefill = chunk > 1
+        self.tokens = batch * chunk
         scale = 1.0
         W, caches = [], []
         for l in layers:
             W.append(synth.layer_weights(shape, l, args.seed, device=device))
             nope = is_nope(l, shape.n_layers)
-            cap, win = (ctx + 8, 0) if nope else (shape.window, shape.window)
+            cap, win = (ctx + chunk + 8, 0) if nope else (shape.window + chunk - 1, shape.window)
             c = synth.kv_cache(shape, batch, cap, args.seed, l, fp8=fp8, k_scale=scale,
                                v_scale=scale, device=device)
             caches.append(B.KVCache(c["k"], c["v"], win, scale, scale))
         self.shape = shape
         self.stack = BeamStack(shape, W, caches, first_layer=layers[0], device=device)
-        self.seq = torch.arange(batch, dtype=torch.int32, device=device)
-        self.pos = torch.full((batch,), ctx + 1, dtype=torch.int32, device=device)
-        self.max_pos = ctx + 1
-        self.e = synth.activations(batch, shape.hidden, args.seed, "h", device)
+        self.seq, self.pos = synth.prefill_positions([ctx] * batch, chunk, device)
+        self.max_pos = ctx + chunk
+        self.e = synth.activations(self.tokens, shape.hidden, args.seed, "h", device)
         self.W = W
         self.caches = caches
 
     def step_calls(self):
         """The library calls of one step as (name, fn) closures over fixed buffers."""
         B, st = self.B, self.stack
-        T = self.batch
+        T = self.tokens
         b = st.buffers(T)
         ws = st.ws.get(B.workspace_bytes(st.cfgs[0], T, self.max_pos))
-        calls = [("input", lambda: b["h"].copy_(self.e)),
-                 ("pre_norm", lambda: B.beam_boundary_norm(None, b["h"], b["u"], None,
+        b["h"].copy_(self.e)
+        calls = [("pre_norm", lambda: B.beam_boundary_norm(None, b["h"], b["u"], None,
                                                            st.W[0]["attn_pre"], 1,
                                                            st.cfgs[0].eps))]
         for i in range(st.L):
@@ -217,6 +222,28 @@ class Workload:
                                                W["mlp_post"], nxt, 2 * l + 3, cfg.eps)))
         return calls, b
 
+    def flops(self):
+        """Algorithmic FLOPs of one step per call kind (tensor-core contractions) and the
+        router's FP32 FLOPs."""
+        s = self.shape
+        T, H = self.tokens, s.hidden
+        out = {}
+        for i, l in enumerate(self.layers):
+            nope = is_nope(l, s.n_layers)
+            keys = 0
+            for t in range(self.chunk):
+                p = self.ctx + 1 + t
+                keys += p if nope else min(s.window, p)
+            keys *= self.batch
+            out[f"L{l}.qkv_gate"] = 2.0 * T * s.qkvg_rows * H
+            out[f"L{l}.attn"] = 4.0 * s.head_dim * s.n_q * keys + 2.0 * T * H * s.q_rows
+            if l in s.dense_layers:
+                out[f"L{l}.dense_mlp"] = 2.0 * T * 3 * H * s.d_ff_dense
+            else:
+                out[f"L{l}.moe"] = 2.0 * T * s.topk * 3 * H * s.d_ff_expert
+                out[f"L{l}.route"] = 2.0 * T * s.n_experts * H
+        return out
+
     def touched_experts(self, b):
         """Distinct experts each MoE layer's routing selected in the last step."""
         return len(set(b["idx"].cpu().numpy().ravel().tolist()))
@@ -229,7 +256,7 @@ class Workload:
             nope = is_nope(l, shape.n_layers)
             keys = self.ctx + 1 if nope else min(shape.window, self.ctx + 1)
             elem = 1 if self.fp8 else 2
-            kv = self.batch * keys * shape.n_kv * shape.head_dim * 2 * elem
+            kv = self.batch * (keys + self.chunk - 1) * shape.n_kv * shape.head_dim * 2 * elem
             dense = l in shape.dense_layers
             per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv)
             tot += per[l]
@@ -320,12 +347,14 @@ def run_ours(args, rank, world, device):
         for l in moe_layers:
             touched[l] = n
     algo_bytes, per_layer = wl.algorithmic_bytes(touched)
-    us_per_token_layer = ms_step * 1000.0 / (wl.batch * world) / len(wl.layers)
+    us_per_token_layer = ms_step * 1000.0 / (wl.tokens * world) / len(wl.layers)
+    tokens_per_s = wl.tokens * world / (ms_step * 1e-3)
     hbm, hbm_kind = peaks()
     layer_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
 
     roof = None
-    if per_call_us:
+    tensor_total = None
+    if per_call_us and not wl.prefill:
         dom = max(per_call_us, key=per_call_us.get)
         dom_bytes, dom_key = dominant_bytes(wl, dom, touched)
         dom_gbs = dom_bytes / (per_call_us[dom] * 1e-6) / 1e9
@@ -333,24 +362,45 @@ def run_ours(args, rank, world, device):
                 "unit": "GB/s", "frac": round(dom_gbs / hbm, 4),
                 "traffic": ncu_traffic(dom_key), "bytes_per_launch": dom_bytes,
                 "duration_us": round(per_call_us[dom], 2), "peak_kind": hbm_kind}
+    elif per_call_us:
+        tf_peak, tf_kind = tensor_peak()
+        fl = wl.flops()
+        dom = max((k for k in per_call_us if k in fl and not k.endswith(".route")),
+                  key=per_call_us.get)
+        ach = fl[dom] / (per_call_us[dom] * 1e-6) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": tf_peak,
+                "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
+                "traffic": ncu_traffic(dom.split(".")[1] + "_prefill"),
+                "flops_per_launch": fl[dom], "duration_us": round(per_call_us[dom], 2),
+                "peak_kind": tf_kind}
+        tc_flops = sum(v for k, v in fl.items() if not k.endswith(".route"))
+        gemm_keys = [k for k in fl if k.endswith((".qkv_gate", ".dense_mlp", ".moe"))]
+        gemm_us = sum(per_call_us[k] for k in gemm_keys)
+        gemm_fl = sum(fl[k] for k in gemm_keys)
+        tensor_total = {
+            "step_tflops": round(tc_flops / (ms_step * 1e-3) / 1e12, 1),
+            "gemm_calls_tflops": round(gemm_fl / (gemm_us * 1e-6) / 1e12, 1),
+            "gemm_calls_frac": round(gemm_fl / (gemm_us * 1e-6) / 1e12 / tf_peak, 4),
+            "peak": tf_peak, "peak_kind": tf_kind}
 
     e2e = run_e2e(args, wl, step_graph, stream, world)
     res = {
         "metric": METRIC,
-        "value": round(us_per_token_layer, 3),
-        "unit": "us/token/layer",
+        "value": round(tokens_per_s, 1) if wl.prefill else round(us_per_token_layer, 3),
+        "unit": "tokens/s" if wl.prefill else "us/token/layer",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
-        "higher_is_better": False,
+        "higher_is_better": bool(wl.prefill),
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) activations and KV cache, random-init N(0,0.02) weights",
         "config": {
             "workload": args.workload, "layers": wl.layers, "batch": wl.batch,
-            "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
+            "new_tokens_per_seq": wl.chunk, "context": wl.ctx,
+            "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
             "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
             "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
             "parallelism": "replicas" if world > 1 else "single",
@@ -361,6 +411,7 @@ def run_ours(args, rank, world, device):
                       "achieved_gbs": round(layer_gbs, 1), "peak_gbs": hbm,
                       "frac": round(layer_gbs / hbm, 4), "peak_kind": hbm_kind},
         "roofline": roof,
+        "tensor": tensor_total,
         "per_call_us": {k: round(v, 2) for k, v in per_call_us.items()},
         "e2e": e2e,
         "gpu_launches": launches_step * args.steps,
@@ -369,6 +420,15 @@ def run_ours(args, rank, world, device):
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, wl, budget_s=args.cpu_budget)
     return res
+
+
+def tensor_peak():
+    """Dense BF16 tensor peak for a kernel timed inside a long step: the sustained figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured (sustained)"
+    return 1700.0, "fallback (sustained)"
 
 
 def dominant_bytes(wl, name, touched):
@@ -402,14 +462,17 @@ def run_e2e(args, wl, step_graph, stream, world):
     with torch.cuda.stream(stream):
         t0.record(stream)
         for _ in range(args.steps):
-            wl.e.copy_(h_host, non_blocking=True)
+            b["h"].copy_(h_host, non_blocking=True)
             step_graph.replay()
             out_host.copy_(b["h"], non_blocking=True)
         t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
     nbytes = h_host.numel() * h_host.element_size()
-    return {"value": round(ms * 1000.0 / (wl.batch * world) / len(wl.layers), 3),
+    if wl.prefill:
+        return {"value": round(wl.tokens * world / (ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+    return {"value": round(ms * 1000.0 / (wl.tokens * world) / len(wl.layers), 3),
             "unit": "us/token/layer", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
 
 
@@ -468,9 +531,9 @@ def cpu_baseline(args, wl, budget_s=15.0):
         t_total += time.perf_counter() - t
         n += 1
     us = t_total / n * 1e6 / len(wl.layers)
-    return {"value": round(us, 1), "unit": "us/token/layer", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{n} x one token of sequence 0 through layers {wl.layers} "
+    val, unit = (round(n / t_total, 3), "tokens/s") if wl.prefill else (round(us, 1), "us/token/layer")
+    return {"value": val, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} x the first new token of sequence 0 through layers {wl.layers} "
                       f"(context {wl.ctx}); float64 NumPy oracle, {t_total:.1f} s"}
 
 
@@ -486,19 +549,20 @@ def run_reference(args, rank, world, device):
         run()
     dt = (time.perf_counter() - t) / args.steps
     us = dt * 1e6 / len(wl.layers)
+    val, unit = (round(1.0 / dt, 3), "tokens/s") if wl.prefill else (round(us, 1), "us/token/layer")
     return {
-        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/token/layer",
+        "impl": "reference", "metric": METRIC, "value": val, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt * 1000, 2), "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": round(dt * 1000, 2), "higher_is_better": bool(wl.prefill),
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the CUDA arm)",
         "config": {"workload": args.workload, "layers": wl.layers, "batch": 1,
                    "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
                    "sample": "one token of sequence 0 per step"},
-        "cpu_baseline": {"value": round(us, 1), "unit": "us/token/layer",
-                         "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": "one token of sequence 0 through the held layers per step"},
-        "e2e": {"value": round(us, 1), "unit": "us/token/layer", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": val, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "the first new token of sequence 0 through the held layers"
+                                   " per step"},
+        "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
@@ -511,7 +575,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="swa_decode",
-                    choices=["swa_decode", "nope_decode", "stack_decode"])
+                    choices=["swa_decode", "nope_decode", "stack_decode", "stack_prefill"])
+    ap.add_argument("--seqs", type=int, default=8)
+    ap.add_argument("--chunk", type=int, default=2048)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--context", type=int, default=100_000)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])

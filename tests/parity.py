@@ -79,3 +79,88 @@ def route_margins(cfg, u, w_router, corr_bias):
 
 def device_tensor(x, device="cuda"):
     return x.to(device) if isinstance(x, torch.Tensor) else torch.as_tensor(x, device=device)
+
+
+# ---------------------------------------------------------------------------------------
+# Chained steps: bars scaled by the oracle's own rounding-order sensitivity
+# ---------------------------------------------------------------------------------------
+
+def flatten_trace(trace, h_final=None, prefix=""):
+    """Oracle or GPU layer trace -> {name: float64 array}; router logits under 'L{i}.logits'."""
+    out = {}
+    for i, tr in enumerate(trace):
+        for k in ("q", "attn", "mlp"):
+            v = tr[k]
+            out[f"{prefix}L{i}.{k}"] = v if isinstance(v, np.ndarray) else np64(v)
+        r = tr.get("route")
+        if r is not None:
+            lg = r[0]
+            out[f"{prefix}L{i}.logits"] = lg.astype(np.float64) if isinstance(lg, np.ndarray) \
+                else lg.cpu().double().numpy()
+    if h_final is not None:
+        out[prefix + "h"] = h_final if isinstance(h_final, np.ndarray) else np64(h_final)
+    return out
+
+
+def noise_floor(run, n=2):
+    """run() -> flattened oracle outputs of a chained computation, computed from scratch.
+    Returns (reference, floors) where floors[name] = (max-abs-rel, mean-rel, max |delta|)
+    of n reruns under FP32-level perturbation of every rounding point, against the reference."""
+    from oracle.noise import perturbed_rounding
+    ref = run()
+    floors = {k: (0.0, 0.0, 0.0) for k in ref}
+    for s in range(n):
+        with perturbed_rounding(seed=s + 1):
+            alt = run()
+        for k in ref:
+            a, r = alt[k], ref[k]
+            floors[k] = (max(floors[k][0], max_abs_rel(a, r)), max(floors[k][1], mean_rel(a, r)),
+                         max(floors[k][2], float(np.max(np.abs(a - r)))))
+    return ref, floors
+
+
+def assert_chained_close(got, ref, floors, fp8=False, factor=3.0):
+    """Stated bars, or factor x the oracle's own perturbation divergence where that is larger."""
+    report = {}
+    for k in ref:
+        if k.endswith(".logits"):
+            continue
+        lim_mx = max(FP8_MAX_REL if fp8 else BF16_MAX_REL, factor * floors[k][0])
+        lim_mn = max(FP8_MEAN_REL if fp8 else BF16_MEAN_REL, factor * floors[k][1])
+        a = got[k]
+        mx, mn = max_abs_rel(a, ref[k]), mean_rel(a, ref[k])
+        assert np.all(np.isfinite(a)), f"{k}: non-finite"
+        assert mx <= lim_mx and mn <= lim_mn, \
+            f"{k}: max-abs-rel {mx:.3e} (<= {lim_mx:.3e}), mean-rel {mn:.3e} (<= {lim_mn:.3e})"
+        report[k] = (mx, mn, lim_mx, lim_mn)
+    return report
+
+
+def route_margin_ok(shape, trace, weights, floors):
+    """Every MoE layer's routing must be decided by more than the perturbation moves the
+    scores: margins (oracle FP32 scores) >= max(1e-6, 10 x the largest score shift)."""
+    for i, tr in enumerate(trace):
+        if tr.get("route") is None:
+            continue
+        shift = 0.25 * floors[f"L{i}.logits"][2]      # sigmoid slope <= 1/4
+        g, e = route_margins(shape, tr["mlp_in"], weights[i]["router"], weights[i]["corr_bias"])
+        if min(g, e) < max(1e-6, 10.0 * shift):
+            return False
+    return True
+
+
+def codes_close(got_codes, ref_codes, max_frac=0.01):
+    """FP8 cache codes: equal, or the neighbouring code (a rounding decision the two sides
+    took from FP32 values a few ulps apart), in at most max_frac of the entries."""
+    import oracle.codecs as C
+    grid = np.unique(C.e4m3_table()[np.isfinite(C.e4m3_table())])
+    pos = {v: i for i, v in enumerate(grid)}
+    gv = C.e4m3_decode(got_codes).ravel()
+    rv = C.e4m3_decode(ref_codes).ravel()
+    diff = gv != rv
+    if not np.any(diff):
+        return
+    gi = np.array([pos[v] for v in gv[diff]])
+    ri = np.array([pos[v] for v in rv[diff]])
+    assert np.all(np.abs(gi - ri) <= 1), "fp8 codes differ by more than one step"
+    assert np.mean(diff) <= max_frac, f"{np.mean(diff):.3%} of fp8 codes differ"
