@@ -9,11 +9,12 @@ Workloads (seeded synthetic inputs, random-init weights; shapes of the Beam laye
                (--batch, --context, --kv; the 8-K / batch-128 / FP8 case is
                --batch 128 --context 8192 --kv fp8; batch 1 / 100K / BF16 by default)
 
-A step is one pass of the whole layer (or stack) over one batch of new tokens. Inputs are
-resident in HBM when the timed region starts; each step streams far more than the 129 MB L2
-(the layer's weights), so no flush is needed. Steps run as per-call CUDA graphs (one per
-library call) with CUDA events between them, which gives the step time and each call's
-time from the same timed region.
+A step is one pass of the whole layer (or stack) over one batch of new tokens; the residual
+stream h it updates in place carries over to the next step. Inputs are resident in HBM when
+the timed region starts; each step streams far more than the 129 MB L2 (the layer's weights),
+so no flush is needed. The K timed steps are captured as one CUDA graph with a timing event
+(an external event node) before every library call, so the step time and each call's time
+come from the same replay.
 
 --impl reference times the CPU oracle on the same workload instead (a bounded sample per step).
 """
@@ -453,7 +454,7 @@ def dominant_bytes(wl, name, touched):
 def run_e2e(args, wl, step_graph, stream, world):
     """Same step with the tokens' hidden state copied in from pinned host memory and the
     output h copied back, both inside the timed region."""
-    b = wl.stack.buffers(wl.batch)
+    b = wl.stack.buffers(wl.tokens)
     h_host = wl.e.cpu().pin_memory()
     out_host = torch.empty_like(h_host).pin_memory()
     t0 = torch.cuda.Event(enable_timing=True)

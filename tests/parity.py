@@ -136,31 +136,33 @@ def assert_chained_close(got, ref, floors, fp8=False, factor=3.0):
     return report
 
 
+ROUTE_MARGIN_FACTOR = 4.0
+
+
 def route_margin_ok(shape, trace, weights, floors):
     """Every MoE layer's routing must be decided by more than the perturbation moves the
-    scores: margins (oracle FP32 scores) >= max(1e-6, 10 x the largest score shift)."""
+    scores: margins (oracle FP32 scores) >= max(1e-6, 4 x the largest score shift)."""
     for i, tr in enumerate(trace):
         if tr.get("route") is None:
             continue
         shift = 0.25 * floors[f"L{i}.logits"][2]      # sigmoid slope <= 1/4
         g, e = route_margins(shape, tr["mlp_in"], weights[i]["router"], weights[i]["corr_bias"])
-        if min(g, e) < max(1e-6, 10.0 * shift):
+        if min(g, e) < max(1e-6, ROUTE_MARGIN_FACTOR * shift):
             return False
     return True
 
 
-def codes_close(got_codes, ref_codes, max_frac=0.01):
-    """FP8 cache codes: equal, or the neighbouring code (a rounding decision the two sides
-    took from FP32 values a few ulps apart), in at most max_frac of the entries."""
+def codes_close(got_codes, ref_codes, scale, max_frac=0.02):
+    """FP8 cache codes. The two sides quantise FP32 values that differ by rounding: a bf16
+    flip in the projection output moves a rotated element by up to ~2^-8 of its largest
+    partner, so elements near zero may move several fine (subnormal) steps. Bound: every
+    decoded value within one e4m3 step (1/8 relative) of the oracle's plus 2^-6 of the
+    head's largest magnitude; at most max_frac of the codes differ; mean-rel <= 2e-3."""
     import oracle.codecs as C
-    grid = np.unique(C.e4m3_table()[np.isfinite(C.e4m3_table())])
-    pos = {v: i for i, v in enumerate(grid)}
-    gv = C.e4m3_decode(got_codes).ravel()
-    rv = C.e4m3_decode(ref_codes).ravel()
-    diff = gv != rv
-    if not np.any(diff):
-        return
-    gi = np.array([pos[v] for v in gv[diff]])
-    ri = np.array([pos[v] for v in rv[diff]])
-    assert np.all(np.abs(gi - ri) <= 1), "fp8 codes differ by more than one step"
-    assert np.mean(diff) <= max_frac, f"{np.mean(diff):.3%} of fp8 codes differ"
+    gv = C.e4m3_decode(got_codes).astype(np.float64) * scale
+    rv = C.e4m3_decode(ref_codes).astype(np.float64) * scale
+    bound = 0.125 * np.abs(rv) + 2.0 ** -6 * np.max(np.abs(rv), axis=-1, keepdims=True)
+    assert np.all(np.abs(gv - rv) <= bound), "fp8 values differ beyond one step"
+    assert np.mean(got_codes != ref_codes) <= max_frac, \
+        f"{np.mean(got_codes != ref_codes):.3%} of fp8 codes differ"
+    assert mean_rel(gv, rv) <= FP8_MEAN_REL

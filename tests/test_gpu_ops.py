@@ -112,8 +112,8 @@ def test_qkv_gate(case, nope, fp8):
     for s, p in zip(seqs, positions):
         if fp8:
             sl = oc.slot(p)
-            codes_close(oc_gpu.k[s][:, sl], oc.k[s][:, sl])
-            codes_close(oc_gpu.v[s][:, sl], oc.v[s][:, sl])
+            codes_close(oc_gpu.k[s][:, sl], oc.k[s][:, sl], kc.k_scale)
+            codes_close(oc_gpu.v[s][:, sl], oc.v[s][:, sl], kc.v_scale)
         else:
             kg, vg = oc_gpu.load(s, np.array([p]))
             kr, vr = oc.load(s, np.array([p]))
