@@ -60,6 +60,7 @@ _SIGS = {
     "beam_status_string": [_I],
     "beam_launch_count": [],
     "beam_gemm_bf16": [_P, _I, _I, _I, _P, _I, _I, _P, _I, _I, _P],
+    "beam_route_noalloc": [_P, _P, _P, _P, _I, _P, _P, _P],
 }
 _RES = {"beam_workspace_bytes": _Z, "beam_kv_cache_bytes": _Z,
         "beam_status_string": ctypes.c_char_p, "beam_launch_count": ctypes.c_uint64}
@@ -240,3 +241,11 @@ def beam_gemm_bf16(a, b, c, stream=None):
     _check(lib().beam_gemm_bf16(_ptr(a), M, K, a.stride(0), _ptr(b), N, b.stride(0), _ptr(c),
                                 c.stride(0), int(c.dtype == torch.bfloat16), _stream(stream)),
            "beam_gemm_bf16")
+
+
+def beam_route_noalloc(cfg: LayerCfg, u, w_router, corr_bias, topk_idx, topk_w, stream=None):
+    """beam_route without caller scratch (the logits live in the library's static array)."""
+    c = cfg.c()
+    _check(lib().beam_route_noalloc(ctypes.byref(c), _ptr(u), _ptr(w_router), _ptr(corr_bias),
+                                    u.shape[0], _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
+           "beam_route_noalloc")

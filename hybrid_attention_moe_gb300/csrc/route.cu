@@ -5,6 +5,8 @@
 // (a dedicated small-batch FP32 router kernel).
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace beam {
@@ -206,6 +208,80 @@ extern "C" beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u,
     lg = cv.take<float>(size_t(T) * E);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   }
+  if (T <= 32)
+    router_gemv_kernel<<<E, 256, 0, st>>>(u, w_router, T, H, E, lg);
+  else
+    router_gemm_kernel<<<dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), 256, 0, st>>>(
+        u, w_router, T, H, E, lg);
+  note_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
+  router_topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
+                                                  cfg->topk, cfg->route_scale, topk_idx, topk_w);
+  note_launches(1);
+  return launch_status();
+}
+
+// ------------------------------------------------------------------------------------------
+// Allocation-free router
+//
+// Some callers cannot hand the library any scratch memory: a serving engine that has given all
+// free device memory to its KV-cache pool, or a runtime whose device memory is partitioned up
+// front and that may not call cudaMalloc (or any allocating library) afterwards. For them the
+// router's one piece of scratch -- the FP32 logits when the caller does not want them back --
+// lives in a fixed array in the library's own device memory instead of a caller workspace.
+// ------------------------------------------------------------------------------------------
+namespace beam {
+namespace {
+
+// Logits scratch of the allocation-free router: 65536 floats (256 KiB), i.e. up to
+// T * n_experts <= 65536 (256 tokens at 256 experts). Every GPU that loads the library holds
+// one copy of it until the process exits.
+constexpr int kNoAllocLogits = 65536;
+static __device__ __align__(256) float g_route_scratch[kNoAllocLogits];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_dev[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device, with that device
+// current, and cached.
+float* scratch_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_dev[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_dev[dev] = static_cast<float*>(p);
+  }
+  return g_scratch_dev[dev];
+}
+
+}  // namespace
+}  // namespace beam
+
+extern "C" beam_status beam_route_noalloc(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                          const float* w_router, const float* corr_bias, int T,
+                                          int32_t* topk_idx, float* topk_w,
+                                          beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !w_router || !corr_bias || !topk_idx || !topk_w)
+    return BEAM_ERR_INVALID_ARG;
+  const int E = cfg->n_experts, G = cfg->n_groups, H = cfg->hidden;
+  if (H <= 0 || (H & 7) || E <= 0 || G <= 0 || E % G != 0 || cfg->topk_groups < 1 ||
+      cfg->topk_groups > G || cfg->topk < 1 || cfg->topk > cfg->topk_groups * (E / G) ||
+      E / G < 2)
+    return BEAM_ERR_INVALID_ARG;
+  if (E > kMaxE || G > kMaxG || cfg->topk > kMaxK) return BEAM_ERR_UNSUPPORTED;
+  if (size_t(T) * size_t(E) > size_t(kNoAllocLogits)) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_router)) return BEAM_ERR_INVALID_ARG;
+  if (T == 0) return BEAM_OK;
+  float* lg = scratch_on_current_device();
+  if (lg == nullptr) return BEAM_ERR_CUDA;
+  // the GEMV/GEMM writes every logit of the T x E block before the top-k reads it, so the
+  // scratch needs no clearing between calls
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (T <= 32)
     router_gemv_kernel<<<E, 256, 0, st>>>(u, w_router, T, H, E, lg);
   else

@@ -15,7 +15,8 @@
  *    weights are [out][in] so each output row is contiguous along the reduction axis.
  *  - The caller owns every buffer: weights, activations, caches and the workspace. The
  *    library allocates no device memory and keeps no state between calls except one
- *    status word per device (beam_get_device_status).
+ *    status word per device (beam_get_device_status) and the fixed scratch array of
+ *    beam_route_noalloc.
  *  - Every call is asynchronous on `stream` (NULL = the legacy default stream). Argument
  *    checks on sizes, enum values and pointer alignment are synchronous: a call that fails
  *    them returns BEAM_ERR_INVALID_ARG (bad argument) or BEAM_ERR_UNSUPPORTED (valid but
@@ -163,6 +164,24 @@ beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q, const beam_
 beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u, const float* w_router,
                        const float* corr_bias, int T, float* logits, int32_t* topk_idx,
                        float* topk_w, void* ws, size_t ws_bytes, beam_stream_t stream);
+
+/* Allocation-free variant of beam_route, for callers that cannot provide device scratch: for
+ * example a serving engine that has given all free device memory to its KV-cache pool, or a
+ * runtime that must not call cudaMalloc (or any allocating library) once it is running.
+ * (The Beam pages have no counterpart; this is an interface convenience.)
+ * Same arguments and results as beam_route without logits, ws and ws_bytes. The router's
+ * logits go to a fixed scratch array inside the library: 65536 floats (256 KiB) of device
+ * memory that every GPU loading the library holds until the process exits, so it needs
+ * T * n_experts <= 65536 (256 tokens at 256 experts); larger calls return
+ * BEAM_ERR_INVALID_ARG and launch nothing. The call allocates nothing. The first call on a
+ * device looks up the array's device address on that device (once, with it current); make
+ * that first call before any stream capture. All calls on a device share the one array and
+ * leave their logits in it; each call overwrites the whole T x E block it reads, so nothing
+ * needs clearing, but calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race on the array and give undefined results. */
+beam_status beam_route_noalloc(const beam_layer_cfg* cfg, const beam_bf16* u,
+                               const float* w_router, const float* corr_bias, int T,
+                               int32_t* topk_idx, float* topk_w, beam_stream_t stream);
 
 /* Routed SwiGLU experts with the weighted combine (Beam page, MoE section: 256 experts,
  * d_ff 2560, no shared expert; change 3 combines the top-8 outputs). Only the selected
