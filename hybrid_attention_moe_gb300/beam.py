@@ -50,7 +50,7 @@ _Z = ctypes.c_size_t
 _SIGS = {
     "beam_boundary_norm": [_P, _P, _P, _P, _P, _I, _I, _I, _F, _P],
     "beam_qkv_gate": [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P],
-    "beam_attn": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _P],
+    "beam_attn": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
     "beam_route": [_P, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P],
     "beam_moe": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_dense_mlp": [_P, _P, _P, _P, _I, _P, _P, _Z, _P],
@@ -192,11 +192,14 @@ def beam_qkv_gate(cfg: LayerCfg, u, w_qkvg, q_norm_w, k_norm_w, seq_id, pos, q_o
 
 
 def beam_attn(cfg: LayerCfg, q, g, gate_bias, cache: KVCache, seq_id, pos, max_pos, w_o, out,
-              ws: torch.Tensor, stream=None):
+              ws: torch.Tensor, stream=None, max_q_per_seq=None):
+    """max_q_per_seq: most tokens of one sequence in the call (1 for decode); None = T."""
     c, kc = cfg.c(), cache.c()
+    mq = q.shape[0] if max_q_per_seq is None else int(max_q_per_seq)
     _check(lib().beam_attn(ctypes.byref(c), _ptr(q), _ptr(g), _ptr(gate_bias), ctypes.byref(kc),
-                           _ptr(seq_id), _ptr(pos), q.shape[0], int(max_pos), _ptr(w_o),
-                           _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "beam_attn")
+                           _ptr(seq_id), _ptr(pos), q.shape[0], int(max_pos), max(1, mq),
+                           _ptr(w_o), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "beam_attn")
 
 
 def beam_route(cfg: LayerCfg, u, w_router, corr_bias, logits, topk_idx, topk_w,

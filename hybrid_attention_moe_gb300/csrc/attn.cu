@@ -201,6 +201,52 @@ __device__ __forceinline__ void load_q(const uint16_t* q, uint32_t (&qa)[D / 16]
   }
 }
 
+// Merge the splits of one (token, KV head), normalise, round, gate, round. Run by the last
+// split CTA of the pair to finish; the partials of the other CTAs are read through L2. The
+// per-split (max, sum) pairs are staged in shared memory first, so each output element then
+// needs one pass of independent loads over the splits.
+constexpr int kMergeMaxSplits = 64;
+__device__ __forceinline__ void merge_gate(const float* part_acc, const float* part_ml,
+                                           int n_splits, int n_q, int n_kv, int D, float v_scale,
+                                           const uint16_t* __restrict__ gpre,
+                                           const uint16_t* __restrict__ gate_bias,
+                                           uint16_t* __restrict__ og, int t, int hk, float* sh) {
+  const int G = n_q / n_kv;
+  const size_t pbase = (size_t(t) * n_kv + hk) * n_splits;
+  float* w = sh;                              // [kRows][n_splits]: exp2(m_s - M)
+  float* inv = sh + kRows * kMergeMaxSplits;  // [kRows]: 1 / sum_s w_s l_s
+  for (int i = threadIdx.x; i < G * n_splits; i += blockDim.x) {
+    const int row = i / n_splits, sp = i - row * n_splits;
+    w[row * kMergeMaxSplits + sp] = __ldcg(part_ml + ((pbase + sp) * kRows + row) * 2);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int row = threadIdx.x;
+    float M = kNegInf;
+    for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, w[row * kMergeMaxSplits + sp]);
+    float L = 0.f;
+    for (int sp = 0; sp < n_splits; ++sp) {
+      const float f = M == kNegInf ? 0.f : exp2f(w[row * kMergeMaxSplits + sp] - M);
+      w[row * kMergeMaxSplits + sp] = f;
+      L += f * __ldcg(part_ml + ((pbase + sp) * kRows + row) * 2 + 1);
+    }
+    inv[row] = L > 0.f ? v_scale / L : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int row = idx / D, d = idx - row * D;
+    float O = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < n_splits; ++sp)
+      O += w[row * kMergeMaxSplits + sp] * __ldcg(part_acc + ((pbase + sp) * kRows + row) * D + d);
+    const float o = round_bf(O * inv[row]);
+    const int hq = hk * G + row;
+    const size_t oi = (size_t(t) * n_q + hq) * D + d;
+    const float gate = sigmoidf_(bf2f(gpre[oi]) + bf2f(gate_bias[hq]));
+    og[oi] = f2bf(o * gate);
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // Decode: split-K partials
 // ------------------------------------------------------------------------------------------
@@ -208,7 +254,11 @@ template <int D, bool FP8>
 __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_id,
     const int32_t* __restrict__ pos, int n_q, int n_kv, beam_kv_cache kc, int kps, int n_splits,
-    float sl2, float* __restrict__ part_acc, float* __restrict__ part_ml) {
+    float sl2, float* __restrict__ part_acc, float* __restrict__ part_ml, int* __restrict__ done,
+    float v_scale, const uint16_t* __restrict__ gpre, const uint16_t* __restrict__ gate_bias,
+    uint16_t* __restrict__ og) {
+  pdl_trigger();
+  pdl_wait();
   using Gm = TileGeom<D, FP8, kDecKT>;
   constexpr int KT = kDecKT;
   constexpr int DN = D / 8;
@@ -338,33 +388,17 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
       part_ml[(pbase * kRows + row) * 2 + 1] = L;
     }
   }
-}
-
-// Merge the splits of one (token, KV head), normalise, round, gate, round.
-__global__ void __launch_bounds__(256) attn_merge_gate_kernel(
-    const float* __restrict__ part_acc, const float* __restrict__ part_ml, int n_splits, int n_q,
-    int n_kv, int D, float v_scale, const uint16_t* __restrict__ gpre,
-    const uint16_t* __restrict__ gate_bias, uint16_t* __restrict__ og) {
-  const int hk = blockIdx.x, t = blockIdx.y;
-  const int G = n_q / n_kv;
-  const size_t pbase = (size_t(t) * n_kv + hk) * n_splits;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int row = idx / D, d = idx - row * D;
-    float M = kNegInf;
-    for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, part_ml[((pbase + sp) * kRows + row) * 2]);
-    float O = 0.f, L = 0.f;
-    if (M != kNegInf) {
-      for (int sp = 0; sp < n_splits; ++sp) {
-        const float f = exp2f(part_ml[((pbase + sp) * kRows + row) * 2] - M);
-        O += f * part_acc[((pbase + sp) * kRows + row) * D + d];
-        L += f * part_ml[((pbase + sp) * kRows + row) * 2 + 1];
-      }
-    }
-    const float o = L > 0.f ? round_bf(O / L * v_scale) : 0.f;
-    const int hq = hk * G + row;
-    const size_t oi = (size_t(t) * n_q + hq) * D + d;
-    const float gate = sigmoidf_(bf2f(gpre[oi]) + bf2f(gate_bias[hq]));
-    og[oi] = f2bf(o * gate);
+  // the last split CTA of this (token, KV head) merges all splits
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done + t * n_kv + hk, 1) == n_splits - 1;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    // the tile buffers are free now: stage the merge weights there
+    merge_gate(part_acc, part_ml, n_splits, n_q, n_kv, D, v_scale, gpre, gate_bias, og, t, hk,
+               reinterpret_cast<float*>(smem));
   }
 }
 
@@ -377,6 +411,8 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(
     const uint16_t* __restrict__ gate_bias, const int32_t* __restrict__ seq_id,
     const int32_t* __restrict__ pos, int T, int n_q, int n_kv, beam_kv_cache kc, float sl2,
     uint16_t* __restrict__ og) {
+  pdl_trigger();
+  pdl_wait();
   using Gm = TileGeom<D, FP8, kPreKT>;
   constexpr int KT = kPreKT;
   constexpr int DN = D / 8;
@@ -531,7 +567,7 @@ int num_sms() {
   return g_num_sms;
 }
 
-constexpr int kDecodeMaxT = 32;
+constexpr int kDecodeMaxQ = 4;   // split-K per token up to this many tokens per sequence
 
 struct DecodePlan {
   int kps, n_splits;
@@ -542,10 +578,16 @@ DecodePlan decode_plan(int T, int n_kv, int max_keys) {
   int splits = (2 * num_sms() + per - 1) / per;
   const int max_splits = (max_keys + 127) / 128;
   splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
+  if (splits > kMergeMaxSplits) splits = kMergeMaxSplits;
   int kps = (max_keys + splits - 1) / splits;
   kps = (kps + 127) / 128 * 128;
   splits = (max_keys + kps - 1) / kps;
   if (splits < 1) splits = 1;
+  if (splits > kMergeMaxSplits) {   // keep within the merge's staging (never hit in practice)
+    kps = (max_keys + kMergeMaxSplits - 1) / kMergeMaxSplits;
+    kps = (kps + 127) / 128 * 128;
+    splits = (max_keys + kps - 1) / kps;
+  }
   return {kps, splits};
 }
 
@@ -561,7 +603,8 @@ cudaError_t set_smem(K kern, int bytes) {
 template <int D, bool FP8>
 cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_t* pos, int T,
                           int n_q, int n_kv, const beam_kv_cache& kc, DecodePlan pl, float sl2,
-                          float* pacc, float* pml, cudaStream_t st) {
+                          float* pacc, float* pml, int* done, float v_scale, const uint16_t* g,
+                          const uint16_t* gb, uint16_t* og, cudaStream_t st) {
   using Gm = TileGeom<D, FP8, kDecKT>;
   int bytes = kDecWarps * Gm::BYTES;
   const int comb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
@@ -570,9 +613,8 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
   cudaError_t e = set_smem(kern, bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(pl.n_splits, n_kv, T);
-  kern<<<grid, kDecWarps * 32, bytes, st>>>(q, seq_id, pos, n_q, n_kv, kc, pl.kps, pl.n_splits,
-                                            sl2, pacc, pml);
-  note_launches(1);
+  launch_pdl(kern, dim3(grid), dim3(kDecWarps * 32), bytes, st, q, seq_id, pos, n_q, n_kv, kc, pl.kps, pl.n_splits,
+                                            sl2, pacc, pml, done, v_scale, g, gb, og);
   return cudaGetLastError();
 }
 
@@ -586,8 +628,7 @@ cudaError_t launch_prefill(const uint16_t* q, const uint16_t* g, const uint16_t*
   cudaError_t e = set_smem(kern, bytes);
   if (e != cudaSuccess) return e;
   dim3 grid((T + kRows - 1) / kRows, n_kv);
-  kern<<<grid, 32 * (n_q / n_kv), bytes, st>>>(q, g, gb, seq_id, pos, T, n_q, n_kv, kc, sl2, og);
-  note_launches(1);
+  launch_pdl(kern, dim3(grid), dim3(32 * (n_q / n_kv)), bytes, st, q, g, gb, seq_id, pos, T, n_q, n_kv, kc, sl2, og);
   return cudaGetLastError();
 }
 
@@ -595,10 +636,11 @@ cudaError_t launch_prefill(const uint16_t* q, const uint16_t* g, const uint16_t*
 
 size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
   size_t b = align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
-  if (T <= kDecodeMaxT) {
+  {   // the split-K decode form may be chosen for any T (max_q_per_seq <= kDecodeMaxQ)
     const DecodePlan pl = decode_plan(T, c->n_kv, max_keys_of(window, max_pos > 0 ? max_pos : 1));
     const size_t parts = size_t(T) * c->n_kv * pl.n_splits * kRows;
     b += align_up(parts * c->head_dim * 4, 256) + align_up(parts * 2 * 4, 256);
+    b += align_up(size_t(T) * c->n_kv * 4, 256);     // split completion counters
   }
   return b;
 }
@@ -608,14 +650,15 @@ size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
 extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
                                  const beam_bf16* g, const beam_bf16* gate_bias,
                                  const beam_kv_cache* cache, const int32_t* seq_id,
-                                 const int32_t* pos, int T, int max_pos, const beam_bf16* w_o,
-                                 beam_bf16* out, void* ws, size_t ws_bytes,
+                                 const int32_t* pos, int T, int max_pos, int max_q_per_seq,
+                                 const beam_bf16* w_o, beam_bf16* out, void* ws, size_t ws_bytes,
                                  beam_stream_t stream) {
   using namespace beam;
   beam_status stt = check_cfg_attn(cfg);
   if (stt != BEAM_OK) return stt;
   if ((stt = check_cache(cache, cfg)) != BEAM_OK) return stt;
-  if (T < 0 || max_pos < 1 || !q || !g || !gate_bias || !seq_id || !pos || !w_o || !out)
+  if (T < 0 || max_pos < 1 || max_q_per_seq < 1 || !q || !g || !gate_bias || !seq_id || !pos ||
+      !w_o || !out)
     return BEAM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(g) || !aligned16(w_o) || !aligned16(out) || !aligned16(ws))
     return BEAM_ERR_INVALID_ARG;
@@ -627,24 +670,23 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
   Carver cv{static_cast<char*>(ws), ws_bytes};
   uint16_t* og = cv.take<uint16_t>(size_t(T) * HD);
   cudaError_t e;
-  if (T <= kDecodeMaxT) {
+  if (max_q_per_seq <= kDecodeMaxQ) {
     const DecodePlan pl = decode_plan(T, cfg->n_kv, max_keys_of(cache->window, max_pos));
     const size_t parts = size_t(T) * cfg->n_kv * pl.n_splits * kRows;
     float* pacc = cv.take<float>(parts * D);
     float* pml = cv.take<float>(parts * 2);
+    int* done = cv.take<int>(size_t(T) * cfg->n_kv);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(done, 0, size_t(T) * cfg->n_kv * sizeof(int), st) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    const float vs = fp8 ? cache->v_scale : 1.f;
     if (D == 128)
-      e = fp8 ? launch_decode<128, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st)
-              : launch_decode<128, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st);
+      e = fp8 ? launch_decode<128, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st)
+              : launch_decode<128, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st);
     else
-      e = fp8 ? launch_decode<64, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st)
-              : launch_decode<64, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, st);
+      e = fp8 ? launch_decode<64, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st)
+              : launch_decode<64, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
-    attn_merge_gate_kernel<<<dim3(cfg->n_kv, T), 256, 0, st>>>(
-        pacc, pml, pl.n_splits, cfg->n_q, cfg->n_kv, D, fp8 ? cache->v_scale : 1.f, g, gate_bias,
-        og);
-    note_launches(1);
-    if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
   } else {
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
     if (cfg->n_q / cfg->n_kv * 32 > 256) return BEAM_ERR_UNSUPPORTED;

@@ -74,6 +74,13 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
+// Programmatic dependent launch: allow the next kernel to be scheduled; wait until every
+// predecessor's results are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
 __device__ __forceinline__ float siluf_(float z) { return z / (1.0f + __expf(-z)); }
 
@@ -83,6 +90,27 @@ inline bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(
 
 // Host-side count of kernel launches (misc.cu).
 void note_launches(int n);
+
+// Launch with programmatic stream serialization: the kernel may start while its predecessor
+// in the stream finishes; it must execute griddepcontrol.wait (pdl_wait) before reading or
+// writing anything a predecessor touches. Kernels launched this way all begin with
+// pdl_trigger(), so their own successors can be scheduled as their CTAs drain.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  note_launches(1);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 inline beam_status launch_status() {
   cudaError_t e = cudaGetLastError();

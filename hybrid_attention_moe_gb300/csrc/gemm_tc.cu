@@ -27,6 +27,7 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int THREADS = 192;
+constexpr int kGroupM = 16;   // row tiles walked per column tile (dense grids)
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
@@ -101,8 +102,9 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 // One CTA computes output columns [n0, n0 + BN) (kSwiGLU: units [n0, n0 + BN/2)) for A rows
-// [a_row0, a_row0 + rows). Dense GEMMs take a_row0 = 128 * blockIdx.y, b_row0 = 0; grouped
-// GEMMs read (b_row0, a_row0, rows) from a device-side job list (one job per expert row tile).
+// [a_row0, a_row0 + rows). Dense GEMMs map a 1-D grid onto (row tile, column tile) in groups
+// of kGroupM row tiles; grouped GEMMs read (group, a_row0, rows) from a device-side job list
+// (one job per expert row tile), blockIdx.y = job, blockIdx.x = column tile.
 struct GemmParams {
   int M, N, K;           // A rows (bound), output columns (units for kSwiGLU), reduction
   void* C;
@@ -118,8 +120,24 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    GemmParams p) {
-  int b_row0 = 0, a_row0 = blockIdx.y * BM, rows = BM;
-  if (p.jobs != nullptr) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per CTA
+  int b_row0 = 0, a_row0, rows = BM, n0;
+  if (p.jobs == nullptr) {
+    // 1-D grid in groups of kGroupM row tiles per column tile: the CTAs resident at one time
+    // cover a compact block of the output, so both operands' tiles are reused through L2
+    const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + NT - 1) / NT;
+    const int pid = blockIdx.x;
+    const int group = pid / (kGroupM * num_n);
+    const int first_m = group * kGroupM;
+    const int gsize = min(num_m - first_m, kGroupM);
+    const int in_group = pid - group * kGroupM * num_n;
+    a_row0 = (first_m + in_group % gsize) * BM;
+    n0 = (in_group / gsize) * NT;
+  } else {
+    a_row0 = 0;
+    n0 = blockIdx.x * NT;
     if (int(blockIdx.y) >= *p.n_jobs) return;   // uniform for the CTA, before any setup
     const int4 j = p.jobs[blockIdx.y];
     b_row0 = j.x * p.b_stride;
@@ -136,8 +154,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accb = smem_u32(bars + 2 * STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per CTA
-  const int n0 = blockIdx.x * NT;
   const int KB = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -323,8 +339,7 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParam
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, p);
-  note_launches(1);
+  launch_pdl(gemm_tc_kernel<MODE>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -339,7 +354,7 @@ cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* 
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
     return cudaErrorInvalidValue;
   GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
-  dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
   return out_bf16 ? launch<kBF16>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
 }
 
@@ -352,7 +367,7 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, 2 * F, ldb, BN / 2))
     return cudaErrorInvalidValue;
   GemmParams p{M, F, K, C, ldc, nullptr, nullptr, 0, F, nullptr};
-  dim3 grid((F + BN / 2 - 1) / (BN / 2), (M + BM - 1) / BM);
+  dim3 grid(((F + BN / 2 - 1) / (BN / 2)) * ((M + BM - 1) / BM));
   return launch<kSwiGLU>(ta, tb, p, grid, st);
 }
 

@@ -8,6 +8,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "sgemv.cuh"
 
 namespace beam {
 
@@ -82,6 +83,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
                                                    const uint16_t* __restrict__ X, int T,
                                                    float* __restrict__ yf,
                                                    uint16_t* __restrict__ yb, int ldy) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int ROWS = (MODE == kOutSwiGLU) ? 2 * NR : NR;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,19 +127,44 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
   }
 }
 
-// Host launcher: picks the token tile and rows per warp from T.
+int num_sms_cached();
+
+// Small-T dense rows: the shared-memory streamed kernel (1) or the register-pipelined kernel
+// (0); chosen by measurement.
+#ifndef BEAM_DENSE_STREAMED
+#define BEAM_DENSE_STREAMED 0
+#endif
+
+// Host launcher: the register-pipelined kernel with the token tile, rows per warp and chunks in
+// flight picked from T.
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
                                float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
   if (T <= 0 || N <= 0) return cudaSuccess;
+  if (BEAM_DENSE_STREAMED && T <= sg::kMaxT && (K * 2) % 512 == 0 && aligned16(W) &&
+      aligned16(X)) {
+    auto kern = sg::dense_kernel<MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         sg::kSmem);
+    if (e != cudaSuccess) return e;
+    void* y = MODE == kOutF32 ? static_cast<void*>(yf) : static_cast<void*>(yb);
+    launch_pdl(kern, dim3(num_sms_cached()), dim3(sg::kWarps * 32), sg::kSmem, st, W, N, K, X, T, y, ldy);
+    return cudaGetLastError();
+  }
   auto go = [&](auto kern, int nt, int nr) {
     const int warps = (N + nr - 1) / nr;
     dim3 grid((warps + 7) / 8, (T + nt - 1) / nt);
-    kern<<<grid, 256, 0, st>>>(W, N, K, X, T, yf, yb, ldy);
-    note_launches(1);
+    launch_pdl(kern, dim3(grid), dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
   };
-  if (T == 1)
-    go(gemv_kernel<1, 2, 4, MODE>, 1, 2);
+  if (T == 1) {
+    // three rows per warp when that fits the matrix into one wave of 4 CTAs per SM while
+    // still giving every SM at least two CTAs
+    const int ctas3 = (N + 23) / 24;
+    if (MODE != kOutSwiGLU && ctas3 <= 4 * num_sms_cached() && ctas3 >= 2 * num_sms_cached())
+      go(gemv_kernel<1, 3, 4, MODE>, 1, 3);
+    else
+      go(gemv_kernel<1, 2, 8, MODE>, 1, 2);
+  }
   else if (T == 2)
     go(gemv_kernel<2, 2, 4, MODE>, 2, 2);
   else if (T <= 4)

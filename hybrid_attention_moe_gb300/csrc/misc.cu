@@ -9,6 +9,19 @@ namespace beam {
 __device__ unsigned int g_dev_status = 0u;
 
 static std::atomic<unsigned long long> g_launches{0};
+
+// SM count of the current device (cached per device).
+int num_sms_cached() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 152;
+  }
+  return cache[dev];
+}
 void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
 
 size_t qkv_ws_bytes(const beam_layer_cfg* c, int T);

@@ -16,6 +16,13 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "sgemv.cuh"
+
+// Decode down projection: the shared-memory streamed kernel (1) or the register-pipelined
+// warp-per-row kernel (0); chosen by measurement.
+#ifndef BEAM_MOE_DOWN_STREAMED
+#define BEAM_MOE_DOWN_STREAMED 0
+#endif
 
 namespace beam {
 namespace {
@@ -35,12 +42,46 @@ struct MoePlan {
   int* n_jobs;     // [1]
 };
 
+// Exclusive scan over the block of one int per thread; *total gets the sum. ws: 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  __syncthreads();
+  if (lane == 31) ws[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    int t = lane < nw ? ws[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    if (lane < nw) ws[lane] = t;               // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int before = wid > 0 ? ws[wid - 1] : 0;
+  *total = ws[(blockDim.x >> 5) - 1];
+  return before + inc - v;
+}
+
+// Buckets the P = T*k (token, slot) pairs by expert. One CTA of kPlanThreads threads, each
+// owning kPlanItems consecutive experts (E <= 4096).
+constexpr int kPlanItems = 4;
 __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* __restrict__ idx,
                                                                 int P, int E, MoePlan pl) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sh[];
-  int* cnt = sh;            // [E]
-  int* off = sh + E;        // [E+1]
-  int* fill = sh + 2 * E + 1;  // [E]
+  int* cnt = sh;               // [E]
+  int* off = sh + E;           // [E]
+  int* fill = sh + 2 * E;      // [E]
+  __shared__ int scan_ws[32];
   for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; fill[e] = 0; }
   __syncthreads();
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
@@ -49,28 +90,32 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* _
     atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, na = 0;
-    for (int e = 0; e < E; ++e) {
-      off[e] = o;
+  const int e0 = threadIdx.x * kPlanItems;
+  int c_sum = 0, a_sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPlanItems; ++j) {
+    const int e = e0 + j;
+    if (e < E) { c_sum += cnt[e]; a_sum += cnt[e] > 0; }
+  }
+  int c_tot, a_tot;
+  int c_off = block_excl_scan(c_sum, scan_ws, &c_tot);
+  int a_off = block_excl_scan(a_sum, scan_ws, &a_tot);
+#pragma unroll
+  for (int j = 0; j < kPlanItems; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      off[e] = c_off;
       if (cnt[e] > 0) {
-        pl.active[na] = e;
-        pl.act_off[na] = o;
-        ++na;
+        pl.active[a_off] = e;
+        pl.act_off[a_off] = c_off;
+        ++a_off;
       }
-      o += cnt[e];
+      c_off += cnt[e];
     }
-    off[E] = o;
-    pl.act_off[na] = o;
-    *pl.n_active = na;
-    if (pl.jobs != nullptr) {
-      int nj = 0;
-      for (int a = 0; a < na; ++a) {
-        const int e = pl.active[a], o0 = pl.act_off[a], c = pl.act_off[a + 1] - o0;
-        for (int r = 0; r < c; r += 128) pl.jobs[nj++] = make_int4(e, o0 + r, min(128, c - r), 0);
-      }
-      *pl.n_jobs = nj;
-    }
+  }
+  if (threadIdx.x == 0) {
+    pl.act_off[a_tot] = c_tot;
+    *pl.n_active = a_tot;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
@@ -79,13 +124,28 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* _
     const int slot = atomicAdd(&fill[e], 1);
     pl.pairs[off[e] + slot] = i;
   }
+  if (pl.jobs != nullptr) {
+    __threadfence_block();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int nj = 0;
+      for (int a = 0; a < a_tot; ++a) {
+        const int e = pl.active[a], o0 = pl.act_off[a], c = pl.act_off[a + 1] - o0;
+        for (int r = 0; r < c; r += 128) pl.jobs[nj++] = make_int4(e, o0 + r, min(128, c - r), 0);
+      }
+      *pl.n_jobs = nj;
+    }
+  }
 }
 
-// grid (ceil(F / (8 * FPW)), max active experts); warp handles FPW consecutive f units.
-template <int U>
+// grid (ceil(F / 8), max active experts); warp per (active expert, f): gate row f and up
+// row F+f, dotted with up to NT of the expert's pairs per weight pass.
+template <int U, int NT>
 __global__ void __launch_bounds__(256) moe_gate_up_kernel(
     const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
     MoePlan pl, uint16_t* __restrict__ a) {
+  pdl_trigger();
+  pdl_wait();
   const int ai = blockIdx.y;
   if (ai >= *pl.n_active) return;
   const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -95,19 +155,19 @@ __global__ void __launch_bounds__(256) moe_gate_up_kernel(
   const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
   const uint16_t* base = w_gu + size_t(e) * 2 * F * H;
   const uint16_t* w[2] = {base + size_t(f) * H, base + size_t(F + f) * H};
-  for (int pp = p0; pp < p1; pp += kPairTile) {
-    const int nt = min(kPairTile, p1 - pp);
-    int pid[kPairTile];
-    const uint16_t* x[kPairTile];
+  for (int pp = p0; pp < p1; pp += NT) {
+    const int nt = min(NT, p1 - pp);
+    int pid[NT];
+    const uint16_t* x[NT];
 #pragma unroll
-    for (int i = 0; i < kPairTile; ++i) {
+    for (int i = 0; i < NT; ++i) {
       pid[i] = pl.pairs[pp + min(i, nt - 1)];
       x[i] = u + size_t(pid[i] / k) * H;
     }
-    float acc[2][kPairTile];
-    warp_dot<2, kPairTile, U>(w, x, nt, H, acc);
+    float acc[2][NT];
+    warp_dot<2, NT, U>(w, x, nt, H, acc);
 #pragma unroll
-    for (int i = 0; i < kPairTile; ++i)
+    for (int i = 0; i < NT; ++i)
       if (i < nt && lane == i) a[size_t(pid[i]) * F + f] = f2bf(siluf_(acc[0][i]) * acc[1][i]);
   }
 }
@@ -119,6 +179,8 @@ __global__ void __launch_bounds__(256) moe_down_combine_kernel(
     const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn,
     const float* __restrict__ topk_w, int T, int H, int F, int k, MoePlan pl,
     uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float ysh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 8 + warp;
@@ -156,39 +218,48 @@ __global__ void __launch_bounds__(256) moe_down_combine_kernel(
   }
 }
 
-// Unfused form for many pairs: y[pair][h] (FP32) to the workspace, then a combine pass.
-template <int U>
+// Unfused form: warp per (active expert, NR consecutive rows h); y[pair][h] (FP32) to the
+// workspace, then a combine pass.
+template <int U, int NT, int NR>
 __global__ void __launch_bounds__(256) moe_down_kernel(const uint16_t* __restrict__ a,
                                                        const uint16_t* __restrict__ w_dn, int H,
                                                        int F, MoePlan pl, float* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const int ai = blockIdx.y;
   if (ai >= *pl.n_active) return;
-  const int h = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (h >= H) return;
+  const int h0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * NR;
+  if (h0 >= H) return;
   const int lane = threadIdx.x & 31;
   const int e = pl.active[ai];
   const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
-  const uint16_t* w[1] = {w_dn + (size_t(e) * H + h) * F};
-  for (int pp = p0; pp < p1; pp += kPairTile) {
-    const int nt = min(kPairTile, p1 - pp);
-    int pid[kPairTile];
-    const uint16_t* x[kPairTile];
+  const uint16_t* w[NR];
 #pragma unroll
-    for (int i = 0; i < kPairTile; ++i) {
+  for (int r = 0; r < NR; ++r) w[r] = w_dn + (size_t(e) * H + min(h0 + r, H - 1)) * F;
+  for (int pp = p0; pp < p1; pp += NT) {
+    const int nt = min(NT, p1 - pp);
+    int pid[NT];
+    const uint16_t* x[NT];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
       pid[i] = pl.pairs[pp + min(i, nt - 1)];
       x[i] = a + size_t(pid[i]) * F;
     }
-    float acc[1][kPairTile];
-    warp_dot<1, kPairTile, U>(w, x, nt, F, acc);
+    float acc[NR][NT];
+    warp_dot<NR, NT, U>(w, x, nt, F, acc);
 #pragma unroll
-    for (int i = 0; i < kPairTile; ++i)
-      if (i < nt && lane == i) y[size_t(pid[i]) * H + h] = acc[0][i];
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+        if (i < nt && lane == r * NT + i && h0 + r < H) y[size_t(pid[i]) * H + h0 + r] = acc[r][i];
   }
 }
 
 __global__ void moe_combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                                    const int32_t* __restrict__ idx, int T, int H, int k, int E,
                                    uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= size_t(T) * H) return;
   const int t = int(i / H), h = int(i - size_t(t) * H);
@@ -204,6 +275,8 @@ __global__ void moe_combine_kernel(const float* __restrict__ y, const float* __r
 // Rows of u in expert-sorted pair order: us[i] = u[pairs[i] / k].
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ u, int H, int k, MoePlan pl,
                                    int P, uint16_t* __restrict__ us) {
+  pdl_trigger();
+  pdl_wait();
   const int nv = H / 8;
   const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= size_t(P) * nv) return;
@@ -214,6 +287,85 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ u, int H, int k,
 }
 
 int max_jobs(int P, int E) { return (P + 127) / 128 + (P < E ? P : E); }
+
+// Streamed decode form (T <= 4, so an expert meets at most 4 pairs): rows are the
+// (active expert, f) gate/up pairs, spread evenly over every warp of a persistent grid.
+__global__ void __launch_bounds__(sg::kWarps * 32, 1)
+    moe_sg_gate_up_kernel(const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu,
+                          int H, int F, int k, MoePlan pl, uint16_t* __restrict__ act) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring;
+  uint64_t* full;
+  sg::warp_ring(smem, ring, full);
+  int r0, r1;
+  sg::warp_share(*pl.n_active * F, r0, r1);
+  const int lane = threadIdx.x & 31;
+  auto job = [&](int r) {
+    sg::RowJob j;
+    const int a = r / F, f = r - a * F;
+    const int e = pl.active[a], p0 = pl.act_off[a];
+    const int c = min(pl.act_off[a + 1] - p0, sg::kMaxT);
+    const uint16_t* base = w_gu + size_t(e) * 2 * F * H;
+    j.w[0] = base + size_t(f) * H;
+    j.w[1] = base + size_t(F + f) * H;
+#pragma unroll
+    for (int i = 0; i < sg::kMaxT; ++i) {
+      j.pid[i] = pl.pairs[p0 + min(i, c - 1)];
+      j.x[i] = u + size_t(j.pid[i] / k) * H;
+    }
+    j.nt = c;
+    return j;
+  };
+  auto epi = [&](int r, const sg::RowJob& jb, const float (&acc)[2][sg::kMaxT]) {
+    const int f = r % F;
+#pragma unroll
+    for (int i = 0; i < sg::kMaxT; ++i)
+      if (lane == i && i < jb.nt)
+        act[size_t(jb.pid[i]) * F + f] = f2bf(siluf_(acc[0][i]) * acc[1][i]);
+  };
+  sg::stream_rows<2, false>(r0, r1, H, ring, full, job, epi);
+}
+
+// Rows are (active expert, h) rows of W_down; y[pair][h] in FP32 for the combine.
+__global__ void __launch_bounds__(sg::kWarps * 32, 1)
+    moe_sg_down_kernel(const uint16_t* __restrict__ act, const uint16_t* __restrict__ w_dn, int H,
+                       int F, MoePlan pl, float* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring;
+  uint64_t* full;
+  sg::warp_ring(smem, ring, full);
+  int r0, r1;
+  sg::warp_share(*pl.n_active * H, r0, r1);
+  const int lane = threadIdx.x & 31;
+  auto job = [&](int r) {
+    sg::RowJob j;
+    const int a = r / H, h = r - a * H;
+    const int e = pl.active[a], p0 = pl.act_off[a];
+    const int c = min(pl.act_off[a + 1] - p0, sg::kMaxT);
+    j.w[0] = j.w[1] = w_dn + (size_t(e) * H + h) * F;
+#pragma unroll
+    for (int i = 0; i < sg::kMaxT; ++i) {
+      j.pid[i] = pl.pairs[p0 + min(i, c - 1)];
+      j.x[i] = act + size_t(j.pid[i]) * F;
+    }
+    j.nt = c;
+    return j;
+  };
+  auto epi = [&](int r, const sg::RowJob& jb, const float (&acc)[1][sg::kMaxT]) {
+    const int h = r % H;
+#pragma unroll
+    for (int i = 0; i < sg::kMaxT; ++i)
+      if (lane == i && i < jb.nt) y[size_t(jb.pid[i]) * H + h] = acc[0][i];
+  };
+  sg::stream_rows<1, false>(r0, r1, F, ring, full, job, epi);
+}
+
+// Decode form for up to kMoeSmallT tokens (every expert then meets at most kMoeSmallT pairs).
+constexpr int kMoeSmallT = 4;
 
 MoePlan carve_plan(Carver& cv, int E, int P, bool grouped) {
   MoePlan pl;
@@ -237,7 +389,8 @@ size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
     b += align_up(size_t(max_jobs(int(P), int(E))) * 16, 256) + 256;
     b += align_up(P * c->hidden * 2, 256);                       // gathered inputs
   }
-  if (grouped || P > size_t(kFusedMaxPairs)) b += align_up(P * c->hidden * 4, 256);
+  if (grouped || P > size_t(kFusedMaxPairs) || T <= kMoeSmallT)
+    b += align_up(P * c->hidden * 4, 256);
   return b;
 }
 
@@ -268,17 +421,16 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
   MoePlan pl = carve_plan(cv, E, P, grouped);
   uint16_t* act = cv.take<uint16_t>(size_t(P) * F);
   uint16_t* us = grouped ? cv.take<uint16_t>(size_t(P) * H) : nullptr;
-  float* y = (grouped || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
+  const bool small = !grouped && T <= kMoeSmallT;
+  float* y = (grouped || small || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
   if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   const int max_active = P < E ? P : E;
-  moe_plan_kernel<<<1, kPlanThreads, (3 * E + 1) * sizeof(int), st>>>(topk_idx, P, E, pl);
-  note_launches(1);
+  launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
   if (grouped) {
     // gather -> grouped gate/up GEMM with the SwiGLU epilogue (sorted rows) -> grouped down
     // GEMM writing each row back to its (token, slot) pair -> weighted combine
     const size_t nv = size_t(P) * (H / 8);
-    gather_rows_kernel<<<unsigned((nv + 255) / 256), 256, 0, st>>>(u, H, k, pl, P, us);
-    note_launches(1);
+    launch_pdl(gather_rows_kernel, dim3(unsigned((nv + 255) / 256)), dim3(256), 0, st, u, H, k, pl, P, us);
     const int mj = max_jobs(P, E);
     if (tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, w_gate_up, E * 2 * F, 2 * F, H, pl.jobs,
                          pl.n_jobs, mj, F, F, nullptr, act, F, st) != cudaSuccess)
@@ -287,29 +439,52 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
                          0, pl.pairs, y, H, st) != cudaSuccess)
       return BEAM_ERR_CUDA;
     const size_t n = size_t(T) * H;
-    moe_combine_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(y, topk_w, topk_idx, T, H, k,
+    launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w, topk_idx, T, H, k,
                                                                   E, out);
-    note_launches(1);
     return launch_status();
   }
-  moe_gate_up_kernel<4><<<dim3((F + 7) / 8, max_active), 256, 0, st>>>(u, w_gate_up, H, F, k, pl,
-                                                                      act);
-  note_launches(1);
+  if (small) {
+    // decode: plan -> gate/up (SwiGLU) -> down rows per (expert, h) -> combine
+    if (T == 1)
+      launch_pdl(moe_gate_up_kernel<4, 1>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
+                 w_gate_up, H, F, k, pl, act);
+    else
+      launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
+                 w_gate_up, H, F, k, pl, act);
+#if BEAM_MOE_DOWN_STREAMED
+    if (cudaFuncSetAttribute(moe_sg_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             sg::kSmem) != cudaSuccess)
+      return BEAM_ERR_CUDA;
+    launch_pdl(moe_sg_down_kernel, dim3(num_sms_cached()), dim3(sg::kWarps * 32), sg::kSmem, st,
+               act, w_down, H, F, pl, y);
+#else
+    if (T == 1)
+      launch_pdl(moe_down_kernel<8, 1, 2>, dim3((H + 15) / 16, max_active), dim3(256), 0, st,
+                 act, w_down, H, F, pl, y);
+    else
+      launch_pdl(moe_down_kernel<8, 4, 1>, dim3((H + 7) / 8, max_active), dim3(256), 0, st, act,
+                 w_down, H, F, pl, y);
+#endif
+    const size_t n = size_t(T) * H;
+    launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w,
+               topk_idx, T, H, k, E, out);
+    return launch_status();
+  }
+  launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
+             w_gate_up, H, F, k, pl, act);
   if (P <= kFusedMaxPairs) {
     const int smem = 8 * P * int(sizeof(float));
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(moe_down_combine_kernel<8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return BEAM_ERR_CUDA;
-    moe_down_combine_kernel<8><<<(H + 7) / 8, 256, smem, st>>>(act, w_down, topk_w, T, H, F, k,
+    launch_pdl(moe_down_combine_kernel<8>, dim3((H + 7) / 8), dim3(256), smem, st, act, w_down, topk_w, T, H, F, k,
                                                               pl, out);
-    note_launches(1);
   } else {
-    moe_down_kernel<8><<<dim3((H + 7) / 8, max_active), 256, 0, st>>>(act, w_down, H, F, pl, y);
+    launch_pdl(moe_down_kernel<8, 4, 1>, dim3((H + 7) / 8, max_active), dim3(256), 0, st, act, w_down, H, F, pl, y);
     const size_t n = size_t(T) * H;
-    moe_combine_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(y, topk_w, topk_idx, T, H, k,
+    launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w, topk_idx, T, H, k,
                                                                   E, out);
-    note_launches(2);
   }
   return launch_status();
 }

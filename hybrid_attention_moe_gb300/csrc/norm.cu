@@ -10,31 +10,47 @@ namespace {
 
 constexpr int kNormMaxVec = 4;  // 16-byte vectors held per thread
 
-// One CTA per token row. Each thread keeps up to kNormMaxVec vectors of 8 values.
+// One CTA per token row. Each thread holds up to kNormMaxVec 16-byte vectors of every input;
+// all loads are issued up front (the gains before the programmatic-launch wait, since no
+// kernel writes them), so the row costs one memory round trip plus two block reductions.
 __global__ void __launch_bounds__(512) boundary_norm_kernel(
     const uint16_t* __restrict__ x, uint16_t* __restrict__ h, uint16_t* __restrict__ u_out,
     const uint16_t* __restrict__ w_post, const uint16_t* __restrict__ w_pre, int H,
     float c_keep, float c_add, float eps) {
+  pdl_trigger();
   __shared__ float red[32];
   const int nvec = H >> 3;
   const size_t row = size_t(blockIdx.x) * H;
-  float hv[kNormMaxVec][8];
-
-  // residual stream in
+  uint4 wpo[kNormMaxVec], wpr[kNormMaxVec], xr[kNormMaxVec], hr[kNormMaxVec];
 #pragma unroll
   for (int j = 0; j < kNormMaxVec; ++j) {
     const int i = threadIdx.x + j * blockDim.x;
-    if (i < nvec) unpack8(*reinterpret_cast<const uint4*>(h + row + size_t(i) * 8), hv[j]);
+    if (i < nvec) {
+      if (x != nullptr) wpo[j] = __ldg(reinterpret_cast<const uint4*>(w_post) + i);
+      if (u_out != nullptr) wpr[j] = __ldg(reinterpret_cast<const uint4*>(w_pre) + i);
+    }
   }
+  pdl_wait();
+#pragma unroll
+  for (int j = 0; j < kNormMaxVec; ++j) {
+    const int i = threadIdx.x + j * blockDim.x;
+    if (i < nvec) {
+      hr[j] = *reinterpret_cast<const uint4*>(h + row + size_t(i) * 8);
+      if (x != nullptr) xr[j] = *reinterpret_cast<const uint4*>(x + row + size_t(i) * 8);
+    }
+  }
+  float hv[kNormMaxVec][8];
+#pragma unroll
+  for (int j = 0; j < kNormMaxVec; ++j)
+    if (threadIdx.x + j * blockDim.x < nvec) unpack8(hr[j], hv[j]);
 
   if (x != nullptr) {
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kNormMaxVec; ++j) {
-      const int i = threadIdx.x + j * blockDim.x;
-      if (i < nvec) {
+      if (threadIdx.x + j * blockDim.x < nvec) {
         float xv[8];
-        unpack8(*reinterpret_cast<const uint4*>(x + row + size_t(i) * 8), xv);
+        unpack8(xr[j], xv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) ss = fmaf(xv[e], xv[e], ss);
       }
@@ -45,8 +61,8 @@ __global__ void __launch_bounds__(512) boundary_norm_kernel(
       const int i = threadIdx.x + j * blockDim.x;
       if (i < nvec) {
         float xv[8], wv[8];
-        unpack8(*reinterpret_cast<const uint4*>(x + row + size_t(i) * 8), xv);  // L1 hit
-        unpack8(*reinterpret_cast<const uint4*>(w_post + size_t(i) * 8), wv);
+        unpack8(xr[j], xv);
+        unpack8(wpo[j], wv);
         uint32_t packed[4];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -65,8 +81,7 @@ __global__ void __launch_bounds__(512) boundary_norm_kernel(
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kNormMaxVec; ++j) {
-      const int i = threadIdx.x + j * blockDim.x;
-      if (i < nvec) {
+      if (threadIdx.x + j * blockDim.x < nvec) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ss = fmaf(hv[j][e], hv[j][e], ss);
       }
@@ -77,7 +92,7 @@ __global__ void __launch_bounds__(512) boundary_norm_kernel(
       const int i = threadIdx.x + j * blockDim.x;
       if (i < nvec) {
         float wv[8];
-        unpack8(*reinterpret_cast<const uint4*>(w_pre + size_t(i) * 8), wv);
+        unpack8(wpr[j], wv);
         uint32_t packed[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -112,8 +127,7 @@ extern "C" beam_status beam_boundary_norm(const beam_bf16* x, beam_bf16* h, beam
   const double nd = double(n);
   const float c_keep = float(sqrt((nd - 1.0) / nd));
   const float c_add = float(1.0 / sqrt(nd));
-  boundary_norm_kernel<<<T, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+  launch_pdl(boundary_norm_kernel, dim3(T), dim3(threads), 0, reinterpret_cast<cudaStream_t>(stream), 
       x, h, u_out, w_post, w_pre, H, c_keep, c_add, eps);
-  note_launches(1);
   return launch_status();
 }

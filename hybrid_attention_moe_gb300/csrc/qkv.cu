@@ -13,17 +13,24 @@ namespace {
 
 constexpr int kMaxHalf = 64;  // D/2 for D = 128
 
-// One CTA per token. z holds the projection (fp32) of the token: rows Q | K | V | gate.
-// Warps take (kind, head) slots: n_q query heads, n_kv key heads, n_kv value heads and n_q
-// gate heads. Lane l holds elements l, l+32, ... of the head (VPL = D/32 values), so the
+// theta^(-2i/D), i < D/2, computed on the host in double and passed by value.
+struct RopeTab {
+  double inv[kMaxHalf];
+};
+
+// Grid (token, slot group of 8): z holds the projection (fp32) of the token, rows
+// Q | K | V | gate. Each warp takes one (kind, head) slot: n_q query heads, n_kv key heads,
+// n_kv value heads and n_q gate heads. Lane l holds elements l, l+32, ... of the head (VPL = D/32 values), so the
 // RoPE partner i + D/2 of element l + 32j is element j + VPL/2 of the same lane.
 template <int VPL>
 __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
     const float* __restrict__ z, int rows, const uint16_t* __restrict__ qnw,
     const uint16_t* __restrict__ knw, const int32_t* __restrict__ seq_id,
-    const int32_t* __restrict__ pos, int n_q, int n_kv, int nope, float theta, float ss_base,
+    const int32_t* __restrict__ pos, int n_q, int n_kv, int nope, RopeTab rope, float ss_base,
     float ss_exp, float eps, uint16_t* __restrict__ q_out, uint16_t* __restrict__ g_out,
     beam_kv_cache kc) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int D = VPL * 32;
   constexpr int HALF = D / 2;
   __shared__ float cs[kMaxHalf], sn[kMaxHalf];
@@ -42,8 +49,7 @@ __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
     // angle (p-1) * theta^(-2i/D), formed and reduced modulo 2*pi in double precision so
     // that positions around 1e5 keep full single-precision accuracy in cos/sin
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-      const double inv = exp2(-(2.0 * i / D) * log2((double)theta));
-      double ang = double(p - 1) * inv;
+      double ang = double(p - 1) * rope.inv[i];
       const double two_pi = 6.283185307179586476925;
       ang -= two_pi * rint(ang / two_pi);
       float sv, cv;
@@ -59,7 +65,8 @@ __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
   const int lane = threadIdx.x & 31;
   const int nslots = 2 * n_q + 2 * n_kv;
   const float* zt = z + size_t(t) * rows;
-  for (int slot = threadIdx.x >> 5; slot < nslots; slot += blockDim.x >> 5) {
+  for (int slot = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5); slot < nslots;
+       slot += gridDim.y * (blockDim.x >> 5)) {
     int kind, head, row0;
     if (slot < n_q) { kind = 0; head = slot; row0 = head * D; }
     else if (slot < n_q + n_kv) { kind = 1; head = slot - n_q; row0 = (n_q + head) * D; }
@@ -151,14 +158,16 @@ extern "C" beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16*
           : launch_gemv<kOutF32>(w_qkvg, rows, H, u, T, z, nullptr, rows, s);
   if (ge != cudaSuccess) return BEAM_ERR_CUDA;
   const int nope = cfg->kind == BEAM_ATTN_NOPE_SSMAX;
+  RopeTab rope;
+  for (int i = 0; i < D / 2; ++i)
+    rope.inv[i] = pow(double(cfg->rope_theta), -2.0 * double(i) / double(D));
   if (D == 128)
-    qkv_epilogue_kernel<4><<<T, 256, 0, s>>>(z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
-                                             cfg->n_kv, nope, cfg->rope_theta, cfg->ssmax_base,
+    launch_pdl(qkv_epilogue_kernel<4>, dim3(T, (2 * cfg->n_q + 2 * cfg->n_kv + 7) / 8), dim3(256), 0, s, z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
+                                             cfg->n_kv, nope, rope, cfg->ssmax_base,
                                              cfg->ssmax_exp, cfg->eps, q_out, g_out, *cache);
   else
-    qkv_epilogue_kernel<2><<<T, 256, 0, s>>>(z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
-                                             cfg->n_kv, nope, cfg->rope_theta, cfg->ssmax_base,
+    launch_pdl(qkv_epilogue_kernel<2>, dim3(T, (2 * cfg->n_q + 2 * cfg->n_kv + 7) / 8), dim3(256), 0, s, z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
+                                             cfg->n_kv, nope, rope, cfg->ssmax_base,
                                              cfg->ssmax_exp, cfg->eps, q_out, g_out, *cache);
-  note_launches(1);
   return launch_status();
 }

@@ -112,68 +112,79 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 constexpr int kMaxE = 1024, kMaxG = 32, kMaxK = 32;
 
-// One warp per token. s = sigmoid(logit), b = s + bias (FP32); group score = top-2 sum of b.
-__global__ void __launch_bounds__(128) router_topk_kernel(
+// One CTA of 256 threads per token. s = sigmoid(logit), b = s + bias (FP32); group score =
+// sum of the group's two largest b; keep the kG best groups; select the k best b among their
+// experts; every choice breaks ties towards the lower index.
+constexpr int kTopkThreads = 256;
+__global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
     const float* __restrict__ logits, const float* __restrict__ corr_bias, int T, int E, int G,
     int kG, int k, float scale, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  __shared__ float sb[4][kMaxE];
-  __shared__ float ss[4][kMaxE];
-  __shared__ float sg[4][kMaxG];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 4 + warp;
-  if (t >= T) return;
-  float* b = sb[warp];
-  float* s = ss[warp];
-  for (int e = lane; e < E; e += 32) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sb[kMaxE], ss[kMaxE], sg[kMaxG];
+  __shared__ int kept[kMaxG];
+  __shared__ int sel_i[kMaxK];
+  const int t = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const float z = logits[size_t(t) * E + e];
     const float sv = 1.0f / (1.0f + expf(-z));
-    s[e] = sv;
-    b[e] = sv + corr_bias[e];
+    ss[e] = sv;
+    sb[e] = sv + corr_bias[e];
   }
-  __syncwarp();
+  __syncthreads();
   const int per = E / G;
-  if (lane < G) {
+  if (threadIdx.x < G) {
     float m1 = -INFINITY, m2 = -INFINITY;
     for (int j = 0; j < per; ++j) {
-      const float v = b[lane * per + j];
+      const float v = sb[threadIdx.x * per + j];
       if (v > m1) { m2 = m1; m1 = v; } else if (v > m2) { m2 = v; }
     }
-    sg[warp][lane] = m1 + m2;
+    sg[threadIdx.x] = m1 + m2;
   }
-  __syncwarp();
-  // keep the kG best groups
+  __syncthreads();
+  if (warp != 0) return;
+  // kG best groups, listed in increasing group order
   unsigned keep = 0u;
   for (int r = 0; r < kG; ++r) {
-    float v = (lane < G && !((keep >> lane) & 1u)) ? sg[warp][lane] : -INFINITY;
+    float v = (lane < G && !((keep >> lane) & 1u)) ? sg[lane] : -INFINITY;
     int i = lane < G ? lane : 0x7fffffff;
     warp_argmax(v, i);
     keep |= 1u << i;
   }
-  // top-k experts of the kept groups, by b, ties to the lower index
-  float ssum = 0.f;
-  int sel_i[kMaxK];
-  float sel_s[kMaxK];
+  if (lane == 0) {
+    int n = 0;
+    for (int g = 0; g < G; ++g)
+      if ((keep >> g) & 1u) kept[n++] = g;
+  }
+  __syncwarp();
+  // candidates c = lane + 32 j over the kept groups' experts
+  const int ncand = kG * per;
+  unsigned taken = 0u;
   for (int r = 0; r < k; ++r) {
     float v = -INFINITY;
-    int i = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      if (!((keep >> (e / per)) & 1u)) continue;
-      const float be = b[e];
-      if (be > v || (be == v && e < i)) { v = be; i = e; }
+    int best = 0x7fffffff;
+    for (int j = 0; lane + 32 * j < ncand; ++j) {
+      if ((taken >> j) & 1u) continue;
+      const int c = lane + 32 * j;
+      const int e = kept[c / per] * per + c % per;
+      const float be = sb[e];
+      if (be > v || (be == v && e < best)) { v = be; best = e; }
     }
-    warp_argmax(v, i);
-    sel_i[r] = i;
-    sel_s[r] = s[i];
-    ssum += s[i];
-    __syncwarp();
-    if (lane == 0) b[i] = -INFINITY;  // taken
-    __syncwarp();
+    warp_argmax(v, best);
+    for (int j = 0; lane + 32 * j < ncand; ++j) {
+      const int c = lane + 32 * j;
+      if (kept[c / per] * per + c % per == best) taken |= 1u << j;
+    }
+    if (lane == 0) sel_i[r] = best;
   }
-  if (lane == 0) {
-    for (int r = 0; r < k; ++r) {
-      topk_idx[size_t(t) * k + r] = sel_i[r];
-      topk_w[size_t(t) * k + r] = sel_s[r] / ssum * scale;
-    }
+  __syncwarp();
+  if (lane < k) {
+    float ssum = 0.f;
+    for (int r = 0; r < k; ++r) ssum += ss[sel_i[r]];   // selection order, as every lane
+    const int e = sel_i[lane];
+    topk_idx[size_t(t) * k + lane] = e;
+    topk_w[size_t(t) * k + lane] = ss[e] / ssum * scale;
   }
 }
 
@@ -215,7 +226,7 @@ extern "C" beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u,
         u, w_router, T, H, E, lg);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
-  router_topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
+  router_topk_kernel<<<T, kTopkThreads, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
                                                   cfg->topk, cfg->route_scale, topk_idx, topk_w);
   note_launches(1);
   return launch_status();
@@ -289,7 +300,7 @@ extern "C" beam_status beam_route_noalloc(const beam_layer_cfg* cfg, const beam_
         u, w_router, T, H, E, lg);
   note_launches(1);
   if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
-  router_topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
+  router_topk_kernel<<<T, kTopkThreads, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
                                                   cfg->topk, cfg->route_scale, topk_idx, topk_w);
   note_launches(1);
   return launch_status();

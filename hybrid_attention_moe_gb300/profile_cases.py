@@ -79,7 +79,8 @@ def main():
         pos = torch.full((1,), ctx + 1, dtype=torch.int32, device=dev)
         out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(B.workspace_bytes(cf, 1, ctx + 1), dtype=torch.uint8, device=dev)
-        fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + 1, W["w_o"], out, ws)  # noqa: E731
+        fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + 1, W["w_o"], out, ws,  # noqa: E731
+                                 max_q_per_seq=1)
     elif c == "route_decode":
         R = synth.router_weights(shape, 3, 0, device=dev)
         u = synth.activations(1, H, 0, "u", dev)

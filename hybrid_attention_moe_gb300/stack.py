@@ -65,7 +65,7 @@ class BeamStack:
             self._bufs = {T: b}
         return b
 
-    def layer(self, i, b, seq_id, pos, max_pos, ws, stream=None, trace=None):
+    def layer(self, i, b, seq_id, pos, max_pos, ws, stream=None, trace=None, max_q_per_seq=None):
         """The i-th layer held (global index l): from (h, u = its attention pre-norm) to
         (h, u of the next layer)."""
         W, cfg, kc = self.W[i], self.cfgs[i], self.caches[i]
@@ -73,7 +73,7 @@ class BeamStack:
         B.beam_qkv_gate(cfg, b["u"], W["w_qkvg"], W["q_norm"], W["k_norm"], seq_id, pos, b["q"],
                         b["g"], kc, ws, stream)
         B.beam_attn(cfg, b["q"], b["g"], W["gate_bias"], kc, seq_id, pos, max_pos, W["w_o"],
-                    b["a"], ws, stream)
+                    b["a"], ws, stream, max_q_per_seq)
         B.beam_boundary_norm(b["a"], b["h"], b["u"], W["attn_post"], W["mlp_pre"], 2 * l + 2,
                              cfg.eps, stream)
         if trace is not None:
@@ -94,10 +94,11 @@ class BeamStack:
         B.beam_boundary_norm(b["m"], b["h"], b["u"] if nxt is not None else None,
                              W["mlp_post"], nxt, 2 * l + 3, cfg.eps, stream)
 
-    def forward(self, e, seq_id, pos, max_pos, stream=None, trace=None):
+    def forward(self, e, seq_id, pos, max_pos, stream=None, trace=None, max_q_per_seq=None):
         """Runs the held layers for the tokens (seq_id, pos). e [T][H] (bf16) is the residual
         stream entering the first held layer (the embedding when first_layer is 0); it gets
-        its pre-norm first. Returns h after the last residual addition (an internal buffer)."""
+        its pre-norm first. max_q_per_seq: most tokens of one sequence (1 for a decode batch;
+        None = T). Returns h after the last residual addition (an internal buffer)."""
         T = e.shape[0]
         b = self.buffers(T)
         ws = self.ws.get(B.workspace_bytes(self.cfgs[0], T, max_pos))
@@ -105,5 +106,5 @@ class BeamStack:
         B.beam_boundary_norm(None, b["h"], b["u"], None, self.W[0]["attn_pre"], 1,
                              self.cfgs[0].eps, stream)
         for i in range(self.L):
-            self.layer(i, b, seq_id, pos, max_pos, ws, stream, trace)
+            self.layer(i, b, seq_id, pos, max_pos, ws, stream, trace, max_q_per_seq)
         return b["h"]

@@ -146,12 +146,17 @@ beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16* u,
  *  q, g      (device) outputs of beam_qkv_gate for the same tokens.
  *  gate_bias (device) [n_q] bf16.
  *  max_pos   host-side upper bound of pos[] (sizes the key split); larger pos are flagged.
+ *  max_q_per_seq  host-side upper bound of the number of the call's tokens that belong to one
+ *            sequence (1 for a decode batch). Up to 4, every token runs split-K over its keys;
+ *            above, tokens are taken in tiles of 16 consecutive tokens that share K/V tiles,
+ *            which expects the tokens of a sequence to be consecutive in the call (any order
+ *            is still computed correctly, only more slowly).
  *  w_o       (device) [H][n_q*D] bf16.   out (device) [T][H] bf16. */
 beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q, const beam_bf16* g,
                       const beam_bf16* gate_bias, const beam_kv_cache* cache,
                       const int32_t* seq_id, const int32_t* pos, int T, int max_pos,
-                      const beam_bf16* w_o, beam_bf16* out, void* ws, size_t ws_bytes,
-                      beam_stream_t stream);
+                      int max_q_per_seq, const beam_bf16* w_o, beam_bf16* out, void* ws,
+                      size_t ws_bytes, beam_stream_t stream);
 
 /* FP32 router, DeepSeek-V3 style (Beam page, MoE section; change 4): logits = u W_r^T in
  * FP32, s = sigmoid(logits), b = s + corr_bias. Experts form n_groups contiguous groups;

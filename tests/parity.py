@@ -59,6 +59,69 @@ def oracle_cache(kc):
                      window=kc.window)
 
 
+def route_margins_per_token(cfg, b):
+    """Per token: the kept/dropped group-score gap and the k-th/(k+1)-th expert gap inside
+    the kept groups, from biased scores b [T][E]."""
+    per = cfg.n_experts // cfg.n_groups
+    T = b.shape[0]
+    gg, eg = np.zeros(T), np.zeros(T)
+    for t in range(T):
+        bt = b[t].astype(np.float64)
+        gsc = np.sort(bt.reshape(cfg.n_groups, per), axis=1)[:, -2:].sum(axis=1)
+        order = np.lexsort((np.arange(cfg.n_groups), -gsc))
+        gg[t] = gsc[order[cfg.topk_groups - 1]] - gsc[order[cfg.topk_groups]]
+        cand = np.sort(np.concatenate([bt[g * per:(g + 1) * per]
+                                       for g in order[: cfg.topk_groups]]))[::-1]
+        eg[t] = cand[cfg.topk - 1] - cand[cfg.topk]
+    return gg, eg
+
+
+def routing_stable(cfg, logits_ref, logits_alts, corr_bias, factor=3.0):
+    """True when every token's routing is decided by more than the perturbation moves its
+    scores: expert gap >= max(1e-6, factor * shift_t) and group gap >= max(1e-6,
+    2 * factor * shift_t), shift_t = the token's largest sigmoid-score change."""
+    sig = lambda z: 1.0 / (1.0 + np.exp(-np.asarray(z, np.float64)))   # noqa: E731
+    s0 = sig(logits_ref)
+    shift = np.zeros(s0.shape[0])
+    for la in logits_alts:
+        shift = np.maximum(shift, np.max(np.abs(sig(la) - s0), axis=1))
+    b = s0 + np.asarray(corr_bias, np.float64)
+    gg, eg = route_margins_per_token(cfg, b)
+    return bool(np.all(gg >= np.maximum(1e-6, 2 * factor * shift)) and
+                np.all(eg >= np.maximum(1e-6, factor * shift)))
+
+
+def routing_tolerance(cfg, logits_ref, logits_alts, corr_bias, factor=3.0):
+    """Per token: (stable, tol). tol = factor x the token's largest sigmoid-score change under
+    FP32-level perturbation; stable when its expert gap >= max(1e-6, tol) and its group gap
+    >= max(1e-6, 2 tol)."""
+    sig = lambda z: 1.0 / (1.0 + np.exp(-np.asarray(z, np.float64)))   # noqa: E731
+    s0 = sig(logits_ref)
+    shift = np.zeros(s0.shape[0])
+    for la in logits_alts:
+        shift = np.maximum(shift, np.max(np.abs(sig(la) - s0), axis=1))
+    tol = factor * shift
+    gg, eg = route_margins_per_token(cfg, s0 + np.asarray(corr_bias, np.float64))
+    stable = (gg >= np.maximum(1e-6, 2 * tol)) & (eg >= np.maximum(1e-6, tol))
+    return stable, tol
+
+
+def routing_choice_valid(cfg, logits_ref, corr_bias, sel, tol):
+    """Whether expert set `sel` of one token is a correct top-k choice within `tol` of the
+    oracle's biased scores: its groups are among the best up to tol (group scores up to 2 tol)
+    and each selected expert is within tol of the k-th best score of the kept groups."""
+    per = cfg.n_experts // cfg.n_groups
+    b = 1.0 / (1.0 + np.exp(-np.asarray(logits_ref, np.float64))) + np.asarray(corr_bias, np.float64)
+    gsc = np.sort(b.reshape(cfg.n_groups, per), axis=1)[:, -2:].sum(axis=1)
+    kth_group = np.sort(gsc)[::-1][cfg.topk_groups - 1]
+    groups = sorted(set(int(e) // per for e in sel))
+    if len(groups) > cfg.topk_groups or any(gsc[g] < kth_group - 2 * tol for g in groups):
+        return False
+    cand = np.concatenate([b[g * per:(g + 1) * per] for g in groups])
+    kth = np.sort(cand)[::-1][min(cfg.topk, len(cand)) - 1]
+    return len(set(int(e) for e in sel)) == cfg.topk and all(b[int(e)] >= kth - tol for e in sel)
+
+
 def route_margins(cfg, u, w_router, corr_bias):
     """Smallest gap, over tokens, between the kept/dropped group scores and between the k-th
     and (k+1)-th expert scores inside the kept groups (oracle FP32 scores)."""
@@ -102,16 +165,19 @@ def flatten_trace(trace, h_final=None, prefix=""):
     return out
 
 
-def noise_floor(run, n=2):
+def noise_floor(run, n=2, alts_out=None):
     """run() -> flattened oracle outputs of a chained computation, computed from scratch.
     Returns (reference, floors) where floors[name] = (max-abs-rel, mean-rel, max |delta|)
-    of n reruns under FP32-level perturbation of every rounding point, against the reference."""
+    of n reruns under FP32-level perturbation of every rounding point, against the reference.
+    The perturbed outputs are appended to alts_out when given."""
     from oracle.noise import perturbed_rounding
     ref = run()
     floors = {k: (0.0, 0.0, 0.0) for k in ref}
     for s in range(n):
         with perturbed_rounding(seed=s + 1):
             alt = run()
+        if alts_out is not None:
+            alts_out.append(alt)
         for k in ref:
             a, r = alt[k], ref[k]
             floors[k] = (max(floors[k][0], max_abs_rel(a, r)), max(floors[k][1], mean_rel(a, r)),
@@ -119,16 +185,29 @@ def noise_floor(run, n=2):
     return ref, floors
 
 
-def assert_chained_close(got, ref, floors, fp8=False, factor=3.0):
-    """Stated bars, or factor x the oracle's own perturbation divergence where that is larger."""
+def floors_on_rows(ref, alts, keys, rows):
+    """Perturbation floors of `keys` recomputed over the token rows in `rows` only."""
+    out = {}
+    for k in keys:
+        vals = [(max_abs_rel(a[k][rows], ref[k][rows]), mean_rel(a[k][rows], ref[k][rows]),
+                 float(np.max(np.abs(a[k][rows] - ref[k][rows])))) for a in alts]
+        out[k] = tuple(max(v[i] for v in vals) for i in range(3))
+    return out
+
+
+def assert_chained_close(got, ref, floors, fp8=False, factor=3.0, rows=None, row_keys=()):
+    """Stated bars, or factor x the oracle's own perturbation divergence where that is larger.
+    For the keys in row_keys only the token rows in `rows` (a boolean mask) are compared."""
     report = {}
     for k in ref:
-        if k.endswith(".logits"):
+        if k.endswith((".logits", ".idx")):
             continue
         lim_mx = max(FP8_MAX_REL if fp8 else BF16_MAX_REL, factor * floors[k][0])
         lim_mn = max(FP8_MEAN_REL if fp8 else BF16_MEAN_REL, factor * floors[k][1])
-        a = got[k]
-        mx, mn = max_abs_rel(a, ref[k]), mean_rel(a, ref[k])
+        a, r = got[k], ref[k]
+        if rows is not None and k in row_keys:
+            a, r = a[rows], r[rows]
+        mx, mn = max_abs_rel(a, r), mean_rel(a, r)
         assert np.all(np.isfinite(a)), f"{k}: non-finite"
         assert mx <= lim_mx and mn <= lim_mn, \
             f"{k}: max-abs-rel {mx:.3e} (<= {lim_mx:.3e}), mean-rel {mn:.3e} (<= {lim_mn:.3e})"

@@ -140,8 +140,12 @@ ATTN_CASES = [
 @pytest.mark.parametrize("case", range(len(ATTN_CASES)))
 @pytest.mark.parametrize("nope", [False, True])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_attn(case, nope, fp8):
+@pytest.mark.parametrize("form", ["natural", "other"])
+def test_attn(case, nope, fp8, form):
+    """form 'natural' passes the true tokens per sequence (split-K decode up to 4, query tiles
+    above); 'other' forces the other kernel, which must give the same result."""
     shape, ctxs, per = ATTN_CASES[case]
+    mq = per if form == "natural" else (64 if per <= 4 else 1)
     seed = 31 + case
     S = len(ctxs)
     T = S * per
@@ -164,7 +168,7 @@ def test_attn(case, nope, fp8):
     cfg = cfg_of(shape, nope)
     out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
     B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
-                ws_for(cfg, T, max_pos))
+                ws_for(cfg, T, max_pos), max_q_per_seq=mq)
     check_status()
     ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
                       positions, np64(W["w_o"]))
