@@ -7,13 +7,17 @@
 // Decode (few tokens): split-K flash decoding. A CTA takes one (token, KV head, key range);
 // the G query heads of the KV group form the rows of a 16-row tensor-core tile, so every K/V
 // byte read from HBM serves all G heads. Each of the 4 warps streams its own 32-key tiles
-// through a 2-stage cp.async pipeline; partial (max, sum, P.V) go to the workspace and a merge
-// kernel combines the splits, normalises, gates and writes o.
+// through a 2-stage cp.async pipeline. With at most 8 splits the split CTAs of a (token, KV
+// head) form one thread-block cluster and merge their partial (max, sum, P.V) through
+// distributed shared memory, each CTA finishing a slice of the outputs; with more splits the
+// partials go to the workspace and the last split CTA to finish merges them. The merge
+// normalises, applies the output gate and writes o.
 // Prefill (many tokens): a CTA takes 16 consecutive tokens and one KV group; warp w computes
 // query head w of the group for those 16 tokens, all warps sharing each staged K/V tile.
 //
 // P is split into bf16 hi + lo parts for the P.V product, so P carries ~16 significant bits;
 // the logits Q.K^T are exact products of bf16 inputs accumulated in FP32.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -33,7 +37,6 @@ constexpr int kRows = 16;    // tensor-core tile rows
 template <int D, bool FP8, int KT>
 struct TileGeom {
   static constexpr int ROWB = D * 2;          // bf16 row bytes
-  static constexpr int CH = D / 8;            // 16-byte chunks per bf16 row
   static constexpr int RAWROW = FP8 ? D : D * 2;
   static constexpr int RAWCH = RAWROW / 16;   // 16-byte chunks per stored row
   static constexpr int TILEB = KT * ROWB;     // one bf16 tile
@@ -247,10 +250,98 @@ __device__ __forceinline__ void merge_gate(const float* part_acc, const float* p
   }
 }
 
+// Row `row`, column d of the CTA's 4 warp partials: the common max M, the rescaled P.V sum O
+// and the rescaled softmax denominator L.
+__device__ __forceinline__ void combine_warps(const float* sacc_all, const float* sml, int ld,
+                                              int row, int d, float& M, float& O, float& L) {
+  M = kNegInf;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sml[(w * kRows + row) * 2]);
+  O = 0.f;
+  L = 0.f;
+  if (M != kNegInf) {
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float f = exp2f(sml[(w * kRows + row) * 2] - M);
+      O += f * sacc_all[(w * kRows + row) * ld + d];
+      L += f * sml[(w * kRows + row) * 2 + 1];
+    }
+  }
+}
+
+// The cluster form of merge_gate: split s's partial lives in the shared memory of cluster CTA
+// s; CTA `rank` finishes outputs [rank * chunk, (rank + 1) * chunk) of the G x D block.
+constexpr int kClusterMaxSplits = 8;
+__device__ __forceinline__ void merge_gate_cluster(
+    cooperative_groups::cluster_group& cl, float* cO, float* cML, int n_splits, int n_q,
+    int n_kv, int D, float v_scale, const uint16_t* __restrict__ gpre,
+    const uint16_t* __restrict__ gate_bias, uint16_t* __restrict__ og, int t, int hk, float* sh) {
+  const int G = n_q / n_kv;
+  float* w = sh;                                // [kRows][kClusterMaxSplits]: exp2(m_s - M)
+  float* inv = sh + kRows * kClusterMaxSplits;  // [kRows]
+  const float* peerO[kClusterMaxSplits];
+  const float* peerML[kClusterMaxSplits];
+#pragma unroll
+  for (int sp = 0; sp < kClusterMaxSplits; ++sp) {
+    const int r = sp < n_splits ? sp : 0;
+    peerO[sp] = cl.map_shared_rank(cO, r);
+    peerML[sp] = cl.map_shared_rank(cML, r);
+  }
+  if (threadIdx.x < G) {
+    const int row = threadIdx.x;
+    float m[kClusterMaxSplits], l[kClusterMaxSplits];
+    float M = kNegInf;
+#pragma unroll
+    for (int sp = 0; sp < kClusterMaxSplits; ++sp) {
+      if (sp < n_splits) {
+        m[sp] = peerML[sp][row * 2];
+        l[sp] = peerML[sp][row * 2 + 1];
+        M = fmaxf(M, m[sp]);
+      }
+    }
+    float L = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kClusterMaxSplits; ++sp) {
+      if (sp < n_splits) {
+        const float f = M == kNegInf ? 0.f : exp2f(m[sp] - M);
+        w[row * kClusterMaxSplits + sp] = f;
+        L += f * l[sp];
+      }
+    }
+    inv[row] = L > 0.f ? v_scale / L : 0.f;
+  }
+  __syncthreads();
+  const int total = G * D;
+  const int chunk = (total + n_splits - 1) / n_splits;
+  const int i0 = int(cl.block_rank()) * chunk, i1 = min(total, i0 + chunk);
+  for (int idx = i0 + threadIdx.x; idx < i1; idx += blockDim.x) {
+    const int row = idx / D, d = idx - row * D;
+    float O = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kClusterMaxSplits; ++sp)
+      if (sp < n_splits) O += w[row * kClusterMaxSplits + sp] * peerO[sp][row * D + d];
+    const float o = round_bf(O * inv[row]);
+    const int hq = hk * G + row;
+    const size_t oi = (size_t(t) * n_q + hq) * D + d;
+    const float gate = sigmoidf_(bf2f(gpre[oi]) + bf2f(gate_bias[hq]));
+    og[oi] = f2bf(o * gate);
+  }
+}
+
+// Dynamic shared memory of the decode kernel: the 4 warps' tile pipelines, reused for the
+// cross-warp combine, then (cluster form) the CTA's partial for its peers.
+template <int D, bool FP8>
+struct DecodeSmem {
+  static constexpr int kTiles = kDecWarps * TileGeom<D, FP8, kDecKT>::BYTES;
+  static constexpr int kComb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
+  static constexpr int kPartOff = ((kTiles > kComb ? kTiles : kComb) + 127) / 128 * 128;
+  static constexpr int kBytes = kPartOff + (kRows * D + kRows * 2) * 4;
+};
+
 // ------------------------------------------------------------------------------------------
 // Decode: split-K partials
 // ------------------------------------------------------------------------------------------
-template <int D, bool FP8>
+template <int D, bool FP8, bool CLUSTER>
 __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_id,
     const int32_t* __restrict__ pos, int n_q, int n_kv, beam_kv_cache kc, int kps, int n_splits,
@@ -367,38 +458,51 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     }
   }
   __syncthreads();
-  const size_t pbase = (size_t(t) * n_kv + hk) * n_splits + split;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int row = idx / D, d = idx - row * D;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sml[(w * kRows + row) * 2]);
-    float O = 0.f, L = 0.f;
-    if (M != kNegInf) {
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float f = exp2f(sml[(w * kRows + row) * 2] - M);
-        O += f * sacc_all[(w * kRows + row) * ACC_LD + d];
-        L += f * sml[(w * kRows + row) * 2 + 1];
+  if constexpr (CLUSTER) {
+    // this CTA's partial to its own shared memory, above the tile and combine buffers
+    float* cO = reinterpret_cast<float*>(smem + DecodeSmem<D, FP8>::kPartOff);   // [16][D]
+    float* cML = cO + kRows * D;                                                 // [16][2]
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+      const int row = idx / D, d = idx - row * D;
+      float M, O, L;
+      combine_warps(sacc_all, sml, ACC_LD, row, d, M, O, L);
+      cO[row * D + d] = O;
+      if (d == 0) {
+        cML[row * 2] = M;
+        cML[row * 2 + 1] = L;
       }
     }
-    part_acc[(pbase * kRows + row) * D + d] = O;
-    if (d == 0) {
-      part_ml[(pbase * kRows + row) * 2] = M;
-      part_ml[(pbase * kRows + row) * 2 + 1] = L;
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    merge_gate_cluster(cl, cO, cML, n_splits, n_q, n_kv, D, v_scale, gpre, gate_bias, og, t, hk,
+                       reinterpret_cast<float*>(smem));
+    cl.sync();   // peers may still be reading this CTA's partial
+    return;
+  } else {
+    const size_t pbase = (size_t(t) * n_kv + hk) * n_splits + split;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+      const int row = idx / D, d = idx - row * D;
+      float M, O, L;
+      combine_warps(sacc_all, sml, ACC_LD, row, d, M, O, L);
+      part_acc[(pbase * kRows + row) * D + d] = O;
+      if (d == 0) {
+        part_ml[(pbase * kRows + row) * 2] = M;
+        part_ml[(pbase * kRows + row) * 2 + 1] = L;
+      }
     }
-  }
-  // the last split CTA of this (token, KV head) merges all splits
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(done + t * n_kv + hk, 1) == n_splits - 1;
-  __syncthreads();
-  if (s_last) {
+    // the last split CTA of this (token, KV head) merges all splits
+    __shared__ int s_last;
     __threadfence();
-    // the tile buffers are free now: stage the merge weights there
-    merge_gate(part_acc, part_ml, n_splits, n_q, n_kv, D, v_scale, gpre, gate_bias, og, t, hk,
-               reinterpret_cast<float*>(smem));
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(done + t * n_kv + hk, 1) == n_splits - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      // the tile buffers are free now: stage the merge weights there
+      merge_gate(part_acc, part_ml, n_splits, n_q, n_kv, D, v_scale, gpre, gate_bias, og, t, hk,
+                 reinterpret_cast<float*>(smem));
+    }
   }
 }
 
@@ -605,16 +709,22 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
                           int n_q, int n_kv, const beam_kv_cache& kc, DecodePlan pl, float sl2,
                           float* pacc, float* pml, int* done, float v_scale, const uint16_t* g,
                           const uint16_t* gb, uint16_t* og, cudaStream_t st) {
-  using Gm = TileGeom<D, FP8, kDecKT>;
-  int bytes = kDecWarps * Gm::BYTES;
-  const int comb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
-  if (comb > bytes) bytes = comb;
-  auto kern = attn_decode_split_kernel<D, FP8>;
-  cudaError_t e = set_smem(kern, bytes);
+  using Sm = DecodeSmem<D, FP8>;
+  const dim3 grid(pl.n_splits, n_kv, T), block(kDecWarps * 32);
+  if (pl.n_splits <= kClusterMaxSplits) {
+    auto kern = attn_decode_split_kernel<D, FP8, true>;
+    cudaError_t e = set_smem(kern, Sm::kBytes);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl_cluster(kern, grid, block, Sm::kBytes, st, pl.n_splits, q, seq_id, pos, n_q,
+                           n_kv, kc, pl.kps, pl.n_splits, sl2, pacc, pml, done, v_scale, g, gb, og);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  auto kern = attn_decode_split_kernel<D, FP8, false>;
+  cudaError_t e = set_smem(kern, Sm::kPartOff);
   if (e != cudaSuccess) return e;
-  dim3 grid(pl.n_splits, n_kv, T);
-  launch_pdl(kern, dim3(grid), dim3(kDecWarps * 32), bytes, st, q, seq_id, pos, n_q, n_kv, kc, pl.kps, pl.n_splits,
-                                            sl2, pacc, pml, done, v_scale, g, gb, og);
+  launch_pdl(kern, grid, block, Sm::kPartOff, st, q, seq_id, pos, n_q, n_kv, kc, pl.kps,
+             pl.n_splits, sl2, pacc, pml, done, v_scale, g, gb, og);
   return cudaGetLastError();
 }
 
@@ -677,7 +787,9 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     float* pml = cv.take<float>(parts * 2);
     int* done = cv.take<int>(size_t(T) * cfg->n_kv);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
-    if (cudaMemsetAsync(done, 0, size_t(T) * cfg->n_kv * sizeof(int), st) != cudaSuccess)
+    // the cluster form merges on chip; the other counts finished splits from zero
+    if (pl.n_splits > kClusterMaxSplits &&
+        cudaMemsetAsync(done, 0, size_t(T) * cfg->n_kv * sizeof(int), st) != cudaSuccess)
       return BEAM_ERR_CUDA;
     const float vs = fp8 ? cache->v_scale : 1.f;
     if (D == 128)

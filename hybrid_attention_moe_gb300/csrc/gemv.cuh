@@ -8,7 +8,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "sgemv.cuh"
 
 namespace beam {
 
@@ -129,28 +128,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
 
 int num_sms_cached();
 
-// Small-T dense rows: the shared-memory streamed kernel (1) or the register-pipelined kernel
-// (0); chosen by measurement.
-#ifndef BEAM_DENSE_STREAMED
-#define BEAM_DENSE_STREAMED 0
-#endif
-
 // Host launcher: the register-pipelined kernel with the token tile, rows per warp and chunks in
 // flight picked from T.
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
                                float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
   if (T <= 0 || N <= 0) return cudaSuccess;
-  if (BEAM_DENSE_STREAMED && T <= sg::kMaxT && (K * 2) % 512 == 0 && aligned16(W) &&
-      aligned16(X)) {
-    auto kern = sg::dense_kernel<MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         sg::kSmem);
-    if (e != cudaSuccess) return e;
-    void* y = MODE == kOutF32 ? static_cast<void*>(yf) : static_cast<void*>(yb);
-    launch_pdl(kern, dim3(num_sms_cached()), dim3(sg::kWarps * 32), sg::kSmem, st, W, N, K, X, T, y, ldy);
-    return cudaGetLastError();
-  }
   auto go = [&](auto kern, int nt, int nr) {
     const int warps = (N + nr - 1) / nr;
     dim3 grid((warps + 7) / 8, (T + nt - 1) / nt);

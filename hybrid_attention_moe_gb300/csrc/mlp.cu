@@ -16,13 +16,7 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
-#include "sgemv.cuh"
 
-// Decode down projection: the shared-memory streamed kernel (1) or the register-pipelined
-// warp-per-row kernel (0); chosen by measurement.
-#ifndef BEAM_MOE_DOWN_STREAMED
-#define BEAM_MOE_DOWN_STREAMED 0
-#endif
 
 namespace beam {
 namespace {
@@ -32,6 +26,10 @@ constexpr int kPairTile = 4;        // pairs per weight pass in the gate_up / do
 constexpr int kFusedMaxPairs = 1024;  // down+combine in shared memory up to this many pairs
 
 constexpr int kMoeGemmMinT = 32;   // from here the experts run as grouped tensor-core GEMMs
+// Weight chunks in flight per lane in the single-token gate/up and down kernels (4 and 8;
+// 5/10 and 10/10 measured no faster).
+constexpr int kDecodeGateUpU = 4;
+constexpr int kDecodeDownU = 8;
 
 struct MoePlan {
   int* n_active;   // [1]
@@ -138,30 +136,60 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* _
   }
 }
 
+// Expert and pair range of active slot `ai`: from the plan, or -- when one token's k slots are
+// taken as the active list directly (`direct` = that token's expert indices) -- slot ai is
+// expert direct[ai] with the single pair ai. Returns false for an expert index out of range.
+struct ExpertSlot {
+  int e, p0, p1;
+};
+__device__ __forceinline__ bool expert_slot(const MoePlan& pl, const int32_t* direct, int E,
+                                            int ai, ExpertSlot& s) {
+  if (direct != nullptr) {
+    s.e = direct[ai];
+    s.p0 = ai;
+    s.p1 = ai + 1;
+    return s.e >= 0 && s.e < E;
+  }
+  s.e = pl.active[ai];
+  s.p0 = pl.act_off[ai];
+  s.p1 = pl.act_off[ai + 1];
+  return true;
+}
+__device__ __forceinline__ int pair_at(const MoePlan& pl, const int32_t* direct, int i) {
+  return direct != nullptr ? i : pl.pairs[i];
+}
+
 // grid (ceil(F / 8), max active experts); warp per (active expert, f): gate row f and up
-// row F+f, dotted with up to NT of the expert's pairs per weight pass.
+// row F+f, dotted with up to NT of the expert's pairs per weight pass. CTA (0, 0) also clears
+// the n_cnt completion counters of the down kernel that follows.
 template <int U, int NT>
 __global__ void __launch_bounds__(256) moe_gate_up_kernel(
     const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
-    MoePlan pl, uint16_t* __restrict__ a) {
+    MoePlan pl, const int32_t* __restrict__ direct, int E, int* __restrict__ cnt, int n_cnt,
+    uint16_t* __restrict__ a) {
   pdl_trigger();
   pdl_wait();
+  if (cnt != nullptr && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
   const int ai = blockIdx.y;
-  if (ai >= *pl.n_active) return;
+  if (ai >= (direct != nullptr ? k : *pl.n_active)) return;
   const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (f >= F) return;
   const int lane = threadIdx.x & 31;
-  const int e = pl.active[ai];
-  const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
-  const uint16_t* base = w_gu + size_t(e) * 2 * F * H;
+  ExpertSlot es;
+  if (!expert_slot(pl, direct, E, ai, es)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(BEAM_DEV_BAD_EXPERT);
+    return;
+  }
+  const uint16_t* base = w_gu + size_t(es.e) * 2 * F * H;
   const uint16_t* w[2] = {base + size_t(f) * H, base + size_t(F + f) * H};
-  for (int pp = p0; pp < p1; pp += NT) {
-    const int nt = min(NT, p1 - pp);
+  for (int pp = es.p0; pp < es.p1; pp += NT) {
+    const int nt = min(NT, es.p1 - pp);
     int pid[NT];
     const uint16_t* x[NT];
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
-      pid[i] = pl.pairs[pp + min(i, nt - 1)];
+      pid[i] = pair_at(pl, direct, pp + min(i, nt - 1));
       x[i] = u + size_t(pid[i] / k) * H;
     }
     float acc[2][NT];
@@ -218,40 +246,68 @@ __global__ void __launch_bounds__(256) moe_down_combine_kernel(
   }
 }
 
-// Unfused form: warp per (active expert, NR consecutive rows h); y[pair][h] (FP32) to the
-// workspace, then a combine pass.
+// Warp per (active expert, NR consecutive rows h); y[pair][h] (FP32) to the workspace. With
+// completion counters (one per CTA column, cleared by the gate/up kernel), the last CTA of a
+// column to finish also combines its 8*NR rows: out[t][h] = bf16(sum_j w[t][j] y[t*k+j][h]),
+// slots in order, skipping slots whose expert index is out of range. Without counters a
+// separate combine pass follows.
 template <int U, int NT, int NR>
-__global__ void __launch_bounds__(256) moe_down_kernel(const uint16_t* __restrict__ a,
-                                                       const uint16_t* __restrict__ w_dn, int H,
-                                                       int F, MoePlan pl, float* __restrict__ y) {
+__global__ void __launch_bounds__(256) moe_down_kernel(
+    const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn, int H, int F, MoePlan pl,
+    const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, int T, int k, int E, int* __restrict__ cnt,
+    float* __restrict__ y, uint16_t* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
+  const int na = direct != nullptr ? k : *pl.n_active;
   const int ai = blockIdx.y;
-  if (ai >= *pl.n_active) return;
+  if (ai >= max(na, 1)) return;   // uniform over the CTA
   const int h0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * NR;
-  if (h0 >= H) return;
   const int lane = threadIdx.x & 31;
-  const int e = pl.active[ai];
-  const int p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
-  const uint16_t* w[NR];
+  ExpertSlot es;
+  const bool work = ai < na && h0 < H && expert_slot(pl, direct, E, ai, es);
+  if (work) {
+    const uint16_t* w[NR];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) w[r] = w_dn + (size_t(e) * H + min(h0 + r, H - 1)) * F;
-  for (int pp = p0; pp < p1; pp += NT) {
-    const int nt = min(NT, p1 - pp);
-    int pid[NT];
-    const uint16_t* x[NT];
+    for (int r = 0; r < NR; ++r) w[r] = w_dn + (size_t(es.e) * H + min(h0 + r, H - 1)) * F;
+    for (int pp = es.p0; pp < es.p1; pp += NT) {
+      const int nt = min(NT, es.p1 - pp);
+      int pid[NT];
+      const uint16_t* x[NT];
 #pragma unroll
-    for (int i = 0; i < NT; ++i) {
-      pid[i] = pl.pairs[pp + min(i, nt - 1)];
-      x[i] = a + size_t(pid[i]) * F;
+      for (int i = 0; i < NT; ++i) {
+        pid[i] = pair_at(pl, direct, pp + min(i, nt - 1));
+        x[i] = a + size_t(pid[i]) * F;
+      }
+      float acc[NR][NT];
+      warp_dot<NR, NT, U>(w, x, nt, F, acc);
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+          if (i < nt && lane == r * NT + i && h0 + r < H)
+            y[size_t(pid[i]) * H + h0 + r] = acc[r][i];
     }
-    float acc[NR][NT];
-    warp_dot<NR, NT, U>(w, x, nt, F, acc);
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-#pragma unroll
-      for (int i = 0; i < NT; ++i)
-        if (i < nt && lane == r * NT + i && h0 + r < H) y[size_t(pid[i]) * H + h0 + r] = acc[r][i];
+  }
+  if (cnt == nullptr) return;   // uniform over the grid
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int hb = blockIdx.x * 8 * NR;
+  const int nh = min(8 * NR, H - hb);
+  for (int i = threadIdx.x; i < T * nh; i += blockDim.x) {
+    const int t = i / nh, h = hb + (i - t * nh);
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[size_t(t) * k + j];
+      if (e < 0 || e >= E) continue;
+      s = fmaf(topk_w[size_t(t) * k + j], __ldcg(y + (size_t(t) * k + j) * H + h), s);
+    }
+    out[size_t(t) * H + h] = f2bf(s);
   }
 }
 
@@ -288,82 +344,6 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ u, int H, int k,
 
 int max_jobs(int P, int E) { return (P + 127) / 128 + (P < E ? P : E); }
 
-// Streamed decode form (T <= 4, so an expert meets at most 4 pairs): rows are the
-// (active expert, f) gate/up pairs, spread evenly over every warp of a persistent grid.
-__global__ void __launch_bounds__(sg::kWarps * 32, 1)
-    moe_sg_gate_up_kernel(const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu,
-                          int H, int F, int k, MoePlan pl, uint16_t* __restrict__ act) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring;
-  uint64_t* full;
-  sg::warp_ring(smem, ring, full);
-  int r0, r1;
-  sg::warp_share(*pl.n_active * F, r0, r1);
-  const int lane = threadIdx.x & 31;
-  auto job = [&](int r) {
-    sg::RowJob j;
-    const int a = r / F, f = r - a * F;
-    const int e = pl.active[a], p0 = pl.act_off[a];
-    const int c = min(pl.act_off[a + 1] - p0, sg::kMaxT);
-    const uint16_t* base = w_gu + size_t(e) * 2 * F * H;
-    j.w[0] = base + size_t(f) * H;
-    j.w[1] = base + size_t(F + f) * H;
-#pragma unroll
-    for (int i = 0; i < sg::kMaxT; ++i) {
-      j.pid[i] = pl.pairs[p0 + min(i, c - 1)];
-      j.x[i] = u + size_t(j.pid[i] / k) * H;
-    }
-    j.nt = c;
-    return j;
-  };
-  auto epi = [&](int r, const sg::RowJob& jb, const float (&acc)[2][sg::kMaxT]) {
-    const int f = r % F;
-#pragma unroll
-    for (int i = 0; i < sg::kMaxT; ++i)
-      if (lane == i && i < jb.nt)
-        act[size_t(jb.pid[i]) * F + f] = f2bf(siluf_(acc[0][i]) * acc[1][i]);
-  };
-  sg::stream_rows<2, false>(r0, r1, H, ring, full, job, epi);
-}
-
-// Rows are (active expert, h) rows of W_down; y[pair][h] in FP32 for the combine.
-__global__ void __launch_bounds__(sg::kWarps * 32, 1)
-    moe_sg_down_kernel(const uint16_t* __restrict__ act, const uint16_t* __restrict__ w_dn, int H,
-                       int F, MoePlan pl, float* __restrict__ y) {
-  pdl_trigger();
-  pdl_wait();
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring;
-  uint64_t* full;
-  sg::warp_ring(smem, ring, full);
-  int r0, r1;
-  sg::warp_share(*pl.n_active * H, r0, r1);
-  const int lane = threadIdx.x & 31;
-  auto job = [&](int r) {
-    sg::RowJob j;
-    const int a = r / H, h = r - a * H;
-    const int e = pl.active[a], p0 = pl.act_off[a];
-    const int c = min(pl.act_off[a + 1] - p0, sg::kMaxT);
-    j.w[0] = j.w[1] = w_dn + (size_t(e) * H + h) * F;
-#pragma unroll
-    for (int i = 0; i < sg::kMaxT; ++i) {
-      j.pid[i] = pl.pairs[p0 + min(i, c - 1)];
-      j.x[i] = act + size_t(j.pid[i]) * F;
-    }
-    j.nt = c;
-    return j;
-  };
-  auto epi = [&](int r, const sg::RowJob& jb, const float (&acc)[1][sg::kMaxT]) {
-    const int h = r % H;
-#pragma unroll
-    for (int i = 0; i < sg::kMaxT; ++i)
-      if (lane == i && i < jb.nt) y[size_t(jb.pid[i]) * H + h] = acc[0][i];
-  };
-  sg::stream_rows<1, false>(r0, r1, F, ring, full, job, epi);
-}
-
 // Decode form for up to kMoeSmallT tokens (every expert then meets at most kMoeSmallT pairs).
 constexpr int kMoeSmallT = 4;
 
@@ -391,6 +371,7 @@ size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
   }
   if (grouped || P > size_t(kFusedMaxPairs) || T <= kMoeSmallT)
     b += align_up(P * c->hidden * 4, 256);
+  if (T <= kMoeSmallT) b += align_up(size_t(c->hidden / 8 + 1) * 4, 256);   // down counters
   return b;
 }
 
@@ -423,12 +404,13 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
   uint16_t* us = grouped ? cv.take<uint16_t>(size_t(P) * H) : nullptr;
   const bool small = !grouped && T <= kMoeSmallT;
   float* y = (grouped || small || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
+  int* cnt = small ? cv.take<int>(size_t(H / 8 + 1)) : nullptr;
   if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   const int max_active = P < E ? P : E;
-  launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
   if (grouped) {
-    // gather -> grouped gate/up GEMM with the SwiGLU epilogue (sorted rows) -> grouped down
-    // GEMM writing each row back to its (token, slot) pair -> weighted combine
+    // plan -> gather -> grouped gate/up GEMM with the SwiGLU epilogue (sorted rows) -> grouped
+    // down GEMM writing each row back to its (token, slot) pair -> weighted combine
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
     const size_t nv = size_t(P) * (H / 8);
     launch_pdl(gather_rows_kernel, dim3(unsigned((nv + 255) / 256)), dim3(256), 0, st, u, H, k, pl, P, us);
     const int mj = max_jobs(P, E);
@@ -444,34 +426,33 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     return launch_status();
   }
   if (small) {
-    // decode: plan -> gate/up (SwiGLU) -> down rows per (expert, h) -> combine
-    if (T == 1)
-      launch_pdl(moe_gate_up_kernel<4, 1>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
-                 w_gate_up, H, F, k, pl, act);
+    // decode: [plan] -> gate/up (SwiGLU) -> down rows per (expert, h) with the combine done by
+    // the last CTA of each row block. One token needs no plan: its k slots are the active list.
+    const bool direct = T == 1;
+    const int32_t* dix = direct ? topk_idx : nullptr;
+    const int na = direct ? k : max_active;
+    const int nr = direct ? 2 : 1;
+    const int n_cnt = (H + 8 * nr - 1) / (8 * nr);
+    if (!direct)
+      launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+    if (direct)
+      launch_pdl(moe_gate_up_kernel<kDecodeGateUpU, 1>, dim3((F + 7) / 8, na), dim3(256), 0, st,
+                 u, w_gate_up, H, F, k, pl, dix, E, cnt, n_cnt, act);
     else
-      launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
-                 w_gate_up, H, F, k, pl, act);
-#if BEAM_MOE_DOWN_STREAMED
-    if (cudaFuncSetAttribute(moe_sg_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             sg::kSmem) != cudaSuccess)
-      return BEAM_ERR_CUDA;
-    launch_pdl(moe_sg_down_kernel, dim3(num_sms_cached()), dim3(sg::kWarps * 32), sg::kSmem, st,
-               act, w_down, H, F, pl, y);
-#else
-    if (T == 1)
-      launch_pdl(moe_down_kernel<8, 1, 2>, dim3((H + 15) / 16, max_active), dim3(256), 0, st,
-                 act, w_down, H, F, pl, y);
+      launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, na), dim3(256), 0, st, u,
+                 w_gate_up, H, F, k, pl, dix, E, cnt, n_cnt, act);
+    if (direct)
+      launch_pdl(moe_down_kernel<kDecodeDownU, 1, 2>, dim3(n_cnt, na), dim3(256), 0, st, act,
+                 w_down, H, F, pl, dix, topk_idx, topk_w, T, k, E, cnt, y, out);
     else
-      launch_pdl(moe_down_kernel<8, 4, 1>, dim3((H + 7) / 8, max_active), dim3(256), 0, st, act,
-                 w_down, H, F, pl, y);
-#endif
-    const size_t n = size_t(T) * H;
-    launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w,
-               topk_idx, T, H, k, E, out);
+      launch_pdl(moe_down_kernel<8, 4, 1>, dim3(n_cnt, na), dim3(256), 0, st, act, w_down, H,
+                 F, pl, dix, topk_idx, topk_w, T, k, E, cnt, y, out);
     return launch_status();
   }
+  launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
   launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
-             w_gate_up, H, F, k, pl, act);
+             w_gate_up, H, F, k, pl, static_cast<const int32_t*>(nullptr), E,
+             static_cast<int*>(nullptr), 0, act);
   if (P <= kFusedMaxPairs) {
     const int smem = 8 * P * int(sizeof(float));
     if (smem > 48 * 1024 &&
@@ -481,7 +462,9 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     launch_pdl(moe_down_combine_kernel<8>, dim3((H + 7) / 8), dim3(256), smem, st, act, w_down, topk_w, T, H, F, k,
                                                               pl, out);
   } else {
-    launch_pdl(moe_down_kernel<8, 4, 1>, dim3((H + 7) / 8, max_active), dim3(256), 0, st, act, w_down, H, F, pl, y);
+    launch_pdl(moe_down_kernel<8, 4, 1>, dim3((H + 7) / 8, max_active), dim3(256), 0, st, act,
+               w_down, H, F, pl, static_cast<const int32_t*>(nullptr), topk_idx, topk_w, T, k, E,
+               static_cast<int*>(nullptr), y, out);
     const size_t n = size_t(T) * H;
     launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w, topk_idx, T, H, k,
                                                                   E, out);

@@ -13,6 +13,7 @@ namespace beam {
 namespace {
 
 constexpr int kRouteMaxT = 8;  // tokens per CTA pass in the GEMV form
+constexpr int kRouteBatch = 3; // weight chunks in flight per thread in the GEMV form
 
 // Small T: one CTA per expert row; its warps split the hidden axis; every token of a pass
 // reuses the row held in registers/L1.
@@ -20,6 +21,8 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __rest
                                                           const float* __restrict__ wr, int T,
                                                           int H, int E,
                                                           float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[8][kRouteMaxT];
   const int e = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -29,18 +32,32 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __rest
     float acc[kRouteMaxT];
 #pragma unroll
     for (int t = 0; t < kRouteMaxT; ++t) acc[t] = 0.f;
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) {
-      const float4 w0 = ld_stream_f4(row + i * 8);
-      const float4 w1 = ld_stream_f4(row + i * 8 + 4);
+    // kRouteBatch chunks of 8 weights per thread are requested before any is used, so a
+    // 5120-wide row arrives in one round trip
+    for (int i0 = threadIdx.x; i0 < H / 8; i0 += kRouteBatch * blockDim.x) {
+      float4 w0[kRouteBatch], w1[kRouteBatch];
 #pragma unroll
-      for (int t = 0; t < kRouteMaxT; ++t) {
-        if (t < nt) {
-          float x[8];
-          unpack8(__ldg(reinterpret_cast<const uint4*>(u + size_t(t0 + t) * H + i * 8)), x);
-          acc[t] = fmaf(w0.x, x[0], acc[t]); acc[t] = fmaf(w0.y, x[1], acc[t]);
-          acc[t] = fmaf(w0.z, x[2], acc[t]); acc[t] = fmaf(w0.w, x[3], acc[t]);
-          acc[t] = fmaf(w1.x, x[4], acc[t]); acc[t] = fmaf(w1.y, x[5], acc[t]);
-          acc[t] = fmaf(w1.z, x[6], acc[t]); acc[t] = fmaf(w1.w, x[7], acc[t]);
+      for (int b = 0; b < kRouteBatch; ++b) {
+        const int i = i0 + b * blockDim.x;
+        if (i < H / 8) {
+          w0[b] = ld_stream_f4(row + i * 8);
+          w1[b] = ld_stream_f4(row + i * 8 + 4);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kRouteBatch; ++b) {
+        const int i = i0 + b * blockDim.x;
+        if (i >= H / 8) break;
+#pragma unroll
+        for (int t = 0; t < kRouteMaxT; ++t) {
+          if (t < nt) {
+            float x[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(u + size_t(t0 + t) * H + i * 8)), x);
+            acc[t] = fmaf(w0[b].x, x[0], acc[t]); acc[t] = fmaf(w0[b].y, x[1], acc[t]);
+            acc[t] = fmaf(w0[b].z, x[2], acc[t]); acc[t] = fmaf(w0[b].w, x[3], acc[t]);
+            acc[t] = fmaf(w1[b].x, x[4], acc[t]); acc[t] = fmaf(w1[b].y, x[5], acc[t]);
+            acc[t] = fmaf(w1[b].z, x[6], acc[t]); acc[t] = fmaf(w1[b].w, x[7], acc[t]);
+          }
         }
       }
     }
@@ -65,6 +82,8 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __rest
                                                           const float* __restrict__ wr, int T,
                                                           int H, int E,
                                                           float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[kTK][kTM + 4];
   __shared__ float Bs[kTK][kTN + 4];
   const int tm = blockIdx.y * kTM, tn = blockIdx.x * kTN;
@@ -188,6 +207,127 @@ __global__ void __launch_bounds__(kTopkThreads) router_topk_kernel(
   }
 }
 
+// Warp per token (8 tokens per CTA), every decision in registers. Lane l holds experts
+// [l*EPL, (l+1)*EPL); a group of `per` experts spans LPG = per/EPL lanes (a power of two), so
+// the group's top-2 merges across those lanes with xor shuffles. Every lane then sees all G
+// group scores and ranks its own group; the k experts are taken in k rounds of a warp argmax
+// over each lane's best remaining candidate. Same arithmetic and tie rules as
+// router_topk_kernel (sigmoid via expf, group score m1 + m2, ties to the lower index,
+// weights s / sum(s in selection order) * scale).
+template <int EPL>
+__global__ void __launch_bounds__(256) router_topk_warp_kernel(
+    const float* __restrict__ logits, const float* __restrict__ corr_bias, int T, int E, int G,
+    int LPG, int kG, int k, float scale, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int e0 = lane * EPL;
+  const bool active = e0 < E;
+  float b[EPL], sv[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const float z = active ? logits[size_t(t) * E + e0 + j] : 0.f;
+    sv[j] = 1.0f / (1.0f + expf(-z));
+    b[j] = active ? sv[j] + corr_bias[e0 + j] : -INFINITY;
+  }
+  // group score: the two largest b of the group (equal values count twice)
+  float m1 = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    if (b[j] > m1) { m2 = m1; m1 = b[j]; } else if (b[j] > m2) { m2 = b[j]; }
+  }
+  for (int o = 1; o < LPG; o <<= 1) {
+    const float o1 = __shfl_xor_sync(0xffffffffu, m1, o);
+    const float o2 = __shfl_xor_sync(0xffffffffu, m2, o);
+    const float hi = fmaxf(m1, o1), lo = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
+    m1 = hi;
+    m2 = lo;
+  }
+  const float gs = m1 + m2;
+  // rank of this lane's group among the G groups (ties to the lower group index)
+  const int my_g = lane / LPG;
+  int rank = 0;
+  for (int g = 0; g < G; ++g) {
+    const float o = __shfl_sync(0xffffffffu, gs, g * LPG);
+    rank += (o > gs || (o == gs && g < my_g)) ? 1 : 0;
+  }
+  const bool kept = active && rank < kG;
+  unsigned taken = kept ? 0u : 0xffffffffu;
+  int sel_e = 0;
+  float sel_s = 0.f;
+  for (int r = 0; r < k; ++r) {
+    float v = -INFINITY, vs = 0.f;
+    int best = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      if (!((taken >> j) & 1u) && (b[j] > v || best == 0x7fffffff)) {
+        v = b[j];
+        vs = sv[j];
+        best = e0 + j;
+      }
+    }
+    const int mine = best;
+    warp_argmax(v, best);
+    const float s_best = __shfl_sync(0xffffffffu, vs, best / EPL);
+    if (mine == best) taken |= 1u << (best - e0);
+    if (lane == r) { sel_e = best; sel_s = s_best; }
+  }
+  float ssum = 0.f;
+  for (int r = 0; r < k; ++r) ssum += __shfl_sync(0xffffffffu, sel_s, r);   // selection order
+  if (lane < k) {
+    topk_idx[size_t(t) * k + lane] = sel_e;
+    topk_w[size_t(t) * k + lane] = sel_s / ssum * scale;
+  }
+}
+
+// Experts per lane for the warp-per-token top-k, or 0 when the shape does not fit it.
+int topk_epl(int E, int G, int k) {
+  const int per = E / G;
+  if (k > 32) return 0;
+  for (int epl = 1; epl <= 16; epl <<= 1) {
+    if (E > 32 * epl || per % epl != 0) continue;
+    const int lpg = per / epl;
+    if ((lpg & (lpg - 1)) != 0 || lpg > 32) return 0;
+    return epl;
+  }
+  return 0;
+}
+
+beam_status launch_topk(const beam_layer_cfg* cfg, const float* lg, const float* corr_bias,
+                        int T, int32_t* topk_idx, float* topk_w, cudaStream_t st) {
+  const int E = cfg->n_experts, G = cfg->n_groups;
+  const int epl = topk_epl(E, G, cfg->topk);
+  const dim3 grid((T + 7) / 8), block(256);
+  const int lpg = epl > 0 ? E / G / epl : 0;
+  switch (epl) {
+    case 1: launch_pdl(router_topk_warp_kernel<1>, grid, block, 0, st, lg, corr_bias, T, E, G, lpg, cfg->topk_groups, cfg->topk, cfg->route_scale, topk_idx, topk_w); break;
+    case 2: launch_pdl(router_topk_warp_kernel<2>, grid, block, 0, st, lg, corr_bias, T, E, G, lpg, cfg->topk_groups, cfg->topk, cfg->route_scale, topk_idx, topk_w); break;
+    case 4: launch_pdl(router_topk_warp_kernel<4>, grid, block, 0, st, lg, corr_bias, T, E, G, lpg, cfg->topk_groups, cfg->topk, cfg->route_scale, topk_idx, topk_w); break;
+    case 8: launch_pdl(router_topk_warp_kernel<8>, grid, block, 0, st, lg, corr_bias, T, E, G, lpg, cfg->topk_groups, cfg->topk, cfg->route_scale, topk_idx, topk_w); break;
+    case 16: launch_pdl(router_topk_warp_kernel<16>, grid, block, 0, st, lg, corr_bias, T, E, G, lpg, cfg->topk_groups, cfg->topk, cfg->route_scale, topk_idx, topk_w); break;
+    default:
+      router_topk_kernel<<<T, kTopkThreads, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
+                                                      cfg->topk, cfg->route_scale, topk_idx,
+                                                      topk_w);
+      note_launches(1);
+  }
+  return launch_status();
+}
+
+// logits[T][E] = float(u) . w_router^T
+beam_status launch_logits(const uint16_t* u, const float* w_router, int T, int H, int E,
+                          float* lg, cudaStream_t st) {
+  if (T <= 32)
+    launch_pdl(router_gemv_kernel, dim3(E), dim3(256), 0, st, u, w_router, T, H, E, lg);
+  else
+    launch_pdl(router_gemm_kernel, dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), dim3(256), 0,
+               st, u, w_router, T, H, E, lg);
+  return launch_status();
+}
+
 }  // namespace
 
 size_t route_ws_bytes(const beam_layer_cfg* c, int T) {
@@ -219,17 +359,9 @@ extern "C" beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u,
     lg = cv.take<float>(size_t(T) * E);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   }
-  if (T <= 32)
-    router_gemv_kernel<<<E, 256, 0, st>>>(u, w_router, T, H, E, lg);
-  else
-    router_gemm_kernel<<<dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), 256, 0, st>>>(
-        u, w_router, T, H, E, lg);
-  note_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
-  router_topk_kernel<<<T, kTopkThreads, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
-                                                  cfg->topk, cfg->route_scale, topk_idx, topk_w);
-  note_launches(1);
-  return launch_status();
+  const beam_status ls = launch_logits(u, w_router, T, H, E, lg, st);
+  if (ls != BEAM_OK) return ls;
+  return launch_topk(cfg, lg, corr_bias, T, topk_idx, topk_w, st);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -293,15 +425,7 @@ extern "C" beam_status beam_route_noalloc(const beam_layer_cfg* cfg, const beam_
   // the GEMV/GEMM writes every logit of the T x E block before the top-k reads it, so the
   // scratch needs no clearing between calls
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (T <= 32)
-    router_gemv_kernel<<<E, 256, 0, st>>>(u, w_router, T, H, E, lg);
-  else
-    router_gemm_kernel<<<dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), 256, 0, st>>>(
-        u, w_router, T, H, E, lg);
-  note_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return BEAM_ERR_CUDA;
-  router_topk_kernel<<<T, kTopkThreads, 0, st>>>(lg, corr_bias, T, E, G, cfg->topk_groups,
-                                                  cfg->topk, cfg->route_scale, topk_idx, topk_w);
-  note_launches(1);
-  return launch_status();
+  const beam_status ls = launch_logits(u, w_router, T, H, E, lg, st);
+  if (ls != BEAM_OK) return ls;
+  return launch_topk(cfg, lg, corr_bias, T, topk_idx, topk_w, st);
 }

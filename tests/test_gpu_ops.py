@@ -4,6 +4,8 @@ Sizes: the tiny Beam-shaped widths (several tiles and ragged tails at small cost
 full Beam widths (hidden 5120, 48/8 heads of 128, 256 experts) at decode and prefill token
 counts. Both sides get the same tensors; nothing the kernels produce is fed to the oracle.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -177,7 +179,15 @@ def test_attn(case, nope, fp8, form):
 
 # ------------------------------------------------------------------ router ----
 
-@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 77), (BEAM, 1), (BEAM, 8), (BEAM, 300)])
+# Router shapes beside the Beam and tiny ones: 96 experts in 3 groups of 32 (4 experts per lane,
+# a group spanning 8 lanes of the warp-per-token top-k) and 48 experts in 4 groups of 12 (a group
+# not a power-of-two number of lanes: the CTA-per-token top-k).
+ROUTE_96 = dataclasses.replace(TINY, n_experts=96, n_groups=3, topk_groups=2, topk=6)
+ROUTE_48 = dataclasses.replace(TINY, n_experts=48, n_groups=4, topk_groups=2, topk=4)
+
+
+@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 77), (BEAM, 1), (BEAM, 8), (BEAM, 300),
+                                     (ROUTE_96, 5), (ROUTE_48, 1), (ROUTE_48, 40)])
 def test_route(shape, T):
     cfg = cfg_of(shape)
     for attempt in range(20):
@@ -220,12 +230,14 @@ def _random_routing(shape, T, seed, n_used=None):
     return idx.astype(np.int32), w
 
 
-@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 9, None), (TINY, 31, None),
-                                            (TINY, 32, None), (TINY, 300, None), (BEAM, 1, None),
+@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 4, None),
+                                            (TINY, 9, None), (TINY, 31, None), (TINY, 32, None),
+                                            (TINY, 300, None), (BEAM, 1, None), (BEAM, 2, None),
                                             (BEAM, 4, None), (BEAM, 40, 12), (BEAM, 200, 10)])
 def test_moe(shape, T, n_used):
-    """GEMV form below 32 tokens (fused down+combine up to 1024 pairs), grouped tensor-core
-    GEMMs from 32 tokens (n_used limits the distinct experts so several 128-row tiles and
+    """GEMV form below 32 tokens (one token: its slots used directly; up to 4 tokens: the down
+    kernel's last CTA per row block combines; then down+combine in shared memory up to 1024
+    pairs), grouped tensor-core GEMMs from 32 tokens (n_used limits the distinct experts so several 128-row tiles and
     ragged tails occur per expert)."""
     seed = 55 + T
     cfg = cfg_of(shape)
@@ -284,12 +296,21 @@ def test_bad_positions_are_flagged_and_skipped():
     B.beam_qkv_gate(cfg, u, W["w_qkvg"], W["q_norm"], W["k_norm"], bad_seq, pos, q, g, kc,
                     ws_for(cfg, 2))
     assert B.beam_get_device_status() & B.DEV_BAD_SEQ
-    idx = torch.tensor([[0, 1, 99, 2]], dtype=torch.int32, device=DEV)
-    w = torch.full((1, 4), 0.5, dtype=torch.float32, device=DEV)
+    # one token (its slots used directly) and two tokens (through the expert plan): the slot
+    # with an out-of-range expert is flagged and left out of the combine
     wgu, wdn = synth.expert_weights(shape, 0, 1, device=DEV)
-    out = torch.empty((1, shape.hidden), dtype=torch.bfloat16, device=DEV)
-    B.beam_moe(cfg_of(shape), u[:1], idx, w, wgu, wdn, out, ws_for(cfg, 1))
-    assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+    for rows in ([[0, 1, 99, 2]], [[0, 1, 99, 2], [5, -3, 1, 7]]):
+        idx = torch.tensor(rows, dtype=torch.int32, device=DEV)
+        T = idx.shape[0]
+        w = torch.full((T, 4), 0.5, dtype=torch.float32, device=DEV)
+        out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+        B.beam_moe(cfg_of(shape), u[:T], idx, w, wgu, wdn, out, ws_for(cfg, T))
+        assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+        for t in range(T):
+            keep = [j for j in range(4) if 0 <= rows[t][j] < shape.n_experts]
+            ref = O.moe(shape, np64(u[t:t + 1]), np.asarray([[rows[t][j] for j in keep]]),
+                        np.full((1, len(keep)), 0.5), np64(wgu), np64(wdn))
+            assert_close(np64(out[t:t + 1]), ref, "moe out, valid slots")
 
 
 def test_invalid_arguments_return_errors():
