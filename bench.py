@@ -172,7 +172,10 @@ class Workload:
         for l in layers:
             W.append(synth.layer_weights(shape, l, args.seed, device=device))
             nope = is_nope(l, shape.n_layers)
-            cap, win = (ctx + chunk + 8, 0) if nope else (shape.window + chunk - 1, shape.window)
+            # a sliding-window ring holds window + chunk - 1 keys, rounded up to whole 128-key
+            # tiles (the tensor-core prefill walks the ring in tile-aligned slots)
+            cap, win = ((ctx + chunk + 8, 0) if nope else
+                        (-(-(shape.window + chunk - 1) // 128) * 128, shape.window))
             c = synth.kv_cache(shape, batch, cap, args.seed, l, fp8=fp8, k_scale=scale,
                                v_scale=scale, device=device)
             caches.append(B.KVCache(c["k"], c["v"], win, scale, scale))

@@ -20,6 +20,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include "attn_tc.cuh"
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
@@ -752,6 +753,9 @@ size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
     b += align_up(parts * c->head_dim * 4, 256) + align_up(parts * 2 * 4, 256);
     b += align_up(size_t(T) * c->n_kv * 4, 256);     // split completion counters
   }
+  const size_t tcb = atc::ws_bytes(T);                  // or the tensor-core prefill's job list
+  const size_t dec = b - align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
+  if (tcb > dec) b += tcb - dec;
   return b;
 }
 
@@ -798,6 +802,14 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     else
       e = fp8 ? launch_decode<64, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st)
               : launch_decode<64, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st);
+    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+  } else if (atc::prefill_supported(D, cfg->n_q / cfg->n_kv, cache->window, cache->capacity, fp8,
+                                     q, cache->k, cache->v)) {
+    const size_t tcb = atc::ws_bytes(T);
+    void* jw = cv.take<char>(tcb);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    e = atc::prefill(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, D, *cache, sl2, og, jw,
+                     tcb, st);
     if (e != cudaSuccess) return BEAM_ERR_CUDA;
   } else {
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;

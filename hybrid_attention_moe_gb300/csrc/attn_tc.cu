@@ -1,0 +1,616 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05), BF16 KV cache.
+// Beam page, Attention section: 48 query heads share 8 KV heads of dim 128 (GQA); sliding-window
+// layers see the last 512 keys, NoPE layers the whole context (SSMax is already applied to q by
+// the projection epilogue); the output of each head is gated by sigmoid(gate + per-head bias).
+//
+// Work item = (KV head, job), job = up to TPT = floor(128 / G) consecutive tokens of one
+// sequence. The G query heads of those tokens form the 128 rows of one MMA tile (row =
+// token * G + head), so every K/V tile brought on chip serves the whole KV group. A persistent
+// grid walks the items; per item the key axis is streamed in tiles of 128 keys:
+//   S = Q . K^T           tcgen05.mma, A = Q (shared memory), B = K tile, FP32 in TMEM
+//   P = exp2(S * c - m)   softmax warps, thread per row (TMEM lane), online max with lazy
+//                         rescaling of O (only when a row max grows by more than 2^8)
+//   O += P . V            tcgen05.mma, A = P from TMEM, B = V tile (MN-major)
+// P is written back over its S columns as BF16 hi and lo parts (P = hi + lo to ~16 bits), and
+// both are multiplied by V, so the P.V product keeps FP32-level accuracy.
+//
+// Warps: 0 TMA (Q per item, K and V rings), 1 MMA issue (+ zeroing V rows outside the item's
+// key range, which may be uninitialised cache memory), 2-5 softmax and epilogue. TMEM columns:
+// S double buffer [0, 256), O [256, 256 + D). Every wait is bounded: on expiry the CTA records
+// BEAM_DEV_TIMEOUT, lets issued copies land, frees TMEM and returns.
+#include <cuda.h>
+#include <math.h>
+
+#include "attn_tc.cuh"
+#include "common.cuh"
+#include "mma.cuh"
+#include "tcgen05.cuh"
+
+namespace beam {
+namespace atc {
+namespace {
+
+using namespace beam::tc;
+
+constexpr int KT = 128;          // keys per tile
+constexpr int ROWS = 128;        // MMA rows
+constexpr int KSTAGES = 2, VSTAGES = 2;
+constexpr int THREADS = 192;
+constexpr float kRescale = 8.f;  // log2 units
+constexpr float kNegInf = -INFINITY;
+
+struct Job {
+  int t0, n, seq, key_a, key_b, pad0, pad1, pad2;
+};
+
+// Shared memory (offsets from a 1024-aligned base). A 64-column half of a 128-row bf16 tile is
+// 128 rows x 128 B = 16 KB (128-byte swizzle atoms of 8 rows).
+template <int D>
+struct Smem {
+  static constexpr int NH = D / 64;
+  static constexpr int HALF = ROWS * 128;
+  static constexpr int TILE = NH * KT * 128;   // K or V tile
+  static constexpr int Q = 0;
+  static constexpr int K0 = NH * HALF;
+  static constexpr int V0 = K0 + KSTAGES * TILE;
+  static constexpr int BAR = V0 + VSTAGES * TILE;
+  static constexpr int NBAR = 2 + 2 * KSTAGES + 2 * VSTAGES + 6 + 2;
+  static constexpr int BYTES = BAR + NBAR * 8 + 16 + 1024;
+};
+
+struct Params {
+  const Job* jobs;
+  const int* n_jobs;
+  const int32_t* pos;
+  const uint16_t* gpre;
+  const uint16_t* gate_bias;
+  uint16_t* og;
+  int T, n_q, n_kv, G, TPT, window, cap;
+  float sl2;
+};
+
+// Keys of an item, walked in tiles of KT slots. Tile i covers keys key_first + i*KT + c
+// (c < KT) at cache slots (first_slot + i*KT + c) mod cap; a ring cache (window > 0) has
+// cap % KT == 0 and tiles aligned to KT slots, so no tile crosses the end of the ring.
+struct Walk {
+  int n, first_slot, key_first;
+};
+__device__ __forceinline__ Walk walk_of(const Job& J, int window, int cap) {
+  Walk w{0, 0, 1};
+  if (J.key_b < J.key_a) return w;
+  const int s_a = (J.key_a - 1) % cap;
+  const int t_s = window > 0 ? (s_a / KT) * KT : s_a;
+  w.first_slot = t_s;
+  w.key_first = J.key_a - (s_a - t_s);
+  w.n = (J.key_b - w.key_first + KT) / KT;
+  return w;
+}
+
+__device__ __forceinline__ bool row_pos_ok(int p, int window, int cap) {
+  return p >= 1 && !(window == 0 && p > cap);
+}
+
+// ------------------------------------------------------------------------------------------
+// Job plan: runs of consecutive tokens with the same seq_id, cut into jobs of <= TPT tokens;
+// per job the union [key_a, key_b] of its tokens' key ranges. One CTA of 1024 threads.
+// ------------------------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ int block_scan_max_incl(int v, int* ws) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = max(v, n);
+  }
+  __syncthreads();
+  if (lane == 31) ws[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int t = ws[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t = max(t, n);
+    }
+    ws[lane] = t;
+  }
+  __syncthreads();
+  return wid > 0 ? max(v, ws[wid - 1]) : v;
+}
+
+__device__ __forceinline__ int block_scan_sum_excl(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  __syncthreads();
+  if (lane == 31) ws[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    int t = ws[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    ws[lane] = t;
+  }
+  __syncthreads();
+  *total = ws[31];
+  return (wid > 0 ? ws[wid - 1] : 0) + inc - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) attn_tc_plan_kernel(
+    const int32_t* __restrict__ seq_id, const int32_t* __restrict__ pos, int T, int TPT,
+    int window, int cap, int num_seqs, Job* __restrict__ jobs, int* __restrict__ n_jobs) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int ws[32];
+  __shared__ int s_njobs;
+  int carry_start = 0, carry_jobs = 0;
+  for (int base = 0; base < T; base += kPlanThreads) {
+    const int t = base + threadIdx.x;
+    const bool valid = t < T;
+    const int sq = valid ? seq_id[t] : 0;
+    const bool run_start = valid && (t == 0 || seq_id[t - 1] != sq);
+    const int rs = max(carry_start, block_scan_max_incl(run_start ? t : -1, ws));
+    const bool job_start = valid && ((t - rs) % TPT) == 0;
+    int total;
+    const int jpos = carry_jobs + block_scan_sum_excl(job_start ? 1 : 0, ws, &total);
+    if (job_start) jobs[jpos].t0 = t;
+    // the last thread's run start carries into the next chunk
+    __syncthreads();
+    if (threadIdx.x == kPlanThreads - 1) ws[0] = rs;
+    __syncthreads();
+    carry_start = ws[0];
+    carry_jobs += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) s_njobs = carry_jobs;
+  __threadfence_block();
+  __syncthreads();
+  const int nj = s_njobs;
+  for (int jb = threadIdx.x; jb < nj; jb += kPlanThreads) {
+    const int t0 = jobs[jb].t0;
+    const int t1 = jb + 1 < nj ? jobs[jb + 1].t0 : T;
+    Job J;
+    J.t0 = t0;
+    J.n = t1 - t0;
+    J.seq = seq_id[t0];
+    J.key_a = 0x7fffffff;
+    J.key_b = 0;
+    J.pad0 = J.pad1 = J.pad2 = 0;
+    const bool seq_ok = J.seq >= 0 && J.seq < num_seqs;
+    if (!seq_ok) flag(BEAM_DEV_BAD_SEQ);
+    for (int t = t0; t < t1 && seq_ok; ++t) {
+      const int p = pos[t];
+      if (!row_pos_ok(p, window, cap)) {
+        flag(BEAM_DEV_BAD_POSITION);
+        continue;
+      }
+      J.key_a = min(J.key_a, window > 0 ? max(1, p - window + 1) : 1);
+      J.key_b = max(J.key_b, p);
+    }
+    if (J.key_b < J.key_a) J.key_a = 1, J.key_b = 0;
+    jobs[jb + T] = J;   // written to the second half: first-half t0 values are still read
+  }
+  __threadfence_block();
+  __syncthreads();
+  for (int jb = threadIdx.x; jb < nj; jb += kPlanThreads) jobs[jb] = jobs[jb + T];
+  if (threadIdx.x == 0) *n_jobs = nj;
+}
+
+// ------------------------------------------------------------------------------------------
+// The attention kernel
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __grid_constant__ CUtensorMap tv, Params p) {
+  pdl_trigger();
+  pdl_wait();
+  using S = Smem<D>;
+  constexpr uint32_t IDESC_QK = idesc_bf16(ROWS, KT, false);
+  constexpr uint32_t IDESC_PV = idesc_bf16(ROWS, D, true);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + S::Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
+  const uint32_t b0 = smem_u32(bars);
+  const uint32_t q_full = b0, q_empty = b0 + 8;
+  const uint32_t k_full = b0 + 16, k_empty = k_full + 8 * KSTAGES;
+  const uint32_t v_full = k_empty + 8 * KSTAGES, v_empty = v_full + 8 * VSTAGES;
+  const uint32_t s_full = v_empty + 8 * VSTAGES, p_full = s_full + 16, s_free = p_full + 16;
+  const uint32_t o_full = s_free + 16, o_empty = o_full + 8;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::BAR + S::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int njobs = *p.n_jobs;
+  const int n_work = njobs * p.n_kv;
+  const int G = p.G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < KSTAGES; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < VSTAGES; ++s) {
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + 8 * b, 1);
+      mbar_init(p_full + 8 * b, 128);
+      mbar_init(s_free + 8 * b, 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 128);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  {   // Q rows past G * TPT are never written by TMA: keep them zero
+    const int q0 = G * p.TPT;
+    const int n16 = (ROWS - q0) * 8;   // 16-byte chunks per half
+    for (int i = threadIdx.x; i < n16 * S::NH; i += THREADS) {
+      const int h = i / n16, c = i - h * n16;
+      *reinterpret_cast<uint4*>(smem + S::Q + h * S::HALF + q0 * 128 + c * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tO = tmem + 256;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t kc = 0, vc = 0;
+      int item = 0;
+      int last_k[KSTAGES], last_v[VSTAGES], last_q = -1;
+      for (int s = 0; s < KSTAGES; ++s) last_k[s] = -1;
+      for (int s = 0; s < VSTAGES; ++s) last_v[s] = -1;
+      for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++item) {
+        if (*abort_flag) break;
+        const int hk = w / njobs;
+        const Job J = p.jobs[w - hk * njobs];
+        if (!mbar_wait(q_empty, (item & 1) ^ 1)) { *abort_flag = 1; break; }
+        mbar_expect_tx(q_full, uint32_t(S::NH * 128 * G * p.TPT));
+        for (int h = 0; h < S::NH; ++h) tma_load_3d(sQ + h * S::HALF, &tq, 64 * h, hk * G, J.t0, q_full);
+        last_q = item;
+        const Walk wk = walk_of(J, p.window, p.cap);
+        const int zidx = J.seq * p.n_kv + hk;
+        bool bad = false;
+        for (int i = 0; i < wk.n; ++i) {
+          int slot = wk.first_slot + i * KT;
+          if (p.window > 0) slot %= p.cap;
+          const int ks = int(kc % KSTAGES);
+          if (*abort_flag || !mbar_wait(k_empty + 8 * ks, ((kc / KSTAGES) & 1) ^ 1)) { bad = true; break; }
+          mbar_expect_tx(k_full + 8 * ks, uint32_t(S::TILE));
+          for (int h = 0; h < S::NH; ++h)
+            tma_load_3d(sb + S::K0 + ks * S::TILE + h * KT * 128, &tk, 64 * h, slot, zidx, k_full + 8 * ks);
+          last_k[ks] = int(kc);
+          ++kc;
+          const int vs = int(vc % VSTAGES);
+          if (*abort_flag || !mbar_wait(v_empty + 8 * vs, ((vc / VSTAGES) & 1) ^ 1)) { bad = true; break; }
+          mbar_expect_tx(v_full + 8 * vs, uint32_t(S::TILE));
+          for (int h = 0; h < S::NH; ++h)
+            tma_load_3d(sb + S::V0 + vs * S::TILE + h * KT * 128, &tv, 64 * h, slot, zidx, v_full + 8 * vs);
+          last_v[vs] = int(vc);
+          ++vc;
+        }
+        if (bad) { *abort_flag = 1; break; }
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        for (int s = 0; s < KSTAGES; ++s)
+          if (last_k[s] >= 0) mbar_wait(k_full + 8 * s, (uint32_t(last_k[s]) / KSTAGES) & 1);
+        for (int s = 0; s < VSTAGES; ++s)
+          if (last_v[s] >= 0) mbar_wait(v_full + 8 * s, (uint32_t(last_v[s]) / VSTAGES) & 1);
+        if (last_q >= 0) mbar_wait(q_full, uint32_t(last_q) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issue
+    uint32_t kc = 0, vc = 0, g = 0;
+    int item = 0;
+    bool ok = true;
+    // P.V of S tile gg (tile i of the item): zero V rows outside [key_a, key_b], then
+    // O (+)= P_hi . V + P_lo . V
+    auto pv = [&](const Job& J, const Walk& wk, int i, uint32_t gg) {
+      const int vs = int(vc % VSTAGES);
+      bool w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
+                  mbar_wait(p_full + 8 * (gg & 1), (gg >> 1) & 1);
+      if (i == 0) w_ok = w_ok && mbar_wait(o_empty, (uint32_t(item) & 1) ^ 1);
+      if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) { ok = false; return; }
+      const int kb = wk.key_first + i * KT;
+      const int r0 = max(0, J.key_a - kb), r1 = min(KT, J.key_b - kb + 1);
+      if (r0 > 0 || r1 < KT) {
+        uint8_t* vt = smem + S::V0 + vs * S::TILE;
+        const int nz = (r0 + (KT - r1)) * 8;   // 16-byte chunks per half
+        for (int c = lane; c < nz * S::NH; c += 32) {
+          const int h = c / nz, e = c - h * nz;
+          const int row = e / 8 < r0 ? e / 8 : r1 + (e / 8 - r0);
+          *reinterpret_cast<uint4*>(vt + h * KT * 128 + row * 128 + (e % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sv = sb + S::V0 + vs * S::TILE;
+        const uint32_t ts = tmem + (gg & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint64_t bd = smem_desc_mn(sv + kk * 16 * 128, KT * 128, 1024);
+          const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
+          umma_ts(tO, a_hi, bd, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tO, a_hi + 16, bd, IDESC_PV, 1u);
+        }
+        umma_commit(v_empty + 8 * vs);
+        umma_commit(s_free + 8 * (gg & 1));
+      }
+      __syncwarp();
+      ++vc;
+    };
+    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item) {
+      const int hk = w / njobs;
+      const Job J = p.jobs[w - hk * njobs];
+      const Walk wk = walk_of(J, p.window, p.cap);
+      if (!__all_sync(0xffffffffu, mbar_wait(q_full, uint32_t(item) & 1)) || *abort_flag) { ok = false; break; }
+      tc_fence_after();
+      for (int i = 0; i < wk.n && ok; ++i, ++g) {
+        const int ks = int(kc % KSTAGES);
+        bool w_ok = mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1);
+        if (g >= 2) w_ok = w_ok && mbar_wait(s_free + 8 * (g & 1), ((g - 2) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sk = sb + S::K0 + ks * S::TILE;
+          const uint32_t ts = tmem + (g & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            umma_ss(ts, smem_desc(sQ + (kk >> 2) * S::HALF + off),
+                    smem_desc(sk + (kk >> 2) * KT * 128 + off), IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(k_empty + 8 * ks);
+          umma_commit(s_full + 8 * (g & 1));
+          if (i == wk.n - 1) umma_commit(q_empty);
+        }
+        __syncwarp();
+        ++kc;
+        if (i >= 1) pv(J, wk, i - 1, g - 1);
+      }
+      if (!ok) break;
+      if (wk.n >= 1) {
+        pv(J, wk, wk.n - 1, g - 1);
+        if (!ok) break;
+      } else {
+        // no keys: release Q; O is never written, the epilogue stores zeros
+        if (!__all_sync(0xffffffffu, mbar_wait(o_empty, (uint32_t(item) & 1) ^ 1))) { ok = false; break; }
+        if (lane == 0) umma_commit(q_empty);
+      }
+      if (lane == 0) umma_commit(o_full);
+      __syncwarp();
+    }
+    if (!ok) *abort_flag = 1;
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lrow = uint32_t(q4 * 32) << 16;
+    const int tl = r / G, hj = r - tl * G;
+    uint32_t g = 0;
+    int item = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item) {
+      const int hk = w / njobs;
+      const Job J = p.jobs[w - hk * njobs];
+      const Walk wk = walk_of(J, p.window, p.cap);
+      const bool row_ok = tl < p.TPT && tl < J.n;
+      int pr = 0, lo = 1;
+      if (row_ok) {
+        const int pp = p.pos[J.t0 + tl];
+        if (row_pos_ok(pp, p.window, p.cap)) {
+          pr = min(pp, J.key_b);
+          lo = p.window > 0 ? max(1, pp - p.window + 1) : 1;
+        }
+      }
+      float m_ref = kNegInf, l = 0.f;
+      for (int i = 0; i < wk.n; ++i, ++g) {
+        const uint32_t b = g & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * b, (g >> 1) & 1)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ts = tmem + b * 128 + lrow;
+        uint32_t sv[KT];
+#pragma unroll
+        for (int c = 0; c < KT / 32; ++c) tmem_ld32_nowait(ts + 32 * c, sv + 32 * c);
+        tmem_wait_ld();
+        const int kb = wk.key_first + i * KT;
+        const int c_lo = lo - kb, c_hi = pr - kb;   // valid columns [c_lo, c_hi]
+        const bool full = c_lo <= 0 && c_hi >= KT - 1;
+        float mx = kNegInf;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < KT; ++c)
+            if (c >= c_lo && c <= c_hi) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        }
+        const float mt = mx * p.sl2;
+        const bool need = m_ref != kNegInf && mt > m_ref + kRescale;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds the earlier tiles' P.V of this item: wait for the last one, then rescale
+          if (!__all_sync(0xffffffffu, mbar_wait(s_free + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = need ? exp2f(m_ref - mt) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_nowait(tO + lrow + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(tO + lrow + 32 * c, o);
+          }
+          tmem_wait_st();
+          if (need) {
+            l *= f;
+            m_ref = mt;
+          }
+        }
+        if (m_ref == kNegInf) m_ref = mt;   // first keys of the row: O row is still zero
+        const float mref = m_ref == kNegInf ? 0.f : m_ref;
+#pragma unroll
+        for (int c4 = 0; c4 < KT / 32; ++c4) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int c = 32 * c4 + 2 * q;
+            float p0 = exp2f(fmaf(__uint_as_float(sv[c]), p.sl2, -mref));
+            float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), p.sl2, -mref));
+            if (!full) {
+              p0 = (c >= c_lo && c <= c_hi) ? p0 : 0.f;
+              p1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? p1 : 0.f;
+            }
+            l += p0;
+            l += p1;
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            pk[q] = hi;
+            pk[16 + q] = pack_bf16x2(p0 - bf_lo(hi), p1 - bf_hi(hi));
+          }
+          tmem_st32(ts + 32 * c4, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full + 8 * b);
+      }
+      if (!ok) break;
+      // epilogue: o = O / l, rounded, gated, rounded
+      if (!__all_sync(0xffffffffu, mbar_wait(o_full, uint32_t(item) & 1)) || *abort_flag) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t ov[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + lrow + 32 * c, ov + 32 * c);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(o_empty);
+      if (row_ok) {
+        const int t = J.t0 + tl, hq = hk * G + hj;
+        const float inv = (wk.n > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const size_t oi = (size_t(t) * p.n_q + hq) * D;
+        const float gb = bf2f(p.gate_bias[hq]);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 gv = *reinterpret_cast<const uint4*>(p.gpre + oi + 8 * c);
+          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+          uint32_t q[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float o0 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e]) * inv) : 0.f;
+            const float o1 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e + 1]) * inv) : 0.f;
+            const float g0 = sigmoidf_(bf_lo(gw[e]) + gb), g1 = sigmoidf_(bf_hi(gw[e]) + gb);
+            q[e] = pack_bf16x2(o0 * g0, o1 * g1);
+          }
+          *reinterpret_cast<uint4*>(p.og + oi + 8 * c) = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag(BEAM_DEV_TIMEOUT);
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool prefill_supported(int D, int G, int window, int cap, bool fp8, const void* q,
+                       const void* k, const void* v) {
+  if (fp8 || (D != 64 && D != 128) || G < 1 || G > ROWS) return false;
+  if (window > 0 && cap % KT != 0) return false;
+  return aligned16(q) && aligned16(k) && aligned16(v) && tensor_map_encoder_ready();
+}
+
+size_t ws_bytes(int T) { return align_up(size_t(2 * T + 1) * sizeof(Job), 256) + 256; }
+
+cudaError_t prefill(const uint16_t* q, const uint16_t* g, const uint16_t* gate_bias,
+                    const int32_t* seq_id, const int32_t* pos, int T, int n_q, int n_kv, int D,
+                    const beam_kv_cache& kc, float sl2, uint16_t* og, void* ws, size_t ws_len,
+                    cudaStream_t st) {
+  const int G = n_q / n_kv, TPT = ROWS / G;
+  if (ws_len < ws_bytes(T)) return cudaErrorInvalidValue;
+  Job* jobs = static_cast<Job*>(ws);
+  int* n_jobs = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(size_t(2 * T + 1) * sizeof(Job), 256));
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[3] = {uint64_t(D), uint64_t(n_q), uint64_t(T)};
+    const uint64_t str[2] = {uint64_t(D) * 2, uint64_t(n_q) * D * 2};
+    const uint32_t box[3] = {64, uint32_t(G), uint32_t(TPT)};
+    if (!encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {uint64_t(D), uint64_t(kc.capacity), uint64_t(kc.num_seqs) * n_kv};
+    const uint64_t str[2] = {uint64_t(D) * 2, uint64_t(kc.capacity) * D * 2};
+    const uint32_t box[3] = {64, uint32_t(KT), 1};
+    if (!encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kc.k, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kc.v, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  launch_pdl(attn_tc_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_id, pos, T, TPT,
+             kc.window, kc.capacity, kc.num_seqs, jobs, n_jobs);
+  Params prm{jobs, n_jobs, pos, g, gate_bias, og, T, n_q, n_kv, G, TPT, kc.window, kc.capacity, sl2};
+  int grid = num_sms_cached();
+  if (int64_t(T) * n_kv < grid) grid = T * n_kv;
+  if (D == 128) {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
+    if (e != cudaSuccess) return e;
+    launch_pdl(attn_prefill_tc_kernel<128>, dim3(grid), dim3(THREADS), Smem<128>::BYTES, st, mq, mk, mv, prm);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
+    if (e != cudaSuccess) return e;
+    launch_pdl(attn_prefill_tc_kernel<64>, dim3(grid), dim3(THREADS), Smem<64>::BYTES, st, mq, mk, mv, prm);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace atc
+}  // namespace beam

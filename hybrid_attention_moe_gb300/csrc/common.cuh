@@ -91,6 +91,9 @@ inline bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(
 // Host-side count of kernel launches (misc.cu).
 void note_launches(int n);
 
+// Number of SMs of the current device (queried once).
+int num_sms_cached();
+
 // Launch with programmatic stream serialization: the kernel may start while its predecessor
 // in the stream finishes; it must execute griddepcontrol.wait (pdl_wait) before reading or
 // writing anything a predecessor touches. Kernels launched this way all begin with

@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "mma.cuh"
+#include "tcgen05.cuh"
 
 namespace beam {
 namespace tc {
@@ -28,77 +29,10 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int THREADS = 192;
 constexpr int kGroupM = 16;   // row tiles walked per column tile (dense grids)
-constexpr uint32_t kWaitLimit = 1u << 22;
-
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false after kWaitLimit polls (each poll may suspend the thread briefly).
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try(a, parity)) return true;
-  return false;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(mbar)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups of 128 B
-// stacked at 1024 B (stride byte offset); the leading byte offset is unused for this layout.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-  uint64_t d = uint64_t((saddr >> 4) & 0x3FFFu);
-  d |= uint64_t(1) << 16;             // leading byte offset (ignored), 16 B units
-  d |= uint64_t(1024 >> 4) << 32;     // stride byte offset, 16 B units
-  d |= uint64_t(1) << 46;             // descriptor version for tcgen05
-  d |= uint64_t(2) << 61;             // swizzle: 128 B
-  return d;
-}
-
-// Instruction descriptor of kind::f16: BF16 A and B (K-major), FP32 D, M = 128, N = BN.
-constexpr uint32_t kIdesc = (1u << 4)            // D format F32
-                            | (1u << 7)          // A format BF16
-                            | (1u << 10)         // B format BF16
-                            | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN, false);
 
 __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
-          tmem_d),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  umma_ss(tmem_d, a, b, kIdesc, acc);
 }
 
 // One CTA computes output columns [n0, n0 + BN) (kSwiGLU: units [n0, n0 + BN/2)) for A rows
@@ -297,9 +231,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// 2-D bf16 map over rows x inner (row stride ld elements), box box_rows x 64, 128 B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int box_rows) {
+  const uint64_t d[2] = {uint64_t(inner), uint64_t(rows)};
+  const uint64_t st[1] = {uint64_t(ld) * 2};
+  const uint32_t bx[2] = {uint32_t(BK), uint32_t(box_rows)};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, d, st, bx,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
-bool encoder() {
+}  // namespace
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+bool tensor_map_encoder_ready() {
   if (g_encode == nullptr) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -312,19 +259,22 @@ bool encoder() {
   return true;
 }
 
-// 2-D bf16 map over rows x inner (row stride ld elements), box box_rows x 64, 128 B swizzle.
-bool make_map(CUtensorMap* m, const void* base, int inner, int rows, int ld, int box_rows) {
-  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
-  cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
-  cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swz) {
+  if (!tensor_map_encoder_ready() || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return g_encode(m, dt, cuuint32_t(rank), const_cast<void*>(base), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool gemm_supported(const void* A, int lda, const void* B, int ldb, int K) {
   return aligned16(A) && aligned16(B) && (lda % 8) == 0 && (ldb % 8) == 0 && (K % 8) == 0 &&
@@ -349,7 +299,7 @@ cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* 
                       void* C, int ldc, bool out_bf16, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
-  if (!encoder()) return cudaErrorNotSupported;
+  if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
     return cudaErrorInvalidValue;
@@ -362,7 +312,7 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
                         int ldb, uint16_t* C, int ldc, cudaStream_t st) {
   if (M <= 0 || F <= 0) return cudaSuccess;
   if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
-  if (!encoder()) return cudaErrorNotSupported;
+  if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, 2 * F, ldb, BN / 2))
     return cudaErrorInvalidValue;
@@ -377,7 +327,7 @@ cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, con
                          cudaStream_t st) {
   if (M <= 0 || N <= 0 || max_jobs <= 0) return cudaSuccess;
   if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
-  if (!encoder()) return cudaErrorNotSupported;
+  if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const int bbox = mode == kSwiGLU ? BN / 2 : BN;
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, b_rows, ldb, bbox))

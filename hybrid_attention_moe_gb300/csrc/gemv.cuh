@@ -126,8 +126,6 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
   }
 }
 
-int num_sms_cached();
-
 // Host launcher: the register-pipelined kernel with the token tile, rows per warp and chunks in
 // flight picked from T.
 template <int MODE>

@@ -139,13 +139,22 @@ ATTN_CASES = [
 ]
 
 
+# layer kind: NoPE (whole context), sliding window with the smallest ring, sliding window with
+# the ring rounded up to a multiple of 128 slots (the layout the tensor-core prefill kernel
+# takes for a ring)
+ATTN_KINDS = ["nope", "swa", "swa_ring128"]
+
+
 @pytest.mark.parametrize("case", range(len(ATTN_CASES)))
-@pytest.mark.parametrize("nope", [False, True])
+@pytest.mark.parametrize("kind", ATTN_KINDS)
 @pytest.mark.parametrize("fp8", [False, True])
 @pytest.mark.parametrize("form", ["natural", "other"])
-def test_attn(case, nope, fp8, form):
+def test_attn(case, kind, fp8, form):
     """form 'natural' passes the true tokens per sequence (split-K decode up to 4, query tiles
-    above); 'other' forces the other kernel, which must give the same result."""
+    above: tensor-core tiles for a BF16 cache, else mma.sync tiles); 'other' forces the other
+    form, which must give the same result. Cache slots past every query position hold NaN in
+    NoPE layers: no kernel may let them reach a result."""
+    nope = kind == "nope"
     shape, ctxs, per = ATTN_CASES[case]
     mq = per if form == "natural" else (64 if per <= 4 else 1)
     seed = 31 + case
@@ -158,9 +167,15 @@ def test_attn(case, nope, fp8, form):
         cap, window = max_pos + 5, 0
     else:
         cap, window = shape.window + per + 2, shape.window
+        if kind == "swa_ring128":
+            cap = -(-cap // 128) * 128
     scale = (0.0371, 0.5) if fp8 else (1.0, 1.0)
     c = synth.kv_cache(shape, S, cap, seed, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
                        device=DEV)
+    if nope:
+        nan = 0x7F if fp8 else float("nan")     # e4m3fn code 0x7F is NaN
+        c["k"][:, :, max_pos:] = nan
+        c["v"][:, :, max_pos:] = nan
     kc = B.KVCache(c["k"], c["v"], window, *scale)
     q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, seed, ("q",), DEV)
     g = synth.activations(T, shape.q_rows, seed, "g", DEV)
