@@ -59,11 +59,13 @@ _SIGS = {
     "beam_get_device_status": [_P, ctypes.POINTER(ctypes.c_uint32)],
     "beam_status_string": [_I],
     "beam_launch_count": [],
+    "beam_last_cuda_error": [],
     "beam_gemm_bf16": [_P, _I, _I, _I, _P, _I, _I, _P, _I, _I, _P],
     "beam_route_noalloc": [_P, _P, _P, _P, _I, _P, _P, _P],
 }
 _RES = {"beam_workspace_bytes": _Z, "beam_kv_cache_bytes": _Z,
-        "beam_status_string": ctypes.c_char_p, "beam_launch_count": ctypes.c_uint64}
+        "beam_status_string": ctypes.c_char_p, "beam_launch_count": ctypes.c_uint64,
+        "beam_last_cuda_error": ctypes.c_char_p}
 
 _lib = None
 
@@ -87,6 +89,8 @@ def lib():
 def _check(status, what):
     if status != 0:
         msg = lib().beam_status_string(status).decode()
+        if status == 3:
+            msg += " [" + lib().beam_last_cuda_error().decode() + "]"
         raise BeamError(f"{what} failed: {msg} ({status})")
 
 

@@ -792,9 +792,10 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     int* done = cv.take<int>(size_t(T) * cfg->n_kv);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
     // the cluster form merges on chip; the other counts finished splits from zero
-    if (pl.n_splits > kClusterMaxSplits &&
-        cudaMemsetAsync(done, 0, size_t(T) * cfg->n_kv * sizeof(int), st) != cudaSuccess)
-      return BEAM_ERR_CUDA;
+    if (pl.n_splits > kClusterMaxSplits) {
+      const cudaError_t err_ = cudaMemsetAsync(done, 0, size_t(T) * cfg->n_kv * sizeof(int), st);
+      if (err_ != cudaSuccess) return cuda_status(err_);
+    }
     const float vs = fp8 ? cache->v_scale : 1.f;
     if (D == 128)
       e = fp8 ? launch_decode<128, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st)
@@ -802,7 +803,7 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     else
       e = fp8 ? launch_decode<64, true>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st)
               : launch_decode<64, false>(q, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, pl, sl2, pacc, pml, done, vs, g, gate_bias, og, st);
-    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   } else if (atc::prefill_supported(D, cfg->n_q / cfg->n_kv, cache->window, cache->capacity, fp8,
                                      q, cache->k, cache->v)) {
     const size_t tcb = atc::ws_bytes(T);
@@ -810,7 +811,7 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
     e = atc::prefill(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, D, *cache, sl2, og, jw,
                      tcb, st);
-    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   } else {
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
     if (cfg->n_q / cfg->n_kv * 32 > 256) return BEAM_ERR_UNSUPPORTED;
@@ -820,12 +821,12 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     else
       e = fp8 ? launch_prefill<64, true>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st)
               : launch_prefill<64, false>(q, g, gate_bias, seq_id, pos, T, cfg->n_q, cfg->n_kv, *cache, sl2, og, st);
-    if (e != cudaSuccess) return BEAM_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   }
   const cudaError_t ge =
       T >= kGemmMinT && tc::gemm_supported(og, HD, w_o, HD, HD)
           ? tc::gemm_bf16(og, T, HD, HD, w_o, H, HD, out, H, true, st)
           : launch_gemv<kOutBF16>(w_o, H, HD, og, T, nullptr, out, H, st);
-  if (ge != cudaSuccess) return BEAM_ERR_CUDA;
+  if (ge != cudaSuccess) return cuda_status(ge);
   return BEAM_OK;
 }

@@ -3,10 +3,11 @@
 // layers see the last 512 keys, NoPE layers the whole context (SSMax is already applied to q by
 // the projection epilogue); the output of each head is gated by sigmoid(gate + per-head bias).
 //
-// Work item = (KV head, job), job = up to TPT = floor(128 / G) consecutive tokens of one
-// sequence. The G query heads of those tokens form the 128 rows of one MMA tile (row =
-// token * G + head), so every K/V tile brought on chip serves the whole KV group. A persistent
-// grid walks the items; per item the key axis is streamed in tiles of 128 keys:
+// Work item = (KV head, job), job = up to 2 TPT consecutive tokens of one sequence, TPT =
+// floor(128 / G). The G query heads of TPT tokens form the 128 rows of one MMA tile (row =
+// token * G + head); a job holds two such query tiles, A and B, so every K/V tile brought on
+// chip serves 2 TPT tokens of the whole KV group. A persistent grid walks the items; per item
+// the key axis is streamed in tiles of 128 keys, and for each query tile:
 //   S = Q . K^T           tcgen05.mma, A = Q (shared memory), B = K tile, FP32 in TMEM
 //   P = exp2(S * c - m)   softmax warps, thread per row (TMEM lane), online max with lazy
 //                         rescaling of O (only when a row max grows by more than 2^8)
@@ -15,9 +16,11 @@
 // both are multiplied by V, so the P.V product keeps FP32-level accuracy.
 //
 // Warps: 0 TMA (Q per item, K and V rings), 1 MMA issue (+ zeroing V rows outside the item's
-// key range, which may be uninitialised cache memory), 2-5 softmax and epilogue. TMEM columns:
-// S double buffer [0, 256), O [256, 256 + D). Every wait is bounded: on expiry the CTA records
-// BEAM_DEV_TIMEOUT, lets issued copies land, frees TMEM and returns.
+// key range, which may be uninitialised cache memory), 2-5 softmax and epilogue of tile A, 6-9
+// of tile B: while one warpgroup turns its S into P, the tensor pipe works on the other tile.
+// TMEM columns: S_A [0, 128), S_B [128, 256), O_A [256, 384), O_B [384, 512). Every wait is
+// bounded: on expiry the CTA records BEAM_DEV_TIMEOUT, lets issued copies land, frees TMEM and
+// returns.
 #include <cuda.h>
 #include <math.h>
 
@@ -35,7 +38,9 @@ using namespace beam::tc;
 constexpr int KT = 128;          // keys per tile
 constexpr int ROWS = 128;        // MMA rows
 constexpr int KSTAGES = 2, VSTAGES = 2;
-constexpr int THREADS = 192;
+// warp 0 TMA, warp 1 MMA, warps 2-17 softmax: query tile u = (warp - 2) / 8, column half
+// (warp - 2) / 4 % 2, TMEM lane quarter warp % 4 -- two threads per row, 64 columns each
+constexpr int THREADS = 576;
 constexpr float kRescale = 8.f;  // log2 units
 constexpr float kNegInf = -INFINITY;
 
@@ -50,12 +55,15 @@ struct Smem {
   static constexpr int NH = D / 64;
   static constexpr int HALF = ROWS * 128;
   static constexpr int TILE = NH * KT * 128;   // K or V tile
-  static constexpr int Q = 0;
-  static constexpr int K0 = NH * HALF;
+  static constexpr int Q = 0;                  // query tiles A and B
+  static constexpr int K0 = 2 * NH * HALF;
   static constexpr int V0 = K0 + KSTAGES * TILE;
   static constexpr int BAR = V0 + VSTAGES * TILE;
-  static constexpr int NBAR = 2 + 2 * KSTAGES + 2 * VSTAGES + 6 + 2;
-  static constexpr int BYTES = BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int NBAR = 2 + 2 * KSTAGES + 2 * VSTAGES + 10;
+  // row max (slots 0-1, by key-tile parity) and row sum (slots 2-3, by item parity) exchange
+  // between the two threads of a row: [slot][query tile][row][half] floats
+  static constexpr int XCH = BAR + NBAR * 8 + 16;
+  static constexpr int BYTES = XCH + 4 * 2 * 128 * 2 * 4 + 1024;
 };
 
 struct Params {
@@ -84,6 +92,14 @@ __device__ __forceinline__ Walk walk_of(const Job& J, int window, int cap) {
   w.key_first = J.key_a - (s_a - t_s);
   w.n = (J.key_b - w.key_first + KT) / KT;
   return w;
+}
+
+// 2^x by the SFU's approximate exp2 instruction (relative error below 2^-22; subnormal results
+// flush to zero, far below what a softmax row sum can notice).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ bool row_pos_ok(int p, int window, int cap) {
@@ -208,7 +224,9 @@ __global__ void __launch_bounds__(kPlanThreads) attn_tc_plan_kernel(
 // The attention kernel
 // ------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
+// 18 warps share the register file of 4 SM sub-partitions (16K registers each); two of them
+// hold 5 warps, so a thread gets at most 16384 / (5 * 32) -> 96 registers
+__global__ void __maxnreg__(96) attn_prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, Params p) {
   pdl_trigger();
@@ -220,14 +238,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t sQ = sb + S::Q;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR);
   const uint32_t b0 = smem_u32(bars);
   const uint32_t q_full = b0, q_empty = b0 + 8;
   const uint32_t k_full = b0 + 16, k_empty = k_full + 8 * KSTAGES;
   const uint32_t v_full = k_empty + 8 * KSTAGES, v_empty = v_full + 8 * VSTAGES;
+  // per query tile u: s_full[u], p_full[u], s_free[u], o_full[u], o_empty[u]
   const uint32_t s_full = v_empty + 8 * VSTAGES, p_full = s_full + 16, s_free = p_full + 16;
-  const uint32_t o_full = s_free + 16, o_empty = o_full + 8;
+  const uint32_t o_full = s_free + 16, o_empty = o_full + 16;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::BAR + S::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -246,21 +264,21 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
       mbar_init(v_full + 8 * s, 1);
       mbar_init(v_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full + 8 * b, 1);
-      mbar_init(p_full + 8 * b, 128);
-      mbar_init(s_free + 8 * b, 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(s_full + 8 * u, 1);
+      mbar_init(p_full + 8 * u, 256);
+      mbar_init(s_free + 8 * u, 1);
+      mbar_init(o_full + 8 * u, 1);
+      mbar_init(o_empty + 8 * u, 256);
     }
-    mbar_init(o_full, 1);
-    mbar_init(o_empty, 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   {   // Q rows past G * TPT are never written by TMA: keep them zero
     const int q0 = G * p.TPT;
     const int n16 = (ROWS - q0) * 8;   // 16-byte chunks per half
-    for (int i = threadIdx.x; i < n16 * S::NH; i += THREADS) {
-      const int h = i / n16, c = i - h * n16;
+    for (int i = threadIdx.x; i < n16 * S::NH * 2; i += THREADS) {
+      const int h = i / n16, c = i - h * n16;   // h: tile * NH + half
       *reinterpret_cast<uint4*>(smem + S::Q + h * S::HALF + q0 * 128 + c * 16) =
           make_uint4(0, 0, 0, 0);
     }
@@ -275,8 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t tO = tmem + 256;
+  const uint32_t tmem = *tmem_holder;   // S of tile u at column 128 u, O of tile u at 256 + 128 u
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -291,8 +308,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
         const int hk = w / njobs;
         const Job J = p.jobs[w - hk * njobs];
         if (!mbar_wait(q_empty, (item & 1) ^ 1)) { *abort_flag = 1; break; }
-        mbar_expect_tx(q_full, uint32_t(S::NH * 128 * G * p.TPT));
-        for (int h = 0; h < S::NH; ++h) tma_load_3d(sQ + h * S::HALF, &tq, 64 * h, hk * G, J.t0, q_full);
+        mbar_expect_tx(q_full, uint32_t(2 * S::NH * 128 * G * p.TPT));
+        for (int u = 0; u < 2; ++u)
+          for (int h = 0; h < S::NH; ++h)
+            tma_load_3d(sb + S::Q + (u * S::NH + h) * S::HALF, &tq, 64 * h, hk * G,
+                        J.t0 + u * p.TPT, q_full);
         last_q = item;
         const Walk wk = walk_of(J, p.window, p.cap);
         const int zidx = J.seq * p.n_kv + hk;
@@ -328,155 +348,241 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
-    uint32_t kc = 0, vc = 0, g = 0;
+    // Issue order per key tile j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1). Each P.V waits for
+    // its softmax warpgroup; the next S of the same query tile follows it at once. tcgen05.mma
+    // operations issued by one thread execute in issue order (an implicitly pipelined pair in
+    // the PTX memory model), so QK_u(j+1) overwrites the TMEM columns holding P_u(j) only after
+    // PV_u(j) has read them, and while one warpgroup computes its P the tensor pipe works
+    // through the other tile's P.V and the next S.
+    uint32_t kc = 0, vc = 0, pt = 0;   // pt: key tiles of earlier items (per query tile)
     int item = 0;
     bool ok = true;
-    // P.V of S tile gg (tile i of the item): zero V rows outside [key_a, key_b], then
-    // O (+)= P_hi . V + P_lo . V
-    auto pv = [&](const Job& J, const Walk& wk, int i, uint32_t gg) {
-      const int vs = int(vc % VSTAGES);
-      bool w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
-                  mbar_wait(p_full + 8 * (gg & 1), (gg >> 1) & 1);
-      if (i == 0) w_ok = w_ok && mbar_wait(o_empty, (uint32_t(item) & 1) ^ 1);
-      if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) { ok = false; return; }
-      const int kb = wk.key_first + i * KT;
-      const int r0 = max(0, J.key_a - kb), r1 = min(KT, J.key_b - kb + 1);
-      if (r0 > 0 || r1 < KT) {
-        uint8_t* vt = smem + S::V0 + vs * S::TILE;
-        const int nz = (r0 + (KT - r1)) * 8;   // 16-byte chunks per half
-        for (int c = lane; c < nz * S::NH; c += 32) {
-          const int h = c / nz, e = c - h * nz;
-          const int row = e / 8 < r0 ? e / 8 : r1 + (e / 8 - r0);
-          *reinterpret_cast<uint4*>(vt + h * KT * 128 + row * 128 + (e % 8) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      tc_fence_after();
+    auto all = [&](bool v) { return __all_sync(0xffffffffu, v) && !*abort_flag; };
+    // descriptors of stage 0 / query tile 0; others differ only in the start address field,
+    // (address >> 4) in the low 14 bits, which no offset below carries out of
+    const uint64_t dq0 = smem_desc(sb + S::Q), dk0 = smem_desc(sb + S::K0);
+    const uint64_t dv0 = smem_desc_mn(sb + S::V0, KT * 128, 1024);
+    auto qk = [&](int u, int ks) {
       if (lane == 0) {
-        const uint32_t sv = sb + S::V0 + vs * S::TILE;
-        const uint32_t ts = tmem + (gg & 1) * 128;
+        const uint64_t dq = dq0 + uint64_t((u * S::NH * S::HALF) >> 4);
+        const uint64_t dk = dk0 + uint64_t((ks * S::TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint64_t bd = smem_desc_mn(sv + kk * 16 * 128, KT * 128, 1024);
-          const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
-          umma_ts(tO, a_hi, bd, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-          umma_ts(tO, a_hi + 16, bd, IDESC_PV, 1u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk & 3) * 32) >> 4;
+          umma_ss(tmem + 128 * u, dq + ((kk >> 2) * S::HALF >> 4) + off,
+                  dk + ((kk >> 2) * KT * 128 >> 4) + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(v_empty + 8 * vs);
-        umma_commit(s_free + 8 * (gg & 1));
+        umma_commit(s_full + 8 * u);
       }
       __syncwarp();
-      ++vc;
+    };
+    auto pv = [&](int u, int vs, bool first) {
+      if (lane == 0) {
+        const uint64_t dv = dv0 + uint64_t((vs * S::TILE) >> 4);
+        const uint32_t ts = tmem + 128 * u, to = tmem + 256 + 128 * u;
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint64_t bd = dv + uint64_t((kk * 16 * 128) >> 4);
+          const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
+          umma_ts(to, a_hi, bd, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+          umma_ts(to, a_hi + 16, bd, IDESC_PV, 1u);
+        }
+        umma_commit(s_free + 8 * u);
+      }
+      __syncwarp();
     };
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item) {
       const int hk = w / njobs;
       const Job J = p.jobs[w - hk * njobs];
       const Walk wk = walk_of(J, p.window, p.cap);
-      if (!__all_sync(0xffffffffu, mbar_wait(q_full, uint32_t(item) & 1)) || *abort_flag) { ok = false; break; }
+      const uint32_t oph = (uint32_t(item) & 1) ^ 1;   // o_empty parity for this item
+      if (!all(mbar_wait(q_full, uint32_t(item) & 1))) { ok = false; break; }
       tc_fence_after();
-      for (int i = 0; i < wk.n && ok; ++i, ++g) {
-        const int ks = int(kc % KSTAGES);
-        bool w_ok = mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1);
-        if (g >= 2) w_ok = w_ok && mbar_wait(s_free + 8 * (g & 1), ((g - 2) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, w_ok) || *abort_flag) { ok = false; break; }
-        tc_fence_after();
+      if (wk.n == 0) {
+        // no keys: release Q; O is never written, the epilogue stores zeros
+        if (!all(mbar_wait(o_empty, oph) && mbar_wait(o_empty + 8, oph))) { ok = false; break; }
         if (lane == 0) {
-          const uint32_t sk = sb + S::K0 + ks * S::TILE;
-          const uint32_t ts = tmem + (g & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk & 3) * 32;
-            umma_ss(ts, smem_desc(sQ + (kk >> 2) * S::HALF + off),
-                    smem_desc(sk + (kk >> 2) * KT * 128 + off), IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(k_empty + 8 * ks);
-          umma_commit(s_full + 8 * (g & 1));
-          if (i == wk.n - 1) umma_commit(q_empty);
+          umma_commit(q_empty);
+          umma_commit(o_full);
+          umma_commit(o_full + 8);
         }
         __syncwarp();
-        ++kc;
-        if (i >= 1) pv(J, wk, i - 1, g - 1);
+        continue;
+      }
+      int ks = int(kc % KSTAGES);
+      if (!all(mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1))) { ok = false; break; }
+      tc_fence_after();
+      qk(0, ks);
+      qk(1, ks);
+      if (lane == 0) {
+        umma_commit(k_empty + 8 * ks);
+        if (wk.n == 1) umma_commit(q_empty);
+      }
+      __syncwarp();
+      ++kc;
+      uint32_t gt_i = 0;   // key tiles of this item done
+      for (int i = 0; i < wk.n; ++i) {
+        const int vs = int(vc % VSTAGES);
+        const bool more = i + 1 < wk.n;
+        // ---- query tile A: P.V of tile i, then S of tile i + 1
+        bool w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
+                    mbar_wait(p_full, (pt + gt_i) & 1);
+        if (i == 0) w_ok = w_ok && mbar_wait(o_empty, oph);
+        if (more) {
+          ks = int(kc % KSTAGES);
+          w_ok = w_ok && mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1);
+        }
+        if (!all(w_ok)) { ok = false; break; }
+        const int kb = wk.key_first + i * KT;
+        const int r0 = max(0, J.key_a - kb), r1 = min(KT, J.key_b - kb + 1);
+        if (r0 > 0 || r1 < KT) {
+          // V rows outside [key_a, key_b] may hold uninitialised memory: zero them
+          uint8_t* vt = smem + S::V0 + vs * S::TILE;
+          const int nz = (r0 + (KT - r1)) * 8;   // 16-byte chunks per half
+          for (int c = lane; c < nz * S::NH; c += 32) {
+            const int h = c / nz, e = c - h * nz;
+            const int row = e / 8 < r0 ? e / 8 : r1 + (e / 8 - r0);
+            *reinterpret_cast<uint4*>(vt + h * KT * 128 + row * 128 + (e % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        pv(0, vs, i == 0);
+        if (lane == 0 && !more) umma_commit(o_full);
+        __syncwarp();
+        if (more) qk(0, ks);
+        // ---- query tile B
+        w_ok = mbar_wait(p_full + 8, (pt + gt_i) & 1);
+        if (i == 0) w_ok = w_ok && mbar_wait(o_empty + 8, oph);
+        if (!all(w_ok)) { ok = false; break; }
+        tc_fence_after();
+        pv(1, vs, i == 0);
+        if (lane == 0) {
+          umma_commit(v_empty + 8 * vs);
+          if (!more) umma_commit(o_full + 8);
+        }
+        __syncwarp();
+        ++vc;
+        if (more) {
+          qk(1, ks);
+          if (lane == 0) {
+            umma_commit(k_empty + 8 * ks);
+            if (i + 1 == wk.n - 1) umma_commit(q_empty);
+          }
+          __syncwarp();
+          ++kc;
+        }
+        ++gt_i;
       }
       if (!ok) break;
-      if (wk.n >= 1) {
-        pv(J, wk, wk.n - 1, g - 1);
-        if (!ok) break;
-      } else {
-        // no keys: release Q; O is never written, the epilogue stores zeros
-        if (!__all_sync(0xffffffffu, mbar_wait(o_empty, (uint32_t(item) & 1) ^ 1))) { ok = false; break; }
-        if (lane == 0) umma_commit(q_empty);
-      }
-      if (lane == 0) umma_commit(o_full);
-      __syncwarp();
+      pt += uint32_t(wk.n);
     }
     if (!ok) *abort_flag = 1;
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
+    const int u = (warp - 2) >> 3;           // query tile
+    const int half = ((warp - 2) >> 2) & 1;  // columns [64 half, 64 half + 64) of S and O
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lrow = uint32_t(q4 * 32) << 16;
+    const uint32_t ts = tmem + 128 * u + 64 * half + lrow;
+    const uint32_t to = tmem + 256 + 128 * u + 64 * half + lrow;
+    const uint32_t my_s_full = s_full + 8 * u, my_p_full = p_full + 8 * u;
+    const uint32_t my_s_free = s_free + 8 * u, my_o_full = o_full + 8 * u;
+    const uint32_t my_o_empty = o_empty + 8 * u;
+    // the two threads of a row meet at a named barrier of their two warps
+    const uint32_t pair_bar = 1 + u * 4 + q4;
+    float* xch = reinterpret_cast<float*>(smem + S::XCH);   // [parity][u][row][half]
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    // every exit decision is taken by both threads of a row together, so neither can leave
+    // while the other waits at their barrier
+    auto pair_all = [&](bool v) {
+      uint32_t res;
+      asm volatile(
+          "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.and.pred po, %2, 64, pi; selp.u32 %0, 1, 0, po; }"
+          : "=r"(res)
+          : "r"(uint32_t(v)), "r"(pair_bar)
+          : "memory");
+      return res != 0;
+    };
     const int tl = r / G, hj = r - tl * G;
-    uint32_t g = 0;
+    uint32_t gt = 0;
     int item = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item) {
       const int hk = w / njobs;
       const Job J = p.jobs[w - hk * njobs];
       const Walk wk = walk_of(J, p.window, p.cap);
-      const bool row_ok = tl < p.TPT && tl < J.n;
+      const int tj = u * p.TPT + tl;           // token index within the job
+      const bool row_ok = tl < p.TPT && tj < J.n;
       int pr = 0, lo = 1;
       if (row_ok) {
-        const int pp = p.pos[J.t0 + tl];
+        const int pp = p.pos[J.t0 + tj];
         if (row_pos_ok(pp, p.window, p.cap)) {
           pr = min(pp, J.key_b);
           lo = p.window > 0 ? max(1, pp - p.window + 1) : 1;
         }
       }
       float m_ref = kNegInf, l = 0.f;
-      for (int i = 0; i < wk.n; ++i, ++g) {
-        const uint32_t b = g & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * b, (g >> 1) & 1)) || *abort_flag) {
+      for (int i = 0; i < wk.n; ++i) {
+        const uint32_t G_ = gt + uint32_t(i);
+        if (!pair_all(mbar_wait(my_s_full, G_ & 1) && !*abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t ts = tmem + b * 128 + lrow;
-        uint32_t sv[KT];
+        const int kb = wk.key_first + i * KT + 64 * half;
+        const int c_lo = lo - kb, c_hi = pr - kb;   // valid columns [c_lo, c_hi] of this half
+        float mh;
+        {
+          // row max of this half, 32 columns at a time; columns outside the row's keys become
+          // -inf, in TMEM too, so P below needs no mask
+          const bool full = __all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 63);
+          float mx[8];
 #pragma unroll
-        for (int c = 0; c < KT / 32; ++c) tmem_ld32_nowait(ts + 32 * c, sv + 32 * c);
-        tmem_wait_ld();
-        const int kb = wk.key_first + i * KT;
-        const int c_lo = lo - kb, c_hi = pr - kb;   // valid columns [c_lo, c_hi]
-        const bool full = c_lo <= 0 && c_hi >= KT - 1;
-        float mx = kNegInf;
-        if (full) {
+          for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
+#pragma unroll 1
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t sv[32];
+            tmem_ld32_nowait(ts + 32 * c2, sv);
+            tmem_wait_ld();
+            if (!full) {
 #pragma unroll
-          for (int c = 0; c < KT; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
-        } else {
+              for (int c = 0; c < 32; ++c)
+                if (32 * c2 + c < c_lo || 32 * c2 + c > c_hi) sv[c] = __float_as_uint(kNegInf);
+              tmem_st32(ts + 32 * c2, sv);
+              tmem_wait_st();
+            }
 #pragma unroll
-          for (int c = 0; c < KT; ++c)
-            if (c >= c_lo && c <= c_hi) mx = fmaxf(mx, __uint_as_float(sv[c]));
+            for (int c = 0; c < 32; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+          mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         }
-        const float mt = mx * p.sl2;
+        float* xm = xch + ((G_ & 1) * 2 + u) * 256;
+        xm[r * 2 + half] = mh;
+        pair_sync();
+        const float mt = fmaxf(mh, xm[r * 2 + (half ^ 1)]) * p.sl2;
         const bool need = m_ref != kNegInf && mt > m_ref + kRescale;
         if (__any_sync(0xffffffffu, need)) {
           // O holds the earlier tiles' P.V of this item: wait for the last one, then rescale
-          if (!__all_sync(0xffffffffu, mbar_wait(s_free + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1))) {
+          if (!pair_all(mbar_wait(my_s_free, (G_ - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float f = need ? exp2f(m_ref - mt) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32_nowait(tO + lrow + 32 * c, o);
+            tmem_ld32_nowait(to + 32 * c, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(tO + lrow + 32 * c, o);
+            tmem_st32(to + 32 * c, o);
           }
           tmem_wait_st();
           if (need) {
@@ -485,64 +591,73 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
           }
         }
         if (m_ref == kNegInf) m_ref = mt;   // first keys of the row: O row is still zero
-        const float mref = m_ref == kNegInf ? 0.f : m_ref;
+        const float nmref = m_ref == kNegInf ? 0.f : -m_ref;
+        float ls[8];
 #pragma unroll
-        for (int c4 = 0; c4 < KT / 32; ++c4) {
-          uint32_t pk[32];
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 2; ++c4) {
+          uint32_t v[32], pk[32];
+          tmem_ld32_nowait(ts + 32 * c4, v);
+          tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const int c = 32 * c4 + 2 * q;
-            float p0 = exp2f(fmaf(__uint_as_float(sv[c]), p.sl2, -mref));
-            float p1 = exp2f(fmaf(__uint_as_float(sv[c + 1]), p.sl2, -mref));
-            if (!full) {
-              p0 = (c >= c_lo && c <= c_hi) ? p0 : 0.f;
-              p1 = (c + 1 >= c_lo && c + 1 <= c_hi) ? p1 : 0.f;
-            }
-            l += p0;
-            l += p1;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.sl2, nmref));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.sl2, nmref));
+            ls[(2 * q) & 7] += p0;
+            ls[(2 * q + 1) & 7] += p1;
             const uint32_t hi = pack_bf16x2(p0, p1);
             pk[q] = hi;
             pk[16 + q] = pack_bf16x2(p0 - bf_lo(hi), p1 - bf_hi(hi));
           }
           tmem_st32(ts + 32 * c4, pk);
         }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_full + 8 * b);
+        mbar_arrive(my_p_full);
       }
       if (!ok) break;
-      // epilogue: o = O / l, rounded, gated, rounded
-      if (!__all_sync(0xffffffffu, mbar_wait(o_full, uint32_t(item) & 1)) || *abort_flag) {
+      gt += uint32_t(wk.n);
+      // epilogue: o = O / l, rounded, gated, rounded; l is the sum of the row's two halves
+      if (!pair_all(mbar_wait(my_o_full, uint32_t(item) & 1) && !*abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t ov[D];
+      float* xl = xch + ((2 + (item & 1)) * 2 + u) * 256;
+      xl[r * 2 + half] = l;
+      pair_sync();
+      const float lt = l + xl[r * 2 + (half ^ 1)];
+      const float inv = (wk.n > 0 && lt > 0.f) ? 1.f / lt : 0.f;
+      const int t = J.t0 + tj, hq = hk * G + hj;
+      const size_t oi = (size_t(row_ok ? t : 0) * p.n_q + hq) * D + 64 * half;
+      const float gb = row_ok ? bf2f(p.gate_bias[hq]) : 0.f;
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t ov[32];
+        tmem_ld32_nowait(to + 32 * c2, ov);
+        tmem_wait_ld();
+        if (row_ok) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + lrow + 32 * c, ov + 32 * c);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(o_empty);
-      if (row_ok) {
-        const int t = J.t0 + tl, hq = hk * G + hj;
-        const float inv = (wk.n > 0 && l > 0.f) ? 1.f / l : 0.f;
-        const size_t oi = (size_t(t) * p.n_q + hq) * D;
-        const float gb = bf2f(p.gate_bias[hq]);
+          for (int c = 0; c < 4; ++c) {
+            const size_t oc = oi + 32 * c2 + 8 * c;
+            const uint4 gv = *reinterpret_cast<const uint4*>(p.gpre + oc);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            uint32_t q[4];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 gv = *reinterpret_cast<const uint4*>(p.gpre + oi + 8 * c);
-          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-          uint32_t q[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float o0 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e]) * inv) : 0.f;
-            const float o1 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e + 1]) * inv) : 0.f;
-            const float g0 = sigmoidf_(bf_lo(gw[e]) + gb), g1 = sigmoidf_(bf_hi(gw[e]) + gb);
-            q[e] = pack_bf16x2(o0 * g0, o1 * g1);
+            for (int e = 0; e < 4; ++e) {
+              const float o0 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e]) * inv) : 0.f;
+              const float o1 = inv > 0.f ? round_bf(__uint_as_float(ov[8 * c + 2 * e + 1]) * inv) : 0.f;
+              const float g0 = sigmoidf_(bf_lo(gw[e]) + gb), g1 = sigmoidf_(bf_hi(gw[e]) + gb);
+              q[e] = pack_bf16x2(o0 * g0, o1 * g1);
+            }
+            *reinterpret_cast<uint4*>(p.og + oc) = make_uint4(q[0], q[1], q[2], q[3]);
           }
-          *reinterpret_cast<uint4*>(p.og + oi + 8 * c) = make_uint4(q[0], q[1], q[2], q[3]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(my_o_empty);
     }
     if (!ok) *abort_flag = 1;
   }
@@ -559,7 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_prefill_tc_kernel(
 
 bool prefill_supported(int D, int G, int window, int cap, bool fp8, const void* q,
                        const void* k, const void* v) {
-  if (fp8 || (D != 64 && D != 128) || G < 1 || G > ROWS) return false;
+  if (fp8 || D != 128 || G < 1 || G > ROWS) return false;
   if (window > 0 && cap % KT != 0) return false;
   return aligned16(q) && aligned16(k) && aligned16(v) && tensor_map_encoder_ready();
 }
@@ -593,22 +708,15 @@ cudaError_t prefill(const uint16_t* q, const uint16_t* g, const uint16_t* gate_b
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  launch_pdl(attn_tc_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_id, pos, T, TPT,
+  launch_pdl(attn_tc_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_id, pos, T, 2 * TPT,
              kc.window, kc.capacity, kc.num_seqs, jobs, n_jobs);
   Params prm{jobs, n_jobs, pos, g, gate_bias, og, T, n_q, n_kv, G, TPT, kc.window, kc.capacity, sl2};
   int grid = num_sms_cached();
   if (int64_t(T) * n_kv < grid) grid = T * n_kv;
-  if (D == 128) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
-    if (e != cudaSuccess) return e;
-    launch_pdl(attn_prefill_tc_kernel<128>, dim3(grid), dim3(THREADS), Smem<128>::BYTES, st, mq, mk, mv, prm);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<64>::BYTES);
-    if (e != cudaSuccess) return e;
-    launch_pdl(attn_prefill_tc_kernel<64>, dim3(grid), dim3(THREADS), Smem<64>::BYTES, st, mq, mk, mv, prm);
-  }
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
+  if (e != cudaSuccess) return e;
+  launch_pdl(attn_prefill_tc_kernel<128>, dim3(grid), dim3(THREADS), Smem<128>::BYTES, st, mq, mk, mv, prm);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@
 namespace beam {
 namespace atc {
 
-// Whether the tensor-core prefill kernel handles this call: BF16 cache, head_dim 64 or 128,
+// Whether the tensor-core prefill kernel handles this call: BF16 cache, head_dim 128,
 // G = n_q / n_kv <= 128 query heads per KV head, a ring cache (window > 0) whose capacity is a
 // multiple of 128 slots, 16-byte aligned q and cache.
 bool prefill_supported(int D, int G, int window, int cap, bool fp8, const void* q, const void* k,

@@ -137,10 +137,16 @@ inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 bl
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-inline beam_status launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA;
+// Records the CUDA error behind a BEAM_ERR_CUDA for beam_last_cuda_error (per host thread).
+void note_cuda_error(cudaError_t e);
+
+inline beam_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return BEAM_OK;
+  note_cuda_error(e);
+  return BEAM_ERR_CUDA;
 }
+
+inline beam_status launch_status() { return cuda_status(cudaGetLastError()); }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

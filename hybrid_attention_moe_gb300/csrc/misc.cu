@@ -24,6 +24,9 @@ int num_sms_cached() {
 }
 void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+void note_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
 size_t qkv_ws_bytes(const beam_layer_cfg* c, int T);
 size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window);
 size_t route_ws_bytes(const beam_layer_cfg* c, int T);
@@ -75,3 +78,7 @@ extern "C" const char* beam_status_string(beam_status s) {
 }
 
 extern "C" uint64_t beam_launch_count(void) { return beam::g_launches.load(); }
+
+extern "C" const char* beam_last_cuda_error(void) {
+  return cudaGetErrorName(beam::g_last_cuda_error);
+}

@@ -414,12 +414,12 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     const size_t nv = size_t(P) * (H / 8);
     launch_pdl(gather_rows_kernel, dim3(unsigned((nv + 255) / 256)), dim3(256), 0, st, u, H, k, pl, P, us);
     const int mj = max_jobs(P, E);
-    if (tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, w_gate_up, E * 2 * F, 2 * F, H, pl.jobs,
-                         pl.n_jobs, mj, F, F, nullptr, act, F, st) != cudaSuccess)
-      return BEAM_ERR_CUDA;
-    if (tc::gemm_grouped(tc::kF32, act, P, F, F, w_down, E * H, H, F, pl.jobs, pl.n_jobs, mj, H,
-                         0, pl.pairs, y, H, st) != cudaSuccess)
-      return BEAM_ERR_CUDA;
+    if (const cudaError_t err_ = tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, w_gate_up, E * 2 * F, 2 * F, H, pl.jobs,
+                         pl.n_jobs, mj, F, F, nullptr, act, F, st); err_ != cudaSuccess)
+      return cuda_status(err_);
+    if (const cudaError_t err_ = tc::gemm_grouped(tc::kF32, act, P, F, F, w_down, E * H, H, F, pl.jobs, pl.n_jobs, mj, H,
+                         0, pl.pairs, y, H, st); err_ != cudaSuccess)
+      return cuda_status(err_);
     const size_t n = size_t(T) * H;
     launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y, topk_w, topk_idx, T, H, k,
                                                                   E, out);
@@ -455,10 +455,11 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
              static_cast<int*>(nullptr), 0, act);
   if (P <= kFusedMaxPairs) {
     const int smem = 8 * P * int(sizeof(float));
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(moe_down_combine_kernel<8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return BEAM_ERR_CUDA;
+    if (smem > 48 * 1024) {
+      const cudaError_t err_ = cudaFuncSetAttribute(
+          moe_down_combine_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err_ != cudaSuccess) return cuda_status(err_);
+    }
     launch_pdl(moe_down_combine_kernel<8>, dim3((H + 7) / 8), dim3(256), smem, st, act, w_down, topk_w, T, H, F, k,
                                                               pl, out);
   } else {
@@ -491,15 +492,15 @@ extern "C" beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16
   const bool tcore = T >= kGemmMinT && tc::gemm_supported(u, H, w_gate_up, H, H) &&
                      tc::gemm_supported(act, Fd, w_down, Fd, Fd);
   if (tcore) {
-    if (tc::gemm_swiglu(u, T, H, H, w_gate_up, Fd, H, act, Fd, st) != cudaSuccess)
-      return BEAM_ERR_CUDA;
-    if (tc::gemm_bf16(act, T, Fd, Fd, w_down, H, Fd, out, H, true, st) != cudaSuccess)
-      return BEAM_ERR_CUDA;
+    if (const cudaError_t err_ = tc::gemm_swiglu(u, T, H, H, w_gate_up, Fd, H, act, Fd, st); err_ != cudaSuccess)
+      return cuda_status(err_);
+    if (const cudaError_t err_ = tc::gemm_bf16(act, T, Fd, Fd, w_down, H, Fd, out, H, true, st); err_ != cudaSuccess)
+      return cuda_status(err_);
     return BEAM_OK;
   }
-  if (launch_gemv<kOutSwiGLU>(w_gate_up, Fd, H, u, T, nullptr, act, Fd, st) != cudaSuccess)
-    return BEAM_ERR_CUDA;
-  if (launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st) != cudaSuccess)
-    return BEAM_ERR_CUDA;
+  if (const cudaError_t err_ = launch_gemv<kOutSwiGLU>(w_gate_up, Fd, H, u, T, nullptr, act, Fd, st); err_ != cudaSuccess)
+    return cuda_status(err_);
+  if (const cudaError_t err_ = launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st); err_ != cudaSuccess)
+    return cuda_status(err_);
   return BEAM_OK;
 }

@@ -156,7 +156,7 @@ extern "C" beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16*
       T >= kGemmMinT && tc::gemm_supported(u, H, w_qkvg, H, H)
           ? tc::gemm_bf16(u, T, H, H, w_qkvg, rows, H, z, rows, false, s)
           : launch_gemv<kOutF32>(w_qkvg, rows, H, u, T, z, nullptr, rows, s);
-  if (ge != cudaSuccess) return BEAM_ERR_CUDA;
+  if (ge != cudaSuccess) return cuda_status(ge);
   const int nope = cfg->kind == BEAM_ATTN_NOPE_SSMAX;
   RopeTab rope;
   for (int i = 0; i < D / 2; ++i)

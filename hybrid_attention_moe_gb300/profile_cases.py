@@ -9,7 +9,9 @@ warm-up launches and capture one or a few real ones. Usage:
 Cases: moe_decode (batch-1 expert GEMVs over 8 selected experts of a 32-expert pool),
 qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (100K keys),
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
-moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts).
+moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts), attn_nope_prefill
+(tensor-core attention: one sequence, 2048 new tokens after --ctx cached keys, NoPE, BF16 KV),
+attn_swa_prefill (the same over a 512-key sliding window, 8 sequences).
 """
 from __future__ import annotations
 
@@ -34,6 +36,7 @@ def main():
     ap.add_argument("--case", required=True)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--ctx", type=int, default=16384)
     args = ap.parse_args()
     _build.build()
     dev = "cuda"
@@ -81,6 +84,24 @@ def main():
         ws = torch.empty(B.workspace_bytes(cf, 1, ctx + 1), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + 1, W["w_o"], out, ws,  # noqa: E731
                                  max_q_per_seq=1)
+    elif c in ("attn_nope_prefill", "attn_swa_prefill"):
+        nope = c == "attn_nope_prefill"
+        S, chunk = (1, 2048) if nope else (8, 2048)
+        ctx = args.ctx
+        cf = B.LayerCfg.from_shape(shape, B.BEAM_ATTN_NOPE_SSMAX if nope else B.BEAM_ATTN_SWA_ROPE)
+        W = synth.attention_weights(shape, 5, 0, device=dev)
+        cap, win = (ctx + chunk + 8, 0) if nope else (-(-(shape.window + chunk - 1) // 128) * 128,
+                                                      shape.window)
+        kv = synth.kv_cache(shape, S, cap, 0, device=dev)
+        kc = B.KVCache(kv["k"], kv["v"], win)
+        T = S * chunk
+        q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, 0, ("q",), dev)
+        gg = synth.activations(T, shape.q_rows, 0, "g", dev)
+        seq, pos = synth.prefill_positions([ctx] * S, chunk, dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(B.workspace_bytes(cf, T, ctx + chunk), dtype=torch.uint8, device=dev)
+        fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + chunk, W["w_o"],  # noqa: E731
+                                 out, ws, max_q_per_seq=chunk)
     elif c == "route_decode":
         R = synth.router_weights(shape, 3, 0, device=dev)
         u = synth.activations(1, H, 0, "u", dev)

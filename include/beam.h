@@ -231,6 +231,10 @@ uint64_t beam_launch_count(void);
 /* Static description of a status code. */
 const char* beam_status_string(beam_status s);
 
+/* Name of the last CUDA runtime error behind a BEAM_ERR_CUDA returned to the calling thread
+ * ("cudaSuccess" if there was none); a static string, valid for the process lifetime. */
+const char* beam_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
