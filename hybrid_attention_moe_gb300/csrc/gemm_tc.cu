@@ -194,16 +194,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         } else if (row_ok && col < p.N) {
-          if (MODE == kF32) {
+          if (MODE == kF32 || MODE == kF32Add) {
             float* dst = static_cast<float*>(p.C) + size_t(crow) * p.ldc + col;
             if (col + 16 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<float4*>(dst)[i] =
-                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              for (int i = 0; i < 4; ++i) {
+                float4 o = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                if (MODE == kF32Add) {
+                  const float4 c = reinterpret_cast<const float4*>(dst)[i];
+                  o.x += c.x;
+                  o.y += c.y;
+                  o.z += c.z;
+                  o.w += c.w;
+                }
+                reinterpret_cast<float4*>(dst)[i] = o;
+              }
             } else {
-              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = __uint_as_float(v[i]);
+              for (int i = 0; i < 16 && col + i < p.N; ++i)
+                dst[i] = MODE == kF32Add ? dst[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
             }
           } else {
             uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
@@ -306,6 +315,19 @@ cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* 
   GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
   dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
   return out_bf16 ? launch<kBF16>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
+}
+
+cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N,
+                         int ldb, float* C, int ldc, bool accumulate, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
+  if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
+    return cudaErrorInvalidValue;
+  GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
+  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
+  return accumulate ? launch<kF32Add>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
 }
 
 cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,

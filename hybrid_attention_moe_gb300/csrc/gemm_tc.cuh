@@ -14,8 +14,13 @@ cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* 
 
 bool gemm_supported(const void* A, int lda, const void* B, int ldb, int K);
 
+// FP32 C[M][N] = A . B^T, or C += A . B^T when accumulate (each element read and rewritten
+// once by the CTA that owns it).
+cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N,
+                         int ldb, float* C, int ldc, bool accumulate, cudaStream_t st);
+
 // Epilogue modes of the grouped GEMM.
-enum GemmMode { kF32 = 0, kBF16 = 1, kSwiGLU = 2 };
+enum GemmMode { kF32 = 0, kBF16 = 1, kSwiGLU = 2, kF32Add = 3 };
 
 // C[M][F] = bf16(silu(A . Bg^T) * (A . Bu^T)), B = [gate rows F; up rows F] x K.
 cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,

@@ -8,12 +8,21 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_tc.cuh"
 
 namespace beam {
 namespace {
 
 constexpr int kRouteMaxT = 8;  // tokens per CTA pass in the GEMV form
 constexpr int kRouteBatch = 3; // weight chunks in flight per thread in the GEMV form
+// From this many tokens the logits run on the tensor cores: every FP32 router weight is split
+// exactly into three BF16 parts, w = hi + mid + lo (hi = bf16(w), mid = bf16(w - hi),
+// lo = w - hi - mid, each step exact), the BF16 activations times each part are exact FP32
+// products, and one BF16 GEMM against the stacked [hi; mid; lo] rows accumulates them in FP32;
+// logit = (u.hi + u.mid) + u.lo. Below it (decode, and every size the allocation-free router
+// accepts) the FP32 SIMT kernels run.
+constexpr int kRouteTcMinT = 512;
+constexpr int kRouteKChunks = 8;   // K chains of the tensor-core logits (640 at hidden 5120)
 
 // Small T: one CTA per expert row; its warps split the hidden axis; every token of a pass
 // reuses the row held in registers/L1.
@@ -117,6 +126,34 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __rest
       const int t = tm + ty * 4 + i, e = tn + tx * 4 + j;
       if (t < T && e < E) logits[size_t(t) * E + e] = acc[i][j];
     }
+}
+
+// w3 = [hi; mid; lo] of the n FP32 weights (three stacked copies of the E x H matrix).
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ w, size_t n,
+                                                           uint16_t* __restrict__ w3) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float x = w[i];
+  const uint16_t hi = f2bf(x);
+  const float r1 = x - bf2f(hi);
+  const uint16_t mid = f2bf(r1);
+  w3[i] = hi;
+  w3[n + i] = mid;
+  w3[2 * n + i] = f2bf(r1 - bf2f(mid));
+}
+
+// logits[t][e] = (c[t][e] + c[t][E + e]) + c[t][2E + e], c = u . [hi; mid; lo]^T
+__global__ void __launch_bounds__(256) router_sum3_kernel(const float* __restrict__ c, int T,
+                                                          int E, float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= size_t(T) * E) return;
+  const size_t t = i / E, e = i - t * E;
+  const float* ct = c + t * 3 * E;
+  logits[i] = (ct[e] + ct[E + e]) + ct[2 * E + e];
 }
 
 // Warp-wide argmax of (value, index), ties to the lower index.
@@ -331,7 +368,11 @@ beam_status launch_logits(const uint16_t* u, const float* w_router, int T, int H
 }  // namespace
 
 size_t route_ws_bytes(const beam_layer_cfg* c, int T) {
-  return align_up(size_t(T) * c->n_experts * sizeof(float), 256);
+  size_t b = align_up(size_t(T) * c->n_experts * sizeof(float), 256);
+  if (T >= kRouteTcMinT)
+    b += align_up(size_t(3) * c->n_experts * c->hidden * 2, 256) +
+         align_up(size_t(T) * 3 * c->n_experts * sizeof(float), 256);
+  return b;
 }
 
 }  // namespace beam
@@ -353,11 +394,28 @@ extern "C" beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u,
     return BEAM_ERR_INVALID_ARG;
   if (T == 0) return BEAM_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
   float* lg = logits;
-  if (lg == nullptr) {
-    Carver cv{static_cast<char*>(ws), ws_bytes};
-    lg = cv.take<float>(size_t(T) * E);
+  if (lg == nullptr) lg = cv.take<float>(size_t(T) * E);
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  if (T >= kRouteTcMinT && tc::gemm_supported(u, H, u, H, H)) {
+    const size_t n = size_t(E) * H;
+    uint16_t* w3 = cv.take<uint16_t>(3 * n);
+    float* c3 = cv.take<float>(size_t(T) * 3 * E);
     if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    launch_pdl(router_split_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, w_router, n, w3);
+    // the tensor pipe's FP32 accumulation loses about 2^-24 of the running sum per K step of
+    // 16, so the reduction runs as kRouteKChunks chains summed in FP32 memory
+    const int kc = (H % (8 * kRouteKChunks) == 0) ? H / kRouteKChunks : H;
+    for (int k0 = 0; k0 < H; k0 += kc) {
+      if (const cudaError_t e = tc::gemm_f32_acc(u + k0, T, kc, H, w3 + k0, 3 * E, H, c3, 3 * E,
+                                                 k0 > 0, st);
+          e != cudaSuccess)
+        return cuda_status(e);
+    }
+    const size_t nl = size_t(T) * E;
+    launch_pdl(router_sum3_kernel, dim3(unsigned((nl + 255) / 256)), dim3(256), 0, st, c3, T, E, lg);
+    return launch_topk(cfg, lg, corr_bias, T, topk_idx, topk_w, st);
   }
   const beam_status ls = launch_logits(u, w_router, T, H, E, lg, st);
   if (ls != BEAM_OK) return ls;

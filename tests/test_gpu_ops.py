@@ -202,8 +202,11 @@ ROUTE_48 = dataclasses.replace(TINY, n_experts=48, n_groups=4, topk_groups=2, to
 
 
 @pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 77), (BEAM, 1), (BEAM, 8), (BEAM, 300),
-                                     (ROUTE_96, 5), (ROUTE_48, 1), (ROUTE_48, 40)])
+                                     (ROUTE_96, 5), (ROUTE_48, 1), (ROUTE_48, 40),
+                                     (TINY, 700), (BEAM, 1030)])
 def test_route(shape, T):
+    """FP32 SIMT logits below 512 tokens; from 512 the tensor-core GEMM over the exact
+    three-part BF16 split of the FP32 router weights (same logits to FP32 rounding)."""
     cfg = cfg_of(shape)
     for attempt in range(20):
         seed = 1000 * attempt + T
