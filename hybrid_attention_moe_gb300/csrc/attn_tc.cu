@@ -42,6 +42,12 @@ constexpr int KSTAGES = 2, VSTAGES = 2;
 // (warp - 2) / 4 % 2, TMEM lane quarter warp % 4 -- two threads per row, 64 columns each
 constexpr int THREADS = 576;
 constexpr float kRescale = 8.f;  // log2 units
+// The tensor pipe's FP32 accumulation drops about 2^-24 of the running sum per MMA (measured:
+// 1.8e-5 relative over 320 accumulating MMAs). O of a 100K-key row would take ~12.5K of them,
+// so every kFlushTiles key tiles the softmax warps add O from TMEM into an FP32 scratch row
+// (round-to-nearest adds) and the next P.V starts a fresh TMEM accumulator.
+constexpr int kFlushTiles = 64;
+constexpr int kMaxGrid = 256;    // persistent CTAs at most (scratch is sized for this many)
 constexpr float kNegInf = -INFINITY;
 
 struct Job {
@@ -73,6 +79,7 @@ struct Params {
   const uint16_t* gpre;
   const uint16_t* gate_bias;
   uint16_t* og;
+  float* oacc;   // per CTA [2][128][128] FP32: O of the chunks already flushed
   int T, n_q, n_kv, G, TPT, window, cap;
   float sl2;
 };
@@ -355,6 +362,7 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
     // PV_u(j) has read them, and while one warpgroup computes its P the tensor pipe works
     // through the other tile's P.V and the next S.
     uint32_t kc = 0, vc = 0, pt = 0;   // pt: key tiles of earlier items (per query tile)
+    uint32_t ostart = 0;                // fresh O accumulations started so far (per query tile)
     int item = 0;
     bool ok = true;
     auto all = [&](bool v) { return __all_sync(0xffffffffu, v) && !*abort_flag; };
@@ -395,12 +403,13 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
       const int hk = w / njobs;
       const Job J = p.jobs[w - hk * njobs];
       const Walk wk = walk_of(J, p.window, p.cap);
-      const uint32_t oph = (uint32_t(item) & 1) ^ 1;   // o_empty parity for this item
       if (!all(mbar_wait(q_full, uint32_t(item) & 1))) { ok = false; break; }
       tc_fence_after();
       if (wk.n == 0) {
         // no keys: release Q; O is never written, the epilogue stores zeros
+        const uint32_t oph = (ostart & 1) ^ 1;
         if (!all(mbar_wait(o_empty, oph) && mbar_wait(o_empty + 8, oph))) { ok = false; break; }
+        ++ostart;
         if (lane == 0) {
           umma_commit(q_empty);
           umma_commit(o_full);
@@ -424,10 +433,14 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
       for (int i = 0; i < wk.n; ++i) {
         const int vs = int(vc % VSTAGES);
         const bool more = i + 1 < wk.n;
+        // a fresh O accumulation at the item's first tile and after each flush; it waits until
+        // the softmax warps have taken the previous one out of TMEM
+        const bool fresh = i % kFlushTiles == 0;
+        const uint32_t oph = (ostart & 1) ^ 1;
         // ---- query tile A: P.V of tile i, then S of tile i + 1
         bool w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
                     mbar_wait(p_full, (pt + gt_i) & 1);
-        if (i == 0) w_ok = w_ok && mbar_wait(o_empty, oph);
+        if (fresh) w_ok = w_ok && mbar_wait(o_empty, oph);
         if (more) {
           ks = int(kc % KSTAGES);
           w_ok = w_ok && mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1);
@@ -449,16 +462,17 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
           __syncwarp();
         }
         tc_fence_after();
-        pv(0, vs, i == 0);
+        pv(0, vs, fresh);
         if (lane == 0 && !more) umma_commit(o_full);
         __syncwarp();
         if (more) qk(0, ks);
         // ---- query tile B
         w_ok = mbar_wait(p_full + 8, (pt + gt_i) & 1);
-        if (i == 0) w_ok = w_ok && mbar_wait(o_empty + 8, oph);
+        if (fresh) w_ok = w_ok && mbar_wait(o_empty + 8, oph);
         if (!all(w_ok)) { ok = false; break; }
+        if (fresh) ++ostart;
         tc_fence_after();
-        pv(1, vs, i == 0);
+        pv(1, vs, fresh);
         if (lane == 0) {
           umma_commit(v_empty + 8 * vs);
           if (!more) umma_commit(o_full + 8);
@@ -526,6 +540,8 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         }
       }
       float m_ref = kNegInf, l = 0.f;
+      bool flushed = false;   // oacc holds earlier chunks of this item
+      float* oacc = p.oacc + ((size_t(blockIdx.x) * 2 + u) * 128 + r) * 128 + 64 * half;
       for (int i = 0; i < wk.n; ++i) {
         const uint32_t G_ = gt + uint32_t(i);
         if (!pair_all(mbar_wait(my_s_full, G_ & 1) && !*abort_flag)) {
@@ -585,6 +601,17 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
             tmem_st32(to + 32 * c, o);
           }
           tmem_wait_st();
+          if (flushed && need) {
+#pragma unroll 4
+            for (int c = 0; c < 64; c += 4) {
+              float4 a = *reinterpret_cast<float4*>(oacc + c);
+              a.x *= f;
+              a.y *= f;
+              a.z *= f;
+              a.w *= f;
+              *reinterpret_cast<float4*>(oacc + c) = a;
+            }
+          }
           if (need) {
             l *= f;
             m_ref = mt;
@@ -616,6 +643,37 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(my_p_full);
+        if ((i + 1) % kFlushTiles == 0 && i + 1 < wk.n) {
+          // flush: once this tile's P.V has completed, add O into the FP32 scratch row and
+          // hand TMEM back for a fresh accumulation
+          if (!pair_all(mbar_wait(my_s_free, G_ & 1) && !*abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t ov[32];
+            tmem_ld32_nowait(to + 32 * c2, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              float4 a = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                     __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+              if (flushed) {
+                const float4 b = *reinterpret_cast<const float4*>(oacc + 32 * c2 + c);
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+              }
+              *reinterpret_cast<float4*>(oacc + 32 * c2 + c) = a;
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(my_o_empty);
+          flushed = true;
+        }
       }
       if (!ok) break;
       gt += uint32_t(wk.n);
@@ -638,6 +696,11 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         uint32_t ov[32];
         tmem_ld32_nowait(to + 32 * c2, ov);
         tmem_wait_ld();
+        if (flushed) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            ov[c] = __float_as_uint(__uint_as_float(ov[c]) + oacc[32 * c2 + c]);
+        }
         if (row_ok) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -679,7 +742,10 @@ bool prefill_supported(int D, int G, int window, int cap, bool fp8, const void* 
   return aligned16(q) && aligned16(k) && aligned16(v) && tensor_map_encoder_ready();
 }
 
-size_t ws_bytes(int T) { return align_up(size_t(2 * T + 1) * sizeof(Job), 256) + 256; }
+size_t ws_bytes(int T) {
+  return align_up(size_t(2 * T + 1) * sizeof(Job), 256) + 256 +
+         size_t(kMaxGrid) * 2 * 128 * 128 * sizeof(float);
+}
 
 cudaError_t prefill(const uint16_t* q, const uint16_t* g, const uint16_t* gate_bias,
                     const int32_t* seq_id, const int32_t* pos, int T, int n_q, int n_kv, int D,
@@ -710,8 +776,11 @@ cudaError_t prefill(const uint16_t* q, const uint16_t* g, const uint16_t* gate_b
   }
   launch_pdl(attn_tc_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, seq_id, pos, T, 2 * TPT,
              kc.window, kc.capacity, kc.num_seqs, jobs, n_jobs);
-  Params prm{jobs, n_jobs, pos, g, gate_bias, og, T, n_q, n_kv, G, TPT, kc.window, kc.capacity, sl2};
+  float* oacc = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                        align_up(size_t(2 * T + 1) * sizeof(Job), 256) + 256);
+  Params prm{jobs, n_jobs, pos, g, gate_bias, og, oacc, T, n_q, n_kv, G, TPT, kc.window, kc.capacity, sl2};
   int grid = num_sms_cached();
+  if (grid > kMaxGrid) grid = kMaxGrid;
   if (int64_t(T) * n_kv < grid) grid = T * n_kv;
   cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<128>::BYTES);
