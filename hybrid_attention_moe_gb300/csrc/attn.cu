@@ -31,7 +31,11 @@ namespace {
 
 constexpr float kNegInf = -INFINITY;
 constexpr int kDecWarps = 4;
-constexpr int kDecKT = 32;   // keys per warp tile (decode)
+// Keys per warp tile (decode): 32 when 2-8 split CTAs of a (token, KV head) form a cluster;
+// 16 with a single split or with many splits merged through the workspace, which fits two
+// CTAs on an SM -- twice the tiles in flight (measured: NoPE batch 1 at 100K keys 180 -> 124
+// us, batch-128 stack layer 1350 -> 1140 us; clusters of 5 at batch 8 were 7% faster at 32).
+constexpr int kDecKTCluster = 32, kDecKTSplit = 16;
 constexpr int kPreKT = 64;   // keys per CTA tile (prefill)
 constexpr int kRows = 16;    // tensor-core tile rows
 
@@ -331,9 +335,9 @@ __device__ __forceinline__ void merge_gate_cluster(
 
 // Dynamic shared memory of the decode kernel: the 4 warps' tile pipelines, reused for the
 // cross-warp combine, then (cluster form) the CTA's partial for its peers.
-template <int D, bool FP8>
+template <int D, bool FP8, int KT>
 struct DecodeSmem {
-  static constexpr int kTiles = kDecWarps * TileGeom<D, FP8, kDecKT>::BYTES;
+  static constexpr int kTiles = kDecWarps * TileGeom<D, FP8, KT>::BYTES;
   static constexpr int kComb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
   static constexpr int kPartOff = ((kTiles > kComb ? kTiles : kComb) + 127) / 128 * 128;
   static constexpr int kBytes = kPartOff + (kRows * D + kRows * 2) * 4;
@@ -342,7 +346,7 @@ struct DecodeSmem {
 // ------------------------------------------------------------------------------------------
 // Decode: split-K partials
 // ------------------------------------------------------------------------------------------
-template <int D, bool FP8, bool CLUSTER>
+template <int D, bool FP8, bool CLUSTER, int KT>
 __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_id,
     const int32_t* __restrict__ pos, int n_q, int n_kv, beam_kv_cache kc, int kps, int n_splits,
@@ -351,8 +355,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     uint16_t* __restrict__ og) {
   pdl_trigger();
   pdl_wait();
-  using Gm = TileGeom<D, FP8, kDecKT>;
-  constexpr int KT = kDecKT;
+  using Gm = TileGeom<D, FP8, KT>;
   constexpr int DN = D / 8;
   extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, hk = blockIdx.y, t = blockIdx.z;
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
   __syncthreads();
   if constexpr (CLUSTER) {
     // this CTA's partial to its own shared memory, above the tile and combine buffers
-    float* cO = reinterpret_cast<float*>(smem + DecodeSmem<D, FP8>::kPartOff);   // [16][D]
+    float* cO = reinterpret_cast<float*>(smem + DecodeSmem<D, FP8, KT>::kPartOff);   // [16][D]
     float* cML = cO + kRows * D;                                                 // [16][2]
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
       const int row = idx / D, d = idx - row * D;
@@ -710,10 +713,21 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
                           int n_q, int n_kv, const beam_kv_cache& kc, DecodePlan pl, float sl2,
                           float* pacc, float* pml, int* done, float v_scale, const uint16_t* g,
                           const uint16_t* gb, uint16_t* og, cudaStream_t st) {
-  using Sm = DecodeSmem<D, FP8>;
   const dim3 grid(pl.n_splits, n_kv, T), block(kDecWarps * 32);
+  if (pl.n_splits == 1) {
+    // one split per (token, KV head): many small CTAs, two per SM
+    using Sm = DecodeSmem<D, FP8, kDecKTSplit>;
+    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTSplit>;
+    cudaError_t e = set_smem(kern, Sm::kBytes);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl_cluster(kern, grid, block, Sm::kBytes, st, 1, q, seq_id, pos, n_q, n_kv, kc,
+                           pl.kps, pl.n_splits, sl2, pacc, pml, done, v_scale, g, gb, og);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   if (pl.n_splits <= kClusterMaxSplits) {
-    auto kern = attn_decode_split_kernel<D, FP8, true>;
+    using Sm = DecodeSmem<D, FP8, kDecKTCluster>;
+    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTCluster>;
     cudaError_t e = set_smem(kern, Sm::kBytes);
     if (e != cudaSuccess) return e;
     e = launch_pdl_cluster(kern, grid, block, Sm::kBytes, st, pl.n_splits, q, seq_id, pos, n_q,
@@ -721,7 +735,8 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  auto kern = attn_decode_split_kernel<D, FP8, false>;
+  using Sm = DecodeSmem<D, FP8, kDecKTSplit>;
+  auto kern = attn_decode_split_kernel<D, FP8, false, kDecKTSplit>;
   cudaError_t e = set_smem(kern, Sm::kPartOff);
   if (e != cudaSuccess) return e;
   launch_pdl(kern, grid, block, Sm::kPartOff, st, q, seq_id, pos, n_q, n_kv, kc, pl.kps,

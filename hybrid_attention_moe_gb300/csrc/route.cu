@@ -15,13 +15,14 @@ namespace {
 
 constexpr int kRouteMaxT = 8;  // tokens per CTA pass in the GEMV form
 constexpr int kRouteBatch = 3; // weight chunks in flight per thread in the GEMV form
-// From this many tokens the logits run on the tensor cores: every FP32 router weight is split
+// Above kRouteGemvMaxT tokens the logits run on the tensor cores: every FP32 router weight is split
 // exactly into three BF16 parts, w = hi + mid + lo (hi = bf16(w), mid = bf16(w - hi),
 // lo = w - hi - mid, each step exact), the BF16 activations times each part are exact FP32
 // products, and one BF16 GEMM against the stacked [hi; mid; lo] rows accumulates them in FP32;
-// logit = (u.hi + u.mid) + u.lo. Below it (decode, and every size the allocation-free router
-// accepts) the FP32 SIMT kernels run.
-constexpr int kRouteTcMinT = 512;
+// logit = (u.hi + u.mid) + u.lo. Up to kRouteGemvMaxT tokens (decode, and every size the
+// allocation-free router accepts) the FP32 SIMT GEMV runs, one CTA per expert row.
+constexpr int kRouteTcMinT = 257;
+constexpr int kRouteGemvMaxT = 256;   // up to here the GEMV form (the allocation-free router's range)
 constexpr int kRouteKChunks = 8;   // K chains of the tensor-core logits (640 at hidden 5120)
 
 // Small T: one CTA per expert row; its warps split the hidden axis; every token of a pass
@@ -86,20 +87,25 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __rest
 }
 
 // Large T: 64 x 64 output tiles, FP32 SIMT, bf16 activations widened on the fly.
-constexpr int kTM = 64, kTN = 64, kTK = 32;
-__global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __restrict__ u,
-                                                          const float* __restrict__ wr, int T,
-                                                          int H, int E,
-                                                          float* __restrict__ logits) {
+// FP32 SIMT tiles of TILE tokens x TILE experts, each thread an R x R block of outputs. Every
+// logit is one FMA chain over k = 0 .. H-1 in order, whatever the tile size, so the tile size
+// changes the parallelism, not the result (64 x 64 tiles, used where the tensor-core form
+// does not apply).
+constexpr int kTK = 32;
+template <int TILE, int R>
+__global__ void __launch_bounds__((TILE / R) * (TILE / R)) router_gemm_kernel(
+    const uint16_t* __restrict__ u, const float* __restrict__ wr, int T, int H, int E,
+    float* __restrict__ logits) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float As[kTK][kTM + 4];
-  __shared__ float Bs[kTK][kTN + 4];
-  const int tm = blockIdx.y * kTM, tn = blockIdx.x * kTN;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
+  constexpr int NT = (TILE / R) * (TILE / R), TW = TILE / R;
+  __shared__ float As[kTK][TILE + 4];
+  __shared__ float Bs[kTK][TILE + 4];
+  const int tm = blockIdx.y * TILE, tn = blockIdx.x * TILE;
+  const int tx = threadIdx.x % TW, ty = threadIdx.x / TW;
+  float acc[R][R] = {};
   for (int k0 = 0; k0 < H; k0 += kTK) {
-    for (int i = threadIdx.x; i < kTM * kTK; i += 256) {
+    for (int i = threadIdx.x; i < TILE * kTK; i += NT) {
       const int r = i / kTK, k = i - r * kTK;
       const int t = tm + r;
       As[k][r] = (t < T && k0 + k < H) ? bf2f(u[size_t(t) * H + k0 + k]) : 0.f;
@@ -109,21 +115,21 @@ __global__ void __launch_bounds__(256) router_gemm_kernel(const uint16_t* __rest
     __syncthreads();
 #pragma unroll 8
     for (int k = 0; k < kTK; ++k) {
-      float a[4], b[4];
+      float a[R], b[R];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { a[i] = As[k][ty * 4 + i]; b[i] = Bs[k][tx * 4 + i]; }
+      for (int i = 0; i < R; ++i) { a[i] = As[k][ty * R + i]; b[i] = Bs[k][tx * R + i]; }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < R; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < R; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int t = tm + ty * 4 + i, e = tn + tx * 4 + j;
+    for (int j = 0; j < R; ++j) {
+      const int t = tm + ty * R + i, e = tn + tx * R + j;
       if (t < T && e < E) logits[size_t(t) * E + e] = acc[i][j];
     }
 }
@@ -357,11 +363,11 @@ beam_status launch_topk(const beam_layer_cfg* cfg, const float* lg, const float*
 // logits[T][E] = float(u) . w_router^T
 beam_status launch_logits(const uint16_t* u, const float* w_router, int T, int H, int E,
                           float* lg, cudaStream_t st) {
-  if (T <= 32)
+  if (T <= kRouteGemvMaxT)
     launch_pdl(router_gemv_kernel, dim3(E), dim3(256), 0, st, u, w_router, T, H, E, lg);
   else
-    launch_pdl(router_gemm_kernel, dim3((E + kTN - 1) / kTN, (T + kTM - 1) / kTM), dim3(256), 0,
-               st, u, w_router, T, H, E, lg);
+    launch_pdl(router_gemm_kernel<64, 4>, dim3((E + 63) / 64, (T + 63) / 64), dim3(256), 0, st,
+               u, w_router, T, H, E, lg);
   return launch_status();
 }
 
