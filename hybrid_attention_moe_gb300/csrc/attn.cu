@@ -683,7 +683,15 @@ struct DecodePlan {
 
 DecodePlan decode_plan(int T, int n_kv, int max_keys) {
   const int per = T * n_kv;
-  int splits = (2 * num_sms() + per - 1) / per;
+  // CTAs resident at once (two per SM); the split count fills whole waves of them: the
+  // smallest multiple (up to 4) of the resident slots that the (token, KV head) count divides
+  const int slots = 2 * num_sms();
+  int splits = 1;
+  if (per < slots) {
+    int w = 1;
+    while (w < 4 && (slots * w) % per != 0) ++w;
+    splits = (slots * w + per - 1) / per;
+  }
   const int max_splits = (max_keys + 127) / 128;
   splits = splits < 1 ? 1 : (splits > max_splits ? max_splits : splits);
   if (splits > kMergeMaxSplits) splits = kMergeMaxSplits;
