@@ -83,14 +83,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
                                                    float* __restrict__ yf,
                                                    uint16_t* __restrict__ yb, int ldy) {
   pdl_trigger();
-  pdl_wait();
   constexpr int ROWS = (MODE == kOutSwiGLU) ? 2 * NR : NR;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int unit0 = warp * NR;
   if (unit0 >= N) return;
   const int t0 = blockIdx.y * NT;
-  const int nt = min(NT, T - t0);
   const uint16_t* w[ROWS];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
@@ -102,6 +100,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
       w[r] = W + size_t(unit) * K;
     }
   }
+  // the weights are no predecessor's output: start them towards L2 before waiting
+  if (lane == 0 && blockIdx.y == 0 && (K & 7) == 0) {
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+      if ((reinterpret_cast<uintptr_t>(w[r]) & 15) == 0) l2_prefetch(w[r], uint32_t(K) * 2);
+  }
+  pdl_wait();
+  const int nt = min(NT, T - t0);
   const uint16_t* x[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) x[t] = X + size_t(t0 + min(t, nt - 1)) * K;

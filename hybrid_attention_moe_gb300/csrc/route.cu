@@ -32,11 +32,14 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint16_t* __rest
                                                           int H, int E,
                                                           float* __restrict__ logits) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[8][kRouteMaxT];
   const int e = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = wr + size_t(e) * H;
+  // the router weights are no predecessor's output: start the row towards L2 before waiting
+  if (threadIdx.x == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0)
+    l2_prefetch(row, uint32_t(H) * 4);
+  pdl_wait();
   for (int t0 = 0; t0 < T; t0 += kRouteMaxT) {
     const int nt = min(kRouteMaxT, T - t0);
     float acc[kRouteMaxT];
