@@ -497,9 +497,13 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     }
     // the last split CTA of this (token, KV head) merges all splits
     __shared__ int s_last;
-    __threadfence();
+    // the CTA barrier orders every thread's partial stores before thread 0's device-scope
+    // fence, which releases them with the counter increment
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(done + t * n_kv + hk, 1) == n_splits - 1;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = atomicAdd(done + t * n_kv + hk, 1) == n_splits - 1;
+    }
     __syncthreads();
     if (s_last) {
       __threadfence();

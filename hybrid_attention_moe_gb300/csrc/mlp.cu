@@ -26,10 +26,12 @@ constexpr int kPairTile = 4;        // pairs per weight pass in the gate_up / do
 constexpr int kFusedMaxPairs = 1024;  // down+combine in shared memory up to this many pairs
 
 constexpr int kMoeGemmMinT = 32;   // from here the experts run as grouped tensor-core GEMMs
-// Weight chunks in flight per lane in the single-token gate/up and down kernels (4 and 8;
-// 5/10 and 10/10 measured no faster).
+// Weight chunks in flight per lane in the single-token gate/up and down kernels. The down kernel
+// takes 4 rows of 2560 per warp, 5 chunks each (20 KB per warp in two full round trips):
+// measured 8-10 us faster than 2 rows x 8 chunks (a third, ragged round trip per warp).
 constexpr int kDecodeGateUpU = 4;
-constexpr int kDecodeDownU = 8;
+constexpr int kDecodeDownU = 5;
+constexpr int kDecodeDownNR = 4;   // rows per warp in the one-token down kernel
 
 struct MoePlan {
   int* n_active;   // [1]
@@ -291,9 +293,13 @@ __global__ void __launch_bounds__(256) moe_down_kernel(
   }
   if (cnt == nullptr) return;   // uniform over the grid
   __shared__ int s_last;
-  __threadfence();
+  // the CTA barrier orders every thread's y stores before thread 0's device-scope fence,
+  // which releases them with the counter increment
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -431,7 +437,7 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     const bool direct = T == 1;
     const int32_t* dix = direct ? topk_idx : nullptr;
     const int na = direct ? k : max_active;
-    const int nr = direct ? 2 : 1;
+    const int nr = direct ? kDecodeDownNR : 1;
     const int n_cnt = (H + 8 * nr - 1) / (8 * nr);
     if (!direct)
       launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
@@ -442,7 +448,7 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
       launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, na), dim3(256), 0, st, u,
                  w_gate_up, H, F, k, pl, dix, E, cnt, n_cnt, act);
     if (direct)
-      launch_pdl(moe_down_kernel<kDecodeDownU, 1, 2>, dim3(n_cnt, na), dim3(256), 0, st, act,
+      launch_pdl(moe_down_kernel<kDecodeDownU, 1, kDecodeDownNR>, dim3(n_cnt, na), dim3(256), 0, st, act,
                  w_down, H, F, pl, dix, topk_idx, topk_w, T, k, E, cnt, y, out);
     else
       launch_pdl(moe_down_kernel<8, 4, 1>, dim3(n_cnt, na), dim3(256), 0, st, act, w_down, H,
