@@ -100,8 +100,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
       w[r] = W + size_t(unit) * K;
     }
   }
-  // the weights are no predecessor's output: start them towards L2 before waiting
-  if (lane == 0 && blockIdx.y == 0 && (K & 7) == 0) {
+  // the weights are no predecessor's output: start them towards L2 before waiting -- the
+  // first 64 MB of matrices up to 160 MB (QKV+gate, o_proj). Measured: prefetching the
+  // 419 MB dense gate/up matrix, whole or in part, slowed it (the prefetches evict each other
+  // and the demand loads from the 129 MB L2).
+  constexpr size_t kPrefetchBudget = size_t(64) << 20, kPrefetchMaxMatrix = size_t(160) << 20;
+  const size_t matrix_bytes = size_t(MODE == kOutSwiGLU ? 2 * N : N) * size_t(K) * 2;
+  if (lane == 0 && blockIdx.y == 0 && (K & 7) == 0 && matrix_bytes <= kPrefetchMaxMatrix &&
+      size_t(warp) * ROWS * size_t(K) * 2 < kPrefetchBudget) {
 #pragma unroll
     for (int r = 0; r < ROWS; ++r)
       if ((reinterpret_cast<uintptr_t>(w[r]) & 15) == 0) l2_prefetch(w[r], uint32_t(K) * 2);

@@ -28,8 +28,11 @@ constexpr int kFusedMaxPairs = 1024;  // down+combine in shared memory up to thi
 constexpr int kMoeGemmMinT = 32;   // from here the experts run as grouped tensor-core GEMMs
 // Weight chunks in flight per lane in the single-token gate/up and down kernels. The down kernel
 // takes 4 rows of 2560 per warp, 5 chunks each (20 KB per warp in two full round trips):
-// measured 8-10 us faster than 2 rows x 8 chunks (a third, ragged round trip per warp).
-constexpr int kDecodeGateUpU = 4;
+// measured 8-10 us faster than 2 rows x 8 chunks (a third, ragged round trip per warp). The
+// gate/up kernel takes 2 (gate, up) row pairs of 5120 per warp, 5 chunks each: 5 us faster than
+// one pair with 4 chunks.
+constexpr int kDecodeGateUpU = 5;
+constexpr int kDecodeGateUpFPW = 2;   // gate/up row pairs per warp in the one-token kernel
 constexpr int kDecodeDownU = 5;
 constexpr int kDecodeDownNR = 4;   // rows per warp in the one-token down kernel
 
@@ -164,7 +167,7 @@ __device__ __forceinline__ int pair_at(const MoePlan& pl, const int32_t* direct,
 // grid (ceil(F / 8), max active experts); warp per (active expert, f): gate row f and up
 // row F+f, dotted with up to NT of the expert's pairs per weight pass. CTA (0, 0) also clears
 // the n_cnt completion counters of the down kernel that follows.
-template <int U, int NT>
+template <int U, int NT, int FPW>
 __global__ void __launch_bounds__(256) moe_gate_up_kernel(
     const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
     MoePlan pl, const int32_t* __restrict__ direct, int E, int* __restrict__ cnt, int n_cnt,
@@ -175,8 +178,8 @@ __global__ void __launch_bounds__(256) moe_gate_up_kernel(
     for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
   const int ai = blockIdx.y;
   if (ai >= (direct != nullptr ? k : *pl.n_active)) return;
-  const int f = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (f >= F) return;
+  const int f0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * FPW;
+  if (f0 >= F) return;
   const int lane = threadIdx.x & 31;
   ExpertSlot es;
   if (!expert_slot(pl, direct, E, ai, es)) {
@@ -184,7 +187,13 @@ __global__ void __launch_bounds__(256) moe_gate_up_kernel(
     return;
   }
   const uint16_t* base = w_gu + size_t(es.e) * 2 * F * H;
-  const uint16_t* w[2] = {base + size_t(f) * H, base + size_t(F + f) * H};
+  const uint16_t* w[2 * FPW];
+#pragma unroll
+  for (int j = 0; j < FPW; ++j) {
+    const int f = min(f0 + j, F - 1);
+    w[2 * j] = base + size_t(f) * H;
+    w[2 * j + 1] = base + size_t(F + f) * H;
+  }
   for (int pp = es.p0; pp < es.p1; pp += NT) {
     const int nt = min(NT, es.p1 - pp);
     int pid[NT];
@@ -194,11 +203,14 @@ __global__ void __launch_bounds__(256) moe_gate_up_kernel(
       pid[i] = pair_at(pl, direct, pp + min(i, nt - 1));
       x[i] = u + size_t(pid[i] / k) * H;
     }
-    float acc[2][NT];
-    warp_dot<2, NT, U>(w, x, nt, H, acc);
+    float acc[2 * FPW][NT];
+    warp_dot<2 * FPW, NT, U>(w, x, nt, H, acc);
 #pragma unroll
-    for (int i = 0; i < NT; ++i)
-      if (i < nt && lane == i) a[size_t(pid[i]) * F + f] = f2bf(siluf_(acc[0][i]) * acc[1][i]);
+    for (int j = 0; j < FPW; ++j)
+#pragma unroll
+      for (int i = 0; i < NT; ++i)
+        if (i < nt && lane == j * NT + i && f0 + j < F)
+          a[size_t(pid[i]) * F + f0 + j] = f2bf(siluf_(acc[2 * j][i]) * acc[2 * j + 1][i]);
   }
 }
 
@@ -442,10 +454,11 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     if (!direct)
       launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
     if (direct)
-      launch_pdl(moe_gate_up_kernel<kDecodeGateUpU, 1>, dim3((F + 7) / 8, na), dim3(256), 0, st,
+      launch_pdl(moe_gate_up_kernel<kDecodeGateUpU, 1, kDecodeGateUpFPW>,
+                 dim3((F + 8 * kDecodeGateUpFPW - 1) / (8 * kDecodeGateUpFPW), na), dim3(256), 0, st,
                  u, w_gate_up, H, F, k, pl, dix, E, cnt, n_cnt, act);
     else
-      launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, na), dim3(256), 0, st, u,
+      launch_pdl(moe_gate_up_kernel<4, 4, 1>, dim3((F + 7) / 8, na), dim3(256), 0, st, u,
                  w_gate_up, H, F, k, pl, dix, E, cnt, n_cnt, act);
     if (direct)
       launch_pdl(moe_down_kernel<kDecodeDownU, 1, kDecodeDownNR>, dim3(n_cnt, na), dim3(256), 0, st, act,
@@ -456,7 +469,7 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
     return launch_status();
   }
   launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
-  launch_pdl(moe_gate_up_kernel<4, 4>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
+  launch_pdl(moe_gate_up_kernel<4, 4, 1>, dim3((F + 7) / 8, max_active), dim3(256), 0, st, u,
              w_gate_up, H, F, k, pl, static_cast<const int32_t*>(nullptr), E,
              static_cast<int*>(nullptr), 0, act);
   if (P <= kFusedMaxPairs) {
