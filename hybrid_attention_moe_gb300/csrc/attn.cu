@@ -36,6 +36,9 @@ constexpr int kDecWarps = 4;
 // CTAs on an SM -- twice the tiles in flight (measured: NoPE batch 1 at 100K keys 180 -> 124
 // us, batch-128 stack layer 1350 -> 1140 us; clusters of 5 at batch 8 were 7% faster at 32).
 constexpr int kDecKTCluster = 32, kDecKTSplit = 16;
+// cp.async stages per warp with 16-key tiles: three keep two CTAs on an SM with two tiles in
+// flight per warp
+constexpr int kDecStagesSplit = 3;
 constexpr int kPreKT = 64;   // keys per CTA tile (prefill)
 constexpr int kRows = 16;    // tensor-core tile rows
 
@@ -335,9 +338,16 @@ __device__ __forceinline__ void merge_gate_cluster(
 
 // Dynamic shared memory of the decode kernel: the 4 warps' tile pipelines, reused for the
 // cross-warp combine, then (cluster form) the CTA's partial for its peers.
-template <int D, bool FP8, int KT>
+// Per-warp pipeline of the decode kernel: ST stages of raw K and V tiles, plus (fp8 only) one
+// converted K and V tile.
+template <int D, bool FP8, int KT, int ST>
+__host__ __device__ constexpr int dec_warp_bytes() {
+  return 2 * ST * TileGeom<D, FP8, KT>::RAWB + (FP8 ? 2 * TileGeom<D, FP8, KT>::TILEB : 0);
+}
+
+template <int D, bool FP8, int KT, int ST>
 struct DecodeSmem {
-  static constexpr int kTiles = kDecWarps * TileGeom<D, FP8, KT>::BYTES;
+  static constexpr int kTiles = kDecWarps * dec_warp_bytes<D, FP8, KT, ST>();
   static constexpr int kComb = (kDecWarps * kRows * (D + 4) + kDecWarps * kRows * 2) * 4;
   static constexpr int kPartOff = ((kTiles > kComb ? kTiles : kComb) + 127) / 128 * 128;
   static constexpr int kBytes = kPartOff + (kRows * D + kRows * 2) * 4;
@@ -346,7 +356,7 @@ struct DecodeSmem {
 // ------------------------------------------------------------------------------------------
 // Decode: split-K partials
 // ------------------------------------------------------------------------------------------
-template <int D, bool FP8, bool CLUSTER, int KT>
+template <int D, bool FP8, bool CLUSTER, int KT, int ST>
 __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     const uint16_t* __restrict__ q, const int32_t* __restrict__ seq_id,
     const int32_t* __restrict__ pos, int n_q, int n_kv, beam_kv_cache kc, int kps, int n_splits,
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
   for (int n = 0; n < DN; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
   float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
 
-  uint8_t* wbase = smem + warp * Gm::BYTES;
+  uint8_t* wbase = smem + warp * dec_warp_bytes<D, FP8, KT, ST>();
   const size_t head_off = (size_t(ok ? s : 0) * n_kv + hk) * kc.capacity;
   const uint8_t* kbase = static_cast<const uint8_t*>(kc.k) + head_off * Gm::RAWROW;
   const uint8_t* vbase = static_cast<const uint8_t*>(kc.v) + head_off * Gm::RAWROW;
@@ -404,17 +414,21 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
     issue_tile<D, FP8, KT>(kd, kbase, s0, kc.capacity, k_end - key0, lane, 32);
     issue_tile<D, FP8, KT>(kd + Gm::RAWB, vbase, s0, kc.capacity, k_end - key0, lane, 32);
   };
-  if (my_tiles > 0) issue(0, 0);
-  cp_async_commit();
-  for (int i = 0; i < my_tiles; ++i) {
-    if (i + 1 < my_tiles) issue(i + 1, (i + 1) & 1);
+  // ST-stage cp.async pipeline: tiles i+1 .. i+ST-1 are in flight while tile i is computed
+#pragma unroll
+  for (int s = 0; s < ST - 1; ++s) {
+    if (s < my_tiles) issue(s, s);
     cp_async_commit();
-    cp_async_wait<1>();
+  }
+  for (int i = 0; i < my_tiles; ++i) {
+    if (i + ST - 1 < my_tiles) issue(i + ST - 1, (i + ST - 1) % ST);
+    cp_async_commit();
+    cp_async_wait<ST - 1>();
     __syncwarp();
-    const uint8_t* kt = wbase + (i & 1) * 2 * Gm::RAWB;
+    const uint8_t* kt = wbase + (i % ST) * 2 * Gm::RAWB;
     const uint8_t* vt = kt + Gm::RAWB;
     if (FP8) {
-      uint8_t* cvt = wbase + 4 * Gm::RAWB;
+      uint8_t* cvt = wbase + 2 * ST * Gm::RAWB;
       convert_tile<D, KT>(kt, cvt, lane, 32);
       convert_tile<D, KT>(vt, cvt + Gm::TILEB, lane, 32);
       __syncwarp();
@@ -464,7 +478,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) attn_decode_split_kernel(
   __syncthreads();
   if constexpr (CLUSTER) {
     // this CTA's partial to its own shared memory, above the tile and combine buffers
-    float* cO = reinterpret_cast<float*>(smem + DecodeSmem<D, FP8, KT>::kPartOff);   // [16][D]
+    float* cO = reinterpret_cast<float*>(smem + DecodeSmem<D, FP8, KT, ST>::kPartOff);   // [16][D]
     float* cML = cO + kRows * D;                                                 // [16][2]
     for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
       const int row = idx / D, d = idx - row * D;
@@ -728,8 +742,8 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
   const dim3 grid(pl.n_splits, n_kv, T), block(kDecWarps * 32);
   if (pl.n_splits == 1) {
     // one split per (token, KV head): many small CTAs, two per SM
-    using Sm = DecodeSmem<D, FP8, kDecKTSplit>;
-    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTSplit>;
+    using Sm = DecodeSmem<D, FP8, kDecKTSplit, kDecStagesSplit>;
+    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTSplit, kDecStagesSplit>;
     cudaError_t e = set_smem(kern, Sm::kBytes);
     if (e != cudaSuccess) return e;
     e = launch_pdl_cluster(kern, grid, block, Sm::kBytes, st, 1, q, seq_id, pos, n_q, n_kv, kc,
@@ -738,8 +752,8 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
     return cudaGetLastError();
   }
   if (pl.n_splits <= kClusterMaxSplits) {
-    using Sm = DecodeSmem<D, FP8, kDecKTCluster>;
-    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTCluster>;
+    using Sm = DecodeSmem<D, FP8, kDecKTCluster, 2>;
+    auto kern = attn_decode_split_kernel<D, FP8, true, kDecKTCluster, 2>;
     cudaError_t e = set_smem(kern, Sm::kBytes);
     if (e != cudaSuccess) return e;
     e = launch_pdl_cluster(kern, grid, block, Sm::kBytes, st, pl.n_splits, q, seq_id, pos, n_q,
@@ -747,8 +761,8 @@ cudaError_t launch_decode(const uint16_t* q, const int32_t* seq_id, const int32_
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
-  using Sm = DecodeSmem<D, FP8, kDecKTSplit>;
-  auto kern = attn_decode_split_kernel<D, FP8, false, kDecKTSplit>;
+  using Sm = DecodeSmem<D, FP8, kDecKTSplit, kDecStagesSplit>;
+  auto kern = attn_decode_split_kernel<D, FP8, false, kDecKTSplit, kDecStagesSplit>;
   cudaError_t e = set_smem(kern, Sm::kPartOff);
   if (e != cudaSuccess) return e;
   launch_pdl(kern, grid, block, Sm::kPartOff, st, q, seq_id, pos, n_q, n_kv, kc, pl.kps,
