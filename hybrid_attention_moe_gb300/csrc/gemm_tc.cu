@@ -50,10 +50,81 @@ struct GemmParams {
   const int* row_map;    // optional: C row of A row r is row_map[r]
 };
 
+// The QKV epilogue for one token row and one 128-column head of the tile (kQKV mode).
+__device__ __forceinline__ void qkv_head_epilogue(const QkvEpilogue& e, uint32_t taddr, int t,
+                                                  bool tok_ok, int head, int p, int s,
+                                                  bool kv_ok, float ssmax) {
+  constexpr int QD = 128;
+  float v[QD];
+#pragma unroll
+  for (int c = 0; c < QD / 16; ++c) {
+    uint32_t r[16];
+    tmem_ld16(taddr + uint32_t(c * 16), r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[c * 16 + i] = __uint_as_float(r[i]);
+  }
+  if (!tok_ok) return;
+  const int nq = e.n_q, nkv = e.n_kv;
+  const int kind = head < nq ? 0 : head < nq + nkv ? 1 : head < nq + 2 * nkv ? 2 : 3;
+#pragma unroll
+  for (int i = 0; i < QD; ++i) v[i] = round_bf(v[i]);   // the projection's bf16 output
+  if (kind <= 1) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < QD; ++i) ss = fmaf(v[i], v[i], ss);
+    const float rn = rsqrtf(ss / float(QD) + e.eps);
+    const uint16_t* gw = kind == 0 ? e.q_norm : e.k_norm;
+#pragma unroll
+    for (int i = 0; i < QD; ++i) v[i] = v[i] * rn * bf2f(gw[i]);
+    if (!e.nope) {
+      const float2* cs = e.rope + size_t(t) * (QD / 2);
+#pragma unroll
+      for (int i = 0; i < QD / 2; ++i) {
+        const float2 c = cs[i];
+        const float a = v[i], b = v[i + QD / 2];
+        v[i] = a * c.x - b * c.y;
+        v[i + QD / 2] = b * c.x + a * c.y;
+      }
+    } else if (kind == 0) {
+#pragma unroll
+      for (int i = 0; i < QD; ++i) v[i] *= ssmax;
+    }
+  }
+  if (kind == 0 || kind == 3) {
+    uint16_t* dst = kind == 0 ? e.q_out + (size_t(t) * nq + head) * QD
+                              : e.g_out + size_t(t) * nq * QD + size_t(head - nq - 2 * nkv) * QD;
+#pragma unroll
+    for (int i = 0; i < QD; i += 8)
+      *reinterpret_cast<uint4*>(dst + i) =
+          make_uint4(pack_bf2(v[i], v[i + 1]), pack_bf2(v[i + 2], v[i + 3]),
+                     pack_bf2(v[i + 4], v[i + 5]), pack_bf2(v[i + 6], v[i + 7]));
+    return;
+  }
+  if (!kv_ok) return;
+  const beam_kv_cache& kc = e.cache;
+  const int kvh = kind == 1 ? head - nq : head - nq - nkv;
+  const int slot = (p - 1) % kc.capacity;
+  const size_t base = ((size_t(s) * nkv + kvh) * kc.capacity + slot) * QD;
+  if (kc.dtype == BEAM_KV_BF16) {
+    uint16_t* dst = static_cast<uint16_t*>(kind == 1 ? kc.k : kc.v) + base;
+#pragma unroll
+    for (int i = 0; i < QD; i += 8)
+      *reinterpret_cast<uint4*>(dst + i) =
+          make_uint4(pack_bf2(v[i], v[i + 1]), pack_bf2(v[i + 2], v[i + 3]),
+                     pack_bf2(v[i + 4], v[i + 5]), pack_bf2(v[i + 6], v[i + 7]));
+  } else {
+    uint8_t* dst = static_cast<uint8_t*>(kind == 1 ? kc.k : kc.v) + base;
+    const float sc = kind == 1 ? kc.k_scale : kc.v_scale;
+#pragma unroll
+    for (int i = 0; i < QD; ++i)
+      dst[i] = __nv_cvt_float_to_fp8(__fdiv_rn(v[i], sc), __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                   GemmParams p) {
+                   GemmParams p, QkvEpilogue qe) {
   pdl_trigger();
   pdl_wait();
   constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per CTA
@@ -167,8 +238,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool row_ok = r < rows && arow < p.M;
     const int crow = row_ok ? (p.row_map ? p.row_map[arow] : arow) : 0;
     const uint32_t tbase = tmem + (uint32_t(quad * 32) << 16);
-    // tcgen05.ld is warp-collective: take the decision once for the whole warp
-    if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+    if (MODE == kQKV) {
+      // per token row: two 128-column heads of the packed projection
+      int pp = 0, sq = 0;
+      bool kv_ok = false;
+      float ssmax = 1.f;
+      if (row_ok) {
+        pp = qe.pos[arow];
+        sq = qe.seq_id[arow];
+        const beam_kv_cache& kc = qe.cache;
+        const bool bad_p = pp < 1 || (kc.window == 0 && pp > kc.capacity);
+        const bool bad_s = sq < 0 || sq >= kc.num_seqs;
+        if (n0 == 0 && bad_p) flag(BEAM_DEV_BAD_POSITION);
+        if (n0 == 0 && bad_s) flag(BEAM_DEV_BAD_SEQ);
+        kv_ok = !bad_p && !bad_s;
+        if (qe.nope)
+          ssmax = float(pow(1.0 + double(pp) / double(qe.ss_base), double(qe.ss_exp)));
+      }
+      if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+#pragma unroll 1
+        for (int hh = 0; hh < BN / 128; ++hh) {
+          const int head = n0 / 128 + hh;
+          if (head * 128 >= p.N) break;   // uniform over the CTA
+          qkv_head_epilogue(qe, tbase + uint32_t(hh * 128), arow, row_ok, head, pp, sq, kv_ok,
+                            ssmax);
+        }
+      }
+    } else if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+      // tcgen05.ld is warp-collective: the decision is taken once for the whole warp
 #pragma unroll 1
       for (int c = 0; c < NT / 16; ++c) {
         uint32_t v[16];
@@ -294,11 +391,11 @@ namespace {
 
 template <int MODE>
 cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, dim3 grid,
-                   cudaStream_t st) {
+                   cudaStream_t st, const QkvEpilogue& qe = QkvEpilogue{}) {
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  launch_pdl(gemm_tc_kernel<MODE>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, ta, tb, p);
+  launch_pdl(gemm_tc_kernel<MODE>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, ta, tb, p, qe);
   return cudaGetLastError();
 }
 
@@ -328,6 +425,19 @@ cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_
   GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
   dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
   return accumulate ? launch<kF32Add>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
+}
+
+cudaError_t gemm_qkv(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N, int ldb,
+                     const QkvEpilogue& qe, cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (!gemm_supported(A, lda, B, ldb, K) || N % 128 != 0) return cudaErrorInvalidValue;
+  if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
+    return cudaErrorInvalidValue;
+  GemmParams p{M, N, K, nullptr, 0, nullptr, nullptr, 0, 0, nullptr};
+  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
+  return launch<kQKV>(ta, tb, p, grid, st, qe);
 }
 
 cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,

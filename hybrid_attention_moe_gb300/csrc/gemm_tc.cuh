@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/beam.h"
+
 namespace beam {
 namespace tc {
 
@@ -20,7 +22,31 @@ cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_
                          int ldb, float* C, int ldc, bool accumulate, cudaStream_t st);
 
 // Epilogue modes of the grouped GEMM.
-enum GemmMode { kF32 = 0, kBF16 = 1, kSwiGLU = 2, kF32Add = 3 };
+enum GemmMode { kF32 = 0, kBF16 = 1, kSwiGLU = 2, kF32Add = 3, kQKV = 4 };
+
+// Epilogue of the packed QKV+gate projection (head dim 128): the output columns are the heads
+// Q (n_q) | K (n_kv) | V (n_kv) | gate (n_q). Per token row: round to bf16; Q and K heads
+// RMS-normalised over the head with one shared [128] gain each, then rotated by the token's
+// (cos, sin) table row (sliding-window layers) or, for Q on NoPE layers, scaled by
+// (1 + p / ss_base)^ss_exp; q' and g stored in bf16, k and v written into the cache slot
+// (p - 1) % capacity (bf16, or e4m3 codes of value / scale). Positions and sequence ids out of
+// range set the device status bits and skip the cache write.
+struct QkvEpilogue {
+  uint16_t* q_out;          // [T][n_q][128]
+  uint16_t* g_out;          // [T][n_q * 128]
+  beam_kv_cache cache;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  const uint16_t* q_norm;   // [128]
+  const uint16_t* k_norm;   // [128]
+  const float2* rope;       // [T][64] (cos, sin); nullptr on NoPE layers
+  int n_q, n_kv, nope;
+  float ss_base, ss_exp, eps;
+};
+
+// The projection A . B^T (B = w_qkvg, N = (2 n_q + 2 n_kv) * 128 rows) with the QKV epilogue.
+cudaError_t gemm_qkv(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N, int ldb,
+                     const QkvEpilogue& e, cudaStream_t st);
 
 // C[M][F] = bf16(silu(A . Bg^T) * (A . Bu^T)), B = [gate rows F; up rows F] x K.
 cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,

@@ -123,6 +123,24 @@ __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
   }
 }
 
+// (cos, sin) of angle (p - 1) * theta^(-2i/D) for each token's position, i < D/2: the RoPE
+// rows the tensor-core projection's epilogue reads (same double-precision reduction as above).
+__global__ void __launch_bounds__(256) rope_table_kernel(const int32_t* __restrict__ pos, int T,
+                                                         int half, RopeTab rope,
+                                                         float2* __restrict__ tab) {
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * half) return;
+  const int t = i / half, j = i - t * half;
+  double ang = double(pos[t] - 1) * rope.inv[j];
+  const double two_pi = 6.283185307179586476925;
+  ang -= two_pi * rint(ang / two_pi);
+  float sv, cv;
+  sincosf(float(ang), &sv, &cv);
+  tab[i] = make_float2(cv, sv);
+}
+
 }  // namespace
 
 size_t qkv_ws_bytes(const beam_layer_cfg* c, int T) {
@@ -152,15 +170,27 @@ extern "C" beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16*
   float* z = cv.take<float>(size_t(T) * rows);
   if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int nope = cfg->kind == BEAM_ATTN_NOPE_SSMAX;
+  RopeTab rope;
+  for (int i = 0; i < D / 2; ++i)
+    rope.inv[i] = pow(double(cfg->rope_theta), -2.0 * double(i) / double(D));
+  if (T >= kGemmMinT && D == 128 && tc::gemm_supported(u, H, w_qkvg, H, H) && aligned16(q_out) &&
+      aligned16(g_out) && aligned16(cache->k) && aligned16(cache->v)) {
+    // prefill: the projection's epilogue does the norms, RoPE/SSMax and the cache write
+    float2* tab = reinterpret_cast<float2*>(z);   // the FP32 projection buffer is unused here
+    if (!nope)
+      launch_pdl(rope_table_kernel, dim3((T * (D / 2) + 255) / 256), dim3(256), 0, s, pos, T,
+                 D / 2, rope, tab);
+    tc::QkvEpilogue e{q_out, g_out, *cache, seq_id, pos, q_norm_w, k_norm_w,
+                      nope ? nullptr : tab, cfg->n_q, cfg->n_kv, nope, cfg->ssmax_base,
+                      cfg->ssmax_exp, cfg->eps};
+    return cuda_status(tc::gemm_qkv(u, T, H, H, w_qkvg, rows, H, e, s));
+  }
   const cudaError_t ge =
       T >= kGemmMinT && tc::gemm_supported(u, H, w_qkvg, H, H)
           ? tc::gemm_bf16(u, T, H, H, w_qkvg, rows, H, z, rows, false, s)
           : launch_gemv<kOutF32>(w_qkvg, rows, H, u, T, z, nullptr, rows, s);
   if (ge != cudaSuccess) return cuda_status(ge);
-  const int nope = cfg->kind == BEAM_ATTN_NOPE_SSMAX;
-  RopeTab rope;
-  for (int i = 0; i < D / 2; ++i)
-    rope.inv[i] = pow(double(cfg->rope_theta), -2.0 * double(i) / double(D));
   if (D == 128)
     launch_pdl(qkv_epilogue_kernel<4>, dim3(T, (2 * cfg->n_q + 2 * cfg->n_kv + 7) / 8), dim3(256), 0, s, z, rows, q_norm_w, k_norm_w, seq_id, pos, cfg->n_q,
                                              cfg->n_kv, nope, rope, cfg->ssmax_base,

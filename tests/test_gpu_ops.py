@@ -331,6 +331,33 @@ def test_bad_positions_are_flagged_and_skipped():
             assert_close(np64(out[t:t + 1]), ref, "moe out, valid slots")
 
 
+def test_bad_positions_flagged_in_the_tensor_core_projection():
+    """The prefill projection (tensor-core GEMM with the norm/RoPE/cache epilogue, 64 tokens at
+    full width) flags a position < 1, a position past a NoPE cache and an out-of-range
+    sequence, and writes only the valid tokens' cache slots."""
+    shape, T = BEAM, 64
+    cfg = cfg_of(shape, nope=True)
+    positions = list(range(1, T + 1))
+    W, u, kc, seq, pos = _qkv_inputs(shape, T, 4, positions, [0] * T, False, True)
+    before_k, before_v = kc.k.clone(), kc.v.clone()
+    bad_pos = pos.clone()
+    bad_pos[3], bad_pos[10] = 0, 1_000_000
+    bad_seq = seq.clone()
+    bad_seq[20] = 5
+    q = torch.empty((T, shape.n_q, shape.head_dim), dtype=torch.bfloat16, device=DEV)
+    g = torch.empty((T, shape.q_rows), dtype=torch.bfloat16, device=DEV)
+    B.beam_get_device_status()
+    B.beam_qkv_gate(cfg, u, W["w_qkvg"], W["q_norm"], W["k_norm"], bad_seq, bad_pos, q, g, kc,
+                    ws_for(cfg, T, T))
+    bits = B.beam_get_device_status()
+    assert bits & B.DEV_BAD_POSITION and bits & B.DEV_BAD_SEQ
+    written = set(p - 1 for i, p in enumerate(positions) if i not in (3, 10, 20))
+    untouched = [sl for sl in range(kc.k.shape[2]) if sl not in written]
+    assert torch.equal(kc.k[:, :, untouched], before_k[:, :, untouched])
+    assert torch.equal(kc.v[:, :, untouched], before_v[:, :, untouched])
+    assert not torch.equal(kc.k[:, :, sorted(written)], before_k[:, :, sorted(written)])
+
+
 def test_invalid_arguments_return_errors():
     shape = TINY
     cfg = cfg_of(shape)
