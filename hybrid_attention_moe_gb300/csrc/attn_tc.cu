@@ -44,9 +44,9 @@ constexpr int THREADS = 576;
 constexpr float kRescale = 8.f;  // log2 units
 // The tensor pipe's FP32 accumulation drops about 2^-24 of the running sum per MMA (measured:
 // 1.8e-5 relative over 320 accumulating MMAs). O of a 100K-key row would take ~12.5K of them,
-// so every kFlushTiles key tiles the softmax warps add O from TMEM into an FP32 scratch row
+// so every kFlushTiles key tiles (~2K MMAs) the softmax warps add O from TMEM into an FP32 scratch row
 // (round-to-nearest adds) and the next P.V starts a fresh TMEM accumulator.
-constexpr int kFlushTiles = 64;
+constexpr int kFlushTiles = 128;
 constexpr int kMaxGrid = 256;    // persistent CTAs at most (scratch is sized for this many)
 constexpr float kNegInf = -INFINITY;
 
@@ -107,6 +107,32 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed pairs of FP32 values (one 64-bit register pair) and the paired FMA / add / subtract:
+// each lane of the pair rounds exactly as the scalar instruction would.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 __device__ __forceinline__ bool row_pos_ok(int p, int window, int cap) {
@@ -619,9 +645,10 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         }
         if (m_ref == kNegInf) m_ref = mt;   // first keys of the row: O row is still zero
         const float nmref = m_ref == kNegInf ? 0.f : -m_ref;
-        float ls[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+        // P two columns at a time: one paired FMA for s * c - m, the SFU's exp2 per column,
+        // paired row sums and a paired subtract for the lo parts
+        const uint64_t sl2x2 = f2(p.sl2, p.sl2), nm2 = f2(nmref, nmref);
+        uint64_t ls2[4] = {0, 0, 0, 0};
 #pragma unroll 1
         for (int c4 = 0; c4 < 2; ++c4) {
           uint32_t v[32], pk[32];
@@ -629,17 +656,26 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * q]), p.sl2, nmref));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * q + 1]), p.sl2, nmref));
-            ls[(2 * q) & 7] += p0;
-            ls[(2 * q + 1) & 7] += p1;
+            float x0, x1;
+            f2_split(fma2(f2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1])), sl2x2, nm2),
+                     x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const uint64_t pp = f2(p0, p1);
+            ls2[q & 3] = add2(ls2[q & 3], pp);
             const uint32_t hi = pack_bf16x2(p0, p1);
+            float d0, d1;
+            f2_split(sub2(pp, f2(bf_lo(hi), bf_hi(hi))), d0, d1);
             pk[q] = hi;
-            pk[16 + q] = pack_bf16x2(p0 - bf_lo(hi), p1 - bf_hi(hi));
+            pk[16 + q] = pack_bf16x2(d0, d1);
           }
           tmem_st32(ts + 32 * c4, pk);
         }
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        {
+          float a0, a1, b0, b1;
+          f2_split(add2(ls2[0], ls2[1]), a0, a1);
+          f2_split(add2(ls2[2], ls2[3]), b0, b1);
+          l += (a0 + b0) + (a1 + b1);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(my_p_full);
