@@ -20,6 +20,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include "attn_dec.cuh"
 #include "attn_tc.cuh"
 #include "common.cuh"
 #include "gemm_tc.cuh"
@@ -789,14 +790,22 @@ cudaError_t launch_prefill(const uint16_t* q, const uint16_t* g, const uint16_t*
 size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
   size_t b = align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
   {   // the split-K decode form may be chosen for any T (max_q_per_seq <= kDecodeMaxQ)
+    // partials only when the splits merge through the workspace (more than a cluster)
     const DecodePlan pl = decode_plan(T, c->n_kv, max_keys_of(window, max_pos > 0 ? max_pos : 1));
-    const size_t parts = size_t(T) * c->n_kv * pl.n_splits * kRows;
+    const size_t parts =
+        pl.n_splits > kClusterMaxSplits ? size_t(T) * c->n_kv * pl.n_splits * kRows : 0;
     b += align_up(parts * c->head_dim * 4, 256) + align_up(parts * 2 * 4, 256);
     b += align_up(size_t(T) * c->n_kv * 4, 256);     // split completion counters
   }
-  const size_t tcb = atc::ws_bytes(T);                  // or the tensor-core prefill's job list
+  // or the TMA decode kernel's partials (BF16 or FP8 cache), or the tensor-core prefill's job list
+  size_t alt = atc::ws_bytes(T);
+  const int mp = max_pos > 0 ? max_pos : 1;
+  const size_t d16 = adec::ws_bytes(T, c->n_kv, window, mp, false);
+  const size_t d8 = adec::ws_bytes(T, c->n_kv, window, mp, true);
+  if (d16 > alt) alt = d16;
+  if (d8 > alt) alt = d8;
   const size_t dec = b - align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
-  if (tcb > dec) b += tcb - dec;
+  if (alt > dec) b += alt - dec;
   return b;
 }
 
@@ -825,9 +834,20 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
   Carver cv{static_cast<char*>(ws), ws_bytes};
   uint16_t* og = cv.take<uint16_t>(size_t(T) * HD);
   cudaError_t e;
-  if (max_q_per_seq <= kDecodeMaxQ) {
+  const int G = cfg->n_q / cfg->n_kv;
+  if (max_q_per_seq <= kDecodeMaxQ &&
+      adec::supported(D, G, cache->window, cache->capacity, fp8, cache->k, cache->v,
+                      max_keys_of(cache->window, max_pos))) {
+    const size_t db = adec::ws_bytes(T, cfg->n_kv, cache->window, max_pos, fp8);
+    void* dw = cv.take<char>(db);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    e = adec::decode(q, g, gate_bias, seq_id, pos, T, max_pos, cfg->n_q, cfg->n_kv, *cache, sl2,
+                     fp8 ? cache->v_scale : 1.f, og, dw, db, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  } else if (max_q_per_seq <= kDecodeMaxQ) {
     const DecodePlan pl = decode_plan(T, cfg->n_kv, max_keys_of(cache->window, max_pos));
-    const size_t parts = size_t(T) * cfg->n_kv * pl.n_splits * kRows;
+    const size_t parts =
+        pl.n_splits > kClusterMaxSplits ? size_t(T) * cfg->n_kv * pl.n_splits * kRows : 0;
     float* pacc = cv.take<float>(parts * D);
     float* pml = cv.take<float>(parts * 2);
     int* done = cv.take<int>(size_t(T) * cfg->n_kv);

@@ -1,0 +1,707 @@
+// Long-context decode attention: TMA-fed, warp-specialised split-K flash decoding.
+// Beam page, Attention section: 48 query heads share 8 KV heads of dim 128 (GQA); sliding-window
+// layers see the last 512 keys, NoPE layers the whole context (q already carries RoPE or the
+// SSMax scale); the cache holds BF16 or FP8-e4m3 K/V; each head's output is multiplied by
+// sigmoid(gate + per-head bias) before o_proj.
+//
+// The (token, KV head) pairs are cut into blocks of BK keys, and the flattened (pair, block)
+// space into equal contiguous ranges, one per CTA (one CTA per SM): every SM streams the same
+// number of K/V bytes whatever the batch, and a range may end inside one pair and start the
+// next. Per CTA one producer warp issues TMA loads of whole key blocks (K and V, 128-byte
+// swizzle) into a ring of NST stages; NCW consumer warps each take 16 keys of every block.
+// With G <= 8 query heads per KV head the tiles are computed transposed, so the heads are the
+// 8-wide N side of mma.sync m16n8k16 and no MMA row is padding:
+//   S^T[16 keys x 8 heads]  = K[16 x 128] . Q^T           A = K rows, B = q fragments
+//   O^T[128 x 8 heads]     += V^T[128 x 16 keys] . P^T    A = V (transposed), B = P^T
+// movmatrix (8x8 transposes in registers) turns the accumulator layout of P^T into the B
+// layout. P is split into hi and lo halves, so P carries ~16 significant bits; the running
+// max is rescaled lazily (only when it grows by more than 2^8). At the end of a pair's range
+// the consumer warps combine their partials: a pair that one CTA covers whole is finished in
+// place, otherwise the partial (max, sum, O) goes to the workspace and a small second kernel
+// (programmatic dependent launch) merges the partials of each such pair. The finish
+// normalises, rounds to BF16, gates and rounds again.
+// FP8 cache: K and V bytes become f16 in registers (every e4m3 value is exact in f16) and the
+// MMAs run in f16 with q converted to f16 once. The d axis is permuted the same way in q and K
+// (and undone on the output for V) so that each thread's bytes are contiguous in shared memory.
+// Every wait is bounded: on expiry the CTA records BEAM_DEV_TIMEOUT, stops issuing, lets its
+// issued copies land and finishes without valid results.
+#include <cuda.h>
+#include <math.h>
+
+#include "attn_dec.cuh"
+#include "common.cuh"
+#include "mma.cuh"
+#include "tcgen05.cuh"
+
+namespace beam {
+namespace adec {
+namespace {
+
+using namespace beam::tc;
+
+constexpr float kNegInf = -INFINITY;
+constexpr float kRescale = 8.f;   // log2 units
+constexpr int D = 128;
+constexpr int kHeads = 8;         // MMA N: query heads of one KV group (G <= 8)
+constexpr int kMaxParts = 160;    // partials of one pair at most
+
+template <bool FP8>
+struct Cfg {
+  static constexpr int NCW = FP8 ? 8 : 4;          // consumer warps
+  static constexpr int THREADS = (NCW + 1) * 32;   // + the TMA warp
+  static constexpr int BK = 16 * NCW;              // keys per block
+  static constexpr int ROWB = FP8 ? D : 2 * D;     // bytes of one cached key row
+  static constexpr int KB = BK * ROWB;             // K (or V) bytes of one block
+  static constexpr int STAGE = 2 * KB;
+  static constexpr int NST = 4;
+  static constexpr int OLD = D + 4;                // row stride of the combine buffer (floats)
+  // combine area, after the stages (byte offsets)
+  static constexpr int COMB = NST * STAGE;
+  static constexpr int OW = COMB;                                  // [NCW][8][OLD] O partials
+  static constexpr int MLW = OW + NCW * kHeads * OLD * 4;          // [NCW][8][2] (m, l)
+  static constexpr int FW = MLW + NCW * kHeads * 2 * 4;            // [NCW][8] warp weights
+  static constexpr int LH = FW + NCW * kHeads * 4;                 // [8] sum, [8] max
+  static constexpr int MISC = LH + 2 * kHeads * 4;                 // ints: -, abort, issued
+  static constexpr int BAR = (MISC + 16 + 7) / 8 * 8;
+  static constexpr int BYTES = BAR + 2 * NST * 8 + 1024;           // + alignment slack
+};
+
+struct Params {
+  const uint16_t* q;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  const uint16_t* gpre;
+  const uint16_t* gate_bias;
+  uint16_t* og;
+  float* part_acc;   // [grid][2][8][D]: a CTA's partials of its first and its last pair
+  float* part_ml;    // [grid][2][8][2]
+  int n_q, n_kv, G, num_seqs, cap, window;
+  int NB;            // blocks per pair (sized by max_pos)
+  int R;             // blocks per CTA
+  int total;         // pairs * NB
+  float sl2, v_scale;
+};
+
+// Partial slot of CTA c for pair q: 0 when q is the first pair of c's range, else 1 (a pair
+// that is neither first nor last in a range lies whole inside it and needs no partial).
+__device__ __forceinline__ size_t part_slot(const Params& P, int q, int c) {
+  const int first = int((int64_t(c) * P.R) / P.NB);
+  return size_t(2 * c + (q == first ? 0 : 1));
+}
+
+// Pair q = token * n_kv + KV head: its valid keys are positions [lo, p]; block b holds
+// positions BK*b + 1 .. BK*b + BK, at ring slots starting at (BK*b) mod cap (a ring's capacity
+// is a multiple of BK, so no block crosses the end of the ring). The pair's blocks are
+// blk0 .. blk0 + nbq - 1.
+struct Pair {
+  int t, hk, p, s, lo, blk0, nbq;
+  bool ok;
+  unsigned int bad;
+};
+template <int BK>
+__device__ __forceinline__ Pair pair_of(const Params& P, int q) {
+  Pair r;
+  r.t = q / P.n_kv;
+  r.hk = q - r.t * P.n_kv;
+  r.p = P.pos[r.t];
+  r.s = P.seq_id[r.t];
+  r.bad = 0;
+  if (r.p < 1 || (P.window == 0 && r.p > P.cap)) r.bad = BEAM_DEV_BAD_POSITION;
+  else if (r.s < 0 || r.s >= P.num_seqs) r.bad = BEAM_DEV_BAD_SEQ;
+  r.lo = P.window > 0 ? max(1, r.p - P.window + 1) : 1;
+  r.blk0 = r.bad ? 0 : (r.lo - 1) / BK;
+  r.nbq = r.bad ? 0 : (r.p - 1) / BK - r.blk0 + 1;
+  if (r.nbq > P.NB) {   // a position beyond the host's bound max_pos
+    r.bad = BEAM_DEV_BAD_POSITION;
+    r.nbq = 0;
+  }
+  r.ok = r.bad == 0;
+  return r;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Transpose of the warp's 8x8 b16 matrix held one 32-bit pair per thread.
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f16x2(uint32_t w, float& lo, float& hi) {
+  asm("{.reg .f16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b;}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+}
+// Four e4m3 codes -> two f16x2 words (bytes 0-1 -> lo, bytes 2-3 -> hi), exactly.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{.reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b;}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <int NT>
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+// O^T += V^T . P^T over the warp's 16 keys. MASK: keys outside the pair's range (whose slots
+// may hold anything, NaN included) have their V values replaced by zeros, so that P = 0 there
+// contributes exactly nothing; m01 / m89 select the valid halves of keys (2c, 2c+1) and
+// (2c+8, 2c+9).
+template <bool FP8, bool MASK>
+__device__ __forceinline__ void pv_block(uint32_t vb, const uint32_t (&voff)[4], uint32_t bh0,
+                                         uint32_t bh1, uint32_t bl0, uint32_t bl1, uint32_t m01,
+                                         uint32_t m89, float (&acc)[8][4]) {
+  using C = Cfg<FP8>;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int w = threadIdx.x >> 5;
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t a[4];
+      ldsm_x4_t(vb + (mt >> 2) * (C::KB / 2) + voff[mt & 3], a[0], a[1], a[2], a[3]);
+      if (MASK) {
+        a[0] &= m01;
+        a[1] &= m01;
+        a[2] &= m89;
+        a[3] &= m89;
+      }
+      mma_bf16(acc[mt], a, bh0, bh1);
+      mma_bf16(acc[mt], a, bl0, bl1);
+    }
+  } else {
+    // key rows 16w + {2c, 2c+1, 2c+8, 2c+9}, bytes [16g, 16g + 16): logical row g of m-tile mt
+    // is d = 16g + 2mt, row g + 8 is d = 16g + 2mt + 1
+    const uint32_t rb = vb + (16 * w + 2 * c) * 128;
+    const uint4 q0 = lds128(rb + ((g ^ (2 * c)) << 4));
+    const uint4 q1 = lds128(rb + 128 + ((g ^ (2 * c + 1)) << 4));
+    const uint4 q2 = lds128(rb + 8 * 128 + ((g ^ (2 * c)) << 4));
+    const uint4 q3 = lds128(rb + 9 * 128 + ((g ^ (2 * c + 1)) << 4));
+    const uint32_t r0[4] = {q0.x, q0.y, q0.z, q0.w}, r1[4] = {q1.x, q1.y, q1.z, q1.w};
+    const uint32_t r2[4] = {q2.x, q2.y, q2.z, q2.w}, r3[4] = {q3.x, q3.y, q3.z, q3.w};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+      uint32_t a[4];
+      e4m3x4_to_f16(prmt(r0[mt >> 1], r1[mt >> 1], sel), a[0], a[1]);
+      e4m3x4_to_f16(prmt(r2[mt >> 1], r3[mt >> 1], sel), a[2], a[3]);
+      if (MASK) {
+        a[0] &= m01;
+        a[1] &= m01;
+        a[2] &= m89;
+        a[3] &= m89;
+      }
+      mma_f16(acc[mt], a, bh0, bh1);
+      mma_f16(acc[mt], a, bl0, bl1);
+    }
+  }
+}
+
+// One warp's 16 keys of a staged block: S^T = K . Q^T, online softmax, O^T += V^T . P^T.
+// kb / vb: shared addresses of the block's K and V; kbase: position of the warp's key row 0;
+// the pair's keys are positions [lo, p].
+template <bool FP8>
+__device__ __forceinline__ void warp_block(uint32_t kb, uint32_t vb, const uint32_t (&qb)[8][2],
+                                           const uint32_t (&koff)[4], const uint32_t (&voff)[4],
+                                           int kbase, int lo, int p, float sl2, float (&m)[2],
+                                           float (&l)[2], float (&acc)[8][4]) {
+  using C = Cfg<FP8>;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int w = threadIdx.x >> 5;
+  const int kp0 = kbase + g;
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int kk = 0; kk < 8; kk += 2) {
+      uint32_t a[4], b[4];
+      ldsm_x4(kb + (kk >> 2) * (C::KB / 2) + koff[kk & 3], a[0], a[1], a[2], a[3]);
+      ldsm_x4(kb + ((kk + 1) >> 2) * (C::KB / 2) + koff[(kk + 1) & 3], b[0], b[1], b[2], b[3]);
+      mma_bf16(sa, a, qb[kk][0], qb[kk][1]);
+      mma_bf16(sb, b, qb[kk + 1][0], qb[kk + 1][1]);
+    }
+  } else {
+    // rows 16w + g and 16w + g + 8, bytes [32c, 32c + 32): logical k (16kk + 2c + e [+8]) is
+    // byte 32c + 4kk + e [+2]
+    const uint32_t r0 = kb + (16 * w + g) * 128, r1 = r0 + 8 * 128;
+    const uint4 k00 = lds128(r0 + (((2 * c) ^ g) << 4)), k01 = lds128(r0 + (((2 * c + 1) ^ g) << 4));
+    const uint4 k10 = lds128(r1 + (((2 * c) ^ g) << 4)), k11 = lds128(r1 + (((2 * c + 1) ^ g) << 4));
+    const uint32_t w0[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
+    const uint32_t w1[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a[4];
+      e4m3x4_to_f16(w0[kk], a[0], a[2]);
+      e4m3x4_to_f16(w1[kk], a[1], a[3]);
+      if (kk & 1) mma_f16(sb, a, qb[kk][0], qb[kk][1]);
+      else mma_f16(sa, a, qb[kk][0], qb[kk][1]);
+    }
+  }
+  // S^T fragment: [0] (key g, head 2c), [1] (key g, head 2c+1), [2], [3] key g + 8
+  const bool v0 = kp0 >= lo && kp0 <= p, v1 = kp0 + 8 >= lo && kp0 + 8 <= p;
+  float x[4];
+  x[0] = v0 ? (sa[0] + sb[0]) * sl2 : kNegInf;
+  x[1] = v0 ? (sa[1] + sb[1]) * sl2 : kNegInf;
+  x[2] = v1 ? (sa[2] + sb[2]) * sl2 : kNegInf;
+  x[3] = v1 ? (sa[3] + sb[3]) * sl2 : kNegInf;
+  float mh[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mh[0] = fmaxf(mh[0], __shfl_xor_sync(0xffffffffu, mh[0], o));
+    mh[1] = fmaxf(mh[1], __shfl_xor_sync(0xffffffffu, mh[1], o));
+  }
+  if (__any_sync(0xffffffffu, mh[0] > m[0] + kRescale || mh[1] > m[1] + kRescale)) {
+    float cr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float mn = fmaxf(m[h], mh[h]);
+      cr[h] = m[h] == kNegInf ? 0.f : ex2_approx(m[h] - mn);
+      m[h] = mn;
+      l[h] *= cr[h];
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= cr[0];
+      acc[mt][1] *= cr[1];
+      acc[mt][2] *= cr[0];
+      acc[mt][3] *= cr[1];
+    }
+  }
+  const float ms0 = m[0] == kNegInf ? 0.f : m[0], ms1 = m[1] == kNegInf ? 0.f : m[1];
+  const float p0 = ex2_approx(x[0] - ms0), p1 = ex2_approx(x[1] - ms1);
+  const float p2 = ex2_approx(x[2] - ms0), p3 = ex2_approx(x[3] - ms1);
+  l[0] += p0 + p2;
+  l[1] += p1 + p3;
+  // P (key rows, head columns) as hi + lo, then transposed into the B fragments of P^T:
+  // b0 = (keys 2c, 2c+1; head g), b1 = (keys 2c+8, 2c+9; head g)
+  uint32_t h01, h23, l01, l23;
+  if constexpr (!FP8) {
+    h01 = pack_bf16x2(p0, p1);
+    h23 = pack_bf16x2(p2, p3);
+    l01 = pack_bf16x2(p0 - bf_lo(h01), p1 - bf_hi(h01));
+    l23 = pack_bf16x2(p2 - bf_lo(h23), p3 - bf_hi(h23));
+  } else {
+    float f0, f1, f2, f3;
+    h01 = pack_f16x2(p0, p1);
+    h23 = pack_f16x2(p2, p3);
+    unpack_f16x2(h01, f0, f1);
+    unpack_f16x2(h23, f2, f3);
+    l01 = pack_f16x2(p0 - f0, p1 - f1);
+    l23 = pack_f16x2(p2 - f2, p3 - f3);
+  }
+  const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
+  const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
+  if (kbase >= lo && kbase + 15 <= p) {
+    pv_block<FP8, false>(vb, voff, bh0, bh1, bl0, bl1, 0u, 0u, acc);
+  } else {
+    auto ok = [&](int k) { return kbase + k >= lo && kbase + k <= p; };
+    const uint32_t m01 = (ok(2 * c) ? 0x0000FFFFu : 0u) | (ok(2 * c + 1) ? 0xFFFF0000u : 0u);
+    const uint32_t m89 = (ok(2 * c + 8) ? 0x0000FFFFu : 0u) | (ok(2 * c + 9) ? 0xFFFF0000u : 0u);
+    pv_block<FP8, true>(vb, voff, bh0, bh1, bl0, bl1, m01, m89, acc);
+  }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) attn_decode_tma_kernel(
+    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+    const Params P) {
+  using C = Cfg<FP8>;
+  constexpr int NCT = C::NCW * 32;   // consumer threads
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar_full = sbase + C::BAR, bar_empty = bar_full + 8 * C::NST;
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + C::MISC);   // -, abort, issued
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::NCW);
+    }
+    misc[1] = 0;
+    misc[2] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  const int f_lo = blockIdx.x * P.R, f_hi = min(P.total, f_lo + P.R);
+
+  if (warp == C::NCW) {
+    // ---------------- producer: one lane issues the TMA loads of every block in range
+    if (lane == 0) {
+      int i = 0;
+      bool run = true;
+      for (int f = f_lo; f < f_hi && run;) {
+        const int q = f / P.NB, j0 = f - q * P.NB, j1 = min(P.NB, j0 + (f_hi - f));
+        f += j1 - j0;
+        const Pair pr = pair_of<C::BK>(P, q);
+        const int jl = min(j1, pr.nbq);
+        const int z = pr.s * P.n_kv + pr.hk;
+        for (int j = j0; j < jl; ++j) {
+          const int st = i % C::NST;
+          if (misc[1] != 0 ||
+              (i >= C::NST && !mbar_wait(bar_empty + 8 * st, ((i / C::NST) - 1) & 1))) {
+            misc[1] = 1;
+            run = false;
+            break;
+          }
+          const int b = pr.blk0 + j;
+          const int slot = P.window > 0 ? (C::BK * b) % P.cap : C::BK * b;
+          const uint32_t dk = sbase + st * C::STAGE, dv = dk + C::KB, fb = bar_full + 8 * st;
+          mbar_expect_tx(fb, C::STAGE);
+          if constexpr (FP8) {
+            tma_load_3d(dk, &tk, 0, slot, z, fb);
+            tma_load_3d(dv, &tv, 0, slot, z, fb);
+          } else {
+            tma_load_3d(dk, &tk, 0, slot, z, fb);
+            tma_load_3d(dk + C::KB / 2, &tk, 64, slot, z, fb);
+            tma_load_3d(dv, &tv, 0, slot, z, fb);
+            tma_load_3d(dv + C::KB / 2, &tv, 64, slot, z, fb);
+          }
+          ++i;
+        }
+      }
+      misc[2] = i;
+    }
+  } else {
+    // ---------------- consumers
+    const int w = warp, g = lane >> 2, c = lane & 3;
+    const int ct = threadIdx.x;
+    uint32_t koff[4] = {0, 0, 0, 0}, voff[4] = {0, 0, 0, 0};
+    if constexpr (!FP8) {
+      // ldmatrix row addresses: K (A operand, 16 keys x 16 d): matrices (keys 0-7 | 8-15) x
+      // (d chunk 2kk | 2kk+1); V (A = V^T via .trans): (keys 0-7, chunk 2mt), (0-7, 2mt+1),
+      // (8-15, 2mt), (8-15, 2mt+1). 128-byte swizzle: chunk ^= row % 8.
+      const int rk = 16 * w + ((lane >> 3) & 1) * 8 + (lane & 7), ck = (lane >> 4) & 1;
+      const int rv = 16 * w + ((lane >> 4) & 1) * 8 + (lane & 7), cv = (lane >> 3) & 1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        koff[e] = uint32_t(rk * 128 + (((2 * e + ck) ^ (lane & 7)) << 4));
+        voff[e] = uint32_t(rv * 128 + (((2 * e + cv) ^ (lane & 7)) << 4));
+      }
+    }
+    float* Ow = reinterpret_cast<float*>(sm + C::OW);
+    float* MLw = reinterpret_cast<float*>(sm + C::MLW);
+    float* FWs = reinterpret_cast<float*>(sm + C::FW);
+    float* LHs = reinterpret_cast<float*>(sm + C::LH);   // [0, 8) sums, [8, 16) maxima
+    const int G = P.G;
+    int i = 0;
+    for (int f = f_lo; f < f_hi;) {
+      const int q = f / P.NB, j0 = f - q * P.NB, j1 = min(P.NB, j0 + (f_hi - f));
+      f += j1 - j0;
+      const Pair pr = pair_of<C::BK>(P, q);
+      const int jl = min(j1, pr.nbq);
+      if (pr.bad && j0 == 0 && pr.hk == 0 && ct == 0) flag(pr.bad);
+      // q fragments (B operand, column = head g)
+      uint32_t qb[8][2];
+      {
+        const bool rok = g < G;
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(
+            P.q + (size_t(pr.t) * P.n_q + pr.hk * G + (rok ? g : 0)) * D);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if constexpr (!FP8) {
+            qb[kk][0] = rok ? qr[8 * kk + c] : 0u;
+            qb[kk][1] = rok ? qr[8 * kk + c + 4] : 0u;
+          } else {
+            const uint32_t x0 = rok ? qr[16 * c + 2 * kk] : 0u, x1 = rok ? qr[16 * c + 2 * kk + 1] : 0u;
+            qb[kk][0] = pack_f16x2(bf_lo(x0), bf_hi(x0));
+            qb[kk][1] = pack_f16x2(bf_lo(x1), bf_hi(x1));
+          }
+        }
+      }
+      float acc[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+      for (int j = j0; j < jl; ++j, ++i) {
+        const int st = i % C::NST;
+        bool ok = misc[1] == 0;
+        if (ok) ok = mbar_wait(bar_full + 8 * st, (i / C::NST) & 1);
+        if (__all_sync(0xffffffffu, ok)) {
+          const uint32_t kb = sbase + st * C::STAGE;
+          const int kbase = C::BK * (pr.blk0 + j) + 16 * w + 1;
+          warp_block<FP8>(kb, kb + C::KB, qb, koff, voff, kbase, pr.lo, pr.p, P.sl2, m, l, acc);
+        } else if (lane == 0) {
+          misc[1] = 1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+      }
+      // ---- combine the consumer warps' partials of pair q
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+      }
+      consumer_bar<NCT>();   // the previous pair's readers of the combine area are done
+      {
+        float* ow = Ow + w * kHeads * C::OLD;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int da = FP8 ? 16 * g + 2 * mt : 16 * mt + g;
+          const int db = FP8 ? da + 1 : da + 8;
+          ow[(2 * c) * C::OLD + da] = acc[mt][0];
+          ow[(2 * c + 1) * C::OLD + da] = acc[mt][1];
+          ow[(2 * c) * C::OLD + db] = acc[mt][2];
+          ow[(2 * c + 1) * C::OLD + db] = acc[mt][3];
+        }
+        if (g == 0) {
+          MLw[(w * kHeads + 2 * c) * 2] = m[0];
+          MLw[(w * kHeads + 2 * c) * 2 + 1] = l[0];
+          MLw[(w * kHeads + 2 * c + 1) * 2] = m[1];
+          MLw[(w * kHeads + 2 * c + 1) * 2 + 1] = l[1];
+        }
+      }
+      consumer_bar<NCT>();
+      if (ct < G) {
+        const int h = ct;
+        float M = kNegInf;
+#pragma unroll
+        for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, MLw[(ww * kHeads + h) * 2]);
+        float L = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < C::NCW; ++ww) {
+          const float fw = M == kNegInf ? 0.f : ex2_approx(MLw[(ww * kHeads + h) * 2] - M);
+          FWs[ww * kHeads + h] = fw;
+          L += fw * MLw[(ww * kHeads + h) * 2 + 1];
+        }
+        LHs[h] = L;
+        LHs[kHeads + h] = M;
+      }
+      consumer_bar<NCT>();
+      const int c_first = int((int64_t(q) * P.NB) / P.R);
+      const int c_last = int((int64_t(q + 1) * P.NB - 1) / P.R);
+      const int ncontrib = c_last - c_first + 1;
+      if (ncontrib == 1) {
+        for (int idx = ct; idx < G * D; idx += NCT) {
+          const int h = idx / D, d = idx - h * D;
+          float O = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < C::NCW; ++ww) O += FWs[ww * kHeads + h] * Ow[(ww * kHeads + h) * C::OLD + d];
+          const float L = LHs[h];
+          const float o = round_bf(O * (L > 0.f ? P.v_scale / L : 0.f));
+          const int hq = pr.hk * G + h;
+          const size_t oi = (size_t(pr.t) * P.n_q + hq) * D + d;
+          const float gate = sigmoidf_(bf2f(P.gpre[oi]) + bf2f(P.gate_bias[hq]));
+          P.og[oi] = f2bf(o * gate);
+        }
+      } else {
+        const size_t pb = part_slot(P, q, blockIdx.x) * kHeads;
+        for (int idx = ct; idx < G * D; idx += NCT) {
+          const int h = idx / D, d = idx - h * D;
+          float O = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < C::NCW; ++ww) O += FWs[ww * kHeads + h] * Ow[(ww * kHeads + h) * C::OLD + d];
+          P.part_acc[(pb + h) * D + d] = O;
+        }
+        if (ct < G) {
+          P.part_ml[(pb + ct) * 2] = LHs[kHeads + ct];
+          P.part_ml[(pb + ct) * 2 + 1] = LHs[ct];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == C::NCW && lane == 0) {
+    // normally a no-op: every issued block was consumed; after an expired wait, let the
+    // copies still in flight land before the CTA's shared memory is released
+    const int n = misc[2];
+    for (int k = n > C::NST ? n - C::NST : 0; k < n; ++k)
+      mbar_wait(bar_full + 8 * (k % C::NST), (k / C::NST) & 1);
+    if (misc[1]) flag(BEAM_DEV_TIMEOUT);
+  }
+}
+
+// Finish of the pairs split between CTAs: merge CTA m takes the pair whose first block lies in
+// CTA m's range and that runs on past it (at most one), combines the partials of the CTAs
+// c_first .. c_last, normalises, rounds, gates and rounds.
+constexpr int kMergeThreads = 192;
+__global__ void __launch_bounds__(kMergeThreads) attn_decode_merge_kernel(const Params P) {
+  pdl_trigger();
+  __shared__ float wsh[kHeads][kMaxParts];   // part maxima, then their weights
+  __shared__ float lsh[kHeads][kMaxParts];   // part sums
+  __shared__ float inv[kHeads];
+  __shared__ int sl[kMaxParts];
+  const int m = blockIdx.x;
+  const int f_last = int(min(int64_t(P.total), int64_t(m + 1) * P.R) - 1);
+  const int q = f_last / P.NB;
+  const int c_first = int((int64_t(q) * P.NB) / P.R);
+  const int c_last = int((int64_t(q + 1) * P.NB - 1) / P.R);
+  if (c_first != m || c_last == m) return;
+  pdl_wait();
+  const int n = c_last - c_first + 1, G = P.G;
+  const int t = q / P.n_kv, hk = q - t * P.n_kv;
+  for (int s = threadIdx.x; s < n; s += kMergeThreads) sl[s] = int(part_slot(P, q, m + s) * kHeads);
+  __syncthreads();
+  // every part's (max, sum) fetched at once into shared memory, then reduced per head
+  for (int i = threadIdx.x; i < n * G; i += kMergeThreads) {
+    const int s = i / G, h = i - s * G;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(P.part_ml + (sl[s] + h) * 2));
+    wsh[h][s] = v.x;
+    lsh[h][s] = v.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = kNegInf;
+    for (int s = 0; s < n; ++s) M = fmaxf(M, wsh[h][s]);
+    float L = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const float fw = M == kNegInf ? 0.f : ex2_approx(wsh[h][s] - M);
+      wsh[h][s] = fw;
+      L += fw * lsh[h][s];
+    }
+    inv[h] = L > 0.f ? P.v_scale / L : 0.f;
+  }
+  __syncthreads();
+  // one thread per 4 consecutive outputs of a head; all parts' loads issued 8 at a time
+  for (int o4 = threadIdx.x; o4 < G * (D / 4); o4 += kMergeThreads) {
+    const int h = o4 / (D / 4), d = 4 * (o4 - h * (D / 4));
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 8 <= n; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float4*>(P.part_acc + size_t(sl[s + u] + h) * D + d));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float fw = wsh[h][s + u];
+        O.x += fw * v[u].x;
+        O.y += fw * v[u].y;
+        O.z += fw * v[u].z;
+        O.w += fw * v[u].w;
+      }
+    }
+    for (; s < n; ++s) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(P.part_acc + size_t(sl[s] + h) * D + d));
+      const float fw = wsh[h][s];
+      O.x += fw * v.x;
+      O.y += fw * v.y;
+      O.z += fw * v.z;
+      O.w += fw * v.w;
+    }
+    const int hq = hk * G + h;
+    const size_t oi = (size_t(t) * P.n_q + hq) * D + d;
+    const float gb = bf2f(P.gate_bias[hq]);
+    const uint2 gv = *reinterpret_cast<const uint2*>(P.gpre + oi);
+    const float o0 = round_bf(O.x * inv[h]), o1 = round_bf(O.y * inv[h]);
+    const float o2 = round_bf(O.z * inv[h]), o3 = round_bf(O.w * inv[h]);
+    const uint32_t r0 = pack_bf16x2(o0 * sigmoidf_(bf_lo(gv.x) + gb), o1 * sigmoidf_(bf_hi(gv.x) + gb));
+    const uint32_t r1 = pack_bf16x2(o2 * sigmoidf_(bf_lo(gv.y) + gb), o3 * sigmoidf_(bf_hi(gv.y) + gb));
+    *reinterpret_cast<uint2*>(P.og + oi) = make_uint2(r0, r1);
+  }
+}
+
+struct Plan {
+  int NB, R, grid, total;
+};
+
+Plan make_plan(int T, int n_kv, int window, int max_pos, bool fp8) {
+  const int BK = fp8 ? Cfg<true>::BK : Cfg<false>::BK;
+  const int max_keys = window > 0 ? (max_pos < window ? max_pos : window) : max_pos;
+  Plan pl;
+  pl.NB = (max_keys + BK - 1) / BK + (window > 0 ? 1 : 0);
+  pl.total = T * n_kv * pl.NB;
+  const int sms = num_sms_cached();
+  int grid = pl.total < sms ? pl.total : sms;
+  if (grid < 1) grid = 1;
+  pl.R = (pl.total + grid - 1) / grid;
+  // a pair's blocks meet at most ceil(NB / R) + 1 CTA ranges
+  while ((pl.NB + pl.R - 1) / pl.R + 1 > kMaxParts) ++pl.R;
+  pl.grid = (pl.total + pl.R - 1) / pl.R;
+  return pl;
+}
+
+}  // namespace
+
+bool supported(int D_, int G, int window, int cap, bool fp8, const void* k, const void* v,
+               int max_keys) {
+  if (D_ != D || G < 1 || G > kHeads || max_keys < kMinKeys) return false;
+  const int BK = fp8 ? Cfg<true>::BK : Cfg<false>::BK;
+  if (window > 0 && cap % BK != 0) return false;
+  return aligned16(k) && aligned16(v) && tensor_map_encoder_ready();
+}
+
+size_t ws_bytes(int T, int n_kv, int window, int max_pos, bool fp8) {
+  if (T <= 0 || max_pos < 1) return 0;
+  const Plan pl = make_plan(T, n_kv, window, max_pos, fp8);
+  const size_t parts = size_t(pl.grid) * 2 * kHeads;
+  return align_up(parts * D * 4, 256) + align_up(parts * 2 * 4, 256);
+}
+
+cudaError_t decode(const uint16_t* q, const uint16_t* g, const uint16_t* gate_bias,
+                   const int32_t* seq_id, const int32_t* pos, int T, int max_pos, int n_q,
+                   int n_kv, const beam_kv_cache& kc, float sl2, float v_scale, uint16_t* og,
+                   void* ws, size_t ws_len, cudaStream_t st) {
+  const bool fp8 = kc.dtype == BEAM_KV_FP8_E4M3;
+  const Plan pl = make_plan(T, n_kv, kc.window, max_pos, fp8);
+  if (ws_len < ws_bytes(T, n_kv, kc.window, max_pos, fp8)) return cudaErrorInvalidValue;
+  const size_t parts = size_t(pl.grid) * 2 * kHeads;
+  char* w = static_cast<char*>(ws);
+  float* part_acc = reinterpret_cast<float*>(w);
+  float* part_ml = reinterpret_cast<float*>(w + align_up(parts * D * 4, 256));
+  CUtensorMap mk, mv;
+  {
+    const int rowb = fp8 ? D : 2 * D;
+    const uint64_t dims[3] = {uint64_t(fp8 ? D : D), uint64_t(kc.capacity),
+                              uint64_t(kc.num_seqs) * n_kv};
+    const uint64_t str[2] = {uint64_t(rowb), uint64_t(kc.capacity) * rowb};
+    const uint32_t box[3] = {uint32_t(fp8 ? 128 : 64), uint32_t(fp8 ? Cfg<true>::BK : Cfg<false>::BK), 1};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tiled(&mk, dt, 3, kc.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&mv, dt, 3, kc.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e;
+  Params prm{q,  seq_id, pos, g, gate_bias, og, part_acc, part_ml, n_q, n_kv, n_q / n_kv,
+             kc.num_seqs, kc.capacity, kc.window, pl.NB, pl.R, pl.total, sl2, v_scale};
+  if (fp8) {
+    auto kern = attn_decode_tma_kernel<true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::BYTES);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(pl.grid), dim3(Cfg<true>::THREADS), Cfg<true>::BYTES, st, mk, mv, prm);
+  } else {
+    auto kern = attn_decode_tma_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<false>::BYTES);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(pl.grid), dim3(Cfg<false>::THREADS), Cfg<false>::BYTES, st, mk, mv, prm);
+  }
+  if (e != cudaSuccess) return e;
+  // ranges that are whole multiples of a pair's blocks split no pair: nothing to merge
+  if (pl.R % pl.NB != 0) {
+    e = launch_pdl(attn_decode_merge_kernel, dim3(pl.grid), dim3(kMergeThreads), 0, st, prm);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace adec
+}  // namespace beam
