@@ -138,12 +138,158 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
   }
 }
 
+// The same products on the tensor cores (mma.sync m16n8k16, bf16 in, FP32 accumulate) for up
+// to 8 tokens: a 16-row block of W is the A operand and the tokens are the 8 columns of B, so
+// each 16-byte weight chunk costs a fraction of an instruction instead of 8 FMAs per token.
+// The k axis is permuted inside every 32-element block (a sum does not depend on its order):
+// lane (g, c) loads elements 8c..8c+7 of the block from rows g and g+8 of the row block and
+// from token g, and uses elements {0,1,2,3} as the fragments of the block's first k16 step
+// and {4,5,6,7} as those of the second -- one 16-byte load per row instead of four 4-byte
+// ones, and the same permutation on both operands. KS warps of a CTA split the K blocks of one
+// row block and add their partial tiles in order through shared memory; a CTA holds 8 / KS row
+// blocks. SwiGLU: a row block is 8 gate rows f0..f0+7 and the 8 matching up rows, so one
+// thread ends with both the gate and the up value of its unit.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int MODE, int KS, int U>
+__global__ void __launch_bounds__(256) gemv_mma_kernel(const uint16_t* __restrict__ W, int N,
+                                                       int K, const uint16_t* __restrict__ X,
+                                                       int T, float* __restrict__ yf,
+                                                       uint16_t* __restrict__ yb, int ldy) {
+  pdl_trigger();
+  constexpr int RB = 8 / KS;
+  __shared__ float red[8][32][4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int rb = blockIdx.x * RB + warp / KS, ks = warp % KS;
+  // the two weight rows of this lane (clamped for loads; outputs past N are not written)
+  const uint16_t* w0;
+  const uint16_t* w1;
+  int n_lo, n_hi;
+  if (MODE == kOutSwiGLU) {
+    n_lo = rb * 8 + g;
+    const int f = min(n_lo, N - 1);
+    w0 = W + size_t(f) * K;
+    w1 = W + size_t(N + f) * K;
+    n_hi = n_lo;
+  } else {
+    n_lo = rb * 16 + g;
+    n_hi = n_lo + 8;
+    w0 = W + size_t(min(n_lo, N - 1)) * K;
+    w1 = W + size_t(min(n_hi, N - 1)) * K;
+  }
+  const int nb = K >> 5;
+  const int b0 = ks * nb / KS, b1 = (ks + 1) * nb / KS;
+  // weights are no predecessor's output: start this warp's slice towards L2 before waiting
+  // (matrices up to 160 MB, their first 64 MB, as in gemv_kernel)
+  {
+    constexpr size_t kPrefetchBudget = size_t(64) << 20, kPrefetchMaxMatrix = size_t(160) << 20;
+    const size_t rows = MODE == kOutSwiGLU ? 2 * size_t(N) : size_t(N);
+    const size_t first_row = MODE == kOutSwiGLU ? size_t(rb) * 8 : size_t(rb) * 16;
+    if (rows * size_t(K) * 2 <= kPrefetchMaxMatrix && first_row * K * 2 < kPrefetchBudget &&
+        b1 > b0 && lane < 16) {
+      // lane l < 16 takes row l of the block (SwiGLU: gate rows, then the up rows)
+      size_t r;
+      if (MODE == kOutSwiGLU) r = (lane < 8 ? 0 : size_t(N)) + size_t(min(rb * 8 + (lane & 7), N - 1));
+      else r = size_t(min(rb * 16 + lane, N - 1));
+      l2_prefetch(W + r * K + size_t(b0) * 32, uint32_t(b1 - b0) * 64);
+    }
+  }
+  pdl_wait();
+  const bool tok = g < T;
+  const uint16_t* xr = X + size_t(tok ? g : 0) * K + 8 * c;
+  w0 += 8 * c;
+  w1 += 8 * c;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  int b = b0;
+  for (; b + U <= b1; b += U) {
+    uint4 a[U], h[U], x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      a[u] = ld_stream(w0 + size_t(b + u) * 32);
+      h[u] = ld_stream(w1 + size_t(b + u) * 32);
+      x[u] = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b + u) * 32)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      mma16816(acc, a[u].x, h[u].x, a[u].y, h[u].y, x[u].x, x[u].y);
+      mma16816(acc2, a[u].z, h[u].z, a[u].w, h[u].w, x[u].z, x[u].w);
+    }
+  }
+  for (; b < b1; ++b) {
+    const uint4 a = ld_stream(w0 + size_t(b) * 32), h = ld_stream(w1 + size_t(b) * 32);
+    const uint4 x = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b) * 32)) : make_uint4(0, 0, 0, 0);
+    mma16816(acc, a.x, h.x, a.y, h.y, x.x, x.y);
+    mma16816(acc2, a.z, h.z, a.w, h.w, x.z, x.w);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+  if (KS > 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[warp][lane][i] = acc[i];
+    __syncthreads();
+    if (ks != 0) return;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v = red[warp][lane][i];
+#pragma unroll
+      for (int j = 1; j < KS; ++j) v += red[warp + j][lane][i];
+      acc[i] = v;
+    }
+  }
+  // C fragment: acc[0], acc[1] = (row g; tokens 2c, 2c+1), acc[2], acc[3] = (row g + 8; ...)
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int t = 2 * c + e;
+    if (t >= T) continue;
+    if (MODE == kOutSwiGLU) {
+      if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(siluf_(acc[e]) * acc[2 + e]);
+    } else if (MODE == kOutF32) {
+      if (n_lo < N) yf[size_t(t) * ldy + n_lo] = acc[e];
+      if (n_hi < N) yf[size_t(t) * ldy + n_hi] = acc[2 + e];
+    } else {
+      if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(acc[e]);
+      if (n_hi < N) yb[size_t(t) * ldy + n_hi] = f2bf(acc[2 + e]);
+    }
+  }
+}
+
 // Host launcher: the register-pipelined kernel with the token tile, rows per warp and chunks in
 // flight picked from T.
+// Tensor-core form for 2..8 tokens (K a multiple of 32): KS, the warps sharing a row block,
+// is the smallest power of two that gives at least 16 warps per SM.
+constexpr int kGemvMmaMinT = 2;
+template <int MODE>
+inline cudaError_t launch_gemv_mma(const uint16_t* W, int N, int K, const uint16_t* X, int T,
+                                   float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
+  const int units = MODE == kOutSwiGLU ? (N + 7) / 8 : (N + 15) / 16;
+  const int want = 16 * num_sms_cached();
+  int ks = 1;
+  while (ks < 8 && units * ks < want && (K / 32) >= 2 * ks) ks *= 2;
+  const dim3 grid((units * ks + 7) / 8);
+  switch (ks) {
+    case 1: return launch_pdl(gemv_mma_kernel<MODE, 1, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    case 2: return launch_pdl(gemv_mma_kernel<MODE, 2, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    case 4: return launch_pdl(gemv_mma_kernel<MODE, 4, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    default: return launch_pdl(gemv_mma_kernel<MODE, 8, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+  }
+}
+
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
                                float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
   if (T <= 0 || N <= 0) return cudaSuccess;
+  if (T >= kGemvMmaMinT && T <= 8 && (K & 31) == 0) {
+    const cudaError_t e = launch_gemv_mma<MODE>(W, N, K, X, T, yf, yb, ldy, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   auto go = [&](auto kern, int nt, int nr) {
     const int warps = (N + nr - 1) / nr;
     dim3 grid((warps + 7) / 8, (T + nt - 1) / nt);

@@ -329,6 +329,142 @@ __global__ void __launch_bounds__(256) moe_down_kernel(
   }
 }
 
+// Tensor-core forms of the expert products for 2..31 tokens, after the plan: as in
+// gemv_mma_kernel (gemv.cuh), a warp's 16-row block of one expert's weights is the A operand of
+// mma.sync m16n8k16 and up to 8 of the expert's (token, slot) pairs are the columns of B (more
+// pairs: further passes over the rows), with the k axis permuted inside each 32-element block
+// so that every lane loads whole 16-byte chunks. Gate/up: a warp takes 8 units (8 gate rows and
+// the matching 8 up rows) and writes bf16(silu(gate) * up) per pair; CTA (0, 0) also clears the
+// down kernel's completion counters. Down: a warp takes 16 rows h and writes y[pair][h] in
+// FP32; the last CTA of each 128-row column to finish combines its rows for every token:
+// out[t][h] = bf16(sum_j w[t][j] y[t*k+j][h]), slots in order, slots with an expert index out
+// of range skipped.
+constexpr int kMmaU = 4;
+constexpr int kMmaRowsDown = 128;   // rows h per down CTA (8 warps x 16)
+
+__device__ __forceinline__ void expert_rows_mma(const uint16_t* w0, const uint16_t* w1,
+                                                const uint16_t* xr, bool tok, int K,
+                                                float (&acc)[4]) {
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+  const int nb = K >> 5;
+  int b = 0;
+  for (; b + kMmaU <= nb; b += kMmaU) {
+    uint4 a[kMmaU], h[kMmaU], x[kMmaU];
+#pragma unroll
+    for (int u = 0; u < kMmaU; ++u) {
+      a[u] = ld_stream(w0 + size_t(b + u) * 32);
+      h[u] = ld_stream(w1 + size_t(b + u) * 32);
+      x[u] = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b + u) * 32)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kMmaU; ++u) {
+      mma16816(acc, a[u].x, h[u].x, a[u].y, h[u].y, x[u].x, x[u].y);
+      mma16816(acc2, a[u].z, h[u].z, a[u].w, h[u].w, x[u].z, x[u].w);
+    }
+  }
+  for (; b < nb; ++b) {
+    const uint4 a = ld_stream(w0 + size_t(b) * 32), h = ld_stream(w1 + size_t(b) * 32);
+    const uint4 x = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b) * 32)) : make_uint4(0, 0, 0, 0);
+    mma16816(acc, a.x, h.x, a.y, h.y, x.x, x.y);
+    mma16816(acc2, a.z, h.z, a.w, h.w, x.z, x.w);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+}
+
+// grid (ceil(F / 64), max active experts)
+__global__ void __launch_bounds__(256) moe_gate_up_mma_kernel(
+    const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
+    MoePlan pl, int* __restrict__ cnt, int n_cnt, uint16_t* __restrict__ a) {
+  pdl_trigger();
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < n_cnt; i += blockDim.x) cnt[i] = 0;
+  const int ai = blockIdx.y;
+  if (ai >= *pl.n_active) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int f0 = (blockIdx.x * 8 + warp) * 8;
+  if (f0 >= F) return;
+  const int e = pl.active[ai], p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
+  const int f = min(f0 + g, F - 1);
+  const uint16_t* w0 = w_gu + (size_t(e) * 2 * F + f) * H + 8 * c;
+  const uint16_t* w1 = w_gu + (size_t(e) * 2 * F + F + f) * H + 8 * c;
+  for (int pp = p0; pp < p1; pp += 8) {
+    const int np = min(8, p1 - pp);
+    const bool tok = g < np;
+    const uint16_t* xr = u + size_t(tok ? pl.pairs[pp + g] / k : 0) * H + 8 * c;
+    float acc[4];
+    expert_rows_mma(w0, w1, xr, tok, H, acc);
+    // (row g = gate of unit f0+g, row g+8 = its up) x (pairs pp+2c, pp+2c+1)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = 2 * c + j;
+      if (col < np && f0 + g < F)
+        a[size_t(pl.pairs[pp + col]) * F + f0 + g] = f2bf(siluf_(acc[j]) * acc[2 + j]);
+    }
+  }
+}
+
+// grid (ceil(H / 128), max active experts)
+__global__ void __launch_bounds__(256) moe_down_mma_kernel(
+    const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn, int H, int F, MoePlan pl,
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int k, int E,
+    int* __restrict__ cnt, float* __restrict__ y, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int na = *pl.n_active;
+  const int ai = blockIdx.y;
+  if (ai >= max(na, 1)) return;   // uniform over the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int h0 = blockIdx.x * kMmaRowsDown + warp * 16;
+  if (ai < na && h0 < H) {
+    const int e = pl.active[ai], p0 = pl.act_off[ai], p1 = pl.act_off[ai + 1];
+    const uint16_t* w0 = w_dn + (size_t(e) * H + min(h0 + g, H - 1)) * F + 8 * c;
+    const uint16_t* w1 = w_dn + (size_t(e) * H + min(h0 + g + 8, H - 1)) * F + 8 * c;
+    for (int pp = p0; pp < p1; pp += 8) {
+      const int np = min(8, p1 - pp);
+      const bool tok = g < np;
+      const uint16_t* xr = a + size_t(tok ? pl.pairs[pp + g] : 0) * F + 8 * c;
+      float acc[4];
+      expert_rows_mma(w0, w1, xr, tok, F, acc);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * c + j;
+        if (col < np) {
+          const size_t yo = size_t(pl.pairs[pp + col]) * H;
+          if (h0 + g < H) y[yo + h0 + g] = acc[j];
+          if (h0 + g + 8 < H) y[yo + h0 + g + 8] = acc[2 + j];
+        }
+      }
+    }
+  }
+  __shared__ int s_last;
+  // the CTA barrier orders every thread's y stores before thread 0's device-scope fence,
+  // which releases them with the counter increment
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int hb = blockIdx.x * kMmaRowsDown;
+  const int nh = min(kMmaRowsDown, H - hb);
+  for (int i = threadIdx.x; i < T * nh; i += blockDim.x) {
+    const int t = i / nh, h = hb + (i - t * nh);
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[size_t(t) * k + j];
+      if (e < 0 || e >= E) continue;
+      s = fmaf(topk_w[size_t(t) * k + j], __ldcg(y + (size_t(t) * k + j) * H + h), s);
+    }
+    out[size_t(t) * H + h] = f2bf(s);
+  }
+}
+
 __global__ void moe_combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                                    const int32_t* __restrict__ idx, int T, int H, int k, int E,
                                    uint16_t* __restrict__ out) {
@@ -414,9 +550,10 @@ size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
     b += align_up(size_t(max_jobs(int(P), int(E))) * 16, 256) + 256;
     b += align_up(P * c->hidden * 2, 256);                       // gathered inputs
   }
-  if (grouped || P > size_t(kFusedMaxPairs) || T <= kMoeSmallT)
+  // FP32 per-pair rows and the down kernel's completion counters (decode forms)
+  if (grouped || P > size_t(kFusedMaxPairs) || T < kMoeGemmMinT)
     b += align_up(P * c->hidden * 4, 256);
-  if (T <= kMoeSmallT) b += align_up(size_t(c->hidden / 8 + 1) * 4, 256);   // down counters
+  if (T < kMoeGemmMinT) b += align_up(size_t(c->hidden / 8 + 1) * 4, 256);
   return b;
 }
 
@@ -447,9 +584,11 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
   MoePlan pl = carve_plan(cv, E, P, grouped);
   uint16_t* act = cv.take<uint16_t>(size_t(P) * F);
   uint16_t* us = grouped ? cv.take<uint16_t>(size_t(P) * H) : nullptr;
-  const bool small = !grouped && T <= kMoeSmallT;
-  float* y = (grouped || small || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
-  int* cnt = small ? cv.take<int>(size_t(H / 8 + 1)) : nullptr;
+  // 2..31 tokens: the tensor-core expert products (H and F multiples of 32)
+  const bool mma = !grouped && T >= 2 && T < kMoeGemmMinT && (H & 31) == 0 && (F & 31) == 0;
+  const bool small = !grouped && !mma && T <= kMoeSmallT;
+  float* y = (grouped || small || mma || P > kFusedMaxPairs) ? cv.take<float>(size_t(P) * H) : nullptr;
+  int* cnt = (small || mma) ? cv.take<int>(size_t(H / 8 + 1)) : nullptr;
   if (!cv.ok) return BEAM_ERR_INVALID_ARG;
   const int max_active = P < E ? P : E;
   if (grouped) {
@@ -474,6 +613,15 @@ extern "C" beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u,
       launch_pdl(moe_combine_kernel, dim3(unsigned((n + 255) / 256)), dim3(256), 0, st, y,
                  topk_w, topk_idx, T, H, k, E, out);
     }
+    return launch_status();
+  }
+  if (mma) {
+    const int n_cnt = (H + kMmaRowsDown - 1) / kMmaRowsDown;
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+    launch_pdl(moe_gate_up_mma_kernel, dim3((F + 63) / 64, max_active), dim3(256), 0, st, u,
+               w_gate_up, H, F, k, pl, cnt, n_cnt, act);
+    launch_pdl(moe_down_mma_kernel, dim3(n_cnt, max_active), dim3(256), 0, st, act, w_down, H, F,
+               pl, topk_idx, topk_w, T, k, E, cnt, y, out);
     return launch_status();
   }
   if (small) {

@@ -251,12 +251,14 @@ def _random_routing(shape, T, seed, n_used=None):
 @pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 4, None),
                                             (TINY, 9, None), (TINY, 31, None), (TINY, 32, None),
                                             (TINY, 300, None), (BEAM, 1, None), (BEAM, 2, None),
-                                            (BEAM, 4, None), (BEAM, 40, 12), (BEAM, 200, 10)])
+                                            (BEAM, 4, None), (BEAM, 8, None), (BEAM, 40, 12),
+                                            (BEAM, 200, 10)])
 def test_moe(shape, T, n_used):
-    """GEMV form below 32 tokens (one token: its slots used directly; up to 4 tokens: the down
-    kernel's last CTA per row block combines; then down+combine in shared memory up to 1024
-    pairs), grouped tensor-core GEMMs from 32 tokens (n_used limits the distinct experts so several 128-row tiles and
-    ragged tails occur per expert)."""
+    """One token: its slots used directly by the SIMT weight-streaming kernels; 2 to 31 tokens:
+    mma.sync expert products after the plan (up to 8 pairs of an expert per pass over its
+    rows; T=31 on the tiny shape gives experts more than 8 pairs), the down kernel's last CTA
+    per row block combines; grouped tensor-core GEMMs from 32 tokens (n_used limits the
+    distinct experts so several 128-row tiles and ragged tails occur per expert)."""
     seed = 55 + T
     cfg = cfg_of(shape)
     idx, w = _random_routing(shape, T, seed, n_used)
@@ -282,9 +284,11 @@ def test_moe(shape, T, n_used):
     assert_close(np64(out), ref, "moe out")
 
 
-@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 13), (TINY, 64), (TINY, 200), (BEAM, 1),
-                                     (BEAM, 8), (BEAM, 40), (BEAM, 130)])
+@pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 5), (TINY, 13), (TINY, 64), (TINY, 200),
+                                     (BEAM, 1), (BEAM, 3), (BEAM, 8), (BEAM, 40), (BEAM, 130)])
 def test_dense_mlp(shape, T):
+    """SIMT weight streaming for one token and above 8, mma.sync row blocks for 2 to 8 tokens,
+    tensor-core GEMMs from 64 tokens."""
     seed = 77 + T
     cfg = cfg_of(shape)
     Wd = synth.dense_weights(shape, 0, seed, device=DEV)
