@@ -138,9 +138,10 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
   }
 }
 
-// The same products on the tensor cores (mma.sync m16n8k16, bf16 in, FP32 accumulate) for up
-// to 8 tokens: a 16-row block of W is the A operand and the tokens are the 8 columns of B, so
-// each 16-byte weight chunk costs a fraction of an instruction instead of 8 FMAs per token.
+// The same products on the tensor cores (mma.sync m16n8k16, bf16 in, FP32 accumulate) for 2 to
+// 64 tokens: a 16-row block of W is the A operand and NTL tiles of 8 tokens are the columns of
+// B, so each 16-byte weight chunk, loaded once, costs a few instructions instead of 8 FMAs per
+// token.
 // The k axis is permuted inside every 32-element block (a sum does not depend on its order):
 // lane (g, c) loads elements 8c..8c+7 of the block from rows g and g+8 of the row block and
 // from token g, and uses elements {0,1,2,3} as the fragments of the block's first k16 step
@@ -158,14 +159,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int MODE, int KS, int U>
+template <int MODE, int KS, int NTL, int U>
 __global__ void __launch_bounds__(256) gemv_mma_kernel(const uint16_t* __restrict__ W, int N,
                                                        int K, const uint16_t* __restrict__ X,
                                                        int T, float* __restrict__ yf,
                                                        uint16_t* __restrict__ yb, int ldy) {
   pdl_trigger();
   constexpr int RB = 8 / KS;
-  __shared__ float red[8][32][4];
+  __shared__ float red[8][32][4 * NTL];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int rb = blockIdx.x * RB + warp / KS, ks = warp % KS;
@@ -203,90 +204,127 @@ __global__ void __launch_bounds__(256) gemv_mma_kernel(const uint16_t* __restric
     }
   }
   pdl_wait();
-  const bool tok = g < T;
-  const uint16_t* xr = X + size_t(tok ? g : 0) * K + 8 * c;
+  // n-tile j holds tokens 8j .. 8j+7; lane g loads token 8j + g
+  const uint16_t* xr[NTL];
+  bool tok[NTL];
+#pragma unroll
+  for (int j = 0; j < NTL; ++j) {
+    tok[j] = 8 * j + g < T;
+    xr[j] = X + size_t(tok[j] ? 8 * j + g : 0) * K + 8 * c;
+  }
   w0 += 8 * c;
   w1 += 8 * c;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+  // one accumulator per n-tile; a single tile alternates two (shorter dependency chains)
+  float acc[NTL][4], acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < NTL; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  auto step = [&](const uint4& a, const uint4& h, const uint4 (&x)[NTL]) {
+#pragma unroll
+    for (int j = 0; j < NTL; ++j) {
+      mma16816(acc[j], a.x, h.x, a.y, h.y, x[j].x, x[j].y);
+      if (NTL == 1) mma16816(acc2, a.z, h.z, a.w, h.w, x[j].z, x[j].w);
+      else mma16816(acc[j], a.z, h.z, a.w, h.w, x[j].z, x[j].w);
+    }
+  };
   int b = b0;
   for (; b + U <= b1; b += U) {
-    uint4 a[U], h[U], x[U];
+    uint4 a[U], h[U], x[U][NTL];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       a[u] = ld_stream(w0 + size_t(b + u) * 32);
       h[u] = ld_stream(w1 + size_t(b + u) * 32);
-      x[u] = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b + u) * 32)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < NTL; ++j)
+        x[u][j] = tok[j] ? __ldg(reinterpret_cast<const uint4*>(xr[j] + size_t(b + u) * 32))
+                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      mma16816(acc, a[u].x, h[u].x, a[u].y, h[u].y, x[u].x, x[u].y);
-      mma16816(acc2, a[u].z, h[u].z, a[u].w, h[u].w, x[u].z, x[u].w);
-    }
+    for (int u = 0; u < U; ++u) step(a[u], h[u], x[u]);
   }
   for (; b < b1; ++b) {
     const uint4 a = ld_stream(w0 + size_t(b) * 32), h = ld_stream(w1 + size_t(b) * 32);
-    const uint4 x = tok ? __ldg(reinterpret_cast<const uint4*>(xr + size_t(b) * 32)) : make_uint4(0, 0, 0, 0);
-    mma16816(acc, a.x, h.x, a.y, h.y, x.x, x.y);
-    mma16816(acc2, a.z, h.z, a.w, h.w, x.z, x.w);
-  }
+    uint4 x[NTL];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+    for (int j = 0; j < NTL; ++j)
+      x[j] = tok[j] ? __ldg(reinterpret_cast<const uint4*>(xr[j] + size_t(b) * 32)) : make_uint4(0, 0, 0, 0);
+    step(a, h, x);
+  }
+  if (NTL == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[0][i] += acc2[i];
+  }
   if (KS > 1) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) red[warp][lane][i] = acc[i];
+    for (int j = 0; j < NTL; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[warp][lane][4 * j + i] = acc[j][i];
     __syncthreads();
     if (ks != 0) return;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float v = red[warp][lane][i];
+    for (int j = 0; j < NTL; ++j)
 #pragma unroll
-      for (int j = 1; j < KS; ++j) v += red[warp + j][lane][i];
-      acc[i] = v;
-    }
-  }
-  // C fragment: acc[0], acc[1] = (row g; tokens 2c, 2c+1), acc[2], acc[3] = (row g + 8; ...)
+      for (int i = 0; i < 4; ++i) {
+        float v = red[warp][lane][4 * j + i];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int t = 2 * c + e;
-    if (t >= T) continue;
-    if (MODE == kOutSwiGLU) {
-      if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(siluf_(acc[e]) * acc[2 + e]);
-    } else if (MODE == kOutF32) {
-      if (n_lo < N) yf[size_t(t) * ldy + n_lo] = acc[e];
-      if (n_hi < N) yf[size_t(t) * ldy + n_hi] = acc[2 + e];
-    } else {
-      if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(acc[e]);
-      if (n_hi < N) yb[size_t(t) * ldy + n_hi] = f2bf(acc[2 + e]);
-    }
+        for (int w = 1; w < KS; ++w) v += red[warp + w][lane][4 * j + i];
+        acc[j][i] = v;
+      }
   }
+  // C fragment of tile j: acc[j][0], acc[j][1] = (row g; tokens 8j+2c, 8j+2c+1), acc[j][2],
+  // acc[j][3] = (row g + 8; the same tokens)
+#pragma unroll
+  for (int j = 0; j < NTL; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 8 * j + 2 * c + e;
+      if (t >= T) continue;
+      if (MODE == kOutSwiGLU) {
+        if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(siluf_(acc[j][e]) * acc[j][2 + e]);
+      } else if (MODE == kOutF32) {
+        if (n_lo < N) yf[size_t(t) * ldy + n_lo] = acc[j][e];
+        if (n_hi < N) yf[size_t(t) * ldy + n_hi] = acc[j][2 + e];
+      } else {
+        if (n_lo < N) yb[size_t(t) * ldy + n_lo] = f2bf(acc[j][e]);
+        if (n_hi < N) yb[size_t(t) * ldy + n_hi] = f2bf(acc[j][2 + e]);
+      }
+    }
 }
 
 // Host launcher: the register-pipelined kernel with the token tile, rows per warp and chunks in
 // flight picked from T.
-// Tensor-core form for 2..8 tokens (K a multiple of 32): KS, the warps sharing a row block,
-// is the smallest power of two that gives at least 16 warps per SM.
-constexpr int kGemvMmaMinT = 2;
-template <int MODE>
-inline cudaError_t launch_gemv_mma(const uint16_t* W, int N, int K, const uint16_t* X, int T,
-                                   float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
+// Tensor-core form for 2..64 tokens (K a multiple of 32): KS, the warps sharing a row block,
+// is the smallest power of two that gives at least 16 warps per SM; NTL tiles of 8 tokens per
+// pass over the weights, fewer weight chunks in flight as the token tiles grow.
+constexpr int kGemvMmaMinT = 2, kGemvMmaMaxT = 64;
+template <int MODE, int NTL, int U>
+inline cudaError_t launch_gemv_mma_t(const uint16_t* W, int N, int K, const uint16_t* X, int T,
+                                     float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
   const int units = MODE == kOutSwiGLU ? (N + 7) / 8 : (N + 15) / 16;
   const int want = 16 * num_sms_cached();
   int ks = 1;
   while (ks < 8 && units * ks < want && (K / 32) >= 2 * ks) ks *= 2;
   const dim3 grid((units * ks + 7) / 8);
   switch (ks) {
-    case 1: return launch_pdl(gemv_mma_kernel<MODE, 1, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
-    case 2: return launch_pdl(gemv_mma_kernel<MODE, 2, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
-    case 4: return launch_pdl(gemv_mma_kernel<MODE, 4, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
-    default: return launch_pdl(gemv_mma_kernel<MODE, 8, 4>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    case 1: return launch_pdl(gemv_mma_kernel<MODE, 1, NTL, U>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    case 2: return launch_pdl(gemv_mma_kernel<MODE, 2, NTL, U>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    case 4: return launch_pdl(gemv_mma_kernel<MODE, 4, NTL, U>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
+    default: return launch_pdl(gemv_mma_kernel<MODE, 8, NTL, U>, grid, dim3(256), 0, st, W, N, K, X, T, yf, yb, ldy);
   }
+}
+template <int MODE>
+inline cudaError_t launch_gemv_mma(const uint16_t* W, int N, int K, const uint16_t* X, int T,
+                                   float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
+  if (T <= 8) return launch_gemv_mma_t<MODE, 1, 4>(W, N, K, X, T, yf, yb, ldy, st);
+  if (T <= 16) return launch_gemv_mma_t<MODE, 2, 2>(W, N, K, X, T, yf, yb, ldy, st);
+  if (T <= 32) return launch_gemv_mma_t<MODE, 4, 1>(W, N, K, X, T, yf, yb, ldy, st);
+  return launch_gemv_mma_t<MODE, 8, 1>(W, N, K, X, T, yf, yb, ldy, st);
 }
 
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
                                float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
   if (T <= 0 || N <= 0) return cudaSuccess;
-  if (T >= kGemvMmaMinT && T <= 8 && (K & 31) == 0) {
+  if (T >= kGemvMmaMinT && T <= kGemvMmaMaxT && (K & 31) == 0) {
     const cudaError_t e = launch_gemv_mma<MODE>(W, N, K, X, T, yf, yb, ldy, st);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
