@@ -88,6 +88,23 @@ __device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
 }
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+// SSMax query scale (1 + p / base)^e in FP32 (GB300's FP64 rate is a small fraction of FP32,
+// and a double pow cost several microseconds in a one-thread prologue): 1 + p / base is exact
+// for base a power of two and p < 2^23, and log2 / exp2 keep the relative error near 1e-7.
+__device__ __forceinline__ float ssmax_scale(int p, float base, float e) {
+  return exp2f(e * log2f(1.f + float(p) / base));
+}
+// RoPE angle (p - 1) * inv reduced into about [-pi, pi]: the product in double (positions
+// near 1e5 need more than FP32's 24 bits), the reduction by a multiply with 1 / (2 pi) rather
+// than a double division (any integer multiple of 2 pi may be removed; the error of the
+// removed multiple stays near 1e-11 rad).
+__device__ __forceinline__ float rope_angle(int p, double inv) {
+  double ang = double(p - 1) * inv;
+  constexpr double kTwoPi = 6.283185307179586476925, kInvTwoPi = 0.15915494309189533576888;
+  ang = fma(-kTwoPi, rint(ang * kInvTwoPi), ang);
+  return float(ang);
+}
 __device__ __forceinline__ float siluf_(float z) { return z / (1.0f + __expf(-z)); }
 
 // ---- host-side argument checks ------------------------------------------------------------

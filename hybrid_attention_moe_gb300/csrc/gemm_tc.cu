@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (n0 == 0 && bad_s) flag(BEAM_DEV_BAD_SEQ);
         kv_ok = !bad_p && !bad_s;
         if (qe.nope)
-          ssmax = float(pow(1.0 + double(pp) / double(qe.ss_base), double(qe.ss_exp)));
+          ssmax = ssmax_scale(pp, qe.ss_base, qe.ss_exp);
       }
       if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
 #pragma unroll 1

@@ -46,19 +46,16 @@ __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
     ok_kv = false;
   }
   if (!nope) {
-    // angle (p-1) * theta^(-2i/D), formed and reduced modulo 2*pi in double precision so
+    // angle (p-1) * theta^(-2i/D), formed in double precision and reduced modulo 2*pi so
     // that positions around 1e5 keep full single-precision accuracy in cos/sin
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-      double ang = double(p - 1) * rope.inv[i];
-      const double two_pi = 6.283185307179586476925;
-      ang -= two_pi * rint(ang / two_pi);
       float sv, cv;
-      sincosf(float(ang), &sv, &cv);
+      sincosf(rope_angle(p, rope.inv[i]), &sv, &cv);
       cs[i] = cv;
       sn[i] = sv;
     }
   } else if (threadIdx.x == 0) {
-    s_ssmax = float(pow(1.0 + double(p) / double(ss_base), double(ss_exp)));
+    s_ssmax = ssmax_scale(p, ss_base, ss_exp);
   }
   __syncthreads();
 
@@ -124,7 +121,7 @@ __global__ void __launch_bounds__(256) qkv_epilogue_kernel(
 }
 
 // (cos, sin) of angle (p - 1) * theta^(-2i/D) for each token's position, i < D/2: the RoPE
-// rows the tensor-core projection's epilogue reads (same double-precision reduction as above).
+// rows the tensor-core projection's epilogue reads (same angle reduction as above).
 __global__ void __launch_bounds__(256) rope_table_kernel(const int32_t* __restrict__ pos, int T,
                                                          int half, RopeTab rope,
                                                          float2* __restrict__ tab) {
@@ -133,11 +130,8 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const int32_t* __restri
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * half) return;
   const int t = i / half, j = i - t * half;
-  double ang = double(pos[t] - 1) * rope.inv[j];
-  const double two_pi = 6.283185307179586476925;
-  ang -= two_pi * rint(ang / two_pi);
   float sv, cv;
-  sincosf(float(ang), &sv, &cv);
+  sincosf(rope_angle(pos[t], rope.inv[j]), &sv, &cv);
   tab[i] = make_float2(cv, sv);
 }
 

@@ -6,7 +6,8 @@ warm-up launches and capture one or a few real ones. Usage:
 
     python -m hybrid_attention_moe_gb300.profile_cases --case moe_decode --reps 3
 
-Cases: moe_decode (batch-1 expert GEMVs over 8 selected experts of a 32-expert pool),
+Cases: moe_decode (--tokens tokens, default 1, each over 8 selected experts of a 32-expert
+pool), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
 qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (100K keys),
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
 moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts), attn_nope_prefill
@@ -37,6 +38,7 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--ctx", type=int, default=16384)
+    ap.add_argument("--tokens", type=int, default=1)
     args = ap.parse_args()
     _build.build()
     dev = "cuda"
@@ -46,7 +48,7 @@ def main():
     H = shape.hidden
     c = args.case
     if c == "moe_decode" or c == "moe_prefill":
-        T = 1 if c == "moe_decode" else 2048
+        T = args.tokens if c == "moe_decode" else 2048
         cs = B.LayerCfg.from_shape(small, B.BEAM_ATTN_SWA_ROPE)
         wgu, wdn = synth.expert_weights(small, 3, 0, device=dev)
         u = synth.activations(T, H, 0, "u", dev)
@@ -56,6 +58,13 @@ def main():
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_moe(cs, u, idx, w, wgu, wdn, out, ws)  # noqa: E731
+    elif c == "dense_decode":
+        T = args.tokens
+        Wd = synth.dense_weights(shape, 0, 0, device=dev)
+        u = synth.activations(T, H, 0, "u", dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(B.workspace_bytes(cfg, T, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: B.beam_dense_mlp(cfg, u, Wd["w_gate_up"], Wd["w_down"], out, ws)  # noqa: E731
     elif c == "qkv_decode":
         W = synth.attention_weights(shape, 3, 0, device=dev)
         u = synth.activations(1, H, 0, "u", dev)
