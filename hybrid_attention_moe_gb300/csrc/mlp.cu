@@ -374,8 +374,9 @@ __device__ __forceinline__ void expert_rows_mma(const uint16_t* w0, const uint16
   for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
 }
 
-// grid (ceil(F / 64), max active experts)
-__global__ void __launch_bounds__(256) moe_gate_up_mma_kernel(
+// grid (ceil(F / 64), max active experts). Two CTAs per SM (at most 128 registers): measured
+// 4% faster than one CTA at the compiler's own 213 registers.
+__global__ void __launch_bounds__(256, 2) moe_gate_up_mma_kernel(
     const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
     MoePlan pl, int* __restrict__ cnt, int n_cnt, uint16_t* __restrict__ a) {
   pdl_trigger();
@@ -407,8 +408,8 @@ __global__ void __launch_bounds__(256) moe_gate_up_mma_kernel(
   }
 }
 
-// grid (ceil(H / 128), max active experts)
-__global__ void __launch_bounds__(256) moe_down_mma_kernel(
+// grid (ceil(H / 128), max active experts); two CTAs per SM as above
+__global__ void __launch_bounds__(256, 2) moe_down_mma_kernel(
     const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn, int H, int F, MoePlan pl,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T, int k, int E,
     int* __restrict__ cnt, float* __restrict__ y, uint16_t* __restrict__ out) {
