@@ -1,10 +1,12 @@
 // BF16 tensor-core GEMM for the prefill projections: C[M][N] = A[M][K] . B[N][K]^T, FP32
 // accumulation in tensor memory, written as FP32 or BF16.
 //
-// Blackwell (sm_103a) structure: one CTA per 128 x 256 output tile; a 4-stage shared-memory
-// ring of 64-wide K slices filled by TMA (128-byte swizzle, no multicast), consumed by
-// tcgen05.mma issued from one thread into a 128 x 256 FP32 accumulator in TMEM; four
-// epilogue warps read the accumulator back with tcgen05.ld and store it. Warp roles:
+// Blackwell (sm_103a) structure: a persistent grid (at most one CTA per SM) walks the 128 x 256
+// output tiles; a 4-stage shared-memory ring of 64-wide K slices filled by TMA (128-byte
+// swizzle, no multicast) runs on across tiles, consumed by tcgen05.mma issued from one thread
+// into one of two 128 x 256 FP32 accumulators in TMEM; four epilogue warps read a finished
+// accumulator back with tcgen05.ld and store it while the next tile accumulates into the
+// other. Warp roles:
 //   warp 0 : TMA producer (one elected lane)
 //   warp 1 : TMEM allocation owner and MMA issuer (one elected lane)
 //   warps 2-5 : epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. output rows)
@@ -26,7 +28,7 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;   // ring, alignment, barriers
 constexpr int THREADS = 192;
 constexpr int kGroupM = 16;   // row tiles walked per column tile (dense grids)
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN, false);
@@ -121,43 +123,61 @@ __device__ __forceinline__ void qkv_head_epilogue(const QkvEpilogue& e, uint32_t
   }
 }
 
+// Output tile t of a launch: A rows [a_row0, a_row0 + rows), B rows from b_row0, output
+// columns [n0, n0 + NT). Dense GEMMs walk (row tile, column tile) in groups of kGroupM row
+// tiles per column tile: the tiles the resident CTAs hold at one time cover a compact block of
+// the output, so both operands' tiles are reused through L2. Grouped GEMMs take tile
+// t = job * num_n + column tile.
+struct Tile {
+  int a_row0, b_row0, rows, n0;
+};
+template <int NT>
+__device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, int num_m, int num_n) {
+  Tile r;
+  if (p.jobs == nullptr) {
+    const int group = t / (kGroupM * num_n);
+    const int first_m = group * kGroupM;
+    const int gsize = min(num_m - first_m, kGroupM);
+    const int in_group = t - group * kGroupM * num_n;
+    r.a_row0 = (first_m + in_group % gsize) * BM;
+    r.n0 = (in_group / gsize) * NT;
+    r.b_row0 = 0;
+    r.rows = BM;
+  } else {
+    const int jb = t / num_n;
+    const int4 j = p.jobs[jb];
+    r.n0 = (t - jb * num_n) * NT;
+    r.b_row0 = j.x * p.b_stride;
+    r.a_row0 = j.y;
+    r.rows = j.z;
+  }
+  return r;
+}
+
+// Persistent: CTA c takes tiles c, c + gridDim.x, ... Two 256-column FP32 accumulators in
+// TMEM (512 columns) let the epilogue of tile i run while the MMAs of tile i+1 accumulate into
+// the other buffer, and the TMA ring runs on across tile boundaries, so neither the epilogue
+// nor the pipeline fill of a tile leaves the tensor pipe idle.
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    GemmParams p, QkvEpilogue qe) {
   pdl_trigger();
   pdl_wait();
-  constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per CTA
-  int b_row0 = 0, a_row0, rows = BM, n0;
-  if (p.jobs == nullptr) {
-    // 1-D grid in groups of kGroupM row tiles per column tile: the CTAs resident at one time
-    // cover a compact block of the output, so both operands' tiles are reused through L2
-    const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + NT - 1) / NT;
-    const int pid = blockIdx.x;
-    const int group = pid / (kGroupM * num_n);
-    const int first_m = group * kGroupM;
-    const int gsize = min(num_m - first_m, kGroupM);
-    const int in_group = pid - group * kGroupM * num_n;
-    a_row0 = (first_m + in_group % gsize) * BM;
-    n0 = (in_group / gsize) * NT;
-  } else {
-    a_row0 = 0;
-    n0 = blockIdx.x * NT;
-    if (int(blockIdx.y) >= *p.n_jobs) return;   // uniform for the CTA, before any setup
-    const int4 j = p.jobs[blockIdx.y];
-    b_row0 = j.x * p.b_stride;
-    a_row0 = j.y;
-    rows = j.z;
-  }
+  constexpr int NT = MODE == kSwiGLU ? BN / 2 : BN;   // output columns per tile
+  const int num_n = (p.N + NT - 1) / NT;
+  const int num_m = (p.M + BM - 1) / BM;
+  const int n_tiles = p.jobs == nullptr ? num_m * num_n : *p.n_jobs * num_n;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const uint32_t s_base = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-  const uint32_t accb = smem_u32(bars + 2 * STAGES);
+  const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = accf0 + 16;   // [2] each
+  const uint32_t mma_done = acce0 + 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (p.K + BK - 1) / BK;
 
@@ -166,14 +186,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(accb, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf0 + 8 * a, 1);
+      mbar_init(acce0 + 8 * a, 4);   // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_holder)),
-                 "r"(BN)
+                 "r"(2 * BN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -183,79 +207,107 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (*abort_flag || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
-          *abort_flag = 1;
-          break;
+      int it = 0;   // k-blocks issued, over all tiles of this CTA
+      for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+        const Tile tl = tile_of<NT>(p, t, num_m, num_n);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (*abort_flag || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_expect_tx(full0 + 8 * s, STAGE_BYTES);
+          const uint32_t sa = s_base + s * STAGE_BYTES;
+          tma_load_2d(sa, &ta, kb * BK, tl.a_row0, full0 + 8 * s);
+          if (MODE == kSwiGLU) {
+            tma_load_2d(sa + A_BYTES, &tb, kb * BK, tl.b_row0 + tl.n0, full0 + 8 * s);
+            tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tb, kb * BK, tl.b_row0 + p.up_off + tl.n0,
+                        full0 + 8 * s);
+          } else {
+            tma_load_2d(sa + A_BYTES, &tb, kb * BK, tl.b_row0 + tl.n0, full0 + 8 * s);
+          }
         }
-        mbar_expect_tx(full0 + 8 * s, STAGE_BYTES);
-        const uint32_t sa = s_base + s * STAGE_BYTES;
-        tma_load_2d(sa, &ta, kb * BK, a_row0, full0 + 8 * s);
-        if (MODE == kSwiGLU) {
-          tma_load_2d(sa + A_BYTES, &tb, kb * BK, b_row0 + n0, full0 + 8 * s);
-          tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tb, kb * BK, b_row0 + p.up_off + n0,
-                      full0 + 8 * s);
-        } else {
-          tma_load_2d(sa + A_BYTES, &tb, kb * BK, b_row0 + n0, full0 + 8 * s);
-        }
-        issued = kb + 1;
       }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA's shared memory goes away
-        for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
-          mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1);
-      }
+      // normally a no-op (every issued stage was consumed); after an expired wait, let the
+      // copies already issued land before the CTA's shared memory goes away
+      for (int k = it - 1; k >= 0 && k >= it - STAGES; --k)
+        mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (*abort_flag || !mbar_wait(full0 + 8 * s, ph)) {
+      int it = 0, i = 0;
+      for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++i) {
+        const int ab = i & 1;
+        // the epilogue has drained this accumulator (tile i - 2)
+        if (!mbar_wait(acce0 + 8 * ab, ((i >> 1) & 1) ^ 1)) {
           *abort_flag = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t sa = s_base + s * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t acc = tmem + uint32_t(ab * BN);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (*abort_flag || !mbar_wait(full0 + 8 * s, ph)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sa = s_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          umma(tmem, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), (kb | k) != 0);
-        umma_commit(empty0 + 8 * s);
+          for (int k = 0; k < BK / 16; ++k)
+            umma(acc, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), (kb | k) != 0);
+          umma_commit(empty0 + 8 * s);
+        }
+        umma_commit(accf0 + 8 * ab);   // arrives once every MMA issued above has completed
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
       }
-      umma_commit(accb);   // arrives once every MMA issued above has completed
+      // every MMA of this CTA has completed before TMEM is released (after an early exit the
+      // epilogue may not have waited for them)
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
     }
   } else {
     const int quad = warp & 3;
-    const bool ok = mbar_wait(accb, 0);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (!ok) *abort_flag = 1;
     const int r = quad * 32 + lane;
-    const int arow = a_row0 + r;
-    const bool row_ok = r < rows && arow < p.M;
-    const int crow = row_ok ? (p.row_map ? p.row_map[arow] : arow) : 0;
-    const uint32_t tbase = tmem + (uint32_t(quad * 32) << 16);
-    if (MODE == kQKV) {
-      // per token row: two 128-column heads of the packed projection
-      int pp = 0, sq = 0;
-      bool kv_ok = false;
-      float ssmax = 1.f;
-      if (row_ok) {
-        pp = qe.pos[arow];
-        sq = qe.seq_id[arow];
-        const beam_kv_cache& kc = qe.cache;
-        const bool bad_p = pp < 1 || (kc.window == 0 && pp > kc.capacity);
-        const bool bad_s = sq < 0 || sq >= kc.num_seqs;
-        if (n0 == 0 && bad_p) flag(BEAM_DEV_BAD_POSITION);
-        if (n0 == 0 && bad_s) flag(BEAM_DEV_BAD_SEQ);
-        kv_ok = !bad_p && !bad_s;
-        if (qe.nope)
-          ssmax = ssmax_scale(pp, qe.ss_base, qe.ss_exp);
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+      const int ab = i & 1;
+      const bool ok = !*abort_flag && mbar_wait(accf0 + 8 * ab, (i >> 1) & 1);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      // tcgen05.ld is warp-collective: the decision is taken once for the whole warp
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort_flag = 1;
+        break;
       }
-      if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
+      const Tile tl = tile_of<NT>(p, t, num_m, num_n);
+      const int arow = tl.a_row0 + r;
+      const bool row_ok = r < tl.rows && arow < p.M;
+      const int crow = row_ok ? (p.row_map ? p.row_map[arow] : arow) : 0;
+      const int n0 = tl.n0;
+      const uint32_t tbase = tmem + uint32_t(ab * BN) + (uint32_t(quad * 32) << 16);
+      if (MODE == kQKV) {
+        // per token row: two 128-column heads of the packed projection
+        int pp = 0, sq = 0;
+        bool kv_ok = false;
+        float ssmax = 1.f;
+        if (row_ok) {
+          pp = qe.pos[arow];
+          sq = qe.seq_id[arow];
+          const beam_kv_cache& kc = qe.cache;
+          const bool bad_p = pp < 1 || (kc.window == 0 && pp > kc.capacity);
+          const bool bad_s = sq < 0 || sq >= kc.num_seqs;
+          if (n0 == 0 && bad_p) flag(BEAM_DEV_BAD_POSITION);
+          if (n0 == 0 && bad_s) flag(BEAM_DEV_BAD_SEQ);
+          kv_ok = !bad_p && !bad_s;
+          if (qe.nope) ssmax = ssmax_scale(pp, qe.ss_base, qe.ss_exp);
+        }
 #pragma unroll 1
         for (int hh = 0; hh < BN / 128; ++hh) {
           const int head = n0 / 128 + hh;
@@ -263,76 +315,79 @@ __global__ void __launch_bounds__(THREADS, 1)
           qkv_head_epilogue(qe, tbase + uint32_t(hh * 128), arow, row_ok, head, pp, sq, kv_ok,
                             ssmax);
         }
-      }
-    } else if (__all_sync(0xffffffffu, ok && !*abort_flag)) {
-      // tcgen05.ld is warp-collective: the decision is taken once for the whole warp
+      } else {
 #pragma unroll 1
-      for (int c = 0; c < NT / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tbase + uint32_t(c * 16), v);
-        const int col = n0 + c * 16;
-        if (MODE == kSwiGLU) {
-          uint32_t up[16];
-          tmem_ld16(tbase + uint32_t(BN / 2 + c * 16), up);
-          if (row_ok && col < p.N) {
-            uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
-            float a[16];
+        for (int c = 0; c < NT / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tbase + uint32_t(c * 16), v);
+          const int col = n0 + c * 16;
+          if (MODE == kSwiGLU) {
+            uint32_t up[16];
+            tmem_ld16(tbase + uint32_t(BN / 2 + c * 16), up);
+            if (row_ok && col < p.N) {
+              uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
+              float a[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              a[i] = siluf_(__uint_as_float(v[i])) * __uint_as_float(up[i]);
-            if (col + 16 <= p.N && (p.ldc & 7) == 0) {
-              uint32_t q[8];
+              for (int e = 0; e < 16; ++e)
+                a[e] = siluf_(__uint_as_float(v[e])) * __uint_as_float(up[e]);
+              if (col + 16 <= p.N && (p.ldc & 7) == 0) {
+                uint32_t q[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) q[i] = pack_bf2(a[2 * i], a[2 * i + 1]);
-              reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
-              reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
-            } else {
-              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = f2bf(a[i]);
+                for (int e = 0; e < 8; ++e) q[e] = pack_bf2(a[2 * e], a[2 * e + 1]);
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+              } else {
+                for (int e = 0; e < 16 && col + e < p.N; ++e) dst[e] = f2bf(a[e]);
+              }
             }
-          }
-        } else if (row_ok && col < p.N) {
-          if (MODE == kF32 || MODE == kF32Add) {
-            float* dst = static_cast<float*>(p.C) + size_t(crow) * p.ldc + col;
-            if (col + 16 <= p.N && (p.ldc & 3) == 0) {
+          } else if (row_ok && col < p.N) {
+            if (MODE == kF32 || MODE == kF32Add) {
+              float* dst = static_cast<float*>(p.C) + size_t(crow) * p.ldc + col;
+              if (col + 16 <= p.N && (p.ldc & 3) == 0) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float4 o = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                if (MODE == kF32Add) {
-                  const float4 c = reinterpret_cast<const float4*>(dst)[i];
-                  o.x += c.x;
-                  o.y += c.y;
-                  o.z += c.z;
-                  o.w += c.w;
+                for (int e = 0; e < 4; ++e) {
+                  float4 o = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                  if (MODE == kF32Add) {
+                    const float4 cc = reinterpret_cast<const float4*>(dst)[e];
+                    o.x += cc.x;
+                    o.y += cc.y;
+                    o.z += cc.z;
+                    o.w += cc.w;
+                  }
+                  reinterpret_cast<float4*>(dst)[e] = o;
                 }
-                reinterpret_cast<float4*>(dst)[i] = o;
+              } else {
+                for (int e = 0; e < 16 && col + e < p.N; ++e)
+                  dst[e] = MODE == kF32Add ? dst[e] + __uint_as_float(v[e]) : __uint_as_float(v[e]);
               }
             } else {
-              for (int i = 0; i < 16 && col + i < p.N; ++i)
-                dst[i] = MODE == kF32Add ? dst[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
-            }
-          } else {
-            uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
-            if (col + 16 <= p.N && (p.ldc & 7) == 0) {
-              uint32_t q[8];
+              uint16_t* dst = static_cast<uint16_t*>(p.C) + size_t(crow) * p.ldc + col;
+              if (col + 16 <= p.N && (p.ldc & 7) == 0) {
+                uint32_t q[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                q[i] = pack_bf2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-              reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
-              reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
-            } else {
-              for (int i = 0; i < 16 && col + i < p.N; ++i) dst[i] = f2bf(__uint_as_float(v[i]));
+                for (int e = 0; e < 8; ++e)
+                  q[e] = pack_bf2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(q[4], q[5], q[6], q[7]);
+              } else {
+                for (int e = 0; e < 16 && col + e < p.N; ++e) dst[e] = f2bf(__uint_as_float(v[e]));
+              }
             }
           }
         }
       }
+      // this warp's TMEM reads are done: release the accumulator to the MMA issuer
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * ab);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) flag(BEAM_DEV_TIMEOUT);
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN)
                  : "memory");
   }
 }
@@ -389,13 +444,16 @@ bool gemm_supported(const void* A, int lda, const void* B, int ldb, int K) {
 
 namespace {
 
+// tiles: the number of output tiles (an upper bound for grouped GEMMs); one CTA per SM at most
 template <int MODE>
-cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, dim3 grid,
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int tiles,
                    cudaStream_t st, const QkvEpilogue& qe = QkvEpilogue{}) {
+  const int sms = num_sms_cached();
+  const dim3 grid(tiles < sms ? tiles : sms);
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  launch_pdl(gemm_tc_kernel<MODE>, dim3(grid), dim3(THREADS), SMEM_BYTES, st, ta, tb, p, qe);
+  launch_pdl(gemm_tc_kernel<MODE>, grid, dim3(THREADS), SMEM_BYTES, st, ta, tb, p, qe);
   return cudaGetLastError();
 }
 
@@ -410,8 +468,8 @@ cudaError_t gemm_bf16(const uint16_t* A, int M, int K, int lda, const uint16_t* 
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
     return cudaErrorInvalidValue;
   GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
-  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
-  return out_bf16 ? launch<kBF16>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
+  const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  return out_bf16 ? launch<kBF16>(ta, tb, p, tiles, st) : launch<kF32>(ta, tb, p, tiles, st);
 }
 
 cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N,
@@ -423,8 +481,8 @@ cudaError_t gemm_f32_acc(const uint16_t* A, int M, int K, int lda, const uint16_
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
     return cudaErrorInvalidValue;
   GemmParams p{M, N, K, C, ldc, nullptr, nullptr, 0, 0, nullptr};
-  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
-  return accumulate ? launch<kF32Add>(ta, tb, p, grid, st) : launch<kF32>(ta, tb, p, grid, st);
+  const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  return accumulate ? launch<kF32Add>(ta, tb, p, tiles, st) : launch<kF32>(ta, tb, p, tiles, st);
 }
 
 cudaError_t gemm_qkv(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int N, int ldb,
@@ -436,8 +494,8 @@ cudaError_t gemm_qkv(const uint16_t* A, int M, int K, int lda, const uint16_t* B
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, N, ldb, BN))
     return cudaErrorInvalidValue;
   GemmParams p{M, N, K, nullptr, 0, nullptr, nullptr, 0, 0, nullptr};
-  dim3 grid(((N + BN - 1) / BN) * ((M + BM - 1) / BM));
-  return launch<kQKV>(ta, tb, p, grid, st, qe);
+  const int tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  return launch<kQKV>(ta, tb, p, tiles, st, qe);
 }
 
 cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t* B, int F,
@@ -449,8 +507,8 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, 2 * F, ldb, BN / 2))
     return cudaErrorInvalidValue;
   GemmParams p{M, F, K, C, ldc, nullptr, nullptr, 0, F, nullptr};
-  dim3 grid(((F + BN / 2 - 1) / (BN / 2)) * ((M + BM - 1) / BM));
-  return launch<kSwiGLU>(ta, tb, p, grid, st);
+  const int tiles = ((F + BN / 2 - 1) / (BN / 2)) * ((M + BM - 1) / BM);
+  return launch<kSwiGLU>(ta, tb, p, tiles, st);
 }
 
 cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
@@ -466,10 +524,10 @@ cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, con
     return cudaErrorInvalidValue;
   GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map};
   const int nt = mode == kSwiGLU ? BN / 2 : BN;
-  dim3 grid((N + nt - 1) / nt, max_jobs);
-  if (mode == kSwiGLU) return launch<kSwiGLU>(ta, tb, p, grid, st);
-  if (mode == kBF16) return launch<kBF16>(ta, tb, p, grid, st);
-  return launch<kF32>(ta, tb, p, grid, st);
+  const int tiles = ((N + nt - 1) / nt) * max_jobs;
+  if (mode == kSwiGLU) return launch<kSwiGLU>(ta, tb, p, tiles, st);
+  if (mode == kBF16) return launch<kBF16>(ta, tb, p, tiles, st);
+  return launch<kF32>(ta, tb, p, tiles, st);
 }
 
 }  // namespace tc
