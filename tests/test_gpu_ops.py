@@ -192,6 +192,68 @@ def test_attn(case, kind, fp8, form):
     assert_close(np64(out), ref, "attn out", fp8=fp8)
 
 
+# A sliding window longer than 2048 keys takes the long-context decode kernel when the ring's
+# capacity is a multiple of its key block (64 slots for BF16, 128 for FP8) and the split-K kernel
+# otherwise; the contexts make the window wrap around the ring and one sequence hold fewer
+# keys than the window.
+LONG_WINDOW = dataclasses.replace(BEAM, window=3000)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("cap", [3072, 3136, 3005])
+@pytest.mark.parametrize("per", [1, 3])
+def test_attn_long_window_ring(fp8, cap, per):
+    shape = LONG_WINDOW
+    seed = 71 + cap + per
+    ctxs = [5000, 2999, 7000, 12]
+    S = len(ctxs)
+    T = S * per
+    seqs = [s for s in range(S) for _ in range(per)]
+    positions = [ctxs[s] + 1 + i for s in range(S) for i in range(per)]
+    max_pos = max(positions)
+    scale = (0.0371, 0.5) if fp8 else (1.0, 1.0)
+    c = synth.kv_cache(shape, S, cap, seed, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
+                       device=DEV)
+    kc = B.KVCache(c["k"], c["v"], shape.window, *scale)
+    q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, seed, ("q",), DEV)
+    g = synth.activations(T, shape.q_rows, seed, "g", DEV)
+    W = synth.attention_weights(shape, 0, seed, device=DEV)
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    cfg = cfg_of(shape)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
+                ws_for(cfg, T, max_pos), max_q_per_seq=per)
+    check_status()
+    ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
+                      positions, np64(W["w_o"]))
+    assert_close(np64(out), ref, "attn out", fp8=fp8)
+
+
+def test_long_context_decode_flags_positions_past_max_pos():
+    """The long-context decode kernel sizes its key blocks from max_pos: a token whose position
+    lies past it is flagged and its row left at zero, the other tokens are exact."""
+    shape = BEAM
+    cfg = cfg_of(shape, nope=True)
+    S, cap, max_pos = 2, 5000, 3000
+    c = synth.kv_cache(shape, S, cap, 3, device=DEV)
+    kc = B.KVCache(c["k"], c["v"], 0)
+    seqs, positions = [0, 1], [2500, 4000]
+    q = synth.normal((S, shape.n_q, shape.head_dim), 1.0, 0.0, 3, ("q",), DEV)
+    g = synth.activations(S, shape.q_rows, 3, "g", DEV)
+    W = synth.attention_weights(shape, 0, 3, device=DEV)
+    out = torch.empty((S, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_get_device_status()
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, torch.tensor(seqs, dtype=torch.int32, device=DEV),
+                torch.tensor(positions, dtype=torch.int32, device=DEV), max_pos, W["w_o"], out,
+                ws_for(cfg, S, max_pos), max_q_per_seq=1)
+    assert B.beam_get_device_status() & B.DEV_BAD_POSITION
+    ref = O.attention(shape, np64(q[:1]), np64(g[:1]), np64(W["gate_bias"]), oracle_cache(kc),
+                      seqs[:1], positions[:1], np64(W["w_o"]))
+    assert_close(np64(out[:1]), ref, "attn out, valid token")
+    assert not out[1].float().abs().max().item()
+
+
 # ------------------------------------------------------------------ router ----
 
 # Router shapes beside the Beam and tiny ones: 96 experts in 3 groups of 32 (4 experts per lane,
