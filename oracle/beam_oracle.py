@@ -20,11 +20,11 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32
+from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32, nvfp4_dequant
 
 __all__ = [
     "rmsnorm", "boundary_norm", "rope_inv_freq", "rope", "ssmax_scale", "KVCache",
-    "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "dense_mlp",
+    "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "moe_nvfp4", "dense_mlp",
     "is_nope_layer", "layer_forward", "stack_forward", "kv_values_per_token",
 ]
 
@@ -290,6 +290,20 @@ def moe(cfg, u, idx, w, w_gate_up, w_down):
             acc += float(w[t, j]) * y
         out[t] = acc
     return bf16_round(out)
+
+
+def moe_nvfp4(cfg, u, idx, w, experts):
+    """moe() with NVFP4 expert weights: experts maps expert e -> (gate_up codes [2F][H/2],
+    gate_up block scales [2F][H/16], gate_up matrix scale, down codes [H][F/2], down block
+    scales [H][F/16], down matrix scale). The selected experts' weights are dequantised
+    exactly (every NVFP4 value is a float64 number) and the layer is the BF16-weight one."""
+    used = sorted({int(e) for e in np.asarray(idx).ravel()})
+    gu, dn = {}, {}
+    for e in used:
+        q_gu, s_gu, t_gu, q_dn, s_dn, t_dn = experts[e]
+        gu[e] = nvfp4_dequant(q_gu, s_gu, t_gu)
+        dn[e] = nvfp4_dequant(q_dn, s_dn, t_dn)
+    return moe(cfg, u, idx, w, gu, dn)
 
 
 def dense_mlp(cfg, u, w_gate_up, w_down):

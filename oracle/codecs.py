@@ -11,6 +11,14 @@ infinities; S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 4
 Encoding here is round-to-nearest-even with saturation to +-448 ("satfinite"), the rule the
 Beam page's FP8 KV cache needs (vLLM page, "--kv-cache-dtype fp8"; the quantisation rule
 itself is not printed, so saturation is the stated reading).
+
+FP4 e2m1: 1 sign bit, 2 exponent bits with bias 1, 1 fraction bit; exponent field 0 encodes
+the subnormal m * 0.5; no infinities or NaN, so the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+NVFP4 (the expert weight format the Beam and Flint pages name for the shipped checkpoints;
+the pages do not print its layout, so NVIDIA's published definition is the reading): e2m1
+elements in blocks of 16 consecutive elements of a row, each block scaled by one e4m3 value,
+and the whole matrix by one FP32 value; element = e2m1 * block scale * matrix scale. Two
+elements share a byte, the even element in the low nibble.
 """
 from __future__ import annotations
 
@@ -86,3 +94,41 @@ def e4m3_encode(x) -> np.ndarray:
     code = np.where(np.signbit(x), code | np.uint8(0x80), code)
     code = np.where(np.isnan(x), np.uint8(0x7F), code)
     return code.astype(np.uint8)
+
+
+def e2m1_table() -> np.ndarray:
+    """Value of each of the 16 e2m1 codes (float64)."""
+    vals = np.empty(16, dtype=np.float64)
+    for code in range(16):
+        sign = -1.0 if code & 0x8 else 1.0
+        e = (code >> 1) & 0x3
+        m = code & 0x1
+        vals[code] = sign * (m * 0.5 if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1))
+    return vals
+
+
+_E2M1 = e2m1_table()
+NVFP4_BLOCK = 16
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    return _E2M1[np.asarray(codes, dtype=np.uint8) & np.uint8(0xF)]
+
+
+def nvfp4_unpack(packed) -> np.ndarray:
+    """Codes [..., 2n] of packed bytes [..., n]: element 2i is the low nibble of byte i."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & np.uint8(0xF)
+    out[..., 1::2] = b >> np.uint8(4)
+    return out
+
+
+def nvfp4_dequant(packed, scales, matrix_scale) -> np.ndarray:
+    """Values [rows][K] (float64) of an NVFP4 matrix: packed [rows][K/2] bytes, scales
+    [rows][K/16] e4m3 codes, one FP32 matrix scale."""
+    v = e2m1_decode(nvfp4_unpack(packed))
+    s = e4m3_decode(scales)
+    rows, K = v.shape
+    v = v.reshape(rows, K // NVFP4_BLOCK, NVFP4_BLOCK) * s[:, :, None]
+    return v.reshape(rows, K) * float(np.float32(matrix_scale))

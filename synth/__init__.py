@@ -4,7 +4,8 @@ This package draws random numbers and names layer shapes. It holds none of the l
 arithmetic, so that both sides of every parity test can be fed from it.
 """
 from .beam_inputs import (  # noqa: F401
-    BeamShape, TINY, BEAM, derived_seed, normal, layer_weights, expert_weights,
+    BeamShape, TINY, BEAM, derived_seed, normal, uniform_codes, layer_weights, expert_weights,
+    expert_weights_nvfp4,
     attention_weights, router_weights, dense_weights,
     activations, kv_cache, decode_positions, prefill_positions,
 )

@@ -104,6 +104,44 @@ def expert_weights(shape: BeamShape, layer: int, seed: int, device="cpu", expert
     return w_gu, w_dn
 
 
+def uniform_codes(shape, low, high, seed, names, device="cpu"):
+    """Integers uniform in [low, high) as uint8, with a seed derived from `names`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(derived_seed(seed, *names))
+    return torch.randint(low, high, shape, generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+
+
+# NVFP4 expert weights: every byte of e2m1 code pairs uniform (all 16 codes are numbers),
+# block scales uniform over the e4m3 codes of [0.5, 2) (exponent fields 6 and 7), and one matrix
+# scale of 0.004 per expert matrix, so that weights are of the size of the N(0, 0.02) BF16 ones.
+NVFP4_SCALE_CODES = (0x30, 0x40)
+NVFP4_MATRIX_SCALE = 0.004
+
+
+def expert_weights_nvfp4(shape: BeamShape, layer: int, seed: int, device="cpu", experts=None):
+    """NVFP4 gate/up and down weights of the experts (a dict of tensors): codes [E][2F][H/2]
+    and [E][H][F/2] (uint8, even element in the low nibble), e4m3 block scales [E][2F][H/16]
+    and [E][H][F/16] (uint8), FP32 matrix scales [E]."""
+    E, F, H = shape.n_experts, shape.d_ff_expert, shape.hidden
+    ids = list(range(E) if experts is None else experts)
+    n = len(ids)
+    out = {
+        "gate_up": torch.empty((n, 2 * F, H // 2), dtype=torch.uint8, device=device),
+        "gate_up_scale": torch.empty((n, 2 * F, H // 16), dtype=torch.uint8, device=device),
+        "gate_up_global": torch.full((n,), NVFP4_MATRIX_SCALE, dtype=torch.float32, device=device),
+        "down": torch.empty((n, H, F // 2), dtype=torch.uint8, device=device),
+        "down_scale": torch.empty((n, H, F // 16), dtype=torch.uint8, device=device),
+        "down_global": torch.full((n,), NVFP4_MATRIX_SCALE, dtype=torch.float32, device=device),
+    }
+    lo, hi = NVFP4_SCALE_CODES
+    for i, e in enumerate(ids):
+        out["gate_up"][i] = uniform_codes((2 * F, H // 2), 0, 256, seed, (layer, "nvfp4_gu", e), device)
+        out["gate_up_scale"][i] = uniform_codes((2 * F, H // 16), lo, hi, seed, (layer, "nvfp4_gu_s", e), device)
+        out["down"][i] = uniform_codes((H, F // 2), 0, 256, seed, (layer, "nvfp4_dn", e), device)
+        out["down_scale"][i] = uniform_codes((H, F // 16), lo, hi, seed, (layer, "nvfp4_dn_s", e), device)
+    return out
+
+
 def attention_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
     """Norm gains and the attention sublayer's weights of one layer."""
     H, D = shape.hidden, shape.head_dim

@@ -68,3 +68,45 @@ def test_e4m3_saturates_and_keeps_nan():
     assert codecs.e4m3_encode(np.array([np.nan]))[0] == 0x7F
     # 0.5 * smallest subnormal ties to even: 0
     assert codecs.e4m3_decode(codecs.e4m3_encode(np.array([2.0 ** -10])))[0] == 0.0
+
+
+def test_e2m1_codes_are_the_published_magnitudes():
+    # NVIDIA's FP4 e2m1 lists exactly these eight magnitudes; the sign bit negates them
+    vals = codecs.e2m1_table()
+    assert list(vals[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(vals[8:], -vals[:8])
+    assert np.signbit(vals[8])   # code 8 is -0
+
+
+def test_nvfp4_nibble_order_block_and_matrix_scales():
+    # one row of 32 elements: byte 0 = 0x21 holds element 0 = code 1 (0.5) in its low nibble
+    # and element 1 = code 2 (1.0) in its high nibble; byte 8 = 0xF7 holds element 16 = code 7
+    # (6.0) and element 17 = code 15 (-6.0); block 0 is scaled by e4m3 0x38 = 1.0 and block 1 by
+    # 0x40 = 2.0; the matrix scale is 0.25
+    packed = np.zeros((1, 16), dtype=np.uint8)
+    packed[0, 0] = 0x21
+    packed[0, 8] = 0xF7
+    scales = np.array([[0x38, 0x40]], dtype=np.uint8)
+    v = codecs.nvfp4_dequant(packed, scales, 0.25)
+    expect = np.zeros((1, 32))
+    expect[0, 0], expect[0, 1] = 0.5 * 0.25, 1.0 * 0.25
+    expect[0, 16], expect[0, 17] = 6.0 * 2.0 * 0.25, -6.0 * 2.0 * 0.25
+    assert np.array_equal(v, expect)
+
+
+def test_nvfp4_dequant_matches_element_loop():
+    rng = np.random.default_rng(3)
+    rows, K = 5, 64
+    packed = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    scales = rng.integers(0x30, 0x40, size=(rows, K // 16), dtype=np.uint8)
+    ms = np.float32(0.004)
+    got = codecs.nvfp4_dequant(packed, scales, ms)
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for r in range(rows):
+        for k in range(K):
+            byte = int(packed[r, k // 2])
+            code = byte & 0xF if k % 2 == 0 else byte >> 4
+            val = (-1.0 if code & 8 else 1.0) * mags[code & 7]
+            sc = float(torch.tensor([int(scales[r, k // 16])], dtype=torch.uint8)
+                       .view(torch.float8_e4m3fn).float()[0])
+            assert got[r, k] == val * sc * float(ms)
