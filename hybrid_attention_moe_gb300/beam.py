@@ -53,6 +53,7 @@ _SIGS = {
     "beam_attn": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
     "beam_route": [_P, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P],
     "beam_moe": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
+    "beam_moe_nvfp4": [_P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_dense_mlp": [_P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_workspace_bytes": [_P, _I, _I],
     "beam_kv_cache_bytes": [_I, _I, _I, _I, _I],
@@ -220,6 +221,24 @@ def beam_moe(cfg: LayerCfg, u, topk_idx, topk_w, w_gate_up, w_down, out, ws: tor
     _check(lib().beam_moe(ctypes.byref(c), _ptr(u), _ptr(topk_idx), _ptr(topk_w),
                           _ptr(w_gate_up), _ptr(w_down), u.shape[0], _ptr(out), _ptr(ws),
                           ws.numel(), _stream(stream)), "beam_moe")
+
+
+class NvFp4ExpertsC(ctypes.Structure):
+    _fields_ = [("gate_up", ctypes.c_void_p), ("gate_up_scale", ctypes.c_void_p),
+                ("gate_up_global", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("down_scale", ctypes.c_void_p), ("down_global", ctypes.c_void_p)]
+
+
+def beam_moe_nvfp4(cfg: LayerCfg, u, topk_idx, topk_w, experts: dict, out, ws: torch.Tensor,
+                   stream=None):
+    """experts: the tensors of synth.expert_weights_nvfp4 (gate_up, gate_up_scale,
+    gate_up_global, down, down_scale, down_global)."""
+    c = cfg.c()
+    w = NvFp4ExpertsC(*[_ptr(experts[k]) for k in ("gate_up", "gate_up_scale", "gate_up_global",
+                                                    "down", "down_scale", "down_global")])
+    _check(lib().beam_moe_nvfp4(ctypes.byref(c), _ptr(u), _ptr(topk_idx), _ptr(topk_w),
+                                ctypes.byref(w), u.shape[0], _ptr(out), _ptr(ws), ws.numel(),
+                                _stream(stream)), "beam_moe_nvfp4")
 
 
 def beam_dense_mlp(cfg: LayerCfg, u, w_gate_up, w_down, out, ws: torch.Tensor, stream=None):

@@ -466,6 +466,232 @@ __global__ void __launch_bounds__(256, 2) moe_down_mma_kernel(
   }
 }
 
+// NVFP4 expert weights (beam_moe_nvfp4). The expert products run on mma.sync in f16: an e2m1
+// weight times its e4m3 block scale has at most 6 significant bits and lies in [2^-10, 2688],
+// so it is exact in f16, and so are the BF16 activations of normal f16 magnitude; the FP32
+// matrix scale multiplies the FP32 accumulator. A warp's 16 weight rows are the A operand and up
+// to 8 of the expert's pairs the columns of B. Lane (g, c) loads, per 128-element block of a
+// row, the 16 bytes holding elements [32c, 32c + 32) and their two block scales (a 2-byte load);
+// the k order inside the block is permuted the same way for the token side, so the 32
+// elements serve the block's 8 k16 steps (step s takes elements 4s .. 4s+3).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Eight e2m1 codes (four bytes, even element in the low nibble) -> four f16x2 words, exactly.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t* r) {
+  asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4; cvt.rn.f16x2.e2m1x2 %0, b0;"
+      " cvt.rn.f16x2.e2m1x2 %1, b1; cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3;}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+// Two e4m3 codes -> f16x2 (exact), then each broadcast to both halves.
+__device__ __forceinline__ void e4m3x2_scales(uint16_t codes, uint32_t& lo2, uint32_t& hi2) {
+  uint32_t h2;
+  asm("{.reg .b16 c; mov.b16 c, %1; cvt.rn.f16x2.e4m3x2 %0, c;}" : "=r"(h2) : "h"(codes));
+  lo2 = __byte_perm(h2, 0, 0x1010);
+  hi2 = __byte_perm(h2, 0, 0x3232);
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// acc (rows g, g+8; columns = pairs 2c, 2c+1) += W[rows] . X^T over K; w0 / w1: the two rows'
+// codes (bytes, already offset by 16c), s0 / s1: their block scales (offset by 2c), xr: the
+// lane's token (f16, offset by 32c), tok: whether the lane has a token.
+constexpr int kFp4U = 2;   // 128-element blocks in flight per lane
+__device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w1,
+                                             const uint8_t* s0, const uint8_t* s1,
+                                             const uint16_t* xr, bool tok, int K,
+                                             float (&acc)[4]) {
+  float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+  const int nb = K >> 7;
+  for (int b0 = 0; b0 < nb; b0 += kFp4U) {
+    uint4 q[kFp4U][2];
+    uint16_t sc[kFp4U][2];
+#pragma unroll
+    for (int u = 0; u < kFp4U; ++u) {
+      const int b = min(b0 + u, nb - 1);
+      q[u][0] = ld_stream(w0 + size_t(b) * 64);
+      q[u][1] = ld_stream(w1 + size_t(b) * 64);
+      sc[u][0] = __ldg(reinterpret_cast<const uint16_t*>(s0 + size_t(b) * 8));
+      sc[u][1] = __ldg(reinterpret_cast<const uint16_t*>(s1 + size_t(b) * 8));
+    }
+#pragma unroll
+    for (int u = 0; u < kFp4U; ++u) {
+      if (b0 + u >= nb) break;
+      uint32_t xv[16];
+      if (tok) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 t = __ldg(reinterpret_cast<const uint4*>(xr + size_t(b0 + u) * 128 + 8 * i));
+          xv[4 * i] = t.x;
+          xv[4 * i + 1] = t.y;
+          xv[4 * i + 2] = t.z;
+          xv[4 * i + 3] = t.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xv[i] = 0u;
+      }
+      uint32_t w[2][16];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        uint32_t slo, shi;
+        e4m3x2_scales(sc[u][r], slo, shi);
+        const uint32_t qw[4] = {q[u][r].x, q[u][r].y, q[u][r].z, q[u][r].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          e2m1x8_to_f16(qw[i], &w[r][4 * i]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) w[r][4 * i + e] = hmul2(w[r][4 * i + e], i < 2 ? slo : shi);
+        }
+      }
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        if (st & 1)
+          mma_f16_16816(acc2, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                        xv[2 * st], xv[2 * st + 1]);
+        else
+          mma_f16_16816(acc, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                        xv[2 * st], xv[2 * st + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+}
+
+// u (bf16) -> u16 (f16) for the expert products; zeroes the down kernel's completion counters.
+__global__ void __launch_bounds__(256) fp4_prep_kernel(const uint16_t* __restrict__ u, int n,
+                                                       uint16_t* __restrict__ u16,
+                                                       int* __restrict__ cnt, int n_cnt) {
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_cnt) cnt[i] = 0;
+  if (i < n) u16[i] = f32_to_f16_bits(bf2f(u[i]));
+}
+
+// grid (ceil(F / 64), max active experts); a warp takes 8 units (gate rows f0..f0+7 and the
+// matching up rows). a16[pair][f] = f16(bf16(silu(gate) * up)).
+__global__ void __launch_bounds__(256, 2) moe_gate_up_fp4_kernel(
+    const uint16_t* __restrict__ u16, beam_nvfp4_experts W, int H, int F, int k, MoePlan pl,
+    const int32_t* __restrict__ direct, int E, uint16_t* __restrict__ a16) {
+  pdl_trigger();
+  pdl_wait();
+  const int ai = blockIdx.y;
+  if (ai >= (direct != nullptr ? k : *pl.n_active)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int f0 = (blockIdx.x * 8 + warp) * 8;
+  if (f0 >= F) return;
+  ExpertSlot es;
+  if (!expert_slot(pl, direct, E, ai, es)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(BEAM_DEV_BAD_EXPERT);
+    return;
+  }
+  const int f = min(f0 + g, F - 1);
+  const size_t rg = size_t(es.e) * 2 * F + f, ru = rg + F;
+  const uint8_t* w0 = W.gate_up + rg * (H / 2) + 16 * c;
+  const uint8_t* w1 = W.gate_up + ru * (H / 2) + 16 * c;
+  const uint8_t* s0 = W.gate_up_scale + rg * (H / 16) + 2 * c;
+  const uint8_t* s1 = W.gate_up_scale + ru * (H / 16) + 2 * c;
+  const float gs = W.gate_up_global[es.e];
+  for (int pp = es.p0; pp < es.p1; pp += 8) {
+    const int np = min(8, es.p1 - pp);
+    const bool tok = g < np;
+    const uint16_t* xr = u16 + size_t(tok ? pair_at(pl, direct, pp + g) / k : 0) * H + 32 * c;
+    float acc[4];
+    fp4_rows_mma(w0, w1, s0, s1, xr, tok, H, acc);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = 2 * c + j;
+      if (col < np && f0 + g < F) {
+        const float a = round_bf(siluf_(acc[j] * gs) * (acc[2 + j] * gs));
+        a16[size_t(pair_at(pl, direct, pp + col)) * F + f0 + g] = f32_to_f16_bits(a);
+      }
+    }
+  }
+}
+
+// grid (ceil(H / 128), max active experts); a warp takes 16 rows h; y[pair][h] in FP32; the
+// last CTA of each 128-row column combines its rows for every token, slots in order.
+__global__ void __launch_bounds__(256, 2) moe_down_fp4_kernel(
+    const uint16_t* __restrict__ a16, beam_nvfp4_experts W, int H, int F, MoePlan pl,
+    const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, int T, int k, int E, int* __restrict__ cnt,
+    float* __restrict__ y, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int na = direct != nullptr ? k : *pl.n_active;
+  const int ai = blockIdx.y;
+  if (ai >= max(na, 1)) return;   // uniform over the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int h0 = blockIdx.x * kMmaRowsDown + warp * 16;
+  ExpertSlot es;
+  if (ai < na && h0 < H && expert_slot(pl, direct, E, ai, es)) {
+    const size_t r0 = size_t(es.e) * H + min(h0 + g, H - 1);
+    const size_t r1 = size_t(es.e) * H + min(h0 + g + 8, H - 1);
+    const uint8_t* w0 = W.down + r0 * (F / 2) + 16 * c;
+    const uint8_t* w1 = W.down + r1 * (F / 2) + 16 * c;
+    const uint8_t* s0 = W.down_scale + r0 * (F / 16) + 2 * c;
+    const uint8_t* s1 = W.down_scale + r1 * (F / 16) + 2 * c;
+    const float gs = W.down_global[es.e];
+    for (int pp = es.p0; pp < es.p1; pp += 8) {
+      const int np = min(8, es.p1 - pp);
+      const bool tok = g < np;
+      const uint16_t* xr = a16 + size_t(tok ? pair_at(pl, direct, pp + g) : 0) * F + 32 * c;
+      float acc[4];
+      fp4_rows_mma(w0, w1, s0, s1, xr, tok, F, acc);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * c + j;
+        if (col < np) {
+          const size_t yo = size_t(pair_at(pl, direct, pp + col)) * H;
+          if (h0 + g < H) y[yo + h0 + g] = acc[j] * gs;
+          if (h0 + g + 8 < H) y[yo + h0 + g + 8] = acc[2 + j] * gs;
+        }
+      }
+    }
+  }
+  __shared__ int s_last;
+  // the CTA barrier orders every thread's y stores before thread 0's device-scope fence,
+  // which releases them with the counter increment
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int hb = blockIdx.x * kMmaRowsDown;
+  const int nh = min(kMmaRowsDown, H - hb);
+  for (int i = threadIdx.x; i < T * nh; i += blockDim.x) {
+    const int t = i / nh, h = hb + (i - t * nh);
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[size_t(t) * k + j];
+      if (e < 0 || e >= E) continue;
+      s = fmaf(topk_w[size_t(t) * k + j], __ldcg(y + (size_t(t) * k + j) * H + h), s);
+    }
+    out[size_t(t) * H + h] = f2bf(s);
+  }
+}
+
 __global__ void moe_combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                                    const int32_t* __restrict__ idx, int T, int H, int k, int E,
                                    uint16_t* __restrict__ out) {
@@ -555,6 +781,7 @@ size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
   if (grouped || P > size_t(kFusedMaxPairs) || T < kMoeGemmMinT)
     b += align_up(P * c->hidden * 4, 256);
   if (T < kMoeGemmMinT) b += align_up(size_t(c->hidden / 8 + 1) * 4, 256);
+  if (T < kMoeGemmMinT) b += align_up(size_t(T) * c->hidden * 2, 256);   // f16 tokens (NVFP4)
   return b;
 }
 
@@ -704,4 +931,46 @@ extern "C" beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16
   if (const cudaError_t err_ = launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st); err_ != cudaSuccess)
     return cuda_status(err_);
   return BEAM_OK;
+}
+
+extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                      const int32_t* topk_idx, const float* topk_w,
+                                      const beam_nvfp4_experts* w, int T, beam_bf16* out,
+                                      void* ws, size_t ws_bytes, beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !topk_idx || !topk_w || !w || !out) return BEAM_ERR_INVALID_ARG;
+  const int H = cfg->hidden, F = cfg->d_ff_expert, E = cfg->n_experts, k = cfg->topk;
+  if (H <= 0 || F <= 0 || E <= 0 || k <= 0) return BEAM_ERR_INVALID_ARG;
+  if (!w->gate_up || !w->gate_up_scale || !w->gate_up_global || !w->down || !w->down_scale ||
+      !w->down_global)
+    return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(ws) || !aligned16(w->gate_up) || !aligned16(w->down) ||
+      !aligned16(w->gate_up_scale) || !aligned16(w->down_scale))
+    return BEAM_ERR_INVALID_ARG;
+  if (E > 4096 || (H & 127) || (F & 127) || T >= kMoeGemmMinT) return BEAM_ERR_UNSUPPORTED;
+  if (T == 0) return BEAM_OK;
+  const int P = T * k;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  MoePlan pl = carve_plan(cv, E, P, false);
+  uint16_t* a16 = cv.take<uint16_t>(size_t(P) * F);
+  float* y = cv.take<float>(size_t(P) * H);
+  int* cnt = cv.take<int>(size_t(H / 8 + 1));
+  uint16_t* u16 = cv.take<uint16_t>(size_t(T) * H);
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  // one token: its k slots are the active list directly; more: the plan groups the pairs
+  const bool direct = T == 1;
+  const int32_t* dix = direct ? topk_idx : nullptr;
+  const int na = direct ? k : (P < E ? P : E);
+  const int n_cnt = (H + kMmaRowsDown - 1) / kMmaRowsDown;
+  const int n = T * H;
+  launch_pdl(fp4_prep_kernel, dim3((max(n, n_cnt) + 255) / 256), dim3(256), 0, st, u, n, u16, cnt,
+             n_cnt);
+  if (!direct)
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+  launch_pdl(moe_gate_up_fp4_kernel, dim3((F + 63) / 64, na), dim3(256), 0, st, u16, *w, H, F, k,
+             pl, dix, E, a16);
+  launch_pdl(moe_down_fp4_kernel, dim3(n_cnt, na), dim3(256), 0, st, a16, *w, H, F, pl, dix,
+             topk_idx, topk_w, T, k, E, cnt, y, out);
+  return launch_status();
 }

@@ -199,6 +199,33 @@ beam_status beam_moe(const beam_layer_cfg* cfg, const beam_bf16* u, const int32_
                      const float* topk_w, const beam_bf16* w_gate_up, const beam_bf16* w_down,
                      int T, beam_bf16* out, void* ws, size_t ws_bytes, beam_stream_t stream);
 
+/* NVFP4 expert weights (the format the Beam and Flint pages name for the shipped
+ * checkpoints; the pages do not print its layout, so this is NVIDIA's published definition):
+ * FP4 e2m1 elements, two per byte with the even element in the low nibble; one e4m3 scale per
+ * 16 consecutive elements of a row; one FP32 scale per expert matrix. Element value =
+ * e2m1 * block scale * matrix scale. All pointers are device pointers, 16-byte aligned.
+ *  gate_up [E][2F][H/2], gate_up_scale [E][2F][H/16], gate_up_global [E] (rows gate, then up)
+ *  down [E][H][F/2], down_scale [E][H][F/16], down_global [E]. */
+typedef struct {
+  const uint8_t* gate_up;
+  const uint8_t* gate_up_scale;
+  const float* gate_up_global;
+  const uint8_t* down;
+  const uint8_t* down_scale;
+  const float* down_global;
+} beam_nvfp4_experts;
+
+/* beam_moe with NVFP4 expert weights (weight-only quantisation: activations stay BF16, the
+ * products run in f16 with FP32 accumulation, every dequantised weight being exact in f16).
+ * Same arguments and results as beam_moe otherwise; the caller's u is rounded to f16 (exact
+ * for BF16 values of magnitude 2^-14 .. 65504). Decode sizes: 1 <= T < 32 tokens; other T,
+ * or H or d_ff not a multiple of 128, return BEAM_ERR_UNSUPPORTED. The workspace is the one
+ * beam_workspace_bytes gives for T. */
+beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16* u,
+                           const int32_t* topk_idx, const float* topk_w,
+                           const beam_nvfp4_experts* w, int T, beam_bf16* out, void* ws,
+                           size_t ws_bytes, beam_stream_t stream);
+
 /* Dense SwiGLU MLP of layers 0-2 (Beam page, MoE section: d_ff 20480; change 7 runs the
  * activation in one kernel). w_gate_up (device) [2*Fd][H], w_down (device) [H][Fd]. */
 beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16* u,

@@ -346,6 +346,71 @@ def test_moe(shape, T, n_used):
     assert_close(np64(out), ref, "moe out")
 
 
+def _nvfp4_experts(shape, used, seed):
+    """NVFP4 expert tensors on the device (only the used experts drawn, the rest zero) and
+    the oracle's view of the used ones."""
+    E, F, H = shape.n_experts, shape.d_ff_expert, shape.hidden
+    part = synth.expert_weights_nvfp4(shape, 0, seed, device=DEV, experts=used)
+    full = {
+        "gate_up": torch.zeros((E, 2 * F, H // 2), dtype=torch.uint8, device=DEV),
+        "gate_up_scale": torch.zeros((E, 2 * F, H // 16), dtype=torch.uint8, device=DEV),
+        "gate_up_global": torch.zeros((E,), dtype=torch.float32, device=DEV),
+        "down": torch.zeros((E, H, F // 2), dtype=torch.uint8, device=DEV),
+        "down_scale": torch.zeros((E, H, F // 16), dtype=torch.uint8, device=DEV),
+        "down_global": torch.zeros((E,), dtype=torch.float32, device=DEV),
+    }
+    for i, e in enumerate(used):
+        for k in full:
+            full[k][e] = part[k][i]
+    host = {k: v.cpu().numpy() for k, v in part.items()}
+    experts = {e: (host["gate_up"][i], host["gate_up_scale"][i], host["gate_up_global"][i],
+                   host["down"][i], host["down_scale"][i], host["down_global"][i])
+               for i, e in enumerate(used)}
+    return full, experts
+
+
+@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 13, None),
+                                            (TINY, 31, 6), (BEAM, 1, None), (BEAM, 2, None),
+                                            (BEAM, 8, None)])
+def test_moe_nvfp4(shape, T, n_used):
+    """NVFP4 expert weights (e2m1 codes, e4m3 block scales, FP32 matrix scales): mma.sync f16
+    products of the dequantised weights, the selected experts only; T=31 over 6 experts gives
+    experts more than 8 pairs (several passes)."""
+    seed = 91 + T
+    cfg = cfg_of(shape)
+    idx, w = _random_routing(shape, T, seed, n_used)
+    used = sorted(set(idx.ravel().tolist()))
+    full, experts = _nvfp4_experts(shape, used, seed)
+    u = synth.activations(T, shape.hidden, seed, "u", DEV)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_moe_nvfp4(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), full,
+                     out, ws_for(cfg, T))
+    check_status()
+    ref = O.moe_nvfp4(shape, np64(u), idx, w.astype(np.float64), experts)
+    assert_close(np64(out), ref, "moe nvfp4 out")
+
+
+def test_moe_nvfp4_bad_expert_slots_flagged_and_skipped():
+    shape = TINY
+    cfg = cfg_of(shape)
+    for rows in ([[0, 1, 99, 2]], [[0, 1, 99, 2], [5, -3, 1, 7]]):
+        T = len(rows)
+        idx = np.asarray(rows, dtype=np.int32)
+        w = np.full((T, 4), 0.5, dtype=np.float32)
+        full, experts = _nvfp4_experts(shape, [0, 1, 2, 5, 7], 4)
+        u = synth.activations(T, shape.hidden, 4, "u", DEV)
+        out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+        B.beam_get_device_status()
+        B.beam_moe_nvfp4(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV),
+                         full, out, ws_for(cfg, T))
+        assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+        for t in range(T):
+            keep = [j for j in range(4) if 0 <= rows[t][j] < shape.n_experts]
+            ref = O.moe_nvfp4(shape, np64(u[t:t + 1]), idx[t:t + 1, keep],
+                              np.full((1, len(keep)), 0.5), experts)
+            assert_close(np64(out[t:t + 1]), ref, "moe nvfp4 out, valid slots")
+
+
 @pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 5), (TINY, 13), (TINY, 64), (TINY, 200),
                                      (BEAM, 1), (BEAM, 3), (BEAM, 8), (BEAM, 40), (BEAM, 130)])
 def test_dense_mlp(shape, T):
