@@ -507,10 +507,68 @@ __device__ __forceinline__ uint16_t f32_to_f16_bits(float f) {
   return r;
 }
 
+constexpr int kFp4U = 2;   // 128-element blocks per load group; two groups are in flight
+struct Fp4Group {
+  uint4 q[kFp4U][2];
+  uint16_t sc[kFp4U][2];
+};
+__device__ __forceinline__ void fp4_load_group(Fp4Group& G, const uint8_t* w0, const uint8_t* w1,
+                                               const uint8_t* s0, const uint8_t* s1, int b0,
+                                               int nb) {
+#pragma unroll
+  for (int u = 0; u < kFp4U; ++u) {
+    const int b = min(b0 + u, nb - 1);
+    G.q[u][0] = ld_stream(w0 + size_t(b) * 64);
+    G.q[u][1] = ld_stream(w1 + size_t(b) * 64);
+    G.sc[u][0] = __ldg(reinterpret_cast<const uint16_t*>(s0 + size_t(b) * 8));
+    G.sc[u][1] = __ldg(reinterpret_cast<const uint16_t*>(s1 + size_t(b) * 8));
+  }
+}
+__device__ __forceinline__ void fp4_block_mma(const uint4 (&q)[2], const uint16_t (&sc)[2],
+                                              const uint16_t* xb, bool tok, float (&acc)[4],
+                                              float (&acc2)[4]) {
+  uint32_t xv[16];
+  if (tok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t = *reinterpret_cast<const uint4*>(xb + 8 * i);
+      xv[4 * i] = t.x;
+      xv[4 * i + 1] = t.y;
+      xv[4 * i + 2] = t.z;
+      xv[4 * i + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xv[i] = 0u;
+  }
+  uint32_t w[2][16];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    uint32_t slo, shi;
+    e4m3x2_scales(sc[r], slo, shi);
+    const uint32_t qw[4] = {q[r].x, q[r].y, q[r].z, q[r].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e2m1x8_to_f16(qw[i], &w[r][4 * i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w[r][4 * i + e] = hmul2(w[r][4 * i + e], i < 2 ? slo : shi);
+    }
+  }
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    if (st & 1)
+      mma_f16_16816(acc2, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                    xv[2 * st], xv[2 * st + 1]);
+    else
+      mma_f16_16816(acc, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                    xv[2 * st], xv[2 * st + 1]);
+  }
+}
+
 // acc (rows g, g+8; columns = pairs 2c, 2c+1) += W[rows] . X^T over K; w0 / w1: the two rows'
 // codes (bytes, already offset by 16c), s0 / s1: their block scales (offset by 2c), xr: the
-// lane's token (f16, offset by 32c), tok: whether the lane has a token.
-constexpr int kFp4U = 2;   // 128-element blocks in flight per lane
+// lane's token (f16, offset by 32c), tok: whether the lane has a token. The loads of the next
+// group of blocks are issued before the current group is converted and multiplied.
 __device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w1,
                                              const uint8_t* s0, const uint8_t* s1,
                                              const uint16_t* xr, bool tok, int K,
@@ -519,57 +577,14 @@ __device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0.f;
   const int nb = K >> 7;
+  Fp4Group cur, nxt;
+  fp4_load_group(cur, w0, w1, s0, s1, 0, nb);
   for (int b0 = 0; b0 < nb; b0 += kFp4U) {
-    uint4 q[kFp4U][2];
-    uint16_t sc[kFp4U][2];
+    if (b0 + kFp4U < nb) fp4_load_group(nxt, w0, w1, s0, s1, b0 + kFp4U, nb);
 #pragma unroll
-    for (int u = 0; u < kFp4U; ++u) {
-      const int b = min(b0 + u, nb - 1);
-      q[u][0] = ld_stream(w0 + size_t(b) * 64);
-      q[u][1] = ld_stream(w1 + size_t(b) * 64);
-      sc[u][0] = __ldg(reinterpret_cast<const uint16_t*>(s0 + size_t(b) * 8));
-      sc[u][1] = __ldg(reinterpret_cast<const uint16_t*>(s1 + size_t(b) * 8));
-    }
-#pragma unroll
-    for (int u = 0; u < kFp4U; ++u) {
-      if (b0 + u >= nb) break;
-      uint32_t xv[16];
-      if (tok) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 t = __ldg(reinterpret_cast<const uint4*>(xr + size_t(b0 + u) * 128 + 8 * i));
-          xv[4 * i] = t.x;
-          xv[4 * i + 1] = t.y;
-          xv[4 * i + 2] = t.z;
-          xv[4 * i + 3] = t.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) xv[i] = 0u;
-      }
-      uint32_t w[2][16];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        uint32_t slo, shi;
-        e4m3x2_scales(sc[u][r], slo, shi);
-        const uint32_t qw[4] = {q[u][r].x, q[u][r].y, q[u][r].z, q[u][r].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          e2m1x8_to_f16(qw[i], &w[r][4 * i]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) w[r][4 * i + e] = hmul2(w[r][4 * i + e], i < 2 ? slo : shi);
-        }
-      }
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        if (st & 1)
-          mma_f16_16816(acc2, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
-                        xv[2 * st], xv[2 * st + 1]);
-        else
-          mma_f16_16816(acc, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
-                        xv[2 * st], xv[2 * st + 1]);
-      }
-    }
+    for (int u = 0; u < kFp4U; ++u)
+      if (b0 + u < nb) fp4_block_mma(cur.q[u], cur.sc[u], xr + size_t(b0 + u) * 128, tok, acc, acc2);
+    cur = nxt;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
@@ -588,7 +603,7 @@ __global__ void __launch_bounds__(256) fp4_prep_kernel(const uint16_t* __restric
 
 // grid (ceil(F / 64), max active experts); a warp takes 8 units (gate rows f0..f0+7 and the
 // matching up rows). a16[pair][f] = f16(bf16(silu(gate) * up)).
-__global__ void __launch_bounds__(256, 2) moe_gate_up_fp4_kernel(
+__global__ void __launch_bounds__(256, 3) moe_gate_up_fp4_kernel(
     const uint16_t* __restrict__ u16, beam_nvfp4_experts W, int H, int F, int k, MoePlan pl,
     const int32_t* __restrict__ direct, int E, uint16_t* __restrict__ a16) {
   pdl_trigger();
@@ -629,7 +644,7 @@ __global__ void __launch_bounds__(256, 2) moe_gate_up_fp4_kernel(
 
 // grid (ceil(H / 128), max active experts); a warp takes 16 rows h; y[pair][h] in FP32; the
 // last CTA of each 128-row column combines its rows for every token, slots in order.
-__global__ void __launch_bounds__(256, 2) moe_down_fp4_kernel(
+__global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
     const uint16_t* __restrict__ a16, beam_nvfp4_experts W, int H, int F, MoePlan pl,
     const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ topk_w, int T, int k, int E, int* __restrict__ cnt,

@@ -7,7 +7,7 @@ warm-up launches and capture one or a few real ones. Usage:
     python -m hybrid_attention_moe_gb300.profile_cases --case moe_decode --reps 3
 
 Cases: moe_decode (--tokens tokens, default 1, each over 8 selected experts of a 32-expert
-pool), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
+pool), moe_decode_nvfp4 (the same with NVFP4 expert weights), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
 qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (100K keys),
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
 moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts), attn_nope_prefill
@@ -58,6 +58,17 @@ def main():
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_moe(cs, u, idx, w, wgu, wdn, out, ws)  # noqa: E731
+    elif c == "moe_decode_nvfp4":
+        T = args.tokens
+        cs = B.LayerCfg.from_shape(small, B.BEAM_ATTN_SWA_ROPE)
+        wq = synth.expert_weights_nvfp4(small, 3, 0, device=dev)
+        u = synth.activations(T, H, 0, "u", dev)
+        g = torch.Generator(device="cpu").manual_seed(0)
+        idx = torch.stack([torch.randperm(32, generator=g)[:8] for _ in range(T)]).int().to(dev)
+        w = torch.full((T, 8), 0.3, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: B.beam_moe_nvfp4(cs, u, idx, w, wq, out, ws)  # noqa: E731
     elif c == "dense_decode":
         T = args.tokens
         Wd = synth.dense_weights(shape, 0, 0, device=dev)
