@@ -16,6 +16,8 @@ so no flush is needed. The K timed steps are captured as one CUDA graph and repl
 between two events; each call's time comes from a second replay of the same K steps with a
 timing event (an external event node) before every call.
 
+--experts nvfp4 gives the MoE layers NVFP4 expert weights (beam_moe_nvfp4; decode workloads).
+
 --impl reference times the CPU oracle on the same workload instead (a bounded sample per step).
 """
 from __future__ import annotations
@@ -56,7 +58,14 @@ def is_nope(l, L):
     return (l + 1) % 6 == 0 or l == L - 1
 
 
-def layer_bytes(shape, dense, n_experts_touched, kv_bytes):
+def expert_bytes(shape, nvfp4):
+    """Weight bytes of one expert: BF16, or NVFP4 (half a byte per element, one e4m3 scale per
+    16 elements, two FP32 matrix scales)."""
+    n = 3 * shape.hidden * shape.d_ff_expert
+    return n // 2 + n // 16 + 8 if nvfp4 else 2 * n
+
+
+def layer_bytes(shape, dense, n_experts_touched, kv_bytes, nvfp4=False):
     """Algorithmic HBM bytes of one layer step: every weight byte the step must read once,
     the KV bytes it must read, the gains; activations are negligible (<0.1%)."""
     H, D = shape.hidden, shape.head_dim
@@ -66,7 +75,7 @@ def layer_bytes(shape, dense, n_experts_touched, kv_bytes):
         b += 3 * H * shape.d_ff_dense * 2
     else:
         b += shape.n_experts * H * 4 + shape.n_experts * 4       # FP32 router
-        b += n_experts_touched * 3 * H * shape.d_ff_expert * 2
+        b += n_experts_touched * expert_bytes(shape, nvfp4)
     return b + kv_bytes
 
 
@@ -168,9 +177,13 @@ class Workload:
         self.prefill = chunk > 1
         self.tokens = batch * chunk
         scale = 1.0
+        self.nvfp4 = args.experts == "nvfp4"
         W, caches = [], []
         for l in layers:
-            W.append(synth.layer_weights(shape, l, args.seed, device=device))
+            W.append(synth.layer_weights(shape, l, args.seed, device=device,
+                                         with_experts=not self.nvfp4))
+            if self.nvfp4 and l not in shape.dense_layers:
+                W[-1]["nvfp4"] = synth.expert_weights_nvfp4(shape, l, args.seed, device=device)
             nope = is_nope(l, shape.n_layers)
             # a sliding-window ring holds window + chunk - 1 keys, rounded up to whole 128-key
             # tiles (the tensor-core prefill walks the ring in tile-aligned slots)
@@ -218,8 +231,10 @@ class Workload:
                     (f"L{l}.route", lambda W=W, cfg=cfg: B.beam_route(
                         cfg, b["u"], W["router"], W["corr_bias"], b["logits"], b["idx"], b["w"],
                         ws)),
-                    (f"L{l}.moe", lambda W=W, cfg=cfg: B.beam_moe(
-                        cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"], ws)),
+                    (f"L{l}.moe", (lambda W=W, cfg=cfg: B.beam_moe_nvfp4(
+                        cfg, b["u"], b["idx"], b["w"], W["nvfp4"], b["m"], ws)) if "nvfp4" in W
+                     else (lambda W=W, cfg=cfg: B.beam_moe(
+                         cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"], ws))),
                 ]
             calls.append((f"L{l}.norm_mlp", lambda W=W, cfg=cfg, l=l, nxt=nxt:
                           B.beam_boundary_norm(b["m"], b["h"], b["u"] if nxt is not None else None,
@@ -262,7 +277,7 @@ class Workload:
             elem = 1 if self.fp8 else 2
             kv = self.batch * (keys + self.chunk - 1) * shape.n_kv * shape.head_dim * 2 * elem
             dense = l in shape.dense_layers
-            per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv)
+            per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv, self.nvfp4)
             tot += per[l]
         return tot, per
 
@@ -416,6 +431,7 @@ def run_ours(args, rank, world, device):
             "workload": args.workload, "layers": wl.layers, "batch": wl.batch,
             "new_tokens_per_seq": wl.chunk, "context": wl.ctx,
             "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
+            "expert_weights": "nvfp4" if wl.nvfp4 else "bf16",
             "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
             "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
             "parallelism": "replicas" if world > 1 else "single",
@@ -451,7 +467,7 @@ def dominant_bytes(wl, name, touched):
     """Algorithmic bytes of one call of the step (weights and cache it must read once)."""
     l = int(name.split(".")[0][1:])
     if name.endswith(".moe"):
-        return touched[l] * 3 * BEAM.hidden * BEAM.d_ff_expert * 2, "moe_decode"
+        return touched[l] * expert_bytes(BEAM, wl.nvfp4), ("moe_decode_nvfp4" if wl.nvfp4 else "moe_decode")
     if name.endswith(".attn"):
         keys = wl.ctx + 1 if is_nope(l, BEAM.n_layers) else min(BEAM.window, wl.ctx + 1)
         elem = 1 if wl.fp8 else 2
@@ -511,11 +527,26 @@ def oracle_sample(args, wl):
                 self.c[e] = np64(self.t[e])
             return self.c[e]
 
+    class LazyNvfp4:
+        """expert -> the six NVFP4 arrays of oracle.moe_nvfp4, copied to the host on first use"""
+        def __init__(self, d):
+            self.d, self.c = d, {}
+
+        def __getitem__(self, e):
+            if e not in self.c:
+                h = {k: v[e].cpu().numpy() for k, v in self.d.items()}
+                self.c[e] = (h["gate_up"], h["gate_up_scale"], float(h["gate_up_global"]),
+                             h["down"], h["down_scale"], float(h["down_global"]))
+            return self.c[e]
+
     Wo = []
     for W in wl.W:
         d = {}
         for k, v in W.items():
-            d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else np64(v)
+            if k == "nvfp4":
+                d["nvfp4_experts"] = LazyNvfp4(v)
+            else:
+                d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else np64(v)
         Wo.append(d)
     caches = []
     for kc in wl.caches:
@@ -574,6 +605,7 @@ def run_reference(args, rank, world, device):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the CUDA arm)",
         "config": {"workload": args.workload, "layers": wl.layers, "batch": 1,
                    "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
+                   "expert_weights": "nvfp4" if wl.nvfp4 else "bf16",
                    "sample": "one token of sequence 0 per step"},
         "cpu_baseline": {"value": val, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": "the first new token of sequence 0 through the held layers"
@@ -597,10 +629,14 @@ def main():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--context", type=int, default=100_000)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--experts", default="bf16", choices=["bf16", "nvfp4"],
+                    help="expert weight format of the MoE layers (decode only for nvfp4)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.experts == "nvfp4" and args.workload == "stack_prefill":
+        ap.error("--experts nvfp4 is a decode format here (beam_moe_nvfp4 takes up to 31 tokens)")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -23,7 +23,9 @@ class BeamStack:
 
     weights: list (one per layer) of dicts of device tensors, keys as made by
              synth.layer_weights (attn_pre, attn_post, mlp_pre, mlp_post, w_qkvg, q_norm,
-             k_norm, gate_bias, w_o, and w_gate_up/w_down (+ router, corr_bias on MoE layers)).
+             k_norm, gate_bias, w_o, and w_gate_up/w_down (+ router, corr_bias on MoE layers);
+             an MoE layer may hold "nvfp4" (synth.expert_weights_nvfp4) instead of
+             w_gate_up/w_down, and then runs beam_moe_nvfp4).
     caches : list of B.KVCache, one per layer (window = W on sliding-window layers, 0 on NoPE).
     """
 
@@ -84,8 +86,11 @@ class BeamStack:
         else:
             B.beam_route(cfg, b["u"], W["router"], W["corr_bias"], b["logits"], b["idx"], b["w"],
                          ws, stream)
-            B.beam_moe(cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"], ws,
-                       stream)
+            if "nvfp4" in W:
+                B.beam_moe_nvfp4(cfg, b["u"], b["idx"], b["w"], W["nvfp4"], b["m"], ws, stream)
+            else:
+                B.beam_moe(cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"],
+                           ws, stream)
         if trace is not None:
             trace[-1]["mlp"] = b["m"].clone()
             if not self.dense[i]:

@@ -338,7 +338,10 @@ def layer_forward(cfg, l, W, h, u, cache, seq_id, pos, next_pre, trace=None):
         r = None
     else:
         logits, idx, w = route(cfg, u, W["router"], W["corr_bias"])
-        m = moe(cfg, u, idx, w, W["w_gate_up"], W["w_down"])
+        if "nvfp4_experts" in W:   # mapping expert -> its six NVFP4 arrays (moe_nvfp4)
+            m = moe_nvfp4(cfg, u, idx, w, W["nvfp4_experts"])
+        else:
+            m = moe(cfg, u, idx, w, W["w_gate_up"], W["w_down"])
         r = (logits, idx, w)
     if trace is not None:
         trace.append({"q": q, "g": g, "attn": a, "mlp_in": u, "mlp": m, "route": r})

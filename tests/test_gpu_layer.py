@@ -38,10 +38,26 @@ class LazyRows:
         return self.cache[e]
 
 
+class LazyNvfp4:
+    """expert -> its six NVFP4 arrays (oracle.moe_nvfp4), copied to the host on first use."""
+
+    def __init__(self, d):
+        self.d, self.c = d, {}
+
+    def __getitem__(self, e):
+        if e not in self.c:
+            h = {k: v[e].cpu().numpy() for k, v in self.d.items()}
+            self.c[e] = (h["gate_up"], h["gate_up_scale"], float(h["gate_up_global"]),
+                         h["down"], h["down_scale"], float(h["down_global"]))
+        return self.c[e]
+
+
 def oracle_weights(W):
     out = {}
     for k, v in W.items():
-        if k in ("w_gate_up", "w_down") and v.dim() == 3:
+        if k == "nvfp4":
+            out["nvfp4_experts"] = LazyNvfp4(v)
+        elif k in ("w_gate_up", "w_down") and v.dim() == 3:
             out[k] = LazyRows(v)
         else:
             out[k] = np64(v)
@@ -140,7 +156,7 @@ def test_tiny_stack_prefill_then_decode_per_layer():
     assert n_tie <= 0.05 * n_tok, f"{n_tie} of {n_tok} token routings took the other side of a tie"
 
 
-def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0):
+def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvfp4=False):
     """One MoE layer of the truncated stack, one decode token per sequence, chained-step bars.
 
     The oracle runs in two stages with the oracle's own functions, in layer_forward's order:
@@ -155,7 +171,9 @@ def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0):
     positions = [c + 1 for c in contexts]
     max_pos = max(positions)
     cap, window = (max_pos + 8, 0) if nope else (shape.window, shape.window)
-    W = synth.layer_weights(shape, layer, seed, device=DEV)
+    W = synth.layer_weights(shape, layer, seed, device=DEV, with_experts=not nvfp4)
+    if nvfp4:
+        W["nvfp4"] = synth.expert_weights_nvfp4(shape, layer, seed, device=DEV)
     c = synth.kv_cache(shape, S, cap, seed, layer, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
                        device=DEV)
     kc = B.KVCache(c["k"], c["v"], window, *scale)
@@ -174,7 +192,10 @@ def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0):
 
     def mlp_half(h1, u1, R):
         logits, idx, w = O.route(shape, u1, R["router"], R["corr_bias"])
-        m = O.moe(shape, u1, idx, w, Wo["w_gate_up"], Wo["w_down"])
+        if nvfp4:
+            m = O.moe_nvfp4(shape, u1, idx, w, Wo["nvfp4_experts"])
+        else:
+            m = O.moe(shape, u1, idx, w, Wo["w_gate_up"], Wo["w_down"])
         h2, _ = O.boundary_norm(m, h1, Wo["mlp_post"], None, 2 * layer + 3, shape.eps)
         return logits, idx, w, m, h2
 
@@ -235,6 +256,13 @@ def test_full_width_swa_moe_layer_decode_ctx4096():
 @pytest.mark.parametrize("batch", [1, 8])
 def test_full_width_nope_moe_layer_decode_ctx100k_bf16(batch):
     _layer_case(BEAM, 5, [100_000] * batch)
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_full_width_swa_moe_layer_decode_nvfp4_experts(batch):
+    """The layer with NVFP4 expert weights (beam_moe_nvfp4 in the stack driver; the oracle's
+    layer dequantises the selected experts)."""
+    _layer_case(BEAM, 3, [4096] * batch, nvfp4=True)
 
 
 def test_full_width_nope_moe_layer_decode_ctx100k_fp8():
