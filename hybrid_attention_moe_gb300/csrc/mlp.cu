@@ -565,21 +565,22 @@ __device__ __forceinline__ void fp4_block_mma(const uint4 (&q)[2], const uint16_
   }
 }
 
-// acc (rows g, g+8; columns = pairs 2c, 2c+1) += W[rows] . X^T over K; w0 / w1: the two rows'
-// codes (bytes, already offset by 16c), s0 / s1: their block scales (offset by 2c), xr: the
-// lane's token (f16, offset by 32c), tok: whether the lane has a token. The loads of the next
-// group of blocks are issued before the current group is converted and multiplied.
+// acc (rows g, g+8; columns = pairs 2c, 2c+1) = W[rows] . X^T over the 128-element blocks
+// [bb, nb); w0 / w1: the two rows' codes (bytes, already offset by 16c), s0 / s1: their block
+// scales (offset by 2c), xr: the lane's token (f16, offset by 32c), tok: whether the lane has a
+// token. The loads of the next group of blocks are issued before the current group is
+// converted and multiplied.
 __device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w1,
                                              const uint8_t* s0, const uint8_t* s1,
-                                             const uint16_t* xr, bool tok, int K,
+                                             const uint16_t* xr, bool tok, int bb, int nb,
                                              float (&acc)[4]) {
   float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0.f;
-  const int nb = K >> 7;
+  // blocks [bb, nb) of the rows
   Fp4Group cur, nxt;
-  fp4_load_group(cur, w0, w1, s0, s1, 0, nb);
-  for (int b0 = 0; b0 < nb; b0 += kFp4U) {
+  fp4_load_group(cur, w0, w1, s0, s1, bb, nb);
+  for (int b0 = bb; b0 < nb; b0 += kFp4U) {
     if (b0 + kFp4U < nb) fp4_load_group(nxt, w0, w1, s0, s1, b0 + kFp4U, nb);
 #pragma unroll
     for (int u = 0; u < kFp4U; ++u)
@@ -588,6 +589,29 @@ __device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
+}
+
+// With KS > 1, KS warps share a row block, each taking a 1/KS share of its K blocks, and add
+// their partial tiles in order through shared memory: a warp's chain of dependent weight loads
+// is KS times shorter and the grid has KS times the CTAs, which few tokens (few active experts,
+// a grid under one wave) need; with many tokens the grid is large enough without it.
+constexpr int kFp4KSMaxT = 4;   // KS = 4 up to this many tokens, else 1
+template <int KS>
+__device__ __forceinline__ bool fp4_reduce_ks(float (&acc)[4], float (*red)[32][4]) {
+  if (KS == 1) return true;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) red[warp][lane][i] = acc[i];
+  __syncthreads();
+  if (warp % KS != 0) return false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v = red[warp][lane][i];
+#pragma unroll
+    for (int j = 1; j < KS; ++j) v += red[warp + j][lane][i];
+    acc[i] = v;
+  }
+  return true;
 }
 
 // u (bf16) -> u16 (f16) for the expert products; zeroes the down kernel's completion counters.
@@ -601,20 +625,22 @@ __global__ void __launch_bounds__(256) fp4_prep_kernel(const uint16_t* __restric
   if (i < n) u16[i] = f32_to_f16_bits(bf2f(u[i]));
 }
 
-// grid (ceil(F / 64), max active experts); a warp takes 8 units (gate rows f0..f0+7 and the
-// matching up rows). a16[pair][f] = f16(bf16(silu(gate) * up)).
+// grid (ceil(F / (64 / KS)), max active experts); a row block is 8 units (gate rows f0..f0+7
+// and the matching up rows), KS warps per row block. a16[pair][f] = f16(bf16(silu(gate) * up)).
+template <int KS>
 __global__ void __launch_bounds__(256, 3) moe_gate_up_fp4_kernel(
     const uint16_t* __restrict__ u16, beam_nvfp4_experts W, int H, int F, int k, MoePlan pl,
     const int32_t* __restrict__ direct, int E, uint16_t* __restrict__ a16) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float red[8][32][4];
   const int ai = blockIdx.y;
-  if (ai >= (direct != nullptr ? k : *pl.n_active)) return;
+  if (ai >= (direct != nullptr ? k : *pl.n_active)) return;   // uniform over the CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int f0 = (blockIdx.x * 8 + warp) * 8;
-  if (f0 >= F) return;
+  const int ks = warp % KS;
+  const int f0 = (blockIdx.x * (8 / KS) + warp / KS) * 8;
   ExpertSlot es;
-  if (!expert_slot(pl, direct, E, ai, es)) {
+  if (!expert_slot(pl, direct, E, ai, es)) {   // uniform over the CTA
     if (blockIdx.x == 0 && threadIdx.x == 0) flag(BEAM_DEV_BAD_EXPERT);
     return;
   }
@@ -625,25 +651,31 @@ __global__ void __launch_bounds__(256, 3) moe_gate_up_fp4_kernel(
   const uint8_t* s0 = W.gate_up_scale + rg * (H / 16) + 2 * c;
   const uint8_t* s1 = W.gate_up_scale + ru * (H / 16) + 2 * c;
   const float gs = W.gate_up_global[es.e];
+  const int nb = H >> 7, bb = ks * nb / KS, be = (ks + 1) * nb / KS;
   for (int pp = es.p0; pp < es.p1; pp += 8) {
     const int np = min(8, es.p1 - pp);
     const bool tok = g < np;
     const uint16_t* xr = u16 + size_t(tok ? pair_at(pl, direct, pp + g) / k : 0) * H + 32 * c;
     float acc[4];
-    fp4_rows_mma(w0, w1, s0, s1, xr, tok, H, acc);
+    fp4_rows_mma(w0, w1, s0, s1, xr, tok, bb, be, acc);
+    if (fp4_reduce_ks<KS>(acc, red)) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int col = 2 * c + j;
-      if (col < np && f0 + g < F) {
-        const float a = round_bf(siluf_(acc[j] * gs) * (acc[2 + j] * gs));
-        a16[size_t(pair_at(pl, direct, pp + col)) * F + f0 + g] = f32_to_f16_bits(a);
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * c + j;
+        if (col < np && f0 + g < F) {
+          const float a = round_bf(siluf_(acc[j] * gs) * (acc[2 + j] * gs));
+          a16[size_t(pair_at(pl, direct, pp + col)) * F + f0 + g] = f32_to_f16_bits(a);
+        }
       }
     }
+    if (KS > 1) __syncthreads();   // the reduction buffer is free for the next pass
   }
 }
 
-// grid (ceil(H / 128), max active experts); a warp takes 16 rows h; y[pair][h] in FP32; the
-// last CTA of each 128-row column combines its rows for every token, slots in order.
+// grid (ceil(H / (128 / KS)), max active experts); a row block is 16 rows h, KS warps per row
+// block; y[pair][h] in FP32; the last CTA of each column of rows combines them for every token,
+// slots in order.
+template <int KS>
 __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
     const uint16_t* __restrict__ a16, beam_nvfp4_experts W, int H, int F, MoePlan pl,
     const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
@@ -651,13 +683,16 @@ __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
     float* __restrict__ y, uint16_t* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float red[8][32][4];
   const int na = direct != nullptr ? k : *pl.n_active;
   const int ai = blockIdx.y;
   if (ai >= max(na, 1)) return;   // uniform over the CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int h0 = blockIdx.x * kMmaRowsDown + warp * 16;
+  constexpr int kRows = 128 / KS;   // rows h per CTA
+  const int ks = warp % KS;
+  const int h0 = blockIdx.x * kRows + (warp / KS) * 16;
   ExpertSlot es;
-  if (ai < na && h0 < H && expert_slot(pl, direct, E, ai, es)) {
+  if (ai < na && expert_slot(pl, direct, E, ai, es)) {   // uniform over the CTA
     const size_t r0 = size_t(es.e) * H + min(h0 + g, H - 1);
     const size_t r1 = size_t(es.e) * H + min(h0 + g + 8, H - 1);
     const uint8_t* w0 = W.down + r0 * (F / 2) + 16 * c;
@@ -665,21 +700,25 @@ __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
     const uint8_t* s0 = W.down_scale + r0 * (F / 16) + 2 * c;
     const uint8_t* s1 = W.down_scale + r1 * (F / 16) + 2 * c;
     const float gs = W.down_global[es.e];
+    const int nb = F >> 7, bb = ks * nb / KS, be = (ks + 1) * nb / KS;
     for (int pp = es.p0; pp < es.p1; pp += 8) {
       const int np = min(8, es.p1 - pp);
       const bool tok = g < np;
       const uint16_t* xr = a16 + size_t(tok ? pair_at(pl, direct, pp + g) : 0) * F + 32 * c;
       float acc[4];
-      fp4_rows_mma(w0, w1, s0, s1, xr, tok, F, acc);
+      fp4_rows_mma(w0, w1, s0, s1, xr, tok, bb, be, acc);
+      if (fp4_reduce_ks<KS>(acc, red)) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int col = 2 * c + j;
-        if (col < np) {
-          const size_t yo = size_t(pair_at(pl, direct, pp + col)) * H;
-          if (h0 + g < H) y[yo + h0 + g] = acc[j] * gs;
-          if (h0 + g + 8 < H) y[yo + h0 + g + 8] = acc[2 + j] * gs;
+        for (int j = 0; j < 2; ++j) {
+          const int col = 2 * c + j;
+          if (col < np) {
+            const size_t yo = size_t(pair_at(pl, direct, pp + col)) * H;
+            if (h0 + g < H) y[yo + h0 + g] = acc[j] * gs;
+            if (h0 + g + 8 < H) y[yo + h0 + g + 8] = acc[2 + j] * gs;
+          }
         }
       }
+      if (KS > 1) __syncthreads();   // the reduction buffer is free for the next pass
     }
   }
   __shared__ int s_last;
@@ -693,8 +732,8 @@ __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int hb = blockIdx.x * kMmaRowsDown;
-  const int nh = min(kMmaRowsDown, H - hb);
+  const int hb = blockIdx.x * kRows;
+  const int nh = min(kRows, H - hb);
   for (int i = threadIdx.x; i < T * nh; i += blockDim.x) {
     const int t = i / nh, h = hb + (i - t * nh);
     float s = 0.f;
@@ -977,15 +1016,23 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
   const bool direct = T == 1;
   const int32_t* dix = direct ? topk_idx : nullptr;
   const int na = direct ? k : (P < E ? P : E);
-  const int n_cnt = (H + kMmaRowsDown - 1) / kMmaRowsDown;
+  const bool split = T <= kFp4KSMaxT;
+  const int rows_down = split ? 32 : 128, units_up = split ? 16 : 64;
+  const int n_cnt = (H + rows_down - 1) / rows_down;
   const int n = T * H;
   launch_pdl(fp4_prep_kernel, dim3((max(n, n_cnt) + 255) / 256), dim3(256), 0, st, u, n, u16, cnt,
              n_cnt);
   if (!direct)
     launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
-  launch_pdl(moe_gate_up_fp4_kernel, dim3((F + 63) / 64, na), dim3(256), 0, st, u16, *w, H, F, k,
-             pl, dix, E, a16);
-  launch_pdl(moe_down_fp4_kernel, dim3(n_cnt, na), dim3(256), 0, st, a16, *w, H, F, pl, dix,
-             topk_idx, topk_w, T, k, E, cnt, y, out);
+  const dim3 gu((F + units_up - 1) / units_up, na), gd(n_cnt, na);
+  if (split) {
+    launch_pdl(moe_gate_up_fp4_kernel<4>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
+    launch_pdl(moe_down_fp4_kernel<4>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+               topk_w, T, k, E, cnt, y, out);
+  } else {
+    launch_pdl(moe_gate_up_fp4_kernel<1>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
+    launch_pdl(moe_down_fp4_kernel<1>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+               topk_w, T, k, E, cnt, y, out);
+  }
   return launch_status();
 }

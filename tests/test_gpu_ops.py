@@ -369,12 +369,13 @@ def _nvfp4_experts(shape, used, seed):
     return full, experts
 
 
-@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 13, None),
-                                            (TINY, 31, 6), (BEAM, 1, None), (BEAM, 2, None),
-                                            (BEAM, 8, None)])
+@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 5, None),
+                                            (TINY, 13, None), (TINY, 31, 6), (BEAM, 1, None),
+                                            (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None)])
 def test_moe_nvfp4(shape, T, n_used):
     """NVFP4 expert weights (e2m1 codes, e4m3 block scales, FP32 matrix scales): mma.sync f16
-    products of the dequantised weights, the selected experts only; T=31 over 6 experts gives
+    products of the dequantised weights, the selected experts only; up to 4 tokens four warps
+    split each row block's K (T=4 and T=5 sit on either side); T=31 over 6 experts gives
     experts more than 8 pairs (several passes)."""
     seed = 91 + T
     cfg = cfg_of(shape)
