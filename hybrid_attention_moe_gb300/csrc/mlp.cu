@@ -595,7 +595,7 @@ __device__ __forceinline__ void fp4_rows_mma(const uint8_t* w0, const uint8_t* w
 // their partial tiles in order through shared memory: a warp's chain of dependent weight loads
 // is KS times shorter and the grid has KS times the CTAs, which few tokens (few active experts,
 // a grid under one wave) need; with many tokens the grid is large enough without it.
-constexpr int kFp4KSMaxT = 4;   // KS = 4 up to this many tokens, else 1
+constexpr int kFp4KSMaxT = 4;   // K split up to this many tokens, else KS = 1
 template <int KS>
 __device__ __forceinline__ bool fp4_reduce_ks(float (&acc)[4], float (*red)[32][4]) {
   if (KS == 1) return true;
@@ -1016,8 +1016,10 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
   const bool direct = T == 1;
   const int32_t* dix = direct ? topk_idx : nullptr;
   const int na = direct ? k : (P < E ? P : E);
+  // up to 4 tokens the gate/up rows are split four ways; the down rows (half as many K blocks)
+  // four ways for one token, two ways for 2-4 (measured fastest each)
   const bool split = T <= kFp4KSMaxT;
-  const int rows_down = split ? 32 : 128, units_up = split ? 16 : 64;
+  const int rows_down = !split ? 128 : T == 1 ? 32 : 64, units_up = split ? 16 : 64;
   const int n_cnt = (H + rows_down - 1) / rows_down;
   const int n = T * H;
   launch_pdl(fp4_prep_kernel, dim3((max(n, n_cnt) + 255) / 256), dim3(256), 0, st, u, n, u16, cnt,
@@ -1027,8 +1029,12 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
   const dim3 gu((F + units_up - 1) / units_up, na), gd(n_cnt, na);
   if (split) {
     launch_pdl(moe_gate_up_fp4_kernel<4>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
-    launch_pdl(moe_down_fp4_kernel<4>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
-               topk_w, T, k, E, cnt, y, out);
+    if (T == 1)
+      launch_pdl(moe_down_fp4_kernel<4>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+                 topk_w, T, k, E, cnt, y, out);
+    else
+      launch_pdl(moe_down_fp4_kernel<2>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+                 topk_w, T, k, E, cnt, y, out);
   } else {
     launch_pdl(moe_gate_up_fp4_kernel<1>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
     launch_pdl(moe_down_fp4_kernel<1>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
