@@ -25,7 +25,7 @@ from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32, nvfp4_dequant
 __all__ = [
     "rmsnorm", "boundary_norm", "rope_inv_freq", "rope", "ssmax_scale", "KVCache",
     "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "moe_nvfp4", "dense_mlp",
-    "is_nope_layer", "layer_forward", "stack_forward", "kv_values_per_token",
+    "is_nope_layer", "layer_forward", "stack_forward", "kv_values_per_token", "lm_head",
 ]
 
 
@@ -351,10 +351,27 @@ def layer_forward(cfg, l, W, h, u, cache, seq_id, pos, next_pre, trace=None):
 
 def stack_forward(cfg, weights, caches, e, seq_id, pos, trace=None):
     """Truncated stack over layers 0..L-1 for the tokens (seq_id, pos) with embeddings e.
-    Returns h after the last residual addition (no final norm: the LM head is out of scope)."""
+    Returns h after the last residual addition (the final norm belongs to the LM head's
+    input: boundary_norm(None, h, None, w_final, 1, eps)[1])."""
     h, u = boundary_norm(None, e, None, weights[0]["attn_pre"], 1, cfg.eps)
     L = cfg.n_layers
     for l in range(L):
         nxt = weights[l + 1]["attn_pre"] if l + 1 < L else None
         h, u = layer_forward(cfg, l, weights[l], h, u, caches[l], seq_id, pos, nxt, trace)
     return h
+
+
+# ---------------------------------------------------------------------------------------
+# LM head with the logit softcap  (AREX feed article on the Day-0 support, output side)
+# ---------------------------------------------------------------------------------------
+
+def lm_head(u, w_lm, softcap=30.0):
+    """Logits of the final-normed hidden state u [T][H] over the vocabulary rows w_lm [V][H]:
+    z = u w_lm^T, then logits = c * tanh(z / c) with c = softcap (30 on the page; c <= 0: no
+    cap). Float64 math, FP32 result. READING: the head's input u is the final pre-norm
+    RMSNorm_final(h) of the last residual stream, rounded to bf16 like every other pre-norm;
+    the pages print neither the final norm nor the vocabulary size."""
+    z = np.asarray(u, dtype=np.float64) @ np.asarray(w_lm, dtype=np.float64).T
+    if softcap > 0:
+        z = softcap * np.tanh(z / softcap)
+    return f32(z)

@@ -450,3 +450,41 @@ def test_stack_prefill_equals_token_by_token_decode():
     assert np.allclose(h_all, ref, rtol=2 ** -7, atol=0) and np.mean(h_all == ref) > 0.99
     rms = np.sqrt(np.mean(h_all ** 2, axis=-1))
     assert np.all((rms > 0.5) & (rms < 2.0))          # the depth-scaled stream stays O(1)
+
+
+# ------------------------------------------------------------------------- LM head ----
+
+def test_lm_head_softcap_closed_forms():
+    """The page's cap c = 30 at closed-form points: tanh(ln 2) = 3/5 and tanh(ln 3) = 4/5 give
+    18 and 24 at z = c ln 2 and c ln 3; the cap is odd, saturates at +-c, is the identity
+    near 0 and keeps the order of the logits. A one-hot u makes z the first column of w_lm."""
+    c = GOLD["logit_softcap"]["value"]
+    zs = np.array([c * math.log(2), c * math.log(3), -c * math.log(2), 0.0, 1e-3, 1e4, -1e4])
+    w = np.zeros((len(zs), 4))
+    w[:, 0] = zs
+    u = np.array([[1.0, 0.0, 0.0, 0.0]])
+    got = O.lm_head(u, w, c)[0]
+    want = [GOLD["softcap_at_30ln2"]["value"], GOLD["softcap_at_30ln3"]["value"],
+            -GOLD["softcap_at_30ln2"]["value"], 0.0, 1e-3, c, -c]
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-9)
+    z = rng(41).standard_normal(1000) * 40.0
+    w = np.zeros((1000, 4))
+    w[:, 0] = z
+    y = O.lm_head(u, w, c)[0]
+    assert np.all(np.abs(y) <= c)
+    assert np.all(np.diff(y[np.argsort(z)]) >= 0)
+
+
+def test_lm_head_projection_brute_force():
+    """z[t][v] = sum_h u[t][h] w_lm[v][h] by explicit loops on small integers (exact), on a
+    case with T, H and V all different, so a transposed operand cannot pass; softcap <= 0
+    leaves z as it is."""
+    r = rng(40)
+    T, H, V = 3, 5, 7
+    u = r.integers(-3, 4, (T, H)).astype(float)
+    w = r.integers(-3, 4, (V, H)).astype(float)
+    z = O.lm_head(u, w, 0.0)
+    assert z.shape == (T, V)
+    for t in range(T):
+        for v in range(V):
+            assert z[t, v] == sum(u[t, h] * w[v, h] for h in range(H))
