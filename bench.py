@@ -413,6 +413,7 @@ def run_ours(args, rank, world, device):
             "gemm_calls_frac": round(gemm_fl / (gemm_us * 1e-6) / 1e12 / tf_peak, 4),
             "peak": tf_peak, "peak_kind": tf_kind}
 
+    head = time_lm_head(args, wl, b, stream) if args.lm_head_vocab > 0 else None
     e2e = run_e2e(args, wl, step_graph, stream, world)
     res = {
         "metric": METRIC,
@@ -447,11 +448,57 @@ def run_ours(args, rank, world, device):
         "per_call_replay_ms_per_step": None if evented_ms is None else round(evented_ms, 4),
         "e2e": e2e,
         "gpu_launches": launches_step * args.steps,
+        **({"lm_head": head} if head is not None else {}),
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, wl, budget_s=args.cpu_budget)
     return res
+
+
+def time_lm_head(args, wl, b, stream):
+    """The LM head after the stack, timed beside the step (its own graph of K calls, CUDA
+    events on the launching stream): the final norm of the last residual stream h, then
+    beam_lm_head over a vocabulary of args.lm_head_vocab rows with the 30*tanh(z/30) cap.
+    Algorithmic bytes per call: the vocabulary rows (V x H bf16), the tokens' u and h, and one
+    write of the FP32 logits."""
+    B = wl.B
+    V, H, T = args.lm_head_vocab, wl.shape.hidden, wl.tokens
+    head = synth.lm_head_weights(wl.shape, V, args.seed, device=wl.device)
+    u = torch.empty((T, H), dtype=torch.bfloat16, device=wl.device)
+    logits = torch.empty((T, V), dtype=torch.float32, device=wl.device)
+    eps = wl.stack.cfgs[0].eps
+
+    def call():
+        B.beam_boundary_norm(None, b["h"], u, None, head["final_norm"], 1, eps)
+        B.beam_lm_head(u, head["w_lm"], logits, softcap=30.0)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(args.steps):
+            call()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    us = t0.elapsed_time(t1) * 1000.0 / args.steps
+    nbytes = V * H * 2 + T * H * 2 * 2 + T * V * 4
+    hbm, hbm_kind = peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"vocab": V, "tokens": T, "softcap": 30.0, "us_per_call": round(us, 2),
+            "bytes_per_call": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": hbm,
+            "frac": round(gbs / hbm, 4), "peak_kind": hbm_kind,
+            "calls": "final norm + beam_lm_head (projection, then the softcap pass)"}
 
 
 def tensor_peak():
@@ -631,10 +678,15 @@ def main():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--experts", default="bf16", choices=["bf16", "nvfp4"],
                     help="expert weight format of the MoE layers (decode only for nvfp4)")
+    ap.add_argument("--lm-head-vocab", type=int, default=0,
+                    help="also time the LM head after the stack over this many vocabulary rows "
+                         "(beside the step; 0: off)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.lm_head_vocab and args.workload == "stack_prefill":
+        ap.error("--lm-head-vocab is timed for decode workloads")
     if args.experts == "nvfp4" and args.workload == "stack_prefill":
         ap.error("--experts nvfp4 is a decode format here (beam_moe_nvfp4 takes up to 31 tokens)")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -63,6 +63,7 @@ _SIGS = {
     "beam_last_cuda_error": [],
     "beam_gemm_bf16": [_P, _I, _I, _I, _P, _I, _I, _P, _I, _I, _P],
     "beam_route_noalloc": [_P, _P, _P, _P, _I, _P, _P, _P],
+    "beam_lm_head": [_P, _P, _I, _I, _I, _F, _P, _P],
 }
 _RES = {"beam_workspace_bytes": _Z, "beam_kv_cache_bytes": _Z,
         "beam_status_string": ctypes.c_char_p, "beam_launch_count": ctypes.c_uint64,
@@ -267,6 +268,15 @@ def beam_gemm_bf16(a, b, c, stream=None):
     _check(lib().beam_gemm_bf16(_ptr(a), M, K, a.stride(0), _ptr(b), N, b.stride(0), _ptr(c),
                                 c.stride(0), int(c.dtype == torch.bfloat16), _stream(stream)),
            "beam_gemm_bf16")
+
+
+def beam_lm_head(u, w_lm, logits, softcap=30.0, stream=None):
+    """logits [T][V] fp32 = softcap * tanh((u w_lm^T) / softcap); u [T][H] bf16 (final-normed),
+    w_lm [V][H] bf16; softcap <= 0: no cap."""
+    T, H = u.shape
+    V = w_lm.shape[0]
+    _check(lib().beam_lm_head(_ptr(u), _ptr(w_lm), T, H, V, float(softcap), _ptr(logits),
+                              _stream(stream)), "beam_lm_head")
 
 
 def beam_route_noalloc(cfg: LayerCfg, u, w_router, corr_bias, topk_idx, topk_w, stream=None):

@@ -241,6 +241,18 @@ beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16* u,
 beam_status beam_gemm_bf16(const beam_bf16* A, int M, int K, int lda, const beam_bf16* B, int N,
                            int ldb, void* C, int ldc, int out_bf16, beam_stream_t stream);
 
+/* LM head with the logit softcap (AREX feed article on vLLM's Day-0 support of
+ * Reflection-Beam-1.0, paragraph on the output side: logits pass through 30 * tanh(z / 30)):
+ *   z[t][v] = u[t] . w_lm[v] (FP32 accumulation),  logits[t][v] = c * tanh(z[t][v] / c),
+ * c = softcap (30 for Beam; softcap <= 0 leaves z uncapped).
+ *  u (device) [T][H] bf16: the final-normed hidden state (beam_boundary_norm's pre-norm output
+ *  with the final norm's gains after the last layer);  w_lm (device) [V][H] bf16, the
+ *  vocabulary rows;  logits (device) [T][V] fp32. u, w_lm and logits 16-byte aligned, H a
+ *  multiple of 8; otherwise (or a NaN softcap) BEAM_ERR_INVALID_ARG and nothing is launched.
+ *  No workspace; T = 0 launches nothing. */
+beam_status beam_lm_head(const beam_bf16* u, const beam_bf16* w_lm, int T, int H, int V,
+                         float softcap, float* logits, beam_stream_t stream);
+
 /* Workspace bytes that every call above needs for T tokens and positions up to max_pos. */
 size_t beam_workspace_bytes(const beam_layer_cfg* cfg, int T, int max_pos);
 

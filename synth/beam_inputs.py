@@ -174,6 +174,15 @@ def dense_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
     }
 
 
+def lm_head_weights(shape: BeamShape, vocab: int, seed: int = 0, device="cpu", std=0.02):
+    """Final norm gains [H] (N(1, 0.1), like the other norms) and vocabulary rows [V][H]."""
+    H = shape.hidden
+    return {
+        "final_norm": normal((H,), 0.1, 1.0, seed, ("final_norm",), device),
+        "w_lm": normal((vocab, H), std, 0.0, seed, ("lm_head",), device),
+    }
+
+
 def layer_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu",
                   dense: bool | None = None, with_experts: bool = True):
     """All weights of one layer as a dict of tensors (row-major [out][in])."""
