@@ -8,6 +8,7 @@ warm-up launches and capture one or a few real ones. Usage:
 
 Cases: moe_decode (--tokens tokens, default 1, each over 8 selected experts of a 32-expert
 pool), moe_decode_nvfp4 (the same with NVFP4 expert weights), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
+lm_head_decode (the LM head with the logit softcap over 32768 vocabulary rows, --tokens tokens),
 qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (100K keys),
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
 moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts), attn_nope_prefill
@@ -69,6 +70,13 @@ def main():
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_moe_nvfp4(cs, u, idx, w, wq, out, ws)  # noqa: E731
+    elif c == "lm_head_decode":
+        # 32768 vocabulary rows at hidden 5120: 336 MB of BF16 weights (more than L2)
+        T, V = args.tokens, 32768
+        Wh = synth.lm_head_weights(shape, V, 0, device=dev)
+        u = synth.activations(T, H, 0, "u_final", dev)
+        logits = torch.empty((T, V), dtype=torch.float32, device=dev)
+        fn = lambda: B.beam_lm_head(u, Wh["w_lm"], logits, softcap=30.0)  # noqa: E731
     elif c == "dense_decode":
         T = args.tokens
         Wd = synth.dense_weights(shape, 0, 0, device=dev)
