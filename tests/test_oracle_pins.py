@@ -416,6 +416,12 @@ def test_shapes_reproduce_page_parameter_counts():
     active = 52 * attn + 3 * dense + 49 * (c.topk * expert + router)
     assert 498e9 < total < GOLD["total_params_b"]["value"] * 1e9
     assert 21e9 < active < GOLD["active_params_b"]["value"] * 1e9
+    # the LM head's vocabulary reading: 201,088 rows (the vocabulary of the Harmony response
+    # format the AREX feed article on the Day-0 support names), one matrix shared by the
+    # embedding and the head, closes both gaps to the printed figures
+    vocab = 201_088 * H
+    assert round((total + vocab) / 1e9) == GOLD["total_params_b"]["value"]
+    assert round((active + vocab) / 1e9) == GOLD["active_params_b"]["value"]
 
 
 # ------------------------------------------------------------------ stack ----
