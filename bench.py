@@ -54,6 +54,32 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x, on every rank (x itself for one rank): a step
+    time taken on each rank becomes the slowest rank's."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job(ms_step, tokens_per_rank, world, n_layers, prefill):
+    """(value, unit) over all ranks: prefill tokens/s = every rank's tokens over the slowest
+    rank's step; decode µs/token/layer = that step over every rank's tokens and the layers."""
+    if prefill:
+        return tokens_per_rank * world / (ms_step * 1e-3), "tokens/s"
+    return ms_step * 1000.0 / (tokens_per_rank * world) / n_layers, "us/token/layer"
+
+
+def emit(res, rank):
+    """Rank 0 prints the JSON line; the other ranks print nothing. Returns whether it printed."""
+    if rank != 0 or res is None:
+        return False
+    print(json.dumps(res), flush=True)
+    return True
+
+
 def is_nope(l, L):
     return (l + 1) % 6 == 0 or l == L - 1
 
@@ -363,10 +389,7 @@ def run_ours(args, rank, world, device):
         for i, name in enumerate(names):
             per_call_us[name] = 1000.0 * float(np.mean(
                 [events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps)]))
-    if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, device)
 
     # experts touched by the routing of the last step (the idx buffer holds the last MoE
     # layer's selection; the others are taken to touch as many)
@@ -377,8 +400,7 @@ def run_ours(args, rank, world, device):
         for l in moe_layers:
             touched[l] = n
     algo_bytes, per_layer = wl.algorithmic_bytes(touched)
-    us_per_token_layer = ms_step * 1000.0 / (wl.tokens * world) / len(wl.layers)
-    tokens_per_s = wl.tokens * world / (ms_step * 1e-3)
+    value, unit = whole_job(ms_step, wl.tokens, world, len(wl.layers), wl.prefill)
     hbm, hbm_kind = peaks()
     layer_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
 
@@ -414,11 +436,11 @@ def run_ours(args, rank, world, device):
             "peak": tf_peak, "peak_kind": tf_kind}
 
     head = time_lm_head(args, wl, b, stream) if args.lm_head_vocab > 0 else None
-    e2e = run_e2e(args, wl, step_graph, stream, world)
+    e2e = run_e2e(args, wl, step_graph, stream, world, device)
     res = {
         "metric": METRIC,
-        "value": round(tokens_per_s, 1) if wl.prefill else round(us_per_token_layer, 3),
-        "unit": "tokens/s" if wl.prefill else "us/token/layer",
+        "value": round(value, 1 if wl.prefill else 3),
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -529,7 +551,7 @@ def dominant_bytes(wl, name, touched):
     return 2 * wl.batch * BEAM.hidden * 2, "norm"
 
 
-def run_e2e(args, wl, step_graph, stream, world):
+def run_e2e(args, wl, step_graph, stream, world, device):
     """Same step with the tokens' hidden state copied in from pinned host memory and the
     output h copied back, both inside the timed region."""
     b = wl.stack.buffers(wl.tokens)
@@ -537,6 +559,9 @@ def run_e2e(args, wl, step_graph, stream, world):
     out_host = torch.empty_like(h_host).pin_memory()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         t0.record(stream)
@@ -546,13 +571,13 @@ def run_e2e(args, wl, step_graph, stream, world):
             out_host.copy_(b["h"], non_blocking=True)
         t1.record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, device)
     nbytes = h_host.numel() * h_host.element_size()
-    if wl.prefill:
-        return {"value": round(wl.tokens * world / (ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
-    return {"value": round(ms * 1000.0 / (wl.tokens * world) / len(wl.layers), 3),
-            "unit": "us/token/layer", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+    value, unit = whole_job(ms, wl.tokens, world, len(wl.layers), wl.prefill)
+    return {"value": round(value, 1 if wl.prefill else 3), "unit": unit,
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
 
 
 # ------------------------------------------------------------------------ oracle arm ----
@@ -702,8 +727,7 @@ def main():
         res = run_reference(args, rank, world, device)
     else:
         res = run_ours(args, rank, world, device)
-    if rank == 0 and res is not None:
-        print(json.dumps(res), flush=True)
+    emit(res, rank)
     if world > 1:
         torch.distributed.destroy_process_group()
 
