@@ -536,7 +536,8 @@ def dominant_bytes(wl, name, touched):
     """Algorithmic bytes of one call of the step (weights and cache it must read once)."""
     l = int(name.split(".")[0][1:])
     if name.endswith(".moe"):
-        return touched[l] * expert_bytes(BEAM, wl.nvfp4), ("moe_decode_nvfp4" if wl.nvfp4 else "moe_decode")
+        key = ("moe_decode_nvfp4" if wl.nvfp4 else "moe_decode") + f"_t{wl.tokens}"
+        return touched[l] * expert_bytes(BEAM, wl.nvfp4), key
     if name.endswith(".attn"):
         keys = wl.ctx + 1 if is_nope(l, BEAM.n_layers) else min(BEAM.window, wl.ctx + 1)
         elem = 1 if wl.fp8 else 2
