@@ -60,3 +60,34 @@ def test_host_only_entry_points(lib):
 def test_library_is_built_for_sm_103a(lib):
     from hybrid_attention_moe_gb300 import build as b
     assert "arch=compute_103a,code=sm_103a" in " ".join(b.ARCH)
+
+
+def test_argument_checks_answer_before_any_launch(lib):
+    """beam_lm_head and beam_moe_nvfp4 reject bad arguments (and return at once for T = 0)
+    before touching the device: every call below returns from the host-side checks, so the
+    16-byte-aligned placeholder addresses are never dereferenced."""
+    import ctypes
+    import synth
+    from hybrid_attention_moe_gb300 import beam as B
+    P = ctypes.c_void_p
+    a, b, c = P(0x10000), P(0x20000), P(0x30000)
+    # LM head: u, w_lm, T, H, V, softcap, logits, stream
+    assert lib.beam_lm_head(None, b, 1, 256, 100, 30.0, c, None) == 1
+    assert lib.beam_lm_head(a, b, 1, 260, 100, 30.0, c, None) == 1          # H % 8 != 0
+    assert lib.beam_lm_head(a, b, 1, 256, 100, float("nan"), c, None) == 1
+    assert lib.beam_lm_head(P(0x10008), b, 1, 256, 100, 30.0, c, None) == 1  # misaligned u
+    assert lib.beam_lm_head(a, b, 0, 256, 100, 30.0, c, None) == 0          # T = 0: nothing
+    # NVFP4 experts: decode sizes only, H and d_ff multiples of 128
+    cfg = B.LayerCfg.from_shape(synth.BEAM, B.BEAM_ATTN_SWA_ROPE).c()
+    ex = B.NvFp4ExpertsC(a, a, a, a, a, a)
+
+    def moe(T, cfg=cfg, ex=ex):
+        return lib.beam_moe_nvfp4(ctypes.byref(cfg), a, b, c, ctypes.byref(ex), T, a, a, 1 << 20,
+                                  None)
+    assert moe(32) == 2 and moe(100) == 2       # from 32 tokens: BEAM_ERR_UNSUPPORTED
+    assert moe(0) == 0
+    odd = B.LayerCfg.from_shape(synth.BEAM, B.BEAM_ATTN_SWA_ROPE).c()
+    odd.hidden = 5120 + 64
+    assert moe(1, cfg=odd) == 2
+    bad = B.NvFp4ExpertsC(a, None, a, a, a, a)
+    assert moe(1, ex=bad) == 1
