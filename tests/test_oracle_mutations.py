@@ -1,0 +1,146 @@
+"""The oracle's pins are strong enough to catch plausible slips: each case below plants one
+mistake in a copy of the oracle's source (on the CPU, in memory; the committed oracle is not
+touched) and checks that at least one of the named pins fails on the mutant. A slip that no
+pin catches would be a gap in the pins."""
+import os
+import types
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC_PATH = os.path.join(os.path.dirname(oracle.__file__), "beam_oracle.py")
+SRC = open(SRC_PATH).read()
+
+# (slip, text in the oracle, planted text, pins that must catch it)
+MUTATIONS = [
+    ("RMSNorm drops its gain",
+     "return x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)",
+     "return x / np.sqrt(ms + eps)",
+     ["test_rmsnorm_unit_rms_and_scale_invariance"]),
+    ("RMSNorm sums instead of averaging",
+     "ms = np.mean(x * x, axis=-1, keepdims=True)",
+     "ms = np.sum(x * x, axis=-1, keepdims=True)",
+     ["test_rmsnorm_unit_rms_and_scale_invariance"]),
+    ("residual coefficients swapped",
+     "h = bf16_round(np.sqrt((n - 1.0) / n) * h + y / np.sqrt(n))",
+     "h = bf16_round(np.sqrt(1.0 / n) * h + y * np.sqrt((n - 1.0) / n))",
+     ["test_residual_first_term_and_coefficients", ("test_depth_scaled_residual_keeps_unit_variance", 3)]),
+    ("residual adds without the depth scaling",
+     "h = bf16_round(np.sqrt((n - 1.0) / n) * h + y / np.sqrt(n))",
+     "h = bf16_round(h + y / np.sqrt(n))",
+     [("test_depth_scaled_residual_keeps_unit_variance", 10), "test_residual_first_term_and_coefficients"]),
+    ("sublayer output not post-normed",
+     "y = bf16_round(rmsnorm(x, w_post, eps))",
+     "y = bf16_round(x)",
+     ["test_residual_first_term_and_coefficients"]),
+    ("RoPE rotation sign flipped",
+     "x2 * c + x1 * s], axis=-1)",
+     "x2 * c - x1 * s], axis=-1)",
+     ["test_rope_closed_forms", "test_rope_invariants"]),
+    ("RoPE frequency exponent halved",
+     "return np.power(float(theta), -2.0 * i / D)",
+     "return np.power(float(theta), -1.0 * i / D)",
+     ["test_rope_closed_forms"]),
+    ("RoPE angle from p instead of p - 1",
+     "m = (pos - 1)[:, None]",
+     "m = pos[:, None]",
+     ["test_qkv_gate_rope_relative_position", "test_rope_closed_forms"]),
+    ("SSMax exponent sign",
+     "return np.power(1.0 + np.asarray(p, dtype=np.float64) / base, expo)",
+     "return np.power(1.0 + np.asarray(p, dtype=np.float64) / base, -expo)",
+     ["test_ssmax_values"]),
+    ("SSMax also scales k",
+     "qn = qn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]",
+     "qn = qn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]\n"
+     "        kn = kn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]",
+     ["test_qkv_gate_nope_scales_q_only"]),
+    ("cache slot p instead of p - 1",
+     "return (np.asarray(p) - 1) % self.capacity",
+     "return np.asarray(p) % self.capacity",
+     ["test_kv_cache_ring_and_fp8_roundtrip"]),
+    ("window one key too wide",
+     "lo = 1 if cache.window == 0 else max(1, p - cache.window + 1)",
+     "lo = 1 if cache.window == 0 else max(1, p - cache.window)",
+     ["test_attention_special_cases", "test_attention_matches_torch_sdpa"]),
+    ("softmax scale 1/D instead of 1/sqrt(D)",
+     "logits = qh @ K[hk, a:b].T / np.sqrt(D)",
+     "logits = qh @ K[hk, a:b].T / D",
+     ["test_attention_matches_torch_sdpa"]),
+    ("query attends to all but itself",
+     "a, b = lo - lo_all, p - lo_all + 1",
+     "a, b = lo - lo_all, max(p - lo_all, lo - lo_all + 1)",
+     ["test_attention_matches_torch_sdpa", "test_attention_special_cases"]),
+    ("GQA heads interleaved instead of grouped",
+     "qh = q[t, hk * grp:(hk + 1) * grp]",
+     "qh = q[t, hk::Hkv]",
+     ["test_attention_gqa_head_mapping_and_gate", "test_attention_matches_torch_sdpa"]),
+    ("gate sigmoid sign flipped",
+     "gate = 1.0 / (1.0 + np.exp(-(np.asarray(g, dtype=np.float64) + gb)))",
+     "gate = 1.0 / (1.0 + np.exp(np.asarray(g, dtype=np.float64) + gb))",
+     ["test_attention_gqa_head_mapping_and_gate"]),
+    ("group score from the best expert only",
+     "gscore = (top2[:, 0] + top2[:, 1]).astype(np.float32)",
+     "gscore = (top2[:, 0] + top2[:, 0]).astype(np.float32)",
+     ["test_route_matches_brute_force_tiny", "test_route_group_choice_full_width"]),
+    ("routing weights from the biased scores",
+     "ssel = s[t, sel].astype(np.float64)",
+     "ssel = b[t, sel].astype(np.float64)",
+     ["test_route_weights_use_unbiased_scores"]),
+    ("routing weights without the 2.5 scale",
+     "w[t] = ssel / ssel.sum() * cfg.route_scale",
+     "w[t] = ssel / ssel.sum()",
+     ["test_route_weights_use_unbiased_scores", "test_route_matches_brute_force_tiny"]),
+    ("expert SwiGLU gate and up swapped",
+     "return bf16_round(silu(gu[:F]) * gu[F:])",
+     "return bf16_round(gu[:F] * silu(gu[F:]))",
+     ["test_moe_equals_dense_with_stacked_experts"]),
+    ("combine ignores the routing weights",
+     "acc += float(w[t, j]) * y",
+     "acc += y",
+     ["test_moe_combine_is_weighted_sum"]),
+    ("NoPE layers every 6th from layer 0",
+     "return (layer + 1) % 6 == 0 or layer == n_layers - 1",
+     "return layer % 6 == 0 or layer == n_layers - 1",
+     ["test_layer_count_gives_104_boundaries"]),
+    ("softcap without the division by c",
+     "z = softcap * np.tanh(z / softcap)",
+     "z = softcap * np.tanh(z)",
+     ["test_lm_head_softcap_closed_forms"]),
+    ("LM head projection transposed",
+     "z = np.asarray(u, dtype=np.float64) @ np.asarray(w_lm, dtype=np.float64).T",
+     "z = (np.asarray(w_lm, dtype=np.float64) @ np.asarray(u, dtype=np.float64).T).T[:, ::-1]",
+     ["test_lm_head_projection_brute_force"]),
+]
+
+
+def mutant(old, new):
+    assert SRC.count(old) == 1, f"mutation site not unique: {old!r}"
+    m = types.ModuleType("oracle_mutant")
+    m.__package__ = "oracle"
+    m.__file__ = SRC_PATH
+    exec(compile(SRC.replace(old, new), SRC_PATH + " (mutant)", "exec"), m.__dict__)
+    return m
+
+
+def fails(pin):
+    name, args = (pin, ()) if isinstance(pin, str) else (pin[0], pin[1:])
+    try:
+        getattr(pins, name)(*args)
+    except Exception:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("slip,old,new,catchers", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_slip(monkeypatch, slip, old, new, catchers):
+    monkeypatch.setattr(pins, "O", mutant(old, new))
+    assert any(fails(p) for p in catchers), f"no pin caught: {slip}"
+
+
+def test_unmutated_oracle_passes_the_same_pins():
+    """Control: every pin named above passes on the oracle as committed."""
+    names = {p if isinstance(p, str) else p for m in MUTATIONS for p in m[3]}
+    for p in sorted(names, key=str):
+        assert not fails(p), p

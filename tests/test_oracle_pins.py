@@ -186,6 +186,9 @@ def test_kv_cache_ring_and_fp8_roundtrip():
     kk, vv = c.load(0, np.arange(4, 8))
     assert np.allclose(kk[0, :, 0], bf16_round(np.arange(4, 8) + 0.001))
     assert np.array_equal(vv[0, :, 0], -np.arange(4, 8))
+    # the layout the C ABI documents: 1-based position p lives in slot (p - 1) % capacity, so
+    # positions 4..7 sit in slots 3, 0, 1, 2 of the raw array
+    assert np.array_equal(c.v[0, 0, :, 0], [-5.0, -6.0, -7.0, -4.0])
     c8 = O.KVCache(np.zeros((1, 1, 4, D), np.uint8), np.zeros((1, 1, 4, D), np.uint8), "fp8",
                    k_scale=0.0371, v_scale=2.0)
     x = rng(10).standard_normal((1, D))
