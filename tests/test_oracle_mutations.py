@@ -8,6 +8,7 @@ import types
 import pytest
 
 import oracle
+import test_oracle_codecs as codec_pins
 import test_oracle_pins as pins
 
 SRC_PATH = os.path.join(os.path.dirname(oracle.__file__), "beam_oracle.py")
@@ -55,7 +56,7 @@ MUTATIONS = [
      "qn = qn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]",
      "qn = qn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]\n"
      "        kn = kn * ssmax_scale(pos, cfg.ssmax_base, cfg.ssmax_exp)[:, None, None]",
-     ["test_qkv_gate_nope_scales_q_only"]),
+     ["test_qkv_gate_packed_row_order", "test_qkv_gate_nope_scales_q_only"]),
     ("cache slot p instead of p - 1",
      "return (np.asarray(p) - 1) % self.capacity",
      "return np.asarray(p) % self.capacity",
@@ -104,6 +105,28 @@ MUTATIONS = [
      "return (layer + 1) % 6 == 0 or layer == n_layers - 1",
      "return layer % 6 == 0 or layer == n_layers - 1",
      ["test_layer_count_gives_104_boundaries"]),
+    ("attention residual index 2l + 1",
+     'h, u = boundary_norm(a, h, W["attn_post"], W["mlp_pre"], 2 * l + 2, cfg.eps)',
+     'h, u = boundary_norm(a, h, W["attn_post"], W["mlp_pre"], 2 * l + 1, cfg.eps)',
+     ["test_residual_index_counts_every_addition"]),
+    ("gate and V rows of the packed projection swapped",
+     "g = z[:, (Hq + 2 * Hkv) * D:]",
+     "g = np.concatenate([z[:, (Hq + Hkv) * D: (Hq + 2 * Hkv) * D]] * (Hq // Hkv), axis=1)",
+     ["test_qkv_gate_packed_row_order"]),
+    ("K and V rows of the packed projection swapped",
+     "k = z[:, Hq * D: (Hq + Hkv) * D].reshape(T, Hkv, D)\n"
+     "    v = z[:, (Hq + Hkv) * D: (Hq + 2 * Hkv) * D].reshape(T, Hkv, D)",
+     "v = z[:, Hq * D: (Hq + Hkv) * D].reshape(T, Hkv, D)\n"
+     "    k = z[:, (Hq + Hkv) * D: (Hq + 2 * Hkv) * D].reshape(T, Hkv, D)",
+     ["test_qkv_gate_packed_row_order", "test_qkv_gate_nope_scales_q_only"]),
+    ("router scores by exp instead of sigmoid",
+     "s = f32(1.0 / (1.0 + np.exp(-logits.astype(np.float64))))",
+     "s = f32(np.exp(logits.astype(np.float64)))",
+     ["test_route_weights_use_unbiased_scores", "test_route_matches_brute_force_tiny"]),
+    ("dense SwiGLU gate and up swapped",
+     "a = bf16_round(silu(gu[:, :Fd]) * gu[:, Fd:])",
+     "a = bf16_round(gu[:, :Fd] * silu(gu[:, Fd:]))",
+     ["test_moe_equals_dense_with_stacked_experts"]),
     ("softcap without the division by c",
      "z = softcap * np.tanh(z / softcap)",
      "z = softcap * np.tanh(z)",
@@ -112,6 +135,45 @@ MUTATIONS = [
      "z = np.asarray(u, dtype=np.float64) @ np.asarray(w_lm, dtype=np.float64).T",
      "z = (np.asarray(w_lm, dtype=np.float64) @ np.asarray(u, dtype=np.float64).T).T[:, ::-1]",
      ["test_lm_head_projection_brute_force"]),
+]
+
+
+CODECS_PATH = os.path.join(os.path.dirname(oracle.__file__), "codecs.py")
+CODECS_SRC = open(CODECS_PATH).read()
+
+CODEC_MUTATIONS = [
+    ("bf16 truncates",
+     "r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)",
+     "r = (u >> np.uint64(16)).astype(np.uint16)",
+     ["test_bf16_encode_random_matches_torch"]),
+    ("bf16 ties away from zero",
+     "r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)",
+     "r = ((u + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)",
+     ["test_bf16_ties_go_to_even"]),
+    ("e4m3 exponent bias 8",
+     "vals[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)",
+     "vals[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 8)",
+     ["test_e4m3_decode_matches_torch_all_codes"]),
+    ("e4m3 does not saturate",
+     "q = np.minimum(q, E4M3_MAX)",
+     "q = q",
+     ["test_e4m3_saturates_and_keeps_nan"]),
+    ("e4m3 subnormal binade misplaced",
+     "e = np.maximum(e, -6.0)",
+     "e = np.maximum(e, -7.0)",
+     ["test_e4m3_encode_in_range_matches_torch"]),
+    ("e2m1 subnormal step 1 instead of 0.5",
+     "vals[code] = sign * (m * 0.5 if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1))",
+     "vals[code] = sign * (m * 1.0 if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1))",
+     ["test_e2m1_codes_are_the_published_magnitudes"]),
+    ("NVFP4 nibble order swapped",
+     "out[..., 0::2] = b & np.uint8(0xF)\n    out[..., 1::2] = b >> np.uint8(4)",
+     "out[..., 1::2] = b & np.uint8(0xF)\n    out[..., 0::2] = b >> np.uint8(4)",
+     ["test_nvfp4_nibble_order_block_and_matrix_scales"]),
+    ("NVFP4 matrix scale dropped",
+     "return v.reshape(rows, K) * float(np.float32(matrix_scale))",
+     "return v.reshape(rows, K)",
+     ["test_nvfp4_nibble_order_block_and_matrix_scales", "test_nvfp4_dequant_matches_element_loop"]),
 ]
 
 
@@ -124,10 +186,18 @@ def mutant(old, new):
     return m
 
 
-def fails(pin):
+def codecs_mutant(old, new):
+    assert CODECS_SRC.count(old) == 1, f"mutation site not unique: {old!r}"
+    m = types.ModuleType("codecs_mutant")
+    m.__file__ = CODECS_PATH
+    exec(compile(CODECS_SRC.replace(old, new), CODECS_PATH + " (mutant)", "exec"), m.__dict__)
+    return m
+
+
+def fails(pin, module=pins):
     name, args = (pin, ()) if isinstance(pin, str) else (pin[0], pin[1:])
     try:
-        getattr(pins, name)(*args)
+        getattr(module, name)(*args)
     except Exception:
         return True
     return False
@@ -139,8 +209,17 @@ def test_pins_catch_planted_slip(monkeypatch, slip, old, new, catchers):
     assert any(fails(p) for p in catchers), f"no pin caught: {slip}"
 
 
+@pytest.mark.parametrize("slip,old,new,catchers", CODEC_MUTATIONS,
+                         ids=[m[0] for m in CODEC_MUTATIONS])
+def test_codec_pins_catch_planted_slip(monkeypatch, slip, old, new, catchers):
+    monkeypatch.setattr(codec_pins, "codecs", codecs_mutant(old, new))
+    assert any(fails(p, codec_pins) for p in catchers), f"no pin caught: {slip}"
+
+
 def test_unmutated_oracle_passes_the_same_pins():
     """Control: every pin named above passes on the oracle as committed."""
-    names = {p if isinstance(p, str) else p for m in MUTATIONS for p in m[3]}
+    names = {p for m in MUTATIONS for p in m[3]}
     for p in sorted(names, key=str):
         assert not fails(p), p
+    for p in sorted({p for m in CODEC_MUTATIONS for p in m[3]}):
+        assert not fails(p, codec_pins), p

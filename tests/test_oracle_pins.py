@@ -147,6 +147,25 @@ def test_qkv_gate_nope_scales_q_only():
     assert g.shape == (2, cfg.n_q * D)
 
 
+def test_qkv_gate_packed_row_order():
+    """The packed projection's rows are Q (Hq*D), K (Hkv*D), V (Hkv*D), gate (Hq*D), the order
+    the Beam page lists them in (change 5). Each block of rows is filled with its own constant
+    c_b, so with any u the projection of block b is c_b * sum(u): the cache's V holds the V
+    block's value unnormalised and g the gate block's (a swapped pair of blocks fails)."""
+    cfg = TINY
+    Hq, Hkv, D = cfg.n_q, cfg.n_kv, cfg.head_dim
+    sizes = [Hq * D, Hkv * D, Hkv * D, Hq * D]
+    consts = [0.5, 0.25, 0.125, 0.0625]
+    w = np.concatenate([np.full((n, cfg.hidden), c) for n, c in zip(sizes, consts)])
+    u = np.full((1, cfg.hidden), 1.0 / cfg.hidden)          # sum(u) = 1
+    cache = O.KVCache(np.zeros((1, Hkv, 8, D)), np.zeros((1, Hkv, 8, D)), window=cfg.window)
+    q, g = O.qkv_gate(cfg, u, w, np.ones(D), np.ones(D), [0], [1], cache, nope=False)
+    assert np.all(g == consts[3])
+    assert np.all(cache.v[0, :, 0] == consts[2])
+    assert np.allclose(cache.k[0, :, 0], 1.0, rtol=2 ** -8)   # a constant row, normed
+    assert np.allclose(q, 1.0, rtol=2 ** -8)
+
+
 def test_qkv_gate_rope_relative_position():
     """Sliding-window layer: q'.k depends only on the distance between the two positions."""
     cfg = TINY
@@ -444,6 +463,28 @@ def _tiny_stack(T_prefill, seed=0):
         caches.append(O.KVCache(z, z.copy(), window=0 if nope else cfg.window))
     e = synth.activations(T_prefill, cfg.hidden, seed, "embed").double().numpy()
     return cfg, Ws, caches, e
+
+
+def test_residual_index_counts_every_addition():
+    """Beam page, MoE and residual-stream section and change 1: the n-th residual addition
+    scales by sqrt((n-1)/n) and 1/sqrt(n), 104 of them for 52 layers after the embedding.
+    Every boundary of a stack takes the next n: the embedding n = 1, then 2, 3, ..., 2L + 1,
+    each once and in order (layer l's attention n = 2l + 2, its MLP n = 2l + 3)."""
+    cfg, Ws, caches, e = _tiny_stack(1)
+    g = O.stack_forward.__globals__          # the module whose boundary_norm the stack calls
+    orig = g["boundary_norm"]
+    seen = []
+
+    def record(x, h, w_post, w_pre, n, eps):
+        seen.append(n)
+        return orig(x, h, w_post, w_pre, n, eps)
+
+    g["boundary_norm"] = record
+    try:
+        O.stack_forward(cfg, Ws, caches, e, [0], [1])
+    finally:
+        g["boundary_norm"] = orig
+    assert seen == list(range(1, 2 * cfg.n_layers + 2))
 
 
 def test_stack_prefill_equals_token_by_token_decode():
