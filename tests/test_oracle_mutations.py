@@ -127,6 +127,24 @@ MUTATIONS = [
      "a = bf16_round(silu(gu[:, :Fd]) * gu[:, Fd:])",
      "a = bf16_round(gu[:, :Fd] * silu(gu[:, Fd:]))",
      ["test_moe_equals_dense_with_stacked_experts"]),
+    ("FP8 cache store multiplies by the scale",
+     "self.k[s, :, sl, :] = e4m3_encode(f32(k_vec) / np.float32(self.k_scale))",
+     "self.k[s, :, sl, :] = e4m3_encode(f32(k_vec) * np.float32(self.k_scale))",
+     ["test_kv_cache_ring_and_fp8_roundtrip"]),
+    ("FP8 cache load divides by the scale",
+     "return e4m3_decode(k) * self.k_scale, e4m3_decode(v) * self.v_scale",
+     "return e4m3_decode(k) / self.k_scale, e4m3_decode(v) * self.v_scale",
+     ["test_kv_cache_ring_and_fp8_roundtrip"]),
+    ("expert ties go to the higher index",
+     "corder = np.lexsort((cand, -b[t, cand].astype(np.float64)))",
+     "corder = np.lexsort((-cand, -b[t, cand].astype(np.float64)))",
+     ["test_route_ties_go_to_lower_index", "test_route_matches_brute_force_tiny", "test_route_group_choice_full_width",
+      "test_route_weights_use_unbiased_scores"]),
+    ("group ties go to the higher index",
+     "gorder = np.lexsort((np.arange(G), -gscore.astype(np.float64)))",
+     "gorder = np.lexsort((-np.arange(G), -gscore.astype(np.float64)))",
+     ["test_route_ties_go_to_lower_index", "test_route_matches_brute_force_tiny", "test_route_group_choice_full_width",
+      "test_route_weights_use_unbiased_scores"]),
     ("softcap without the division by c",
      "z = softcap * np.tanh(z / softcap)",
      "z = softcap * np.tanh(z)",

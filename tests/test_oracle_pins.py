@@ -379,6 +379,26 @@ def test_route_weights_use_unbiased_scores():
 
 # ------------------------------------------------------------------ SwiGLU / MoE ----
 
+def test_route_ties_go_to_lower_index():
+    """READING (ties, not printed): equal scores rank by index, lower first, for groups and for
+    experts. With every expert equal (identical router rows, zero bias) the first
+    topk_groups groups are kept and the topk lowest experts of them chosen, in index order,
+    each weighted route_scale / topk. Equal scores in one group only: the lower one wins."""
+    cfg = TINY
+    u = np.ones((1, cfg.hidden))
+    wr = f32(np.full((cfg.n_experts, cfg.hidden), 0.01))
+    cb = f32(np.zeros(cfg.n_experts))
+    _, idx, w = O.route(cfg, u, wr, cb)
+    assert idx[0].tolist() == list(range(cfg.topk))
+    assert np.allclose(w, cfg.route_scale / cfg.topk)
+    # experts 9 and 13 (groups 2 and 3) tie for the top score: both groups are kept and both
+    # experts chosen, 9 listed first
+    cb2 = cb.copy()
+    cb2[[9, 13]] = 0.5
+    _, idx2, _ = O.route(cfg, u, wr, cb2)
+    assert idx2[0, 0] == 9 and idx2[0, 1] == 13
+
+
 def test_silu_definition():
     z = np.linspace(-30, 30, 1001)
     assert np.allclose(O.silu(z), z * expit(z), rtol=1e-14, atol=1e-300)
