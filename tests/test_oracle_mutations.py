@@ -40,6 +40,10 @@ MUTATIONS = [
      "x2 * c + x1 * s], axis=-1)",
      "x2 * c - x1 * s], axis=-1)",
      ["test_rope_closed_forms", "test_rope_invariants"]),
+    ("RoPE pairs adjacent elements instead of halves",
+     "x1, x2 = x[..., :half], x[..., half:]",
+     "x1, x2 = x[..., 0::2], x[..., 1::2]",
+     ["test_rope_closed_forms", "test_rope_invariants"]),
     ("RoPE frequency exponent halved",
      "return np.power(float(theta), -2.0 * i / D)",
      "return np.power(float(theta), -1.0 * i / D)",
@@ -72,6 +76,10 @@ MUTATIONS = [
     ("query attends to all but itself",
      "a, b = lo - lo_all, p - lo_all + 1",
      "a, b = lo - lo_all, max(p - lo_all, lo - lo_all + 1)",
+     ["test_attention_matches_torch_sdpa", "test_attention_special_cases"]),
+    ("softmax normalised over the query heads",
+     "o[t, hk * grp:(hk + 1) * grp] = (e / e.sum(axis=1, keepdims=True)) @ V[hk, a:b]",
+     "o[t, hk * grp:(hk + 1) * grp] = (e / e.sum(axis=0, keepdims=True)) @ V[hk, a:b]",
      ["test_attention_matches_torch_sdpa", "test_attention_special_cases"]),
     ("GQA heads interleaved instead of grouped",
      "qh = q[t, hk * grp:(hk + 1) * grp]",
