@@ -20,11 +20,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32, nvfp4_dequant
+from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32, fp8_block_dequant, nvfp4_dequant
 
 __all__ = [
     "rmsnorm", "boundary_norm", "rope_inv_freq", "rope", "ssmax_scale", "KVCache",
-    "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "moe_nvfp4", "dense_mlp",
+    "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "moe_nvfp4", "moe_fp8",
+    "dense_mlp",
     "is_nope_layer", "layer_forward", "stack_forward", "kv_values_per_token", "lm_head",
 ]
 
@@ -303,6 +304,20 @@ def moe_nvfp4(cfg, u, idx, w, experts):
         q_gu, s_gu, t_gu, q_dn, s_dn, t_dn = experts[e]
         gu[e] = nvfp4_dequant(q_gu, s_gu, t_gu)
         dn[e] = nvfp4_dequant(q_dn, s_dn, t_dn)
+    return moe(cfg, u, idx, w, gu, dn)
+
+
+def moe_fp8(cfg, u, idx, w, experts):
+    """moe() with block-scaled FP8 expert weights (weight-only: the activations stay bf16):
+    experts maps expert e -> (gate_up codes [2F][H], gate_up scales [2F/128][H/128], down codes
+    [H][F], down scales [H/128][F/128]). The selected experts' weights are dequantised exactly
+    and the layer is the BF16-weight one."""
+    used = sorted({int(e) for e in np.asarray(idx).ravel()})
+    gu, dn = {}, {}
+    for e in used:
+        c_gu, s_gu, c_dn, s_dn = experts[e]
+        gu[e] = fp8_block_dequant(c_gu, s_gu)
+        dn[e] = fp8_block_dequant(c_dn, s_dn)
     return moe(cfg, u, idx, w, gu, dn)
 
 

@@ -19,6 +19,12 @@ the pages do not print its layout, so NVIDIA's published definition is the readi
 elements in blocks of 16 consecutive elements of a row, each block scaled by one e4m3 value,
 and the whole matrix by one FP32 value; element = e2m1 * block scale * matrix scale. Two
 elements share a byte, the even element in the low nibble.
+
+Block-scaled FP8 (the FP8 expert weights: the AREX feed article on the Day-0 support says the
+weights ship in BF16, FP8 and NVFP4 and prints no FP8 layout; the reading is the block-scaled
+e4m3 format of the DeepSeek-V3 release, whose routing the Beam page names): e4m3 codes, one FP32
+scale per 128 x 128 block of the [rows][K] matrix (ragged blocks at the edges); element =
+e4m3 * scale of its block.
 """
 from __future__ import annotations
 
@@ -132,3 +138,17 @@ def nvfp4_dequant(packed, scales, matrix_scale) -> np.ndarray:
     rows, K = v.shape
     v = v.reshape(rows, K // NVFP4_BLOCK, NVFP4_BLOCK) * s[:, :, None]
     return v.reshape(rows, K) * float(np.float32(matrix_scale))
+
+
+FP8_BLOCK = 128
+
+
+def fp8_block_dequant(codes, scales) -> np.ndarray:
+    """Values [rows][K] (float64) of a block-scaled FP8 matrix: codes [rows][K] e4m3 bytes,
+    scales [ceil(rows/128)][ceil(K/128)] FP32, one per 128 x 128 block."""
+    v = e4m3_decode(codes)
+    s = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    rows, K = v.shape
+    rb = np.arange(rows) // FP8_BLOCK
+    kb = np.arange(K) // FP8_BLOCK
+    return v * s[rb[:, None], kb[None, :]]

@@ -5,7 +5,7 @@ arithmetic, so that both sides of every parity test can be fed from it.
 """
 from .beam_inputs import (  # noqa: F401
     BeamShape, TINY, BEAM, derived_seed, normal, uniform_codes, layer_weights, expert_weights,
-    expert_weights_nvfp4, lm_head_weights,
+    expert_weights_nvfp4, expert_weights_fp8, lm_head_weights,
     attention_weights, router_weights, dense_weights,
     activations, kv_cache, decode_positions, prefill_positions,
 )

@@ -142,6 +142,51 @@ def expert_weights_nvfp4(shape: BeamShape, layer: int, seed: int, device="cpu", 
     return out
 
 
+# Block-scaled FP8 expert weights: e4m3 magnitude codes uniform over [0x20, 0x50) (0.125 to
+# 7.5, every code a finite number) with a uniform sign bit, and FP32 scales uniform in
+# [0.004, 0.012) per 128 x 128 block, so that weights are of the size of the N(0, 0.02) BF16 ones.
+FP8_CODES = (0x20, 0x50)
+FP8_SCALE_RANGE = (0.004, 0.012)
+
+
+def fp8_codes(shape, seed, names, device="cpu"):
+    mag = uniform_codes(shape, FP8_CODES[0], FP8_CODES[1], seed, (*names, "mag"), device)
+    sign = uniform_codes(shape, 0, 2, seed, (*names, "sign"), device)
+    return mag | (sign << 7)
+
+
+def fp8_scales(shape, seed, names, device="cpu"):
+    g = torch.Generator(device=device)
+    g.manual_seed(derived_seed(seed, *names))
+    lo, hi = FP8_SCALE_RANGE
+    return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+
+def expert_weights_fp8(shape: BeamShape, layer: int, seed: int, device="cpu", experts=None):
+    """Block-scaled FP8 gate/up and down weights of the experts (a dict of tensors): e4m3
+    codes [E][2F][H] and [E][H][F] (uint8), FP32 scales [E][2F/128][H/128] and
+    [E][H/128][F/128] (blocks rounded up)."""
+    E, F, H = shape.n_experts, shape.d_ff_expert, shape.hidden
+    ids = list(range(E) if experts is None else experts)
+    n = len(ids)
+
+    def blocks(x):
+        return -(-x // 128)
+
+    out = {
+        "gate_up": torch.empty((n, 2 * F, H), dtype=torch.uint8, device=device),
+        "gate_up_scale": torch.empty((n, blocks(2 * F), blocks(H)), dtype=torch.float32, device=device),
+        "down": torch.empty((n, H, F), dtype=torch.uint8, device=device),
+        "down_scale": torch.empty((n, blocks(H), blocks(F)), dtype=torch.float32, device=device),
+    }
+    for i, e in enumerate(ids):
+        out["gate_up"][i] = fp8_codes((2 * F, H), seed, (layer, "fp8_gu", e), device)
+        out["gate_up_scale"][i] = fp8_scales((blocks(2 * F), blocks(H)), seed, (layer, "fp8_gu_s", e), device)
+        out["down"][i] = fp8_codes((H, F), seed, (layer, "fp8_dn", e), device)
+        out["down_scale"][i] = fp8_scales((blocks(H), blocks(F)), seed, (layer, "fp8_dn_s", e), device)
+    return out
+
+
 def attention_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
     """Norm gains and the attention sublayer's weights of one layer."""
     H, D = shape.hidden, shape.head_dim

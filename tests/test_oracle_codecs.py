@@ -110,3 +110,30 @@ def test_nvfp4_dequant_matches_element_loop():
             sc = float(torch.tensor([int(scales[r, k // 16])], dtype=torch.uint8)
                        .view(torch.float8_e4m3fn).float()[0])
             assert got[r, k] == val * sc * float(ms)
+
+
+def test_fp8_block_scales_hand_built():
+    # a 130 x 260 matrix: two row blocks (128 and a ragged 2) and three column blocks (128, 128
+    # and a ragged 4); every code is e4m3 0x38 = 1.0, so each element shows its block's scale
+    codes = np.full((130, 260), 0x38, dtype=np.uint8)
+    scales = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]], dtype=np.float32)
+    v = codecs.fp8_block_dequant(codes, scales)
+    assert v[0, 0] == 1.0 and v[127, 127] == 1.0
+    assert v[127, 128] == 2.0 and v[0, 255] == 2.0 and v[0, 256] == 3.0 and v[127, 259] == 3.0
+    assert v[128, 0] == 4.0 and v[129, 128] == 5.0 and v[129, 259] == 6.0
+    # the code's sign and magnitude carry through: 0xC4 = -(1 + 4/8) * 2^1 = -3
+    codes[129, 259] = 0xC4
+    assert codecs.fp8_block_dequant(codes, scales)[129, 259] == -18.0
+
+
+def test_fp8_block_dequant_matches_element_loop():
+    rng = np.random.default_rng(4)
+    rows, K = 200, 300
+    codes = (rng.integers(0, 0x7F, size=(rows, K), dtype=np.uint8)
+             | (rng.integers(0, 2, size=(rows, K), dtype=np.uint8) << 7)).astype(np.uint8)
+    scales = rng.uniform(0.001, 0.01, size=(2, 3)).astype(np.float32)
+    got = codecs.fp8_block_dequant(codes, scales)
+    dec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    for r in range(rows):
+        for k in range(K):
+            assert got[r, k] == dec[r, k] * float(scales[r // 128, k // 128])

@@ -200,6 +200,14 @@ CODEC_MUTATIONS = [
      "return v.reshape(rows, K) * float(np.float32(matrix_scale))",
      "return v.reshape(rows, K)",
      ["test_nvfp4_nibble_order_block_and_matrix_scales", "test_nvfp4_dequant_matches_element_loop"]),
+    ("FP8 block scale ignored",
+     "return v * s[rb[:, None], kb[None, :]]",
+     "return v",
+     ["test_fp8_block_scales_hand_built", "test_fp8_block_dequant_matches_element_loop"]),
+    ("FP8 block scale indices transposed",
+     "return v * s[rb[:, None], kb[None, :]]",
+     "return v * s[kb[None, :], rb[:, None]]",
+     ["test_fp8_block_scales_hand_built", "test_fp8_block_dequant_matches_element_loop"]),
 ]
 
 

@@ -427,6 +427,38 @@ def test_moe_equals_dense_with_stacked_experts():
     assert np.mean(out == ref) > 0.98
 
 
+def test_moe_fp8_is_the_bf16_layer_on_dequantised_weights():
+    """FP8 experts (weight-only): the layer on e4m3 codes times 128 x 128 block scales equals
+    the BF16-weight layer on those values, decoded here by torch's float8_e4m3fn and expanded
+    block by block with a Kronecker product (independent of the oracle's indexing)."""
+    cfg = TINY
+    H, F = cfg.hidden, cfg.d_ff_expert
+    r = rng(31)
+
+    def codes(rows, K):
+        c = r.integers(0x20, 0x50, size=(rows, K), dtype=np.uint8)
+        return (c | (r.integers(0, 2, size=(rows, K), dtype=np.uint8) << 7)).astype(np.uint8)
+
+    def expand(sc, rows, K):
+        return np.kron(sc.astype(np.float64), np.ones((128, 128)))[:rows, :K]
+
+    def dec(c):
+        return torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).double().numpy()
+
+    experts, gu, dn = {}, {}, {}
+    for e in (1, 4, 6, 9):
+        cg, cd = codes(2 * F, H), codes(H, F)
+        sg = f32(r.uniform(0.002, 0.006, size=(-(-2 * F // 128), -(-H // 128))))
+        sd = f32(r.uniform(0.002, 0.006, size=(-(-H // 128), -(-F // 128))))
+        experts[e] = (cg, sg, cd, sd)
+        gu[e] = dec(cg) * expand(sg, 2 * F, H)
+        dn[e] = dec(cd) * expand(sd, H, F)
+    u = bf16_round(r.standard_normal((3, H)))
+    idx = np.array([[1, 4, 6, 9], [9, 6, 4, 1], [4, 1, 9, 6]])
+    w = f32(r.uniform(0.1, 0.5, size=(3, 4))).astype(np.float64)
+    assert np.array_equal(O.moe_fp8(cfg, u, idx, w, experts), O.moe(cfg, u, idx, w, gu, dn))
+
+
 def test_moe_combine_is_weighted_sum():
     """Doubling one slot's weight adds exactly that expert's output once more."""
     cfg = TINY
