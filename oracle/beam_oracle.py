@@ -355,6 +355,8 @@ def layer_forward(cfg, l, W, h, u, cache, seq_id, pos, next_pre, trace=None):
         logits, idx, w = route(cfg, u, W["router"], W["corr_bias"])
         if "nvfp4_experts" in W:   # mapping expert -> its six NVFP4 arrays (moe_nvfp4)
             m = moe_nvfp4(cfg, u, idx, w, W["nvfp4_experts"])
+        elif "fp8_experts" in W:   # mapping expert -> its four FP8 arrays (moe_fp8)
+            m = moe_fp8(cfg, u, idx, w, W["fp8_experts"])
         else:
             m = moe(cfg, u, idx, w, W["w_gate_up"], W["w_down"])
         r = (logits, idx, w)
