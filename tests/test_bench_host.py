@@ -1,0 +1,47 @@
+"""bench.py's algorithmic-byte accounting (the numerator of every HBM roofline fraction) against
+the per-unit figures worked out from the Beam shapes: a sliding-window MoE layer at batch 1
+reads 846.24 MB (QKV+gate 146.80, o_proj 62.91, FP32 router 5.24, 8 experts 629.15, a
+512-key BF16 window 2.10), the NoPE layer over 100,000 cached keys 1.254 GB, a dense layer
+838.90 MB and an MoE layer without KV 844.15 MB; one BF16 expert 78.64 MB, one NVFP4 expert
+22.12 MB (codes, e4m3 block scales, two FP32 matrix scales)."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from synth import BEAM  # noqa: E402
+
+KV_PER_KEY_BF16 = BEAM.n_kv * BEAM.head_dim * 2 * 2     # K and V of 8 heads x 128, bf16
+
+
+def test_layer_bytes_per_unit():
+    assert bench.expert_bytes(BEAM, False) == 3 * 5120 * 2560 * 2
+    assert bench.expert_bytes(BEAM, True) == 3 * 5120 * 2560 // 2 + 3 * 5120 * 2560 // 16 + 8
+    swa = bench.layer_bytes(BEAM, False, 8, 512 * KV_PER_KEY_BF16)
+    assert abs(swa / 1e6 - 846.24) < 0.005
+    nope = bench.layer_bytes(BEAM, False, 8, 100_001 * KV_PER_KEY_BF16)
+    assert abs(nope / 1e9 - 1.2538) < 5e-4
+    assert abs(bench.layer_bytes(BEAM, True, 0, 0) / 1e6 - 838.90) < 0.005
+    assert abs(bench.layer_bytes(BEAM, False, 8, 0) / 1e6 - 844.15) < 0.005
+    # NVFP4 experts change only the experts' share
+    d = bench.layer_bytes(BEAM, False, 8, 0) - bench.layer_bytes(BEAM, False, 8, 0, nvfp4=True)
+    assert d == 8 * (bench.expert_bytes(BEAM, False) - bench.expert_bytes(BEAM, True))
+
+
+def test_traffic_entries_are_per_call():
+    """profiles/traffic.json holds DRAM bytes per call of the one-token MoE calls: each entry
+    still in force (its sources unchanged since the capture) lies within a few percent above
+    its algorithmic bytes (no re-reads); entries whose sources changed report None."""
+    import json
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for key, nvfp4 in (("moe_decode_t1", False), ("moe_decode_nvfp4_t1", True)):
+        assert algo_ok(d[key]["bytes_per_launch"], 8 * bench.expert_bytes(BEAM, nvfp4)), key
+        t = bench.ncu_traffic(key)
+        assert t is None or t == d[key]["bytes_per_launch"]
+    assert bench.ncu_traffic("moe_decode_t8") is None
+
+
+def algo_ok(traffic, algo):
+    return algo <= traffic < 1.05 * algo
