@@ -69,9 +69,13 @@ class BeamStack:
 
     def layer(self, i, b, seq_id, pos, max_pos, ws, stream=None, trace=None, max_q_per_seq=None):
         """The i-th layer held (global index l): from (h, u = its attention pre-norm) to
-        (h, u of the next layer)."""
+        (h, u of the next layer). With a trace list, appends the layer's intermediate tensors:
+        u_attn, q, g, attn, h_mid (h after the attention residual), mlp_in, mlp, route
+        (logits, idx, w) on MoE layers, and the output h."""
         W, cfg, kc = self.W[i], self.cfgs[i], self.caches[i]
         l = self.ids[i]
+        if trace is not None:
+            trace.append({"u_attn": b["u"].clone()})
         B.beam_qkv_gate(cfg, b["u"], W["w_qkvg"], W["q_norm"], W["k_norm"], seq_id, pos, b["q"],
                         b["g"], kc, ws, stream)
         B.beam_attn(cfg, b["q"], b["g"], W["gate_bias"], kc, seq_id, pos, max_pos, W["w_o"],
@@ -79,8 +83,8 @@ class BeamStack:
         B.beam_boundary_norm(b["a"], b["h"], b["u"], W["attn_post"], W["mlp_pre"], 2 * l + 2,
                              cfg.eps, stream)
         if trace is not None:
-            trace.append({"q": b["q"].clone(), "g": b["g"].clone(), "attn": b["a"].clone(),
-                          "mlp_in": b["u"].clone()})
+            trace[-1].update({"q": b["q"].clone(), "g": b["g"].clone(), "attn": b["a"].clone(),
+                              "h_mid": b["h"].clone(), "mlp_in": b["u"].clone()})
         if self.dense[i]:
             B.beam_dense_mlp(cfg, b["u"], W["w_gate_up"], W["w_down"], b["m"], ws, stream)
         else:
@@ -98,6 +102,8 @@ class BeamStack:
         nxt = self.W[i + 1]["attn_pre"] if i + 1 < self.L else None
         B.beam_boundary_norm(b["m"], b["h"], b["u"] if nxt is not None else None,
                              W["mlp_post"], nxt, 2 * l + 3, cfg.eps, stream)
+        if trace is not None:
+            trace[-1]["h"] = b["h"].clone()
 
     def forward(self, e, seq_id, pos, max_pos, stream=None, trace=None, max_q_per_seq=None):
         """Runs the held layers for the tokens (seq_id, pos). e [T][H] (bf16) is the residual

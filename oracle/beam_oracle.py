@@ -24,8 +24,8 @@ from .codecs import bf16_round, e4m3_decode, e4m3_encode, f32, fp8_block_dequant
 
 __all__ = [
     "rmsnorm", "boundary_norm", "rope_inv_freq", "rope", "ssmax_scale", "KVCache",
-    "qkv_gate", "attention", "route", "route_scores", "silu", "moe", "moe_nvfp4", "moe_fp8",
-    "dense_mlp",
+    "qkv_gate", "attention", "route", "route_scores", "route_gaps", "silu", "moe", "moe_nvfp4",
+    "moe_fp8", "dense_mlp",
     "is_nope_layer", "layer_forward", "stack_forward", "kv_values_per_token", "lm_head",
 ]
 
@@ -256,6 +256,35 @@ def route(cfg, u, w_router, corr_bias):
         idx[t] = sel
         w[t] = ssel / ssel.sum() * cfg.route_scale
     return logits, idx, f32(w)
+
+
+def route_gaps(cfg, b):
+    """How firmly each token's routing is decided, from its biased scores b [T][E].
+
+    group_gap[t]  = group score of the last kept group minus that of the best dropped group
+                    (the kG-th and (kG+1)-th largest group scores; inf when every group is kept)
+    expert_gap[t] = the k-th largest biased score among the kept groups' experts minus the
+                    (k+1)-th (inf when the kept groups hold exactly k experts)
+
+    Group scores are the sums of the two largest b of each group, as in route(). If every b of
+    a token moves by less than group_gap/4 (a group score then moves by less than group_gap/2)
+    and by less than expert_gap/2, route() selects the same groups and the same experts; a gap
+    of 0 is a tie that the index rule decides."""
+    b = np.asarray(b, dtype=np.float64)
+    T, E = b.shape
+    G, kG, k = cfg.n_groups, cfg.topk_groups, cfg.topk
+    per = E // G
+    group_gap = np.full(T, np.inf)
+    expert_gap = np.full(T, np.inf)
+    for t in range(T):
+        gscore = np.sort(b[t].reshape(G, per), axis=1)[:, -2:].sum(axis=1)
+        order = np.lexsort((np.arange(G), -gscore))
+        if kG < G:
+            group_gap[t] = gscore[order[kG - 1]] - gscore[order[kG]]
+        cand = np.sort(np.concatenate([b[t, g * per:(g + 1) * per] for g in order[:kG]]))[::-1]
+        if k < cand.size:
+            expert_gap[t] = cand[k - 1] - cand[k]
+    return group_gap, expert_gap
 
 
 # ---------------------------------------------------------------------------------------

@@ -9,3 +9,4 @@ from .beam_inputs import (  # noqa: F401
     attention_weights, router_weights, dense_weights,
     activations, kv_cache, decode_positions, prefill_positions,
 )
+from .tie_free import MIN_GAP, STACK_MIN_GAP, TINY_STACK_MIN_GAP, first_accepted  # noqa: F401

@@ -203,11 +203,15 @@ def attention_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu")
     }
 
 
-def router_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu"):
+def router_weights(shape: BeamShape, layer: int, seed: int = 0, device="cpu", attempt: int = 0):
+    """FP32 router rows [E][H] and correction bias [E]. attempt > 0 gives an independent
+    redraw (synth.tie_free walks the attempts); attempt 0 is the layer's first draw."""
     E, H = shape.n_experts, shape.hidden
+    tag = () if attempt == 0 else (attempt,)
     return {
-        "router": normal((E, H), 0.02, 0.0, seed, (layer, "router"), device, torch.float32),
-        "corr_bias": normal((E,), 0.01, 0.0, seed, (layer, "corr_bias"), device, torch.float32),
+        "router": normal((E, H), 0.02, 0.0, seed, (layer, "router", *tag), device, torch.float32),
+        "corr_bias": normal((E,), 0.01, 0.0, seed, (layer, "corr_bias", *tag), device,
+                            torch.float32),
     }
 
 

@@ -1,8 +1,6 @@
-"""GPU parity of whole layers and of the truncated stack against the oracle.
+"""GPU parity of single full-width layers against the oracle (the whole stack, end to end,
+is in test_gpu_stack.py).
 
-  - tiny 6-layer stack (hidden 256, 4/2 heads of 64, window 16, 16 experts; layer 0 dense,
-    layer 5 NoPE): prefill of 64 N(0,1) tokens through every layer (filling every cache),
-    then one decode token at p = 65;
   - one full-width sliding-window MoE layer, batch-1 decode at context 4096 (BF16 cache);
   - one full-width NoPE MoE layer with SSMax, decode at context 100,000 per sequence,
     batch 1 and 8 with a BF16 cache, batch 2 with an FP8-e4m3 cache (scale 0.0371).
@@ -15,11 +13,10 @@ import torch
 
 import oracle as O
 import synth
-from synth import BEAM, TINY
+from synth import BEAM
 from hybrid_attention_moe_gb300 import beam as B
 from hybrid_attention_moe_gb300.stack import BeamStack
-from parity import (assert_chained_close, flatten_trace, floors_on_rows, noise_floor, np64,
-                    oracle_cache, routing_choice_valid, routing_stable, routing_tolerance)
+from parity import assert_chained_close, np64, oracle_cache, routing_stable
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -62,98 +59,6 @@ def oracle_weights(W):
         else:
             out[k] = np64(v)
     return out
-
-
-def _check_routing(gpu_tr, ref_tr):
-    for l, (g, r) in enumerate(zip(gpu_tr, ref_tr)):
-        if r["route"] is not None:
-            lg, idx, w = r["route"]
-            gl, gi, gw = g["route"]
-            assert np.array_equal(np.sort(gi.cpu().numpy(), 1), np.sort(idx, 1)), f"layer {l} idx"
-
-
-def _tiny_stack_states(shape, Wo, e, e1, caps, wins):
-    """Oracle run of the tiny stack (64-token prefill, then decode at p = 65) recording, for
-    every layer and phase, the layer's input h and its KV cache just before the layer ran."""
-    import copy
-    L = shape.n_layers
-    oc = [O.KVCache(np.zeros((1, shape.n_kv, caps[l], shape.head_dim), np.float32),
-                    np.zeros((1, shape.n_kv, caps[l], shape.head_dim), np.float32),
-                    window=wins[l]) for l in range(L)]
-    states = []
-    for ph, x, pos in (("pre", np64(e), np.arange(1, 65)), ("dec", np64(e1), np.array([65]))):
-        seq = np.zeros(len(pos), int)
-        h, u = O.boundary_norm(None, x, None, Wo[0]["attn_pre"], 1, shape.eps)
-        for l in range(L):
-            states.append((ph, l, h.copy(), copy.deepcopy(oc[l]), seq, pos))
-            nxt = Wo[l + 1]["attn_pre"] if l + 1 < L else None
-            h, u = O.layer_forward(shape, l, Wo[l], h, u, oc[l], seq, pos, nxt)
-    return states
-
-
-def test_tiny_stack_prefill_then_decode_per_layer():
-    """Every layer of the tiny 6-layer stack, in the 64-token prefill and in the decode step
-    at p = 65, run on the GPU from the oracle's own state at that layer (its input h and its KV
-    cache as the oracle had filled it). A whole-stack comparison is not meaningful at this
-    size: the oracle rerun with FP32-level noise drifts from itself by 3-9% at the end and
-    flips routing. Per layer: outputs within the chained-step bars; routing identical for
-    every token whose margins exceed 3x its score shift under that noise; for the few near-tie
-    tokens the GPU's choice must be a valid top-k within that shift, and those tokens' MLP
-    rows are left out of the numeric comparison."""
-    shape = TINY
-    L = shape.n_layers
-    caps = [128 if O.is_nope_layer(l, L) else 80 for l in range(L)]
-    wins = [0 if O.is_nope_layer(l, L) else shape.window for l in range(L)]
-    seed = 0
-    Wt = [synth.layer_weights(shape, l, seed) for l in range(L)]
-    Wo = [{k: np64(v) for k, v in W.items()} for W in Wt]
-    e = synth.activations(64, shape.hidden, seed, "embed")
-    e1 = synth.activations(1, shape.hidden, seed, "embed_decode")
-    states = _tiny_stack_states(shape, Wo, e, e1, caps, wins)
-    Wd = [{k: v.to(DEV) for k, v in W.items()} for W in Wt]
-    n_tie = n_tok = 0
-    for ph, l, h_in, oc_l, seq, pos in states:
-        def run(h_in=h_in, oc_l=oc_l, l=l, seq=seq, pos=pos):
-            oc = O.KVCache(oc_l.k, oc_l.v, oc_l.dtype, oc_l.k_scale, oc_l.v_scale, oc_l.window)
-            ho, uo = O.boundary_norm(None, h_in, None, Wo[l]["attn_pre"], 1, shape.eps)
-            tr = []
-            out = O.layer_forward(shape, l, Wo[l], ho, uo, oc, seq, pos, None, tr)[0]
-            res = flatten_trace(tr, out)
-            if tr[0]["route"] is not None:
-                res["L0.idx"] = np.sort(tr[0]["route"][1], 1).astype(np.float64)
-            return res
-        alts = []
-        ref, floors = noise_floor(run, alts_out=alts)
-        kc = B.KVCache(torch.from_numpy(np.asarray(oc_l.k, np.float32)).to(torch.bfloat16).to(DEV),
-                       torch.from_numpy(np.asarray(oc_l.v, np.float32)).to(torch.bfloat16).to(DEV),
-                       wins[l])
-        st = BeamStack(shape, [Wd[l]], [kc], first_layer=l)
-        gtr = []
-        out = st.forward(torch.from_numpy(h_in).to(torch.bfloat16).to(DEV),
-                         torch.from_numpy(seq.astype(np.int32)).to(DEV),
-                         torch.from_numpy(pos.astype(np.int32)).to(DEV), int(pos.max()), trace=gtr)
-        assert B.beam_get_device_status() == 0
-        rows = None
-        if "L0.idx" in ref:
-            stable, tol = routing_tolerance(shape, ref["L0.logits"],
-                                            [a_["L0.logits"] for a_ in alts], Wo[l]["corr_bias"])
-            gi = np.sort(gtr[0]["route"][1].cpu().numpy(), 1)
-            same = np.all(gi == ref["L0.idx"], axis=1)
-            assert np.all(same[stable]), f"{ph} layer {l}: routing differs on a stable token"
-            for t in np.nonzero(~same)[0]:
-                assert routing_choice_valid(shape, ref["L0.logits"][t], Wo[l]["corr_bias"],
-                                            gi[t], tol[t]), f"{ph} layer {l}: invalid choice"
-            agree = np.all([np.all(a_["L0.idx"] == ref["L0.idx"], axis=1) for a_ in alts], axis=0)
-            rows = same & agree
-            floors = dict(floors, **floors_on_rows(ref, alts, ("L0.mlp", "h"), rows))
-            n_tie += int(np.sum(~rows))
-            n_tok += len(rows)
-        try:
-            assert_chained_close(flatten_trace(gtr, out), ref, floors, rows=rows,
-                                 row_keys=("L0.mlp", "h"))
-        except AssertionError as err:
-            raise AssertionError(f"{ph} layer {l}: {err}") from None
-    assert n_tie <= 0.05 * n_tok, f"{n_tie} of {n_tok} token routings took the other side of a tie"
 
 
 def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvfp4=False):

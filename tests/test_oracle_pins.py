@@ -399,6 +399,65 @@ def test_route_ties_go_to_lower_index():
     assert idx2[0, 0] == 9 and idx2[0, 1] == 13
 
 
+def test_route_gaps_match_subset_enumeration():
+    """route_gaps against brute force: the group gap is the best total group score of any
+    topk_groups-subset minus the second best (swapping the weakest kept group for the best
+    dropped one), and the expert gap the same over the topk-subsets of the kept groups'
+    experts. Ties planted in one token give a zero gap."""
+    cfg = TINY
+    u, wr, cb = _route_case(cfg, 24, 23)
+    _, _, b = O.route_scores(cfg, u, wr, cb)
+    b = b.astype(np.float64)
+    per = cfg.n_experts // cfg.n_groups
+    b[5] = np.tile(b[5, :per], cfg.n_groups)   # every group alike: tied group scores
+    b[9] = 0.3                                 # every expert alike: tied everywhere
+    gg, eg = O.route_gaps(cfg, b)
+    for t in range(b.shape[0]):
+        gs = [np.sort(b[t, g * per:(g + 1) * per])[-2:].sum() for g in range(cfg.n_groups)]
+        tot = sorted((sum(gs[g] for g in c)
+                      for c in itertools.combinations(range(cfg.n_groups), cfg.topk_groups)),
+                     reverse=True)
+        assert gg[t] == pytest.approx(tot[0] - tot[1], abs=1e-12)
+        best = max(itertools.combinations(range(cfg.n_groups), cfg.topk_groups),
+                   key=lambda c: (sum(gs[g] for g in c), [-g for g in c]))
+        cand = [e for g in best for e in range(g * per, (g + 1) * per)]
+        et = sorted((sum(b[t, e] for e in c) for c in itertools.combinations(cand, cfg.topk)),
+                    reverse=True)
+        assert eg[t] == pytest.approx(et[0] - et[1], abs=1e-12)
+    assert gg[5] == 0.0 and eg[5] > 0.0
+    assert gg[9] == 0.0 and eg[9] == 0.0
+
+
+def test_route_gaps_bound_the_stable_perturbation():
+    """Every biased score moved by less than min(group_gap/4, expert_gap/2) leaves the
+    selection unchanged; a token whose gap is closed flips. Selection taken from route() via
+    the correction bias (b = s + bias), with the sigmoid scores fixed."""
+    cfg = TINY
+    rng = np.random.default_rng(5)
+    u, wr, cb = _route_case(cfg, 32, 24)
+    logits, s, b = O.route_scores(cfg, u, wr, cb)
+    _, idx0, _ = O.route(cfg, u, wr, cb)
+    gg, eg = O.route_gaps(cfg, b)
+    for t in range(32):
+        lim = min(gg[t] / 4, eg[t] / 2)
+        for _ in range(20):
+            d = rng.uniform(-1, 1, cfg.n_experts) * lim * 0.9
+            _, idx1, _ = O.route(cfg, u[t:t + 1], wr, f32(cb.astype(np.float64) + d))
+            assert sorted(idx1[0]) == sorted(idx0[t])
+    # close the expert gap of token 0: lift its best unselected kept-group expert past the
+    # k-th selected one
+    t = 0
+    per = cfg.n_experts // cfg.n_groups
+    groups = sorted({int(e) // per for e in idx0[t]})
+    rest = [e for g in groups for e in range(g * per, (g + 1) * per) if e not in set(idx0[t])]
+    e_in = int(idx0[t][-1])
+    e_out = max(rest, key=lambda e: b[t, e])
+    cb2 = cb.astype(np.float64).copy()
+    cb2[e_out] += eg[t] * 1.5
+    _, idx2, _ = O.route(cfg, u[t:t + 1], wr, f32(cb2))
+    assert e_out in set(idx2[0]) and e_in not in set(idx2[0])
+
+
 def test_silu_definition():
     z = np.linspace(-30, 30, 1001)
     assert np.allclose(O.silu(z), z * expit(z), rtol=1e-14, atol=1e-300)
