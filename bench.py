@@ -1,13 +1,21 @@
 """Benchmark of the Beam decoder-layer forward on GB300 (one JSON line on rank 0).
 
-Workloads (seeded synthetic inputs, random-init weights; shapes of the Beam layer):
-  swa_decode   (default) one full-width sliding-window MoE layer, batch-1 decode, context 4096,
-               BF16 KV cache
-  nope_decode  one full-width NoPE MoE layer with SSMax, decode at context 100,000 per
-               sequence (--batch 1/2/4/8, --kv bf16/fp8)
-  stack_decode the 6-layer truncated stack (layers 0-2 dense, 3-5 MoE, layer 5 NoPE), decode
-               (--batch, --context, --kv; the 8-K / batch-128 / FP8 case is
-               --batch 128 --context 8192 --kv fp8; batch 1 / 100K / BF16 by default)
+Default: the 6-layer truncated stack (layers 0-2 dense SwiGLU, 3-5 256-expert MoE; layers 0-4
+sliding-window, layer 5 NoPE with SSMax) decoding one token of one sequence over 100,000
+cached tokens per layer with a BF16 cache: the line's value is µs per token per layer, with
+the HBM roofline of the step and of its dominant call. The same line carries a "prefill"
+object: the same stack and weights prefilling 8 sequences x 2048 new tokens appended to
+100,000 cached ones (tokens/s, tensor rooflines of the dominant GEMM call and of the NoPE
+attention call, the GEMM calls' share of the BF16 peak).
+
+Other workloads (seeded synthetic inputs, random-init weights; shapes of the Beam layer):
+  stack_decode  --batch/--context/--kv (the 8-K / batch-128 / FP8 case is
+                --batch 128 --context 8192 --kv fp8)
+  stack_prefill --seqs x --chunk new tokens after --context
+  stack_verify  --batch sequences x --chunk (1-16) new tokens each after --context: the
+                multi-token verification step of speculative decoding
+  swa_decode    one full-width sliding-window MoE layer, batch-1 decode, context 4096
+  nope_decode   one full-width NoPE MoE layer, decode at context 100,000 (--batch, --kv)
 
 A step is one pass of the whole layer (or stack) over one batch of new tokens; the residual
 stream h it updates in place carries over to the next step. Inputs are resident in HBM when
@@ -177,39 +185,54 @@ def ncu_traffic(kernel_key):
 
 # --------------------------------------------------------------------------- workloads ----
 
-class Workload:
-    """Holds weights, caches and inputs of one benchmark case on the device."""
+def stack_weights(args, layers, device):
+    """Device weights of the held layers (one dict per layer, synth.layer_weights), with NVFP4
+    expert weights on the MoE layers under --experts nvfp4."""
+    W = []
+    for l in layers:
+        nvfp4 = args.experts == "nvfp4" and l not in BEAM.dense_layers
+        W.append(synth.layer_weights(BEAM, l, args.seed, device=device, with_experts=not nvfp4))
+        if nvfp4:
+            W[-1]["nvfp4"] = synth.expert_weights_nvfp4(BEAM, l, args.seed, device=device)
+    return W
 
-    def __init__(self, args, device):
+
+def workload_shape(kind, args):
+    """(layers, context, sequences, new tokens per sequence) of a workload."""
+    if kind == "swa_decode":
+        return [3], 4096, 1, 1
+    if kind == "nope_decode":
+        return [5], 100_000, args.batch, 1
+    if kind == "stack_prefill":
+        return list(range(6)), args.context, args.seqs, args.chunk
+    if kind == "stack_verify":
+        return list(range(6)), args.context, args.batch, args.chunk
+    return list(range(6)), args.context, args.batch, 1      # stack_decode
+
+
+class Workload:
+    """Weights, caches and inputs of one benchmark case on the device. W: weights to share
+    with another workload over the same layers (else drawn here)."""
+
+    def __init__(self, args, device, kind, W=None):
         from hybrid_attention_moe_gb300 import beam as B
         from hybrid_attention_moe_gb300.stack import BeamStack
         self.B = B
         self.args = args
         self.device = device
+        self.kind = kind
         shape = BEAM
-        kind = args.workload
+        layers, ctx, batch, chunk = workload_shape(kind, args)
         fp8 = args.kv == "fp8"
-        chunk = 1
-        if kind == "swa_decode":
-            layers, ctx, batch = [3], 4096, 1
-        elif kind == "nope_decode":
-            layers, ctx, batch = [5], 100_000, args.batch
-        elif kind == "stack_prefill":
-            layers, ctx, batch, chunk = list(range(6)), args.context, args.seqs, args.chunk
-        else:
-            layers, ctx, batch = list(range(6)), args.context, args.batch
         self.layers, self.ctx, self.batch, self.fp8 = layers, ctx, batch, fp8
         self.chunk = chunk
-        self.prefill = chunk > 1
+        self.prefill = kind == "stack_prefill"
         self.tokens = batch * chunk
         scale = 1.0
         self.nvfp4 = args.experts == "nvfp4"
-        W, caches = [], []
+        W = stack_weights(args, layers, device) if W is None else W
+        caches = []
         for l in layers:
-            W.append(synth.layer_weights(shape, l, args.seed, device=device,
-                                         with_experts=not self.nvfp4))
-            if self.nvfp4 and l not in shape.dense_layers:
-                W[-1]["nvfp4"] = synth.expert_weights_nvfp4(shape, l, args.seed, device=device)
             nope = is_nope(l, shape.n_layers)
             # a sliding-window ring holds window + chunk - 1 keys, rounded up to whole 128-key
             # tiles (the tensor-core prefill walks the ring in tile-aligned slots)
@@ -225,6 +248,16 @@ class Workload:
         self.e = synth.activations(self.tokens, shape.hidden, args.seed, "h", device)
         self.W = W
         self.caches = caches
+
+    def config(self):
+        return {
+            "workload": self.kind, "layers": self.layers, "batch": self.batch,
+            "new_tokens_per_seq": self.chunk, "context": self.ctx,
+            "kv_cache": "fp8_e4m3" if self.fp8 else "bf16",
+            "expert_weights": "nvfp4" if self.nvfp4 else "bf16",
+            "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
+            "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
+        }
 
     def step_calls(self):
         """The library calls of one step as (name, fn) closures over fixed buffers."""
@@ -310,11 +343,12 @@ class Workload:
 
 # --------------------------------------------------------------------------- our arm ----
 
-def run_ours(args, rank, world, device):
-    B_mod = __import__("hybrid_attention_moe_gb300.beam", fromlist=["beam"])
-    import __graft_entry__ as ge
-    ge.build()
-    wl = Workload(args, device)
+def measure(wl, args, world, device):
+    """Times one workload: K steps captured as one CUDA graph and replayed between two events
+    on the launching stream (after W warm-up replays), the per-call breakdown from a second
+    replay with an event before every call, the end-to-end variant through host buffers, and
+    the roofline of the dominant call. Returns the fields of a bench line."""
+    B_mod = wl.B
     calls, b = wl.step_calls()
     names = [n for n, _ in calls]
     stream = torch.cuda.Stream(device)
@@ -399,82 +433,110 @@ def run_ours(args, rank, world, device):
         n = wl.touched_experts(b)
         for l in moe_layers:
             touched[l] = n
-    algo_bytes, per_layer = wl.algorithmic_bytes(touched)
+    algo_bytes, _ = wl.algorithmic_bytes(touched)
     value, unit = whole_job(ms_step, wl.tokens, world, len(wl.layers), wl.prefill)
     hbm, hbm_kind = peaks()
     layer_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
 
-    roof = None
-    tensor_total = None
+    res = {"value": round(value, 1 if wl.prefill else 3), "unit": unit,
+           "ms_per_step": round(ms_step, 4), "higher_is_better": bool(wl.prefill)}
+    if not wl.prefill:
+        res["layer_hbm"] = {"algorithmic_bytes_per_step": algo_bytes,
+                            "achieved_gbs": round(layer_gbs, 1), "peak_gbs": hbm,
+                            "frac": round(layer_gbs / hbm, 4), "peak_kind": hbm_kind}
     if per_call_us and not wl.prefill:
         dom = max(per_call_us, key=per_call_us.get)
         dom_bytes, dom_key = dominant_bytes(wl, dom, touched)
         dom_gbs = dom_bytes / (per_call_us[dom] * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(dom_gbs / hbm, 4),
-                "traffic": ncu_traffic(dom_key), "bytes_per_launch": dom_bytes,
-                "duration_us": round(per_call_us[dom], 2), "peak_kind": hbm_kind}
+        res["roofline"] = {
+            "bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(dom_gbs / hbm, 4), "traffic": ncu_traffic(dom_key),
+            "bytes_per_launch": dom_bytes, "duration_us": round(per_call_us[dom], 2),
+            "peak_kind": hbm_kind}
     elif per_call_us:
         tf_peak, tf_kind = tensor_peak()
         fl = wl.flops()
-        dom = max((k for k in per_call_us if k in fl and not k.endswith(".route")),
-                  key=per_call_us.get)
-        ach = fl[dom] / (per_call_us[dom] * 1e-6) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": tf_peak,
-                "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
-                "traffic": ncu_traffic(dom.split(".")[1] + "_prefill"),
-                "flops_per_launch": fl[dom], "duration_us": round(per_call_us[dom], 2),
-                "peak_kind": tf_kind}
-        tc_flops = sum(v for k, v in fl.items() if not k.endswith(".route"))
+
+        def tensor_roof(key):
+            ach = fl[key] / (per_call_us[key] * 1e-6) / 1e12
+            return {"bound": "tensor", "kernel": key, "achieved": round(ach, 1),
+                    "peak": tf_peak, "unit": "TFLOP/s", "frac": round(ach / tf_peak, 4),
+                    "traffic": ncu_traffic(key.split(".")[1] + "_prefill"),
+                    "flops_per_launch": fl[key], "duration_us": round(per_call_us[key], 2),
+                    "peak_kind": tf_kind}
+
         gemm_keys = [k for k in fl if k.endswith((".qkv_gate", ".dense_mlp", ".moe"))]
+        attn_keys = [k for k in fl if k.endswith(".attn")]
+        res["roofline"] = tensor_roof(max(gemm_keys, key=per_call_us.get))
+        res["attention_roofline"] = tensor_roof(max(attn_keys, key=per_call_us.get))
+        tc_flops = sum(v for k, v in fl.items() if not k.endswith(".route"))
         gemm_us = sum(per_call_us[k] for k in gemm_keys)
         gemm_fl = sum(fl[k] for k in gemm_keys)
-        tensor_total = {
+        res["tensor"] = {
             "step_tflops": round(tc_flops / (ms_step * 1e-3) / 1e12, 1),
+            "step_flops": tc_flops,
             "gemm_calls_tflops": round(gemm_fl / (gemm_us * 1e-6) / 1e12, 1),
             "gemm_calls_frac": round(gemm_fl / (gemm_us * 1e-6) / 1e12 / tf_peak, 4),
             "peak": tf_peak, "peak_kind": tf_kind}
+    res["per_call_us"] = {k: round(v, 2) for k, v in per_call_us.items()}
+    res["per_call_replay_ms_per_step"] = None if evented_ms is None else round(evented_ms, 4)
+    res["timing"] = mode
+    res["e2e"] = run_e2e(args, wl, step_graph, stream, world, device)
+    res["gpu_launches"] = launches_step * args.steps
+    res["clocks"] = clk.summary()
+    res["_stream"], res["_b"] = stream, b
+    return res
 
+
+def run_ours(args, rank, world, device):
+    import __graft_entry__ as ge
+    ge.build()
+    wl = Workload(args, device, args.workload)
+    m = measure(wl, args, world, device)
+    stream, b = m.pop("_stream"), m.pop("_b")
     head = time_lm_head(args, wl, b, stream) if args.lm_head_vocab > 0 else None
-    e2e = run_e2e(args, wl, step_graph, stream, world, device)
     res = {
         "metric": METRIC,
-        "value": round(value, 1 if wl.prefill else 3),
-        "unit": unit,
+        "value": m["value"],
+        "unit": m["unit"],
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
-        "higher_is_better": bool(wl.prefill),
+        "ms_per_step": m["ms_per_step"],
+        "higher_is_better": m["higher_is_better"],
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) activations and KV cache, random-init N(0,0.02) weights",
-        "config": {
-            "workload": args.workload, "layers": wl.layers, "batch": wl.batch,
-            "new_tokens_per_seq": wl.chunk, "context": wl.ctx,
-            "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
-            "expert_weights": "nvfp4" if wl.nvfp4 else "bf16",
-            "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
-            "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
+        "config": dict(wl.config(), **{
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": f"no flush: each step streams {algo_bytes / 1e6:.0f} MB (> 129 MB L2)",
-            "timing": mode,
-        },
-        "layer_hbm": {"algorithmic_bytes_per_step": algo_bytes,
-                      "achieved_gbs": round(layer_gbs, 1), "peak_gbs": hbm,
-                      "frac": round(layer_gbs / hbm, 4), "peak_kind": hbm_kind},
-        "roofline": roof,
-        "tensor": tensor_total,
-        "per_call_us": {k: round(v, 2) for k, v in per_call_us.items()},
-        "per_call_replay_ms_per_step": None if evented_ms is None else round(evented_ms, 4),
-        "e2e": e2e,
-        "gpu_launches": launches_step * args.steps,
-        **({"lm_head": head} if head is not None else {}),
-        "clocks": clk.summary(),
+            "l2": "no flush: each step streams "
+                  f"{wl.algorithmic_bytes({})[0] / 1e6:.0f} MB of weights and cache (> 129 MB L2)",
+            "timing": m["timing"]}),
     }
+    for k in ("layer_hbm", "roofline", "attention_roofline", "tensor", "per_call_us",
+              "per_call_replay_ms_per_step", "e2e", "gpu_launches"):
+        if k in m:
+            res[k] = m[k]
+    if head is not None:
+        res["lm_head"] = head
+    res["clocks"] = m["clocks"]
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, wl, budget_s=args.cpu_budget)
+    if args.workload == "stack_decode" and not args.no_prefill:
+        # the same stack, same weights: prefill of args.seqs x args.chunk new tokens after
+        # args.context cached ones, as its own object of the line
+        del wl.stack, wl.caches
+        torch.cuda.empty_cache()
+        pw = Workload(args, device, "stack_prefill", W=wl.W)
+        p = measure(pw, args, world, device)
+        p.pop("_stream"), p.pop("_b")
+        p["config"] = dict(pw.config(), timing=p.pop("timing"),
+                           l2="no flush: each step streams the stack's weights "
+                              f"({sum(t.numel() * t.element_size() for w in pw.W for t in w.values() if torch.is_tensor(t)) / 1e9:.1f} GB)")
+        if world == 1 and not args.no_cpu_baseline:
+            p["cpu_baseline"] = cpu_baseline(args, pw, budget_s=args.cpu_budget)
+        res["prefill"] = p
     return res
 
 
@@ -539,16 +601,18 @@ def dominant_bytes(wl, name, touched):
         key = ("moe_decode_nvfp4" if wl.nvfp4 else "moe_decode") + f"_t{wl.tokens}"
         return touched[l] * expert_bytes(BEAM, wl.nvfp4), key
     if name.endswith(".attn"):
-        keys = wl.ctx + 1 if is_nope(l, BEAM.n_layers) else min(BEAM.window, wl.ctx + 1)
+        nope = is_nope(l, BEAM.n_layers)
+        keys = wl.ctx + 1 if nope else min(BEAM.window, wl.ctx + 1)
         elem = 1 if wl.fp8 else 2
         kv = wl.batch * keys * BEAM.n_kv * BEAM.head_dim * 2 * elem
-        return kv + BEAM.hidden * BEAM.q_rows * 2, "attn_decode"
+        return kv + BEAM.hidden * BEAM.q_rows * 2, ("attn_nope_decode" if nope else
+                                                     "attn_swa_decode") + f"_t{wl.tokens}"
     if name.endswith(".dense_mlp"):
-        return 3 * BEAM.hidden * BEAM.d_ff_dense * 2, "dense_decode"
+        return 3 * BEAM.hidden * BEAM.d_ff_dense * 2, f"dense_decode_t{wl.tokens}"
     if name.endswith(".route"):
-        return BEAM.n_experts * BEAM.hidden * 4, "route_decode"
+        return BEAM.n_experts * BEAM.hidden * 4, f"route_decode_t{wl.tokens}"
     if name.endswith(".qkv_gate"):
-        return BEAM.qkvg_rows * BEAM.hidden * 2, "qkv_decode"
+        return BEAM.qkvg_rows * BEAM.hidden * 2, f"qkv_decode_t{wl.tokens}"
     return 2 * wl.batch * BEAM.hidden * 2, "norm"
 
 
@@ -583,12 +647,12 @@ def run_e2e(args, wl, step_graph, stream, world, device):
 
 # ------------------------------------------------------------------------ oracle arm ----
 
-def oracle_sample(args, wl):
-    """A bounded oracle workload: the first sequence's new token through the held layers."""
+def oracle_layers(wl):
+    """Host views of the workload's weights and first-sequence caches for the oracle: float32
+    copies (bf16 values are exact; the oracle widens them) and experts fetched on first use."""
     import oracle as O
-    shape = wl.shape
 
-    def np64(t):
+    def host(t):
         return t.float().cpu().numpy()
 
     class Lazy:
@@ -597,7 +661,7 @@ def oracle_sample(args, wl):
 
         def __getitem__(self, e):
             if e not in self.c:
-                self.c[e] = np64(self.t[e])
+                self.c[e] = host(self.t[e])
             return self.c[e]
 
     class LazyNvfp4:
@@ -619,7 +683,7 @@ def oracle_sample(args, wl):
             if k == "nvfp4":
                 d["nvfp4_experts"] = LazyNvfp4(v)
             else:
-                d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else np64(v)
+                d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else host(v)
         Wo.append(d)
     caches = []
     for kc in wl.caches:
@@ -627,15 +691,27 @@ def oracle_sample(args, wl):
             caches.append(O.KVCache(kc.k[:1].cpu().numpy(), kc.v[:1].cpu().numpy(), "fp8",
                                     kc.k_scale, kc.v_scale, window=kc.window))
         else:
-            caches.append(O.KVCache(np64(kc.k[:1]), np64(kc.v[:1]), "bf16", window=kc.window))
-    h0 = np64(wl.e[:1]).astype(np.float64)
-    pos = [wl.ctx + 1]
+            caches.append(O.KVCache(host(kc.k[:1]), host(kc.v[:1]), "bf16", window=kc.window))
+    return Wo, caches
+
+
+def oracle_sample(args, wl, layers=None, n_tokens=1):
+    """A bounded oracle workload: the first n_tokens new tokens of sequence 0 (a decode token,
+    or the head of its prefill chunk) through the held layers (or the given subset)."""
+    import oracle as O
+    shape = wl.shape
+    Wo, caches = oracle_layers(wl)
+    idx = list(range(len(wl.layers))) if layers is None else \
+        [wl.layers.index(l) for l in layers]
+    h0 = wl.e[:n_tokens].float().cpu().numpy().astype(np.float64)
+    pos = [wl.ctx + 1 + t for t in range(n_tokens)]
+    seq = [0] * n_tokens
 
     def run():
-        h, u = O.boundary_norm(None, h0, None, Wo[0]["attn_pre"], 1, shape.eps)
-        for i, l in enumerate(wl.layers):
-            nxt = Wo[i + 1]["attn_pre"] if i + 1 < len(wl.layers) else None
-            h, u = O.layer_forward(shape, l, Wo[i], h, u, caches[i], [0], pos, nxt)
+        h, u = O.boundary_norm(None, h0, None, Wo[idx[0]]["attn_pre"], 1, shape.eps)
+        for j, i in enumerate(idx):
+            nxt = Wo[idx[j + 1]]["attn_pre"] if j + 1 < len(idx) else None
+            h, u = O.layer_forward(shape, wl.layers[i], Wo[i], h, u, caches[i], seq, pos, nxt)
         return h
 
     run()   # untimed: fetches the experts the oracle's own routing picks
@@ -643,46 +719,65 @@ def oracle_sample(args, wl):
 
 
 def cpu_baseline(args, wl, budget_s=15.0):
-    run = oracle_sample(args, wl)
+    """The oracle, as it stands, on the host cores: a bounded sample of the workload, repeated
+    until budget_s of CPU time. Decode: the first sequence's new token through every held
+    layer (µs per token per layer). Prefill: the first PREFILL_SAMPLE tokens of sequence 0's
+    chunk through every layer (tokens/s; the oracle's cost per token is the same for every
+    token of the chunk up to the 2% growth of the NoPE keys across it)."""
+    n_tok = PREFILL_SAMPLE if wl.prefill else 1
+    run = oracle_sample(args, wl, n_tokens=n_tok)
     n, t_total = 0, 0.0
     while t_total < budget_s and n < 50:
         t = time.perf_counter()
         run()
         t_total += time.perf_counter() - t
         n += 1
-    us = t_total / n * 1e6 / len(wl.layers)
-    val, unit = (round(n / t_total, 3), "tokens/s") if wl.prefill else (round(us, 1), "us/token/layer")
+    if wl.prefill:
+        val, unit = round(n * n_tok / t_total, 3), "tokens/s"
+        sample = (f"{n} x the first {n_tok} tokens of sequence 0's {wl.chunk}-token chunk "
+                  f"(positions {wl.ctx + 1}-{wl.ctx + n_tok}) through layers {wl.layers}; "
+                  f"rate extrapolated to the {wl.batch} x {wl.chunk}-token step; float64 "
+                  f"NumPy oracle, {t_total:.1f} s")
+    else:
+        val, unit = round(t_total / n * 1e6 / len(wl.layers), 1), "us/token/layer"
+        sample = (f"{n} x the first new token of sequence 0 through layers {wl.layers} "
+                  f"(context {wl.ctx}); float64 NumPy oracle, {t_total:.1f} s")
     return {"value": val, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} x the first new token of sequence 0 through layers {wl.layers} "
-                      f"(context {wl.ctx}); float64 NumPy oracle, {t_total:.1f} s"}
+            "sample": sample}
+
+
+PREFILL_SAMPLE = 2
 
 
 def run_reference(args, rank, world, device):
+    """The oracle arm: rank 0 times the oracle on the host cores, each step one layer of the
+    workload for the first sequence's first new token (the held layers in turn), so that the
+    whole run stays within minutes; the value is µs per token per layer (tokens/s for
+    prefill, from the first PREFILL_SAMPLE tokens of the chunk per step)."""
     if rank != 0:
         return None
-    wl = Workload(args, device)
-    run = oracle_sample(args, wl)
-    for _ in range(args.warmup):
-        run()
+    wl = Workload(args, device, args.workload)
+    n_tok = PREFILL_SAMPLE if wl.prefill else 1
+    runs = [oracle_sample(args, wl, layers=[l], n_tokens=n_tok) for l in wl.layers]
+    for i in range(args.warmup):
+        runs[i % len(runs)]()
     t = time.perf_counter()
-    for _ in range(args.steps):
-        run()
+    for i in range(args.steps):
+        runs[i % len(runs)]()
     dt = (time.perf_counter() - t) / args.steps
-    us = dt * 1e6 / len(wl.layers)
-    val, unit = (round(1.0 / dt, 3), "tokens/s") if wl.prefill else (round(us, 1), "us/token/layer")
+    val, unit = (round(n_tok / dt, 3), "tokens/s") if wl.prefill else \
+        (round(dt * 1e6, 1), "us/token/layer")
+    sample = (f"per step one layer of {wl.layers} in turn for the first "
+              f"{'new token' if n_tok == 1 else f'{n_tok} tokens of the chunk'} of sequence 0")
     return {
         "impl": "reference", "metric": METRIC, "value": val, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1000, 2), "higher_is_better": bool(wl.prefill),
         "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the CUDA arm)",
-        "config": {"workload": args.workload, "layers": wl.layers, "batch": 1,
-                   "context": wl.ctx, "kv_cache": "fp8_e4m3" if wl.fp8 else "bf16",
-                   "expert_weights": "nvfp4" if wl.nvfp4 else "bf16",
-                   "sample": "one token of sequence 0 per step"},
+        "config": dict(wl.config(), sample=sample),
         "cpu_baseline": {"value": val, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": "the first new token of sequence 0 through the held layers"
-                                   " per step"},
+                         "sample": sample},
         "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -695,10 +790,14 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="swa_decode",
-                    choices=["swa_decode", "nope_decode", "stack_decode", "stack_prefill"])
-    ap.add_argument("--seqs", type=int, default=8)
-    ap.add_argument("--chunk", type=int, default=2048)
+    ap.add_argument("--workload", default="stack_decode",
+                    choices=["stack_decode", "stack_prefill", "stack_verify", "swa_decode",
+                             "nope_decode"])
+    ap.add_argument("--seqs", type=int, default=8, help="prefill: sequences per step")
+    ap.add_argument("--chunk", type=int, default=2048,
+                    help="prefill: new tokens per sequence; stack_verify: tokens per sequence")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="stack_decode: skip the prefill object (same stack, same weights)")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--context", type=int, default=100_000)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])
@@ -715,6 +814,10 @@ def main():
         ap.error("--lm-head-vocab is timed for decode workloads")
     if args.experts == "nvfp4" and args.workload == "stack_prefill":
         ap.error("--experts nvfp4 is a decode format here (beam_moe_nvfp4 takes up to 31 tokens)")
+    if args.experts == "nvfp4":
+        args.no_prefill = True
+    if args.workload == "stack_verify" and not 1 <= args.chunk <= 16:
+        ap.error("stack_verify takes 1-16 new tokens per sequence (--chunk)")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
