@@ -8,6 +8,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "gemv_flat.cuh"
 
 namespace beam {
 
@@ -323,10 +324,30 @@ inline cudaError_t launch_gemv_mma(const uint16_t* W, int N, int K, const uint16
   return launch_gemv_mma_t<MODE, 8, 1>(W, N, K, X, T, yf, yb, ldy, st);
 }
 
+// flat_one_token: at T = 1 the product runs on the balanced one-CTA-per-SM kernel of
+// gemv_flat.cuh when its shape allows. Measured per call at one token (graph replays, 152 SMs):
+// the dense MLP's 419 MB gate/up 74.9 -> 67.2 us and 210 MB down 42.2 -> 34.7 us; the QKV
+// projection (147 MB) 22.7 -> 26.3 us and o_proj (63 MB) no better inside the layer, so only
+// the dense MLP passes true.
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
-                               float* yf, uint16_t* yb, int ldy, cudaStream_t st) {
+                               float* yf, uint16_t* yb, int ldy, cudaStream_t st,
+                               bool flat_one_token = false) {
   if (T <= 0 || N <= 0) return cudaSuccess;
+  if (T == 1 && flat_one_token && flat::supported(K)) {
+    flat::Args a{};
+    a.W = W;
+    a.x = X;
+    a.N = N;
+    a.K = K;
+    a.F = N;
+    a.yf = yf;
+    a.yb = yb;
+    const cudaError_t e = MODE == kOutF32    ? flat::launch<flat::kPlainF32>(a, st)
+                          : MODE == kOutBF16 ? flat::launch<flat::kPlainBF16>(a, st)
+                                             : flat::launch<flat::kSwiGLU>(a, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   if (T >= kGemvMmaMinT && T <= kGemvMmaMaxT && (K & 31) == 0) {
     const cudaError_t e = launch_gemv_mma<MODE>(W, N, K, X, T, yf, yb, ldy, st);
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -980,9 +980,9 @@ extern "C" beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16
       return cuda_status(err_);
     return BEAM_OK;
   }
-  if (const cudaError_t err_ = launch_gemv<kOutSwiGLU>(w_gate_up, Fd, H, u, T, nullptr, act, Fd, st); err_ != cudaSuccess)
+  if (const cudaError_t err_ = launch_gemv<kOutSwiGLU>(w_gate_up, Fd, H, u, T, nullptr, act, Fd, st, true); err_ != cudaSuccess)
     return cuda_status(err_);
-  if (const cudaError_t err_ = launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st); err_ != cudaSuccess)
+  if (const cudaError_t err_ = launch_gemv<kOutBF16>(w_down, H, Fd, act, T, nullptr, out, H, st, true); err_ != cudaSuccess)
     return cuda_status(err_);
   return BEAM_OK;
 }

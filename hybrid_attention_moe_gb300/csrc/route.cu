@@ -20,7 +20,8 @@ constexpr int kRouteBatch = 3; // weight chunks in flight per thread in the GEMV
 // lo = w - hi - mid, each step exact), the BF16 activations times each part are exact FP32
 // products, and one BF16 GEMM against the stacked [hi; mid; lo] rows accumulates them in FP32;
 // logit = (u.hi + u.mid) + u.lo. Up to kRouteGemvMaxT tokens (decode, and every size the
-// allocation-free router accepts) the FP32 SIMT GEMV runs, one CTA per expert row.
+// allocation-free router accepts: it refuses more) the FP32 SIMT GEMV runs, one CTA per
+// expert row.
 constexpr int kRouteTcMinT = 257;
 constexpr int kRouteGemvMaxT = 256;   // up to here the GEMV form (the allocation-free router's range)
 constexpr int kRouteKChunks = 8;   // K chains of the tensor-core logits (640 at hidden 5120)
@@ -455,7 +456,8 @@ float* g_scratch_dev[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. In host code the array's name is
 // only a host-side stand-in, so the address is looked up once per device, with that device
-// current, and cached.
+// current, and cached for the life of the process (the device's primary context is assumed
+// to live as long: after a cudaDeviceReset the cached address would be stale).
 float* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -484,7 +486,10 @@ extern "C" beam_status beam_route_noalloc(const beam_layer_cfg* cfg, const beam_
       E / G < 2)
     return BEAM_ERR_INVALID_ARG;
   if (E > kMaxE || G > kMaxG || cfg->topk > kMaxK) return BEAM_ERR_UNSUPPORTED;
-  if (size_t(T) * size_t(E) > size_t(kNoAllocLogits)) return BEAM_ERR_INVALID_ARG;
+  // beyond kRouteGemvMaxT tokens beam_route takes its tensor-core form, which needs
+  // workspace; the allocation-free call stays within the range where both run the GEMV
+  if (T > kRouteGemvMaxT || size_t(T) * size_t(E) > size_t(kNoAllocLogits))
+    return BEAM_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(w_router)) return BEAM_ERR_INVALID_ARG;
   if (T == 0) return BEAM_OK;
   float* lg = scratch_on_current_device();

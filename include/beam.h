@@ -177,10 +177,13 @@ beam_status beam_route(const beam_layer_cfg* cfg, const beam_bf16* u, const floa
  * Same arguments and results as beam_route without logits, ws and ws_bytes. The router's
  * logits go to a fixed scratch array inside the library: 65536 floats (256 KiB) of device
  * memory that every GPU loading the library holds until the process exits, so it needs
- * T * n_experts <= 65536 (256 tokens at 256 experts); larger calls return
- * BEAM_ERR_INVALID_ARG and launch nothing. The call allocates nothing. The first call on a
- * device looks up the array's device address on that device (once, with it current); make
- * that first call before any stream capture. All calls on a device share the one array and
+ * T <= 256 and T * n_experts <= 65536 (256 tokens at 256 experts); larger calls return
+ * BEAM_ERR_INVALID_ARG and launch nothing. Within that range it runs the same kernels as
+ * beam_route and gives the same results. The call allocates nothing. The first call on a
+ * device looks up the array's device address on that device (once, with it current) and
+ * keeps it for the life of the process: this assumes the device's primary context lives as
+ * long (no cudaDeviceReset between calls). Make that first call before any stream capture.
+ * All calls on a device share the one array and
  * leave their logits in it; each call overwrites the whole T x E block it reads, so nothing
  * needs clearing, but calls whose kernels overlap on the GPU (different streams, no ordering)
  * race on the array and give undefined results. */

@@ -346,6 +346,34 @@ def test_moe(shape, T, n_used):
     assert_close(np64(out), ref, "moe out")
 
 
+@pytest.mark.parametrize("shape", [TINY, BEAM])
+def test_moe_bad_expert_slots_flagged_and_skipped(shape):
+    """One token with two slots naming experts out of range: the status word says so and the
+    output is the combine of the valid slots only (full width: the balanced one-token kernels;
+    tiny: the row-per-warp ones)."""
+    cfg = cfg_of(shape)
+    E, F, H, k = shape.n_experts, shape.d_ff_expert, shape.hidden, shape.topk
+    valid = list(range(k - 2))
+    row = valid[:1] + [E + 5] + valid[1:] + [-2]
+    idx = np.asarray([row], dtype=np.int32)
+    w = np.linspace(0.1, 0.5, k, dtype=np.float32)[None, :]
+    wgu = torch.zeros((E, 2 * F, H), dtype=torch.bfloat16, device=DEV)
+    wdn = torch.zeros((E, H, F), dtype=torch.bfloat16, device=DEV)
+    gu, dn = synth.expert_weights(shape, 0, 7, device=DEV, experts=valid)
+    for i, e in enumerate(valid):
+        wgu[e], wdn[e] = gu[i], dn[i]
+    u = synth.activations(1, H, 7, "u", DEV)
+    out = torch.empty((1, H), dtype=torch.bfloat16, device=DEV)
+    B.beam_get_device_status()
+    B.beam_moe(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), wgu, wdn,
+               out, ws_for(cfg, 1))
+    assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+    keep = [j for j in range(k) if 0 <= row[j] < E]
+    ref = O.moe(shape, np64(u), idx[:, keep], w[:, keep].astype(np.float64),
+                {e: np64(wgu[e]) for e in valid}, {e: np64(wdn[e]) for e in valid})
+    assert_close(np64(out), ref, "moe out, valid slots")
+
+
 def _nvfp4_experts(shape, used, seed):
     """NVFP4 expert tensors on the device (only the used experts drawn, the rest zero) and
     the oracle's view of the used ones."""
@@ -423,6 +451,22 @@ def test_dense_mlp(shape, T):
     u = synth.activations(T, shape.hidden, seed, "u", DEV)
     out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
     B.beam_dense_mlp(cfg, u, Wd["w_gate_up"], Wd["w_down"], out, ws_for(cfg, T))
+    ref = O.dense_mlp(shape, np64(u), np64(Wd["w_gate_up"]), np64(Wd["w_down"]))
+    assert_close(np64(out), ref, "dense out")
+
+
+@pytest.mark.parametrize("hidden,d_ff", [(2304, 2816), (4352, 3328)])
+def test_dense_mlp_one_token_ragged_rows(hidden, d_ff):
+    """One token on the balanced one-CTA-per-SM kernels with widths that split rows and
+    gate/up pairs unevenly over the CTAs and their warps (rows of 9-17 steps of 32 chunks; group
+    counts not multiples of the SM count)."""
+    shape = dataclasses.replace(BEAM, hidden=hidden, d_ff_dense=d_ff)
+    cfg = cfg_of(shape)
+    Wd = synth.dense_weights(shape, 0, 5, device=DEV)
+    u = synth.activations(1, hidden, 5, "u", DEV)
+    out = torch.empty((1, hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_dense_mlp(cfg, u, Wd["w_gate_up"], Wd["w_down"], out, ws_for(cfg, 1))
+    check_status()
     ref = O.dense_mlp(shape, np64(u), np64(Wd["w_gate_up"]), np64(Wd["w_down"]))
     assert_close(np64(out), ref, "dense out")
 

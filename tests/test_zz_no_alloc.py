@@ -33,7 +33,7 @@ def _route_both(shape, T, seed):
     return idx, w, idx_ref, w_ref
 
 
-@pytest.mark.parametrize("shape,T", [(BEAM, 1), (BEAM, 8), (BEAM, 200), (TINY, 77)])
+@pytest.mark.parametrize("shape,T", [(BEAM, 1), (BEAM, 8), (BEAM, 200), (TINY, 77), (TINY, 256)])
 def test_noalloc_route_matches_route_twice(shape, T):
     # two calls in a row: the second must not see anything left by the first
     for seed in (T, T + 1000):
@@ -44,12 +44,16 @@ def test_noalloc_route_matches_route_twice(shape, T):
     assert B.beam_get_device_status() == 0
 
 
-def test_noalloc_route_rejects_oversize():
-    cfg = B.LayerCfg.from_shape(BEAM, B.BEAM_ATTN_SWA_ROPE)
-    T = 257                                        # 257 x 256 logits > 65536
-    u = torch.zeros((T, BEAM.hidden), dtype=torch.bfloat16, device=DEV)
-    R = synth.router_weights(BEAM, 0, 0, device=DEV)
-    idx = torch.empty((T, 8), dtype=torch.int32, device=DEV)
-    w = torch.empty((T, 8), dtype=torch.float32, device=DEV)
+@pytest.mark.parametrize("shape", [BEAM, TINY])
+def test_noalloc_route_rejects_oversize(shape):
+    """257 tokens: past the array at 256 experts (257 x 256 > 65536 logits), and past the
+    256-token range at 16 experts, where the array would still hold the logits but
+    beam_route itself would take its tensor-core form."""
+    cfg = B.LayerCfg.from_shape(shape, B.BEAM_ATTN_SWA_ROPE)
+    T = 257
+    u = torch.zeros((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    R = synth.router_weights(shape, 0, 0, device=DEV)
+    idx = torch.empty((T, shape.topk), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, shape.topk), dtype=torch.float32, device=DEV)
     with pytest.raises(B.BeamError, match="invalid argument"):
         B.beam_route_noalloc(cfg, u, R["router"], R["corr_bias"], idx, w)
