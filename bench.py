@@ -24,7 +24,8 @@ so no flush is needed. The K timed steps are captured as one CUDA graph and repl
 between two events; each call's time comes from a second replay of the same K steps with a
 timing event (an external event node) before every call.
 
---experts nvfp4 gives the MoE layers NVFP4 expert weights (beam_moe_nvfp4; decode workloads).
+--experts nvfp4 / fp8 gives the MoE layers NVFP4 or block-scaled FP8 expert weights
+(beam_moe_nvfp4 / beam_moe_fp8; decode workloads).
 
 --impl reference times the CPU oracle on the same workload instead (a bounded sample per step).
 """
@@ -92,14 +93,21 @@ def is_nope(l, L):
     return (l + 1) % 6 == 0 or l == L - 1
 
 
-def expert_bytes(shape, nvfp4):
-    """Weight bytes of one expert: BF16, or NVFP4 (half a byte per element, one e4m3 scale per
-    16 elements, two FP32 matrix scales)."""
-    n = 3 * shape.hidden * shape.d_ff_expert
-    return n // 2 + n // 16 + 8 if nvfp4 else 2 * n
+def expert_bytes(shape, fmt="bf16"):
+    """Weight bytes of one expert: BF16; NVFP4 (half a byte per element, one e4m3 scale per
+    16 elements, two FP32 matrix scales); or FP8 (a byte per element, one FP32 scale per
+    128 x 128 block of each matrix)."""
+    H, F = shape.hidden, shape.d_ff_expert
+    n = 3 * H * F
+    if fmt == "nvfp4":
+        return n // 2 + n // 16 + 8
+    if fmt == "fp8":
+        blocks = lambda r, c: -(-r // 128) * -(-c // 128)  # noqa: E731
+        return n + 4 * (blocks(2 * F, H) + blocks(H, F))
+    return 2 * n
 
 
-def layer_bytes(shape, dense, n_experts_touched, kv_bytes, nvfp4=False):
+def layer_bytes(shape, dense, n_experts_touched, kv_bytes, fmt="bf16"):
     """Algorithmic HBM bytes of one layer step: every weight byte the step must read once,
     the KV bytes it must read, the gains; activations are negligible (<0.1%)."""
     H, D = shape.hidden, shape.head_dim
@@ -109,7 +117,7 @@ def layer_bytes(shape, dense, n_experts_touched, kv_bytes, nvfp4=False):
         b += 3 * H * shape.d_ff_dense * 2
     else:
         b += shape.n_experts * H * 4 + shape.n_experts * 4       # FP32 router
-        b += n_experts_touched * expert_bytes(shape, nvfp4)
+        b += n_experts_touched * expert_bytes(shape, fmt)
     return b + kv_bytes
 
 
@@ -187,13 +195,15 @@ def ncu_traffic(kernel_key):
 
 def stack_weights(args, layers, device):
     """Device weights of the held layers (one dict per layer, synth.layer_weights), with NVFP4
-    expert weights on the MoE layers under --experts nvfp4."""
+    or FP8 expert weights on the MoE layers under --experts nvfp4 / fp8."""
     W = []
     for l in layers:
-        nvfp4 = args.experts == "nvfp4" and l not in BEAM.dense_layers
-        W.append(synth.layer_weights(BEAM, l, args.seed, device=device, with_experts=not nvfp4))
-        if nvfp4:
+        quant = args.experts != "bf16" and l not in BEAM.dense_layers
+        W.append(synth.layer_weights(BEAM, l, args.seed, device=device, with_experts=not quant))
+        if quant and args.experts == "nvfp4":
             W[-1]["nvfp4"] = synth.expert_weights_nvfp4(BEAM, l, args.seed, device=device)
+        elif quant:
+            W[-1]["fp8"] = synth.expert_weights_fp8(BEAM, l, args.seed, device=device)
     return W
 
 
@@ -229,7 +239,7 @@ class Workload:
         self.prefill = kind == "stack_prefill"
         self.tokens = batch * chunk
         scale = 1.0
-        self.nvfp4 = args.experts == "nvfp4"
+        self.experts = args.experts
         W = stack_weights(args, layers, device) if W is None else W
         caches = []
         for l in layers:
@@ -254,7 +264,7 @@ class Workload:
             "workload": self.kind, "layers": self.layers, "batch": self.batch,
             "new_tokens_per_seq": self.chunk, "context": self.ctx,
             "kv_cache": "fp8_e4m3" if self.fp8 else "bf16",
-            "expert_weights": "nvfp4" if self.nvfp4 else "bf16",
+            "expert_weights": self.experts,
             "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
             "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
         }
@@ -292,6 +302,8 @@ class Workload:
                         ws)),
                     (f"L{l}.moe", (lambda W=W, cfg=cfg: B.beam_moe_nvfp4(
                         cfg, b["u"], b["idx"], b["w"], W["nvfp4"], b["m"], ws)) if "nvfp4" in W
+                     else (lambda W=W, cfg=cfg: B.beam_moe_fp8(
+                         cfg, b["u"], b["idx"], b["w"], W["fp8"], b["m"], ws)) if "fp8" in W
                      else (lambda W=W, cfg=cfg: B.beam_moe(
                          cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"], ws))),
                 ]
@@ -336,7 +348,7 @@ class Workload:
             elem = 1 if self.fp8 else 2
             kv = self.batch * (keys + self.chunk - 1) * shape.n_kv * shape.head_dim * 2 * elem
             dense = l in shape.dense_layers
-            per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv, self.nvfp4)
+            per[l] = layer_bytes(shape, dense, touched.get(l, shape.topk), kv, self.experts)
             tot += per[l]
         return tot, per
 
@@ -598,8 +610,8 @@ def dominant_bytes(wl, name, touched):
     """Algorithmic bytes of one call of the step (weights and cache it must read once)."""
     l = int(name.split(".")[0][1:])
     if name.endswith(".moe"):
-        key = ("moe_decode_nvfp4" if wl.nvfp4 else "moe_decode") + f"_t{wl.tokens}"
-        return touched[l] * expert_bytes(BEAM, wl.nvfp4), key
+        key = "moe_decode" + ("" if wl.experts == "bf16" else "_" + wl.experts) + f"_t{wl.tokens}"
+        return touched[l] * expert_bytes(BEAM, wl.experts), key
     if name.endswith(".attn"):
         nope = is_nope(l, BEAM.n_layers)
         keys = wl.ctx + 1 if nope else min(BEAM.window, wl.ctx + 1)
@@ -676,12 +688,25 @@ def oracle_layers(wl):
                              h["down"], h["down_scale"], float(h["down_global"]))
             return self.c[e]
 
+    class LazyFp8:
+        """expert -> the four FP8 arrays of oracle.moe_fp8, copied to the host on first use"""
+        def __init__(self, d):
+            self.d, self.c = d, {}
+
+        def __getitem__(self, e):
+            if e not in self.c:
+                h = {k: v[e].cpu().numpy() for k, v in self.d.items()}
+                self.c[e] = (h["gate_up"], h["gate_up_scale"], h["down"], h["down_scale"])
+            return self.c[e]
+
     Wo = []
     for W in wl.W:
         d = {}
         for k, v in W.items():
             if k == "nvfp4":
                 d["nvfp4_experts"] = LazyNvfp4(v)
+            elif k == "fp8":
+                d["fp8_experts"] = LazyFp8(v)
             else:
                 d[k] = Lazy(v) if (k in ("w_gate_up", "w_down") and v.dim() == 3) else host(v)
         Wo.append(d)
@@ -801,8 +826,8 @@ def main():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--context", type=int, default=100_000)
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"])
-    ap.add_argument("--experts", default="bf16", choices=["bf16", "nvfp4"],
-                    help="expert weight format of the MoE layers (decode only for nvfp4)")
+    ap.add_argument("--experts", default="bf16", choices=["bf16", "nvfp4", "fp8"],
+                    help="expert weight format of the MoE layers (decode only for nvfp4, fp8)")
     ap.add_argument("--lm-head-vocab", type=int, default=0,
                     help="also time the LM head after the stack over this many vocabulary rows "
                          "(beside the step; 0: off)")
@@ -812,9 +837,10 @@ def main():
     args = ap.parse_args()
     if args.lm_head_vocab and args.workload == "stack_prefill":
         ap.error("--lm-head-vocab is timed for decode workloads")
-    if args.experts == "nvfp4" and args.workload == "stack_prefill":
-        ap.error("--experts nvfp4 is a decode format here (beam_moe_nvfp4 takes up to 31 tokens)")
-    if args.experts == "nvfp4":
+    if args.experts != "bf16" and args.workload == "stack_prefill":
+        ap.error("--experts nvfp4 / fp8 are decode formats here (their kernels take up to 31 "
+                 "tokens)")
+    if args.experts != "bf16":
         args.no_prefill = True
     if args.workload == "stack_verify" and not 1 <= args.chunk <= 16:
         ap.error("stack_verify takes 1-16 new tokens per sequence (--chunk)")

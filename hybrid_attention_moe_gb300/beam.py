@@ -54,6 +54,7 @@ _SIGS = {
     "beam_route": [_P, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P],
     "beam_moe": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_moe_nvfp4": [_P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
+    "beam_moe_fp8": [_P, _P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_dense_mlp": [_P, _P, _P, _P, _I, _P, _P, _Z, _P],
     "beam_workspace_bytes": [_P, _I, _I],
     "beam_kv_cache_bytes": [_I, _I, _I, _I, _I],
@@ -240,6 +241,23 @@ def beam_moe_nvfp4(cfg: LayerCfg, u, topk_idx, topk_w, experts: dict, out, ws: t
     _check(lib().beam_moe_nvfp4(ctypes.byref(c), _ptr(u), _ptr(topk_idx), _ptr(topk_w),
                                 ctypes.byref(w), u.shape[0], _ptr(out), _ptr(ws), ws.numel(),
                                 _stream(stream)), "beam_moe_nvfp4")
+
+
+class Fp8ExpertsC(ctypes.Structure):
+    _fields_ = [("gate_up", ctypes.c_void_p), ("gate_up_scale", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("down_scale", ctypes.c_void_p)]
+
+
+def beam_moe_fp8(cfg: LayerCfg, u, topk_idx, topk_w, experts: dict, out, ws: torch.Tensor,
+                 stream=None):
+    """experts: the tensors of synth.expert_weights_fp8 (gate_up, gate_up_scale, down,
+    down_scale)."""
+    c = cfg.c()
+    w = Fp8ExpertsC(*[_ptr(experts[k]) for k in ("gate_up", "gate_up_scale", "down",
+                                                  "down_scale")])
+    _check(lib().beam_moe_fp8(ctypes.byref(c), _ptr(u), _ptr(topk_idx), _ptr(topk_w),
+                              ctypes.byref(w), u.shape[0], _ptr(out), _ptr(ws), ws.numel(),
+                              _stream(stream)), "beam_moe_fp8")
 
 
 def beam_dense_mlp(cfg: LayerCfg, u, w_gate_up, w_down, out, ws: torch.Tensor, stream=None):

@@ -746,6 +746,219 @@ __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// FP8 (e4m3, one FP32 scale per 128 x 128 block) expert weights, decode: the NVFP4 kernels'
+// layout with one byte per element. Lane (g, c) loads, per 128-element block of each of its
+// two rows, the 32 bytes of elements [32c, 32c + 32) (two 16-byte loads); cvt.rn.f16x2.e4m3x2
+// turns each code pair into f16 exactly; the block's 8 k16 steps accumulate into a fresh FP32
+// partial, which the block's scale (one per MMA row half: the gate/up kernel's upper and lower
+// 8 rows are gate and up rows with their own scale blocks) multiplies into the accumulator.
+// ------------------------------------------------------------------------------------------
+// Four e4m3 codes (one word, first code in the low byte) -> two f16x2 words, exactly.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{.reg .b16 a, b; mov.b32 {a, b}, %2; cvt.rn.f16x2.e4m3x2 %0, a; cvt.rn.f16x2.e4m3x2 %1, b;}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+struct Fp8Block {
+  uint4 q[2][2];   // [row][half]: 32 codes per row
+  float sc[2];     // scale of the block for rows g and g + 8
+};
+
+__device__ __forceinline__ void fp8_load_block(Fp8Block& B, const uint8_t* w0, const uint8_t* w1,
+                                               const float* s0, const float* s1, int b, int nb) {
+  b = min(b, nb - 1);
+  B.q[0][0] = ld_stream(w0 + size_t(b) * 128);
+  B.q[0][1] = ld_stream(w0 + size_t(b) * 128 + 16);
+  B.q[1][0] = ld_stream(w1 + size_t(b) * 128);
+  B.q[1][1] = ld_stream(w1 + size_t(b) * 128 + 16);
+  B.sc[0] = __ldg(s0 + b);
+  B.sc[1] = __ldg(s1 + b);
+}
+
+__device__ __forceinline__ void fp8_block_mma(const Fp8Block& B, const uint16_t* xb, bool tok,
+                                              float (&acc)[4]) {
+  uint32_t xv[16];
+  if (tok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t = *reinterpret_cast<const uint4*>(xb + 8 * i);
+      xv[4 * i] = t.x;
+      xv[4 * i + 1] = t.y;
+      xv[4 * i + 2] = t.z;
+      xv[4 * i + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xv[i] = 0u;
+  }
+  uint32_t w[2][16];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t qw[8] = {B.q[r][0].x, B.q[r][0].y, B.q[r][0].z, B.q[r][0].w,
+                            B.q[r][1].x, B.q[r][1].y, B.q[r][1].z, B.q[r][1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e4m3x4_to_f16(qw[i], w[r][2 * i], w[r][2 * i + 1]);
+  }
+  float p[4] = {0.f, 0.f, 0.f, 0.f}, p2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    if (st & 1)
+      mma_f16_16816(p2, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                    xv[2 * st], xv[2 * st + 1]);
+    else
+      mma_f16_16816(p, w[0][2 * st], w[1][2 * st], w[0][2 * st + 1], w[1][2 * st + 1],
+                    xv[2 * st], xv[2 * st + 1]);
+  }
+  acc[0] = fmaf(B.sc[0], p[0] + p2[0], acc[0]);
+  acc[1] = fmaf(B.sc[0], p[1] + p2[1], acc[1]);
+  acc[2] = fmaf(B.sc[1], p[2] + p2[2], acc[2]);
+  acc[3] = fmaf(B.sc[1], p[3] + p2[3], acc[3]);
+}
+
+// acc (rows g, g+8; columns = pairs 2c, 2c+1) over the 128-element blocks [bb, be); w0 / w1:
+// the two rows' codes (offset by 32c), s0 / s1: their scale rows (one FP32 per block), xr: the
+// lane's token in f16 (offset by 32c). The next block's loads are issued before the current
+// block is converted and multiplied.
+__device__ __forceinline__ void fp8_rows_mma(const uint8_t* w0, const uint8_t* w1,
+                                             const float* s0, const float* s1,
+                                             const uint16_t* xr, bool tok, int bb, int be,
+                                             float (&acc)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+  if (bb >= be) return;
+  Fp8Block cur, nxt;
+  fp8_load_block(cur, w0, w1, s0, s1, bb, be);
+  for (int b = bb; b < be; ++b) {
+    if (b + 1 < be) fp8_load_block(nxt, w0, w1, s0, s1, b + 1, be);
+    fp8_block_mma(cur, xr + size_t(b) * 128, tok, acc);
+    cur = nxt;
+  }
+}
+
+// grid (ceil(F / (64 / KS)), max active experts); a row block is 8 units (gate rows f0..f0+7
+// and the matching up rows), KS warps per row block. a16[pair][f] = f16(bf16(silu(gate) * up)).
+template <int KS>
+__global__ void __launch_bounds__(256, 3) moe_gate_up_fp8_kernel(
+    const uint16_t* __restrict__ u16, beam_fp8_experts W, int H, int F, int k, MoePlan pl,
+    const int32_t* __restrict__ direct, int E, uint16_t* __restrict__ a16) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[8][32][4];
+  const int ai = blockIdx.y;
+  if (ai >= (direct != nullptr ? k : *pl.n_active)) return;   // uniform over the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int ks = warp % KS;
+  const int f0 = (blockIdx.x * (8 / KS) + warp / KS) * 8;
+  ExpertSlot es;
+  if (!expert_slot(pl, direct, E, ai, es)) {   // uniform over the CTA
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(BEAM_DEV_BAD_EXPERT);
+    return;
+  }
+  const int f = min(f0 + g, F - 1);
+  const size_t rg = size_t(es.e) * 2 * F + f, ru = rg + F;
+  const int nb = H >> 7;
+  const uint8_t* w0 = W.gate_up + rg * H + 32 * c;
+  const uint8_t* w1 = W.gate_up + ru * H + 32 * c;
+  // scale rows: expert e's [2F/128][H/128] grid, the row block of the gate and of the up row
+  const float* s0 = W.gate_up_scale + (size_t(es.e) * (2 * F / 128) + f / 128) * nb;
+  const float* s1 = W.gate_up_scale + (size_t(es.e) * (2 * F / 128) + (F + f) / 128) * nb;
+  const int bb = ks * nb / KS, be = (ks + 1) * nb / KS;
+  for (int pp = es.p0; pp < es.p1; pp += 8) {
+    const int np = min(8, es.p1 - pp);
+    const bool tok = g < np;
+    const uint16_t* xr = u16 + size_t(tok ? pair_at(pl, direct, pp + g) / k : 0) * H + 32 * c;
+    float acc[4];
+    fp8_rows_mma(w0, w1, s0, s1, xr, tok, bb, be, acc);
+    if (fp4_reduce_ks<KS>(acc, red)) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 2 * c + j;
+        if (col < np && f0 + g < F) {
+          const float a = round_bf(siluf_(acc[j]) * acc[2 + j]);
+          a16[size_t(pair_at(pl, direct, pp + col)) * F + f0 + g] = f32_to_f16_bits(a);
+        }
+      }
+    }
+    if (KS > 1) __syncthreads();   // the reduction buffer is free for the next pass
+  }
+}
+
+// grid (ceil(H / (128 / KS)), max active experts); a row block is 16 rows h, KS warps per row
+// block; y[pair][h] in FP32; the last CTA of each column of rows combines them for every token,
+// slots in order.
+template <int KS>
+__global__ void __launch_bounds__(256, 3) moe_down_fp8_kernel(
+    const uint16_t* __restrict__ a16, beam_fp8_experts W, int H, int F, MoePlan pl,
+    const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ topk_w, int T, int k, int E, int* __restrict__ cnt,
+    float* __restrict__ y, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[8][32][4];
+  const int na = direct != nullptr ? k : *pl.n_active;
+  const int ai = blockIdx.y;
+  if (ai >= max(na, 1)) return;   // uniform over the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  constexpr int kRows = 128 / KS;   // rows h per CTA
+  const int ks = warp % KS;
+  const int h0 = blockIdx.x * kRows + (warp / KS) * 16;
+  ExpertSlot es;
+  if (ai < na && expert_slot(pl, direct, E, ai, es)) {   // uniform over the CTA
+    const int hr0 = min(h0 + g, H - 1), hr1 = min(h0 + g + 8, H - 1);
+    const size_t r0 = size_t(es.e) * H + hr0, r1 = size_t(es.e) * H + hr1;
+    const int nb = F >> 7;
+    const uint8_t* w0 = W.down + r0 * F + 32 * c;
+    const uint8_t* w1 = W.down + r1 * F + 32 * c;
+    const float* s0 = W.down_scale + (size_t(es.e) * (H / 128) + hr0 / 128) * nb;
+    const float* s1 = W.down_scale + (size_t(es.e) * (H / 128) + hr1 / 128) * nb;
+    const int bb = ks * nb / KS, be = (ks + 1) * nb / KS;
+    for (int pp = es.p0; pp < es.p1; pp += 8) {
+      const int np = min(8, es.p1 - pp);
+      const bool tok = g < np;
+      const uint16_t* xr = a16 + size_t(tok ? pair_at(pl, direct, pp + g) : 0) * F + 32 * c;
+      float acc[4];
+      fp8_rows_mma(w0, w1, s0, s1, xr, tok, bb, be, acc);
+      if (fp4_reduce_ks<KS>(acc, red)) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int col = 2 * c + j;
+          if (col < np) {
+            const size_t yo = size_t(pair_at(pl, direct, pp + col)) * H;
+            if (h0 + g < H) y[yo + h0 + g] = acc[j];
+            if (h0 + g + 8 < H) y[yo + h0 + g + 8] = acc[2 + j];
+          }
+        }
+      }
+      if (KS > 1) __syncthreads();   // the reduction buffer is free for the next pass
+    }
+  }
+  __shared__ int s_last;
+  // the CTA barrier orders every thread's y stores before thread 0's device-scope fence,
+  // which releases them with the counter increment
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(cnt + blockIdx.x, 1) == max(na, 1) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int hb = blockIdx.x * kRows;
+  const int nh = min(kRows, H - hb);
+  for (int i = threadIdx.x; i < T * nh; i += blockDim.x) {
+    const int t = i / nh, h = hb + (i - t * nh);
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[size_t(t) * k + j];
+      if (e < 0 || e >= E) continue;
+      s = fmaf(topk_w[size_t(t) * k + j], __ldcg(y + (size_t(t) * k + j) * H + h), s);
+    }
+    out[size_t(t) * H + h] = f2bf(s);
+  }
+}
+
 __global__ void moe_combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                                    const int32_t* __restrict__ idx, int T, int H, int k, int E,
                                    uint16_t* __restrict__ out) {
@@ -1038,6 +1251,56 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
   } else {
     launch_pdl(moe_gate_up_fp4_kernel<1>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
     launch_pdl(moe_down_fp4_kernel<1>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+               topk_w, T, k, E, cnt, y, out);
+  }
+  return launch_status();
+}
+
+extern "C" beam_status beam_moe_fp8(const beam_layer_cfg* cfg, const beam_bf16* u,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    const beam_fp8_experts* w, int T, beam_bf16* out, void* ws,
+                                    size_t ws_bytes, beam_stream_t stream) {
+  using namespace beam;
+  if (!cfg || T < 0 || !u || !topk_idx || !topk_w || !w || !out || !w->gate_up ||
+      !w->gate_up_scale || !w->down || !w->down_scale)
+    return BEAM_ERR_INVALID_ARG;
+  const int H = cfg->hidden, F = cfg->d_ff_expert, E = cfg->n_experts, k = cfg->topk;
+  if (H <= 0 || F <= 0 || E <= 0 || k <= 0) return BEAM_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(ws) || !aligned16(w->gate_up) || !aligned16(w->down))
+    return BEAM_ERR_INVALID_ARG;
+  if (E > 4096 || (H & 127) || (F & 127) || T >= kMoeGemmMinT) return BEAM_ERR_UNSUPPORTED;
+  if (T == 0) return BEAM_OK;
+  const int P = T * k;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Carver cv{static_cast<char*>(ws), ws_bytes};
+  MoePlan pl = carve_plan(cv, E, P, false);
+  uint16_t* a16 = cv.take<uint16_t>(size_t(P) * F);
+  float* y = cv.take<float>(size_t(P) * H);
+  int* cnt = cv.take<int>(size_t(H / 8 + 1));
+  uint16_t* u16 = cv.take<uint16_t>(size_t(T) * H);
+  if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+  // one token: its k slots are the active list directly; more: the plan groups the pairs
+  const bool direct = T == 1;
+  const int32_t* dix = direct ? topk_idx : nullptr;
+  const int na = direct ? k : (P < E ? P : E);
+  // up to 4 tokens four warps split each row block's K blocks (the grid is under a wave
+  // otherwise); from 5 tokens a warp takes a whole row block
+  const bool split = T <= kFp4KSMaxT;
+  const int rows_down = split ? 32 : 128, units_up = split ? 16 : 64;
+  const int n_cnt = (H + rows_down - 1) / rows_down;
+  const int n = T * H;
+  launch_pdl(fp4_prep_kernel, dim3((max(n, n_cnt) + 255) / 256), dim3(256), 0, st, u, n, u16, cnt,
+             n_cnt);
+  if (!direct)
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+  const dim3 gu((F + units_up - 1) / units_up, na), gd(n_cnt, na);
+  if (split) {
+    launch_pdl(moe_gate_up_fp8_kernel<4>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
+    launch_pdl(moe_down_fp8_kernel<4>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
+               topk_w, T, k, E, cnt, y, out);
+  } else {
+    launch_pdl(moe_gate_up_fp8_kernel<1>, gu, dim3(256), 0, st, u16, *w, H, F, k, pl, dix, E, a16);
+    launch_pdl(moe_down_fp8_kernel<1>, gd, dim3(256), 0, st, a16, *w, H, F, pl, dix, topk_idx,
                topk_w, T, k, E, cnt, y, out);
   }
   return launch_status();

@@ -24,8 +24,9 @@ class BeamStack:
     weights: list (one per layer) of dicts of device tensors, keys as made by
              synth.layer_weights (attn_pre, attn_post, mlp_pre, mlp_post, w_qkvg, q_norm,
              k_norm, gate_bias, w_o, and w_gate_up/w_down (+ router, corr_bias on MoE layers);
-             an MoE layer may hold "nvfp4" (synth.expert_weights_nvfp4) instead of
-             w_gate_up/w_down, and then runs beam_moe_nvfp4).
+             an MoE layer may hold "nvfp4" (synth.expert_weights_nvfp4) or "fp8"
+             (synth.expert_weights_fp8) instead of w_gate_up/w_down, and then runs
+             beam_moe_nvfp4 or beam_moe_fp8).
     caches : list of B.KVCache, one per layer (window = W on sliding-window layers, 0 on NoPE).
     """
 
@@ -92,6 +93,8 @@ class BeamStack:
                          ws, stream)
             if "nvfp4" in W:
                 B.beam_moe_nvfp4(cfg, b["u"], b["idx"], b["w"], W["nvfp4"], b["m"], ws, stream)
+            elif "fp8" in W:
+                B.beam_moe_fp8(cfg, b["u"], b["idx"], b["w"], W["fp8"], b["m"], ws, stream)
             else:
                 B.beam_moe(cfg, b["u"], b["idx"], b["w"], W["w_gate_up"], W["w_down"], b["m"],
                            ws, stream)

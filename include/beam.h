@@ -229,6 +229,30 @@ beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16* u,
                            const beam_nvfp4_experts* w, int T, beam_bf16* out, void* ws,
                            size_t ws_bytes, beam_stream_t stream);
 
+/* Block-scaled FP8 expert weights (the AREX feed article on the Day-0 support says the weights
+ * ship in BF16, FP8 and NVFP4 without printing a layout; this is the block-scaled e4m3 format of
+ * the DeepSeek-V3 release, whose routing the Beam page's MoE section names): e4m3fn codes, one
+ * byte per element, row-major like the BF16 experts; one FP32 scale per 128 x 128 block of
+ * each expert matrix. Element value = code * block scale. Device pointers, 16-byte aligned.
+ *  gate_up [E][2F][H] (rows gate, then up), gate_up_scale [E][2F/128][H/128]
+ *  down [E][H][F], down_scale [E][H/128][F/128]. */
+typedef struct {
+  const uint8_t* gate_up;
+  const float* gate_up_scale;
+  const uint8_t* down;
+  const float* down_scale;
+} beam_fp8_experts;
+
+/* beam_moe with FP8 expert weights (weight-only: activations stay BF16; codes become f16
+ * exactly in registers and the products run in f16 with FP32 accumulation, each 128-element
+ * block's sum multiplied by its FP32 scale). Same arguments and results as beam_moe
+ * otherwise; u is rounded to f16 (exact for BF16 values of magnitude 2^-14 .. 65504). Decode
+ * sizes: 1 <= T < 32 tokens; other T, or H or d_ff not a multiple of 128, return
+ * BEAM_ERR_UNSUPPORTED. The workspace is the one beam_workspace_bytes gives for T. */
+beam_status beam_moe_fp8(const beam_layer_cfg* cfg, const beam_bf16* u, const int32_t* topk_idx,
+                         const float* topk_w, const beam_fp8_experts* w, int T, beam_bf16* out,
+                         void* ws, size_t ws_bytes, beam_stream_t stream);
+
 /* Dense SwiGLU MLP of layers 0-2 (Beam page, MoE section: d_ff 20480; change 7 runs the
  * activation in one kernel). w_gate_up (device) [2*Fd][H], w_down (device) [H][Fd]. */
 beam_status beam_dense_mlp(const beam_layer_cfg* cfg, const beam_bf16* u,

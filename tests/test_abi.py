@@ -91,3 +91,26 @@ def test_argument_checks_answer_before_any_launch(lib):
     assert moe(1, cfg=odd) == 2
     bad = B.NvFp4ExpertsC(a, None, a, a, a, a)
     assert moe(1, ex=bad) == 1
+
+
+def test_fp8_expert_argument_checks(lib):
+    """beam_moe_fp8: decode sizes only (1-31 tokens), H and d_ff multiples of 128, every
+    weight pointer given; all answered on the host before any launch."""
+    import ctypes
+    import synth
+    from hybrid_attention_moe_gb300 import beam as B
+    P = ctypes.c_void_p
+    a, b, c = P(0x10000), P(0x20000), P(0x30000)
+    cfg = B.LayerCfg.from_shape(synth.BEAM, B.BEAM_ATTN_SWA_ROPE).c()
+    ex = B.Fp8ExpertsC(a, a, a, a)
+
+    def moe(T, cfg=cfg, ex=ex):
+        return lib.beam_moe_fp8(ctypes.byref(cfg), a, b, c, ctypes.byref(ex), T, a, a, 1 << 20,
+                                None)
+    assert moe(32) == 2 and moe(100) == 2
+    assert moe(0) == 0
+    odd = B.LayerCfg.from_shape(synth.BEAM, B.BEAM_ATTN_SWA_ROPE).c()
+    odd.d_ff_expert = 2560 + 64
+    assert moe(1, cfg=odd) == 2
+    assert moe(1, ex=B.Fp8ExpertsC(a, None, a, a)) == 1
+    assert moe(1, ex=B.Fp8ExpertsC(P(0x10008), a, a, a)) == 1     # misaligned codes

@@ -17,8 +17,10 @@ KV_PER_KEY_BF16 = BEAM.n_kv * BEAM.head_dim * 2 * 2     # K and V of 8 heads x 1
 
 
 def test_layer_bytes_per_unit():
-    assert bench.expert_bytes(BEAM, False) == 3 * 5120 * 2560 * 2
-    assert bench.expert_bytes(BEAM, True) == 3 * 5120 * 2560 // 2 + 3 * 5120 * 2560 // 16 + 8
+    assert bench.expert_bytes(BEAM) == 3 * 5120 * 2560 * 2
+    assert bench.expert_bytes(BEAM, "nvfp4") == 3 * 5120 * 2560 // 2 + 3 * 5120 * 2560 // 16 + 8
+    # FP8: a byte per element plus one FP32 scale per 128 x 128 block (40 x 40 + 40 x 20)
+    assert bench.expert_bytes(BEAM, "fp8") == 3 * 5120 * 2560 + 4 * (40 * 40 + 40 * 20)
     swa = bench.layer_bytes(BEAM, False, 8, 512 * KV_PER_KEY_BF16)
     assert abs(swa / 1e6 - 846.24) < 0.005
     nope = bench.layer_bytes(BEAM, False, 8, 100_001 * KV_PER_KEY_BF16)
@@ -26,8 +28,8 @@ def test_layer_bytes_per_unit():
     assert abs(bench.layer_bytes(BEAM, True, 0, 0) / 1e6 - 838.90) < 0.005
     assert abs(bench.layer_bytes(BEAM, False, 8, 0) / 1e6 - 844.15) < 0.005
     # NVFP4 experts change only the experts' share
-    d = bench.layer_bytes(BEAM, False, 8, 0) - bench.layer_bytes(BEAM, False, 8, 0, nvfp4=True)
-    assert d == 8 * (bench.expert_bytes(BEAM, False) - bench.expert_bytes(BEAM, True))
+    d = bench.layer_bytes(BEAM, False, 8, 0) - bench.layer_bytes(BEAM, False, 8, 0, "nvfp4")
+    assert d == 8 * (bench.expert_bytes(BEAM) - bench.expert_bytes(BEAM, "nvfp4"))
 
 
 def test_traffic_entries_are_per_call():
@@ -36,8 +38,8 @@ def test_traffic_entries_are_per_call():
     its algorithmic bytes (no re-reads); entries whose sources changed report None."""
     import json
     d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    for key, nvfp4 in (("moe_decode_t1", False), ("moe_decode_nvfp4_t1", True)):
-        assert algo_ok(d[key]["bytes_per_launch"], 8 * bench.expert_bytes(BEAM, nvfp4)), key
+    for key, fmt in (("moe_decode_t1", "bf16"), ("moe_decode_nvfp4_t1", "nvfp4")):
+        assert algo_ok(d[key]["bytes_per_launch"], 8 * bench.expert_bytes(BEAM, fmt)), key
         t = bench.ncu_traffic(key)
         assert t is None or t == d[key]["bytes_per_launch"]
     assert bench.ncu_traffic("moe_decode_t8") is None

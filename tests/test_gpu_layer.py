@@ -49,11 +49,26 @@ class LazyNvfp4:
         return self.c[e]
 
 
+class LazyFp8:
+    """expert -> its four FP8 arrays (oracle.moe_fp8), copied to the host on first use."""
+
+    def __init__(self, d):
+        self.d, self.c = d, {}
+
+    def __getitem__(self, e):
+        if e not in self.c:
+            h = {k: v[e].cpu().numpy() for k, v in self.d.items()}
+            self.c[e] = (h["gate_up"], h["gate_up_scale"], h["down"], h["down_scale"])
+        return self.c[e]
+
+
 def oracle_weights(W):
     out = {}
     for k, v in W.items():
         if k == "nvfp4":
             out["nvfp4_experts"] = LazyNvfp4(v)
+        elif k == "fp8":
+            out["fp8_experts"] = LazyFp8(v)
         elif k in ("w_gate_up", "w_down") and v.dim() == 3:
             out[k] = LazyRows(v)
         else:
@@ -61,7 +76,8 @@ def oracle_weights(W):
     return out
 
 
-def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvfp4=False):
+def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvfp4=False,
+                fp8_experts=False):
     """One MoE layer of the truncated stack, one decode token per sequence, chained-step bars.
 
     The oracle runs in two stages with the oracle's own functions, in layer_forward's order:
@@ -76,9 +92,12 @@ def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvf
     positions = [c + 1 for c in contexts]
     max_pos = max(positions)
     cap, window = (max_pos + 8, 0) if nope else (shape.window, shape.window)
-    W = synth.layer_weights(shape, layer, seed, device=DEV, with_experts=not nvfp4)
+    W = synth.layer_weights(shape, layer, seed, device=DEV,
+                            with_experts=not (nvfp4 or fp8_experts))
     if nvfp4:
         W["nvfp4"] = synth.expert_weights_nvfp4(shape, layer, seed, device=DEV)
+    if fp8_experts:
+        W["fp8"] = synth.expert_weights_fp8(shape, layer, seed, device=DEV)
     c = synth.kv_cache(shape, S, cap, seed, layer, fp8=fp8, k_scale=scale[0], v_scale=scale[1],
                        device=DEV)
     kc = B.KVCache(c["k"], c["v"], window, *scale)
@@ -99,6 +118,8 @@ def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvf
         logits, idx, w = O.route(shape, u1, R["router"], R["corr_bias"])
         if nvfp4:
             m = O.moe_nvfp4(shape, u1, idx, w, Wo["nvfp4_experts"])
+        elif fp8_experts:
+            m = O.moe_fp8(shape, u1, idx, w, Wo["fp8_experts"])
         else:
             m = O.moe(shape, u1, idx, w, Wo["w_gate_up"], Wo["w_down"])
         h2, _ = O.boundary_norm(m, h1, Wo["mlp_post"], None, 2 * layer + 3, shape.eps)
@@ -172,3 +193,10 @@ def test_full_width_swa_moe_layer_decode_nvfp4_experts(batch):
 
 def test_full_width_nope_moe_layer_decode_ctx100k_fp8():
     _layer_case(BEAM, 5, [100_000, 100_000], fp8=True, scale=(0.0371, 0.0371))
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_full_width_swa_moe_layer_decode_fp8_experts(batch):
+    """The layer with block-scaled FP8 expert weights (beam_moe_fp8 in the stack driver; the
+    oracle's layer dequantises the selected experts)."""
+    _layer_case(BEAM, 3, [4096] * batch, fp8_experts=True)

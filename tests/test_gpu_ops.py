@@ -440,6 +440,66 @@ def test_moe_nvfp4_bad_expert_slots_flagged_and_skipped():
             assert_close(np64(out[t:t + 1]), ref, "moe nvfp4 out, valid slots")
 
 
+def _fp8_experts(shape, used, seed):
+    """FP8 expert tensors on the device (only the used experts drawn, the rest zero) and the
+    oracle's view of the used ones (codes and block scales)."""
+    E = shape.n_experts
+    part = synth.expert_weights_fp8(shape, 0, seed, device=DEV, experts=used)
+    full = {k: torch.zeros((E,) + tuple(v.shape[1:]), dtype=v.dtype, device=DEV)
+            for k, v in part.items()}
+    for i, e in enumerate(used):
+        for k in full:
+            full[k][e] = part[k][i]
+    host = {k: v.cpu().numpy() for k, v in part.items()}
+    experts = {e: (host["gate_up"][i], host["gate_up_scale"][i], host["down"][i],
+                   host["down_scale"][i]) for i, e in enumerate(used)}
+    return full, experts
+
+
+@pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 5, None),
+                                            (TINY, 13, None), (TINY, 31, 6), (BEAM, 1, None),
+                                            (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None),
+                                            (BEAM, 31, 20)])
+def test_moe_fp8(shape, T, n_used):
+    """Block-scaled FP8 expert weights (e4m3 codes, one FP32 scale per 128 x 128 block):
+    mma.sync f16 products of the exactly converted codes, each block's sum times its scale;
+    up to 4 tokens four warps split each row block's K (T=4 and T=5 sit on either side);
+    T=31 over 6 experts gives experts more than 8 pairs (several passes)."""
+    seed = 97 + T
+    cfg = cfg_of(shape)
+    idx, w = _random_routing(shape, T, seed, n_used)
+    used = sorted(set(idx.ravel().tolist()))
+    full, experts = _fp8_experts(shape, used, seed)
+    u = synth.activations(T, shape.hidden, seed, "u", DEV)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_moe_fp8(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), full,
+                   out, ws_for(cfg, T))
+    check_status()
+    ref = O.moe_fp8(shape, np64(u), idx, w.astype(np.float64), experts)
+    assert_close(np64(out), ref, "moe fp8 out")
+
+
+def test_moe_fp8_bad_expert_slots_flagged_and_skipped():
+    shape = TINY
+    cfg = cfg_of(shape)
+    for rows in ([[0, 1, 99, 2]], [[0, 1, 99, 2], [5, -3, 1, 7]]):
+        T = len(rows)
+        idx = np.asarray(rows, dtype=np.int32)
+        w = np.full((T, 4), 0.5, dtype=np.float32)
+        full, experts = _fp8_experts(shape, [0, 1, 2, 5, 7], 4)
+        u = synth.activations(T, shape.hidden, 4, "u", DEV)
+        out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+        B.beam_get_device_status()
+        B.beam_moe_fp8(cfg, u, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV),
+                       full, out, ws_for(cfg, T))
+        assert B.beam_get_device_status() & B.DEV_BAD_EXPERT
+        for t in range(T):
+            keep = [j for j in range(4) if 0 <= rows[t][j] < shape.n_experts]
+            ref = O.moe_fp8(shape, np64(u[t:t + 1]), idx[t:t + 1, keep],
+                            np.full((1, len(keep)), 0.5), experts)
+            assert_close(np64(out[t:t + 1]), ref, "moe fp8 out, valid slots")
+
+
 @pytest.mark.parametrize("shape,T", [(TINY, 1), (TINY, 5), (TINY, 13), (TINY, 64), (TINY, 200),
                                      (BEAM, 1), (BEAM, 3), (BEAM, 8), (BEAM, 40), (BEAM, 130)])
 def test_dense_mlp(shape, T):
