@@ -238,6 +238,12 @@ class Workload:
         self.chunk = chunk
         self.prefill = kind == "stack_prefill"
         self.tokens = batch * chunk
+        # the bound on tokens per sequence that beam_attn is given, which picks its form:
+        # split-K decode up to 4 (up to 16 when there are few sequences), query tiles above;
+        # --attn-form forces one or the other (a bound of 1, or one above 16)
+        form = getattr(args, "attn_form", "natural")
+        self.attn_form = form
+        self.q_bound = chunk if form == "natural" else (1 if form == "decode" else max(chunk, 17))
         scale = 1.0
         self.experts = args.experts
         W = stack_weights(args, layers, device) if W is None else W
@@ -265,6 +271,7 @@ class Workload:
             "new_tokens_per_seq": self.chunk, "context": self.ctx,
             "kv_cache": "fp8_e4m3" if self.fp8 else "bf16",
             "expert_weights": self.experts,
+            "attn_form": self.attn_form,
             "hidden": BEAM.hidden, "heads": f"{BEAM.n_q}q/{BEAM.n_kv}kv x {BEAM.head_dim}",
             "experts": f"{BEAM.n_experts} (8 groups, top-4 groups, top-8), d_ff {BEAM.d_ff_expert}",
         }
@@ -288,7 +295,7 @@ class Workload:
                     b["q"], b["g"], kc, ws)),
                 (f"L{l}.attn", lambda W=W, cfg=cfg, kc=kc: B.beam_attn(
                     cfg, b["q"], b["g"], W["gate_bias"], kc, self.seq, self.pos, self.max_pos,
-                    W["w_o"], b["a"], ws, max_q_per_seq=self.chunk)),
+                    W["w_o"], b["a"], ws, max_q_per_seq=self.q_bound)),
                 (f"L{l}.norm_attn", lambda W=W, cfg=cfg, l=l: B.beam_boundary_norm(
                     b["a"], b["h"], b["u"], W["attn_post"], W["mlp_pre"], 2 * l + 2, cfg.eps)),
             ]
@@ -821,6 +828,9 @@ def main():
     ap.add_argument("--seqs", type=int, default=8, help="prefill: sequences per step")
     ap.add_argument("--chunk", type=int, default=2048,
                     help="prefill: new tokens per sequence; stack_verify: tokens per sequence")
+    ap.add_argument("--attn-form", default="natural", choices=["natural", "decode", "prefill"],
+                    help="stack_verify: force beam_attn's split-K decode form or its query-tile "
+                         "prefill form (natural: the library's own choice)")
     ap.add_argument("--no-prefill", action="store_true",
                     help="stack_decode: skip the prefill object (same stack, same weights)")
     ap.add_argument("--batch", type=int, default=1)

@@ -695,6 +695,18 @@ int num_sms() {
 }
 
 constexpr int kDecodeMaxQ = 4;   // split-K per token up to this many tokens per sequence
+// Verification batches of speculative decoding (up to kVerifyMaxQ tokens per sequence): the
+// query-tile prefill form walks one sequence's keys per (KV head, job) item without splitting
+// them, so with fewer items than SMs most SMs idle (one sequence at 100K keys and 8 tokens:
+// 2.8 ms for the NoPE layer); the split-K decode form reads the keys once per token but keeps
+// every SM busy (345 us). The decode form is taken while the call has fewer (sequence, KV
+// head) items than two per SM.
+constexpr int kVerifyMaxQ = 16;
+bool decode_form(int T, int max_q_per_seq, int n_kv) {
+  if (max_q_per_seq <= kDecodeMaxQ) return true;
+  const long seqs = (long(T) + max_q_per_seq - 1) / max_q_per_seq;   // at least this many
+  return max_q_per_seq <= kVerifyMaxQ && seqs * n_kv < 2L * num_sms();
+}
 
 struct DecodePlan {
   int kps, n_splits;
@@ -789,7 +801,7 @@ cudaError_t launch_prefill(const uint16_t* q, const uint16_t* g, const uint16_t*
 
 size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
   size_t b = align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
-  {   // the split-K decode form may be chosen for any T (max_q_per_seq <= kDecodeMaxQ)
+  {   // the split-K decode form may be chosen for any T (decode_form)
     // partials only when the splits merge through the workspace (more than a cluster)
     const DecodePlan pl = decode_plan(T, c->n_kv, max_keys_of(window, max_pos > 0 ? max_pos : 1));
     const size_t parts =
@@ -835,7 +847,8 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
   uint16_t* og = cv.take<uint16_t>(size_t(T) * HD);
   cudaError_t e;
   const int G = cfg->n_q / cfg->n_kv;
-  if (max_q_per_seq <= kDecodeMaxQ &&
+  const bool dec = decode_form(T, max_q_per_seq, cfg->n_kv);
+  if (dec &&
       adec::supported(D, G, cache->window, cache->capacity, fp8, cache->k, cache->v,
                       max_keys_of(cache->window, max_pos))) {
     const size_t db = adec::ws_bytes(T, cfg->n_kv, cache->window, max_pos, fp8);
@@ -844,7 +857,7 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
     e = adec::decode(q, g, gate_bias, seq_id, pos, T, max_pos, cfg->n_q, cfg->n_kv, *cache, sl2,
                      fp8 ? cache->v_scale : 1.f, og, dw, db, st);
     if (e != cudaSuccess) return cuda_status(e);
-  } else if (max_q_per_seq <= kDecodeMaxQ) {
+  } else if (dec) {
     const DecodePlan pl = decode_plan(T, cfg->n_kv, max_keys_of(cache->window, max_pos));
     const size_t parts =
         pl.n_splits > kClusterMaxSplits ? size_t(T) * cfg->n_kv * pl.n_splits * kRows : 0;

@@ -147,8 +147,10 @@ beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16* u,
  *  gate_bias (device) [n_q] bf16.
  *  max_pos   host-side upper bound of pos[] (sizes the key split); larger pos are flagged.
  *  max_q_per_seq  host-side upper bound of the number of the call's tokens that belong to one
- *            sequence (1 for a decode batch). Up to 4, every token runs split-K over its keys;
- *            above, tokens are taken in tiles of 16 consecutive tokens that share K/V tiles,
+ *            sequence (1 for a decode batch). Up to 4 -- and up to 16 (the verification
+ *            batches of speculative decoding) while the call holds fewer than two
+ *            (sequence, KV head) pairs per SM -- every token runs split-K over its keys;
+ *            otherwise tokens are taken in tiles of consecutive tokens that share K/V tiles,
  *            which expects the tokens of a sequence to be consecutive in the call (any order
  *            is still computed correctly, only more slowly).
  *  w_o       (device) [H][n_q*D] bf16.   out (device) [T][H] bf16. */

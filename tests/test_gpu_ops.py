@@ -192,6 +192,43 @@ def test_attn(case, kind, fp8, form):
     assert_close(np64(out), ref, "attn out", fp8=fp8)
 
 
+@pytest.mark.parametrize("q_len", [2, 4, 7, 8])
+@pytest.mark.parametrize("kind", ["nope", "swa_ring128"])
+@pytest.mark.parametrize("form", ["decode", "prefill"])
+def test_attn_verify_batches(q_len, kind, form):
+    """Multi-token verification batches of speculative decoding at full width: q_len new tokens
+    per sequence (2 sequences) after 100,000 cached ones, through both forms of beam_attn --
+    split-K decode (which a bound of 1 always takes, and a true bound up to 16 takes for so
+    few sequences) and the query-tile prefill kernel (a bound above 16) -- whatever q_len is."""
+    shape = BEAM
+    nope = kind == "nope"
+    ctxs = [100_000, 99_123]
+    S = len(ctxs)
+    T = S * q_len
+    seed = 300 + q_len
+    seqs = [s for s in range(S) for _ in range(q_len)]
+    positions = [ctxs[s] + 1 + i for s in range(S) for i in range(q_len)]
+    max_pos = max(positions)
+    cap, window = (max_pos + 5, 0) if nope else (-(-(shape.window + q_len + 2) // 128) * 128,
+                                                  shape.window)
+    c = synth.kv_cache(shape, S, cap, seed, device=DEV)
+    kc = B.KVCache(c["k"], c["v"], window)
+    q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, seed, ("q",), DEV)
+    g = synth.activations(T, shape.q_rows, seed, "g", DEV)
+    W = synth.attention_weights(shape, 0, seed, device=DEV)
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    cfg = cfg_of(shape, nope)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    mq = 1 if form == "decode" else 17   # a bound above 16 always takes the query tiles
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
+                ws_for(cfg, T, max_pos), max_q_per_seq=mq)
+    check_status()
+    ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
+                      positions, np64(W["w_o"]))
+    assert_close(np64(out), ref, "attn out")
+
+
 # A sliding window longer than 2048 keys takes the long-context decode kernel when the ring's
 # capacity is a multiple of its key block (64 slots for BF16, 128 for FP8) and the split-K kernel
 # otherwise; the contexts make the window wrap around the ring and one sequence hold fewer
