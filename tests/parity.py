@@ -34,6 +34,7 @@ def mean_rel(a, r):
 def assert_close(a, r, what, fp8=False):
     mx, mn = max_abs_rel(a, r), mean_rel(a, r)
     lim_mx, lim_mn = (FP8_MAX_REL, FP8_MEAN_REL) if fp8 else (BF16_MAX_REL, BF16_MEAN_REL)
+    print(f"{what}: max-abs-rel {mx:.3e} mean-rel {mn:.3e} (bars {lim_mx} / {lim_mn})")
     assert np.all(np.isfinite(a)), f"{what}: non-finite output"
     assert mx <= lim_mx and mn <= lim_mn, \
         f"{what}: max-abs-rel {mx:.3e} (<= {lim_mx}), mean-rel {mn:.3e} (<= {lim_mn})"

@@ -179,7 +179,7 @@ def test_full_width_swa_moe_layer_decode_ctx4096():
     _layer_case(BEAM, 3, [4096])
 
 
-@pytest.mark.parametrize("batch", [1, 8])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
 def test_full_width_nope_moe_layer_decode_ctx100k_bf16(batch):
     _layer_case(BEAM, 5, [100_000] * batch)
 

@@ -43,14 +43,15 @@ DEV = "cuda"
 
 
 class LazyExperts:
-    """expert index -> float64 host copy of that expert's weights, fetched on first use."""
+    """expert index -> float32 host copy of that expert's weights (exact for bf16; the oracle
+    widens it), fetched on first use."""
 
     def __init__(self, t):
         self.t, self.cache = t, {}
 
     def __getitem__(self, e):
         if e not in self.cache:
-            self.cache[e] = np64(self.t[e])
+            self.cache[e] = self.t[e].float().cpu().numpy()
         return self.cache[e]
 
 
@@ -110,6 +111,10 @@ def stepwise_check(shape, Wo, gtr, e, seq, pos, caches_after, fp8=False):
         mx, mn = assert_close(np64(a) if not isinstance(a, np.ndarray) else a, r,
                               name, fp8_)
         rows.append(f"step {name}: max-abs-rel {mx:.3e} mean-rel {mn:.3e} (stated bar met)")
+
+    # the first boundary: the embedding's pre-norm (residual term 1)
+    chk("L0.u_attn", gtr[0]["u_attn"],
+        O.boundary_norm(None, h_prev, None, Wo[0]["attn_pre"], 1, shape.eps)[1])
 
     for l in range(L):
         t, W = gtr[l], Wo[l]
@@ -279,3 +284,59 @@ def test_tiny_stack_prefill_then_decode_end_to_end():
     assert h_pre.shape == (T, shape.hidden)
     got = trace_dict([gtr_pre, gtr_dec], names, range(L))
     compare_chained(got, ref, floors=floors, widened=[k for k in ref if not k.endswith(".idx")])
+
+
+def test_full_width_stack_prefill_8x2048_ctx100k_stepwise():
+    """The 6-layer stack prefilling 8 sequences x 2048 new tokens after 100,000 cached ones
+    (the prefill configuration; tensor-core projections, grouped expert GEMMs, tensor-core
+    attention over the whole context on the NoPE layer). The oracle cannot follow 16,384 tokens
+    end to end, so 12 tokens spread over three sequences and the chunk (first, middle, last
+    positions) are checked step by step at every layer from the GPU's own inputs, at the stated
+    bars: each token's attention reads the cache the GPU filled, its own earlier chunk tokens
+    included. Routing is compared on tokens whose margins on the GPU's router input clear
+    1e-5 (route_gaps; FP32 summation order cannot split a wider gap)."""
+    shape, seed = BEAM, 0
+    L = shape.n_layers
+    S, chunk, ctx = 8, 2048, 100_000
+    W = [synth.layer_weights(shape, l, seed, device=DEV) for l in range(L)]
+    kcs = []
+    for l in range(L):
+        nope = O.is_nope_layer(l, L)
+        cap, win = ((ctx + chunk + 8, 0) if nope else
+                    (-(-(shape.window + chunk - 1) // 128) * 128, shape.window))
+        c = synth.kv_cache(shape, S, cap, seed, l, device=DEV)
+        kcs.append(B.KVCache(c["k"], c["v"], win))
+    T = S * chunk
+    e = synth.activations(T, shape.hidden, seed, "embed_prefill", DEV)
+    seq, pos = synth.prefill_positions([ctx] * S, chunk, DEV)
+    st = BeamStack(shape, W, kcs, device=DEV)
+    gtr = []
+    st.forward(e, seq, pos, ctx + chunk, trace=gtr, max_q_per_seq=chunk)
+    torch.cuda.synchronize()
+    assert B.beam_get_device_status() == 0
+    seqs = [0, 3, 7]
+    offs = [0, 1, 1023, 2047]
+    rows = [s_ * chunk + o for s_ in seqs for o in offs]
+    Wo = [host_weights(w) for w in W]
+    # keep tokens whose routing is decided by more than FP32 summation order can move
+    keep = []
+    for i, r in enumerate(rows):
+        ok = True
+        for l in range(L):
+            if gtr[l].get("route") is None:
+                continue
+            _, _, b = O.route_scores(shape, np64(gtr[l]["mlp_in"][r:r + 1]), Wo[l]["router"],
+                                     Wo[l]["corr_bias"])
+            gg, eg = O.route_gaps(shape, b)
+            ok = ok and min(gg[0], eg[0]) >= 1e-5
+        if ok:
+            keep.append(i)
+    assert len(keep) >= 10, f"only {len(keep)} of {len(rows)} sampled tokens clear the margin"
+    rows = [rows[i] for i in keep]
+    sub = [{k: (v[rows] if k != "route" else tuple(x[rows] for x in v)) for k, v in t.items()}
+           for t in gtr]
+    seq_h = seq[rows].cpu().numpy()
+    remap = {s_: i for i, s_ in enumerate(sorted(set(seq_h.tolist())))}
+    oseq = np.array([remap[s_] for s_ in seq_h])
+    stepwise_check(shape, Wo, sub, e[rows], oseq, pos[rows].cpu().numpy(),
+                   oracle_caches(kcs, sorted(remap)))
