@@ -7,7 +7,7 @@ warm-up launches and capture one or a few real ones. Usage:
     python -m hybrid_attention_moe_gb300.profile_cases --case moe_decode --reps 3
 
 Cases: moe_decode (--tokens tokens, default 1, each over 8 selected experts of a 32-expert
-pool), moe_decode_nvfp4 (the same with NVFP4 expert weights), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
+pool), moe_decode_nvfp4 / moe_decode_fp8 (the same with NVFP4 / block-scaled FP8 expert weights), dense_decode (the 20480-wide dense SwiGLU MLP for --tokens tokens),
 lm_head_decode (the LM head with the logit softcap over 32768 vocabulary rows, --tokens tokens),
 qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (100K keys),
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
@@ -70,6 +70,17 @@ def main():
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_moe_nvfp4(cs, u, idx, w, wq, out, ws)  # noqa: E731
+    elif c == "moe_decode_fp8":
+        T = args.tokens
+        cs = B.LayerCfg.from_shape(small, B.BEAM_ATTN_SWA_ROPE)
+        wq = synth.expert_weights_fp8(small, 3, 0, device=dev)
+        u = synth.activations(T, H, 0, "u", dev)
+        g = torch.Generator(device="cpu").manual_seed(0)
+        idx = torch.stack([torch.randperm(32, generator=g)[:8] for _ in range(T)]).int().to(dev)
+        w = torch.full((T, 8), 0.3, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(B.workspace_bytes(cs, T, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: B.beam_moe_fp8(cs, u, idx, w, wq, out, ws)  # noqa: E731
     elif c == "lm_head_decode":
         # 32768 vocabulary rows at hidden 5120: 336 MB of BF16 weights (more than L2)
         T, V = args.tokens, 32768
