@@ -33,15 +33,22 @@ def test_layer_bytes_per_unit():
 
 
 def test_traffic_entries_are_per_call():
-    """profiles/traffic.json holds DRAM bytes per call of the one-token MoE calls: each entry
-    still in force (its sources unchanged since the capture) lies within a few percent above
-    its algorithmic bytes (no re-reads); entries whose sources changed report None."""
+    """profiles/traffic.json holds DRAM bytes per call of the one-token dense-MLP and expert
+    calls (BF16, FP8, NVFP4): each lies within a few percent above its algorithmic bytes (no
+    re-reads) and is the sum of its kernels' read and write bytes; entries whose sources
+    changed since the capture report None."""
     import json
     d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    for key, fmt in (("moe_decode_t1", "bf16"), ("moe_decode_nvfp4_t1", "nvfp4")):
+    for key, fmt in (("moe_decode_t1", "bf16"), ("moe_decode_nvfp4_t1", "nvfp4"),
+                     ("moe_decode_fp8_t1", "fp8")):
         assert algo_ok(d[key]["bytes_per_launch"], 8 * bench.expert_bytes(BEAM, fmt)), key
         t = bench.ncu_traffic(key)
         assert t is None or t == d[key]["bytes_per_launch"]
+    dense = 3 * BEAM.hidden * BEAM.d_ff_dense * 2
+    assert algo_ok(d["dense_decode_t1"]["bytes_per_launch"], dense)
+    for key in ("dense_decode_t1", "moe_decode_t1", "moe_decode_fp8_t1", "moe_decode_nvfp4_t1"):
+        e = d[key]
+        assert e["bytes_per_launch"] == sum(r + w for r, w in e["kernels"].values()), key
     assert bench.ncu_traffic("moe_decode_t8") is None
 
 
