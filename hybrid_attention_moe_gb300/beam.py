@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libbeam.so")
 
 BEAM_KV_BF16, BEAM_KV_FP8_E4M3 = 0, 1
 BEAM_ATTN_SWA_ROPE, BEAM_ATTN_NOPE_SSMAX = 0, 1
-DEV_BAD_POSITION, DEV_BAD_SEQ, DEV_BAD_EXPERT = 0x1, 0x2, 0x4
+DEV_BAD_POSITION, DEV_BAD_SEQ, DEV_BAD_EXPERT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 
 class BeamError(RuntimeError):
@@ -65,6 +65,7 @@ _SIGS = {
     "beam_gemm_bf16": [_P, _I, _I, _I, _P, _I, _I, _P, _I, _I, _P],
     "beam_route_noalloc": [_P, _P, _P, _P, _I, _P, _P, _P],
     "beam_lm_head": [_P, _P, _I, _I, _I, _F, _P, _P],
+    "beam_selftest_wait_timeout": [_P],
 }
 _RES = {"beam_workspace_bytes": _Z, "beam_kv_cache_bytes": _Z,
         "beam_status_string": ctypes.c_char_p, "beam_launch_count": ctypes.c_uint64,
@@ -303,3 +304,9 @@ def beam_route_noalloc(cfg: LayerCfg, u, w_router, corr_bias, topk_idx, topk_w, 
     _check(lib().beam_route_noalloc(ctypes.byref(c), _ptr(u), _ptr(w_router), _ptr(corr_bias),
                                     u.shape[0], _ptr(topk_idx), _ptr(topk_w), _stream(stream)),
            "beam_route_noalloc")
+
+
+def beam_selftest_wait_timeout(stream=None):
+    """Runs the library's bounded on-device wait against a barrier nothing completes (see
+    include/beam.h); the status word then holds DEV_TIMEOUT."""
+    _check(lib().beam_selftest_wait_timeout(_stream(stream)), "beam_selftest_wait_timeout")

@@ -3,6 +3,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace beam {
 
@@ -81,4 +82,24 @@ extern "C" uint64_t beam_launch_count(void) { return beam::g_launches.load(); }
 
 extern "C" const char* beam_last_cuda_error(void) {
   return cudaGetErrorName(beam::g_last_cuda_error);
+}
+
+namespace beam {
+namespace {
+// One thread waits on a barrier that expects one arrival and never gets it.
+__global__ void wait_timeout_selftest_kernel() {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  tc::mbar_init(a, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!tc::mbar_wait(a, 0)) flag(BEAM_DEV_TIMEOUT);
+}
+}  // namespace
+}  // namespace beam
+
+extern "C" beam_status beam_selftest_wait_timeout(beam_stream_t stream) {
+  using namespace beam;
+  wait_timeout_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  note_launches(1);
+  return launch_status();
 }

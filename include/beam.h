@@ -292,6 +292,13 @@ size_t beam_kv_cache_bytes(int num_seqs, int n_kv, int capacity, int head_dim, i
  * `stream` first. */
 beam_status beam_get_device_status(beam_stream_t stream, uint32_t* bits);
 
+/* Diagnostic of the on-device timeout path: launches one thread that waits, with the bounded
+ * mbarrier wait every tensor-core and TMA kernel of the library uses, on a shared-memory barrier
+ * that nothing completes (no copy or MMA is issued). The wait gives up after its poll limit
+ * (of the order of a second) and records BEAM_DEV_TIMEOUT in the status word, which
+ * beam_get_device_status then reports; the context stays usable. Asynchronous on `stream`. */
+beam_status beam_selftest_wait_timeout(beam_stream_t stream);
+
 /* Number of CUDA kernels the library has launched in this process (host-side counter,
  * thread-safe; for benchmarks that report their own launches). */
 uint64_t beam_launch_count(void);

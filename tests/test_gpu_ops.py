@@ -653,3 +653,27 @@ def test_invalid_arguments_return_errors():
                         torch.empty((2, 4, 96), dtype=torch.bfloat16, device=DEV),
                         torch.empty((2, 384), dtype=torch.bfloat16, device=DEV), kc,
                         ws_for(cfg, 2))
+
+
+def test_expired_device_wait_is_reported_and_the_context_survives():
+    """The bounded mbarrier wait of the tensor-core and TMA kernels, run on a barrier that
+    nothing completes (no copy or MMA in flight), gives up, records DEV_TIMEOUT, and the next
+    call on the device works."""
+    import time
+    B.beam_get_device_status()
+    t0 = time.perf_counter()
+    B.beam_selftest_wait_timeout()
+    assert B.beam_get_device_status() & B.DEV_TIMEOUT
+    print(f"bounded wait expired after {time.perf_counter() - t0:.2f} s")
+    assert B.beam_get_device_status() == 0            # reading cleared it
+    shape = BEAM
+    x = synth.activations(2, shape.hidden, 5, "x", DEV)
+    h = synth.activations(2, shape.hidden, 5, "h", DEV)
+    u = torch.empty_like(h)
+    w = synth.normal((shape.hidden,), 0.1, 1.0, 5, ("w",), DEV)
+    h0 = np64(h)
+    B.beam_boundary_norm(x, h, u, w, w, 4, shape.eps)
+    check_status()
+    hr, ur = O.boundary_norm(np64(x), h0, np64(w), np64(w), 4, shape.eps)
+    assert_close(np64(h), hr, "h after the expired wait")
+    assert_close(np64(u), ur, "u after the expired wait")
