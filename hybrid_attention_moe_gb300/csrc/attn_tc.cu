@@ -354,14 +354,14 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
           int slot = wk.first_slot + i * KT;
           if (p.window > 0) slot %= p.cap;
           const int ks = int(kc % KSTAGES);
-          if (*abort_flag || !mbar_wait(k_empty + 8 * ks, ((kc / KSTAGES) & 1) ^ 1)) { bad = true; break; }
+          if (!mbar_wait(k_empty + 8 * ks, ((kc / KSTAGES) & 1) ^ 1)) { bad = true; break; }
           mbar_expect_tx(k_full + 8 * ks, uint32_t(S::TILE));
           for (int h = 0; h < S::NH; ++h)
             tma_load_3d(sb + S::K0 + ks * S::TILE + h * KT * 128, &tk, 64 * h, slot, zidx, k_full + 8 * ks);
           last_k[ks] = int(kc);
           ++kc;
           const int vs = int(vc % VSTAGES);
-          if (*abort_flag || !mbar_wait(v_empty + 8 * vs, ((vc / VSTAGES) & 1) ^ 1)) { bad = true; break; }
+          if (!mbar_wait(v_empty + 8 * vs, ((vc / VSTAGES) & 1) ^ 1)) { bad = true; break; }
           mbar_expect_tx(v_full + 8 * vs, uint32_t(S::TILE));
           for (int h = 0; h < S::NH; ++h)
             tma_load_3d(sb + S::V0 + vs * S::TILE + h * KT * 128, &tv, 64 * h, slot, zidx, v_full + 8 * vs);
@@ -392,34 +392,44 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
     int item = 0;
     bool ok = true;
     auto all = [&](bool v) { return __all_sync(0xffffffffu, v) && !*abort_flag; };
+    // In the key-tile loop the abort flag is not read: a shared-memory load takes ~130 cycles
+    // while the tensor pipe streams operands, and the pipe holds under 200 cycles of queued
+    // MMAs. A role that gave up stops arriving, so the next wait here expires instead.
+    auto all_fast = [&](bool v) { return __all_sync(0xffffffffu, v); };
     // descriptors of stage 0 / query tile 0; others differ only in the start address field,
     // (address >> 4) in the low 14 bits, which no offset below carries out of
     const uint64_t dq0 = smem_desc(sb + S::Q), dk0 = smem_desc(sb + S::K0);
     const uint64_t dv0 = smem_desc_mn(sb + S::V0, KT * 128, 1024);
+    // The tensor pipe queues only ~3 MMAs of these shapes (~170 cycles of work), so the issue
+    // path is kept short: descriptors are stepped in their low word (the address field) only.
+    const uint32_t dq0_hi = uint32_t(dq0 >> 32), dk0_hi = uint32_t(dk0 >> 32);
     auto qk = [&](int u, int ks) {
       if (lane == 0) {
-        const uint64_t dq = dq0 + uint64_t((u * S::NH * S::HALF) >> 4);
-        const uint64_t dk = dk0 + uint64_t((ks * S::TILE) >> 4);
+        const uint32_t qlo = uint32_t(dq0) + uint32_t((u * S::NH * S::HALF) >> 4);
+        const uint32_t klo = uint32_t(dk0) + uint32_t((ks * S::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk & 3) * 32) >> 4;
-          umma_ss(tmem + 128 * u, dq + ((kk >> 2) * S::HALF >> 4) + off,
-                  dk + ((kk >> 2) * KT * 128 >> 4) + off, IDESC_QK, kk > 0 ? 1u : 0u);
+          umma_ss_w(tmem + 128 * u, qlo + ((kk >> 2) * S::HALF >> 4) + off, dq0_hi,
+                    klo + ((kk >> 2) * KT * 128 >> 4) + off, dk0_hi, IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(s_full + 8 * u);
       }
       __syncwarp();
     };
+    const uint32_t dv0_hi = uint32_t(dv0 >> 32);
     auto pv = [&](int u, int vs, bool first) {
       if (lane == 0) {
-        const uint64_t dv = dv0 + uint64_t((vs * S::TILE) >> 4);
+        const uint32_t blo = uint32_t(dv0) + uint32_t((vs * S::TILE) >> 4);
         const uint32_t ts = tmem + 128 * u, to = tmem + 256 + 128 * u;
+        umma_ts_w(to, ts, blo, dv0_hi, IDESC_PV, first ? 0u : 1u);
+        umma_ts_w(to, ts + 16, blo, dv0_hi, IDESC_PV, 1u);
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          const uint64_t bd = dv + uint64_t((kk * 16 * 128) >> 4);
+        for (int kk = 1; kk < KT / 16; ++kk) {
+          const uint32_t b = blo + uint32_t((kk * 16 * 128) >> 4);
           const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
-          umma_ts(to, a_hi, bd, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-          umma_ts(to, a_hi + 16, bd, IDESC_PV, 1u);
+          umma_ts_acc(to, a_hi, b, dv0_hi, IDESC_PV);
+          umma_ts_acc(to, a_hi + 16, b, dv0_hi, IDESC_PV);
         }
         umma_commit(s_free + 8 * u);
       }
@@ -464,14 +474,20 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         const bool fresh = i % kFlushTiles == 0;
         const uint32_t oph = (ostart & 1) ^ 1;
         // ---- query tile A: P.V of tile i, then S of tile i + 1
-        bool w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
-                    mbar_wait(p_full, (pt + gt_i) & 1);
-        if (fresh) w_ok = w_ok && mbar_wait(o_empty, oph);
-        if (more) {
-          ks = int(kc % KSTAGES);
-          w_ok = w_ok && mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1);
+        if (more) ks = int(kc % KSTAGES);
+        // the tile's barriers polled together (their latencies overlap), then waited for one by
+        // one only if one was not yet complete
+        const bool r_v = mbar_try(v_full + 8 * vs, (vc / VSTAGES) & 1);
+        const bool r_p = mbar_try(p_full, (pt + gt_i) & 1);
+        const bool r_k = !more || mbar_try(k_full + 8 * ks, (kc / KSTAGES) & 1);
+        const bool r_o = !fresh || mbar_try(o_empty, oph);
+        bool w_ok = r_v && r_p && r_k && r_o;
+        if (!w_ok) {
+          w_ok = mbar_wait(v_full + 8 * vs, (vc / VSTAGES) & 1) &&
+                 mbar_wait(p_full, (pt + gt_i) & 1) && (!fresh || mbar_wait(o_empty, oph)) &&
+                 (!more || mbar_wait(k_full + 8 * ks, (kc / KSTAGES) & 1));
         }
-        if (!all(w_ok)) { ok = false; break; }
+        if (!all_fast(w_ok)) { ok = false; break; }
         const int kb = wk.key_first + i * KT;
         const int r0 = max(0, J.key_a - kb), r1 = min(KT, J.key_b - kb + 1);
         if (r0 > 0 || r1 < KT) {
@@ -491,11 +507,12 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         pv(0, vs, fresh);
         if (lane == 0 && !more) umma_commit(o_full);
         __syncwarp();
+        const bool r_pb = mbar_test(p_full + 8, (pt + gt_i) & 1);   // answered while QK_A issues
         if (more) qk(0, ks);
         // ---- query tile B
-        w_ok = mbar_wait(p_full + 8, (pt + gt_i) & 1);
+        w_ok = r_pb || mbar_wait(p_full + 8, (pt + gt_i) & 1);
         if (fresh) w_ok = w_ok && mbar_wait(o_empty + 8, oph);
-        if (!all(w_ok)) { ok = false; break; }
+        if (!all_fast(w_ok)) { ok = false; break; }
         if (fresh) ++ostart;
         tc_fence_after();
         pv(1, vs, fresh);
@@ -570,7 +587,7 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
       float* oacc = p.oacc + ((size_t(blockIdx.x) * 2 + u) * 128 + r) * 128 + 64 * half;
       for (int i = 0; i < wk.n; ++i) {
         const uint32_t G_ = gt + uint32_t(i);
-        if (!pair_all(mbar_wait(my_s_full, G_ & 1) && !*abort_flag)) {
+        if (!pair_all(mbar_wait(my_s_full, G_ & 1))) {
           ok = false;
           break;
         }

@@ -34,6 +34,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase (try_wait may suspend the thread while the phase is pending).
+__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait: false after kWaitLimit polls (each poll may suspend the thread briefly).
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
@@ -108,6 +118,36 @@ __device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
           tmem_d),
       "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem] with each descriptor passed as its two 32-bit words.
+__device__ __forceinline__ void umma_ss_w(uint32_t tmem_d, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; .reg .b64 ad, bd; setp.ne.b32 p, %6, 0; mov.b64 ad, {%1, %2};"
+      " mov.b64 bd, {%3, %4}; tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p; }" ::"r"(
+          tmem_d),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem] with the B descriptor passed as its two 32-bit words (callers
+// that step through a tile change only the low word, the start address field).
+__device__ __forceinline__ void umma_ts_w(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
+                                          uint32_t b_hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; .reg .b64 bd; setp.ne.b32 p, %5, 0; mov.b64 bd, {%2, %3};"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p; }" ::"r"(tmem_d),
+      "r"(tmem_a), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The same, always accumulating into D.
+__device__ __forceinline__ void umma_ts_acc(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{ .reg .pred p; .reg .b64 bd; setp.eq.u32 p, 0, 0; mov.b64 bd, {%2, %3};"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p; }" ::"r"(tmem_d),
+      "r"(tmem_a), "r"(b_lo), "r"(b_hi), "r"(idesc)
       : "memory");
 }
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
