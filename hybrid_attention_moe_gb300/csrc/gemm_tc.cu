@@ -33,10 +33,6 @@ constexpr int THREADS = 192;
 constexpr int kGroupM = 16;   // row tiles walked per column tile (dense grids)
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN, false);
 
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
-  umma_ss(tmem_d, a, b, kIdesc, acc);
-}
-
 // One CTA computes output columns [n0, n0 + BN) (kSwiGLU: units [n0, n0 + BN/2)) for A rows
 // [a_row0, a_row0 + rows). Dense GEMMs map a 1-D grid onto (row tile, column tile) in groups
 // of kGroupM row tiles; grouped GEMMs read (group, a_row0, rows) from a device-side job list
@@ -213,7 +209,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (*abort_flag || !mbar_wait(empty0 + 8 * s, ph ^ 1)) {
+          // the abort flag is read per tile, not per k-block: under a busy tensor pipe a
+          // shared-memory load takes ~130 cycles (a role that gave up stops arriving, so this
+          // wait then expires)
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1)) {
             *abort_flag = 1;
             break;
           }
@@ -236,6 +235,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // descriptor of the ring's first byte: A and B tiles of every stage differ from it only
+      // in the start address field (shared-memory offsets >> 4 stay below 2^14)
+      const uint64_t d0 = smem_desc(s_base);
+      const uint32_t d_lo0 = uint32_t(d0), d_hi = uint32_t(d0 >> 32);
       int it = 0, i = 0;
       for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++i) {
         const int ab = i & 1;
@@ -247,19 +250,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t acc = tmem + uint32_t(ab * BN);
         bool ok = true;
+        // The tensor pipe queues only ~3 MMAs (~350 cycles of work at this shape): the issue
+        // path per k-block is one barrier poll, the descriptors stepped in their low word (the
+        // start address field) and the four MMAs.
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (*abort_flag || !mbar_wait(full0 + 8 * s, ph)) {
+          if (!mbar_wait(full0 + 8 * s, ph)) {
             ok = false;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t sa = s_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t alo = d_lo0 + uint32_t((s * STAGE_BYTES) >> 4);
+          const uint32_t blo = alo + uint32_t(A_BYTES >> 4);
+          umma_ss_w(acc, alo, d_hi, blo, d_hi, kIdesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma(acc, smem_desc(sa + 32 * k), smem_desc(sb + 32 * k), (kb | k) != 0);
+          for (int k = 1; k < BK / 16; ++k)
+            umma_ss_w(acc, alo + uint32_t((32 * k) >> 4), d_hi, blo + uint32_t((32 * k) >> 4), d_hi,
+                      kIdesc, 1u);
           umma_commit(empty0 + 8 * s);
         }
         umma_commit(accf0 + 8 * ab);   // arrives once every MMA issued above has completed
