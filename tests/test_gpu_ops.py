@@ -434,8 +434,13 @@ def _nvfp4_experts(shape, used, seed):
     return full, experts
 
 
+# a second small shape (hidden and d_ff multiples of 256, 4 of 16 experts per token)
+NVFP4_MID = dataclasses.replace(TINY, hidden=512, d_ff_expert=256)
+
+
 @pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 5, None),
-                                            (TINY, 13, None), (TINY, 31, 6), (BEAM, 1, None),
+                                            (TINY, 13, None), (TINY, 31, 6), (NVFP4_MID, 1, None),
+                                            (NVFP4_MID, 2, None), (BEAM, 1, None),
                                             (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None)])
 def test_moe_nvfp4(shape, T, n_used):
     """NVFP4 expert weights (e2m1 codes, e4m3 block scales, FP32 matrix scales): mma.sync f16
@@ -456,8 +461,8 @@ def test_moe_nvfp4(shape, T, n_used):
     assert_close(np64(out), ref, "moe nvfp4 out")
 
 
-def test_moe_nvfp4_bad_expert_slots_flagged_and_skipped():
-    shape = TINY
+@pytest.mark.parametrize("shape", [TINY, NVFP4_MID])
+def test_moe_nvfp4_bad_expert_slots_flagged_and_skipped(shape):
     cfg = cfg_of(shape)
     for rows in ([[0, 1, 99, 2]], [[0, 1, 99, 2], [5, -3, 1, 7]]):
         T = len(rows)
