@@ -41,7 +41,8 @@ struct GemmParams {
   int M, N, K;           // A rows (bound), output columns (units for kSwiGLU), reduction
   void* C;
   int ldc;
-  const int4* jobs;      // grouped: {group, a_row0, rows, -}; nullptr for a dense GEMM
+  const int4* jobs;      // grouped: {group, a_row0, rows, group's first job | its jobs << 20};
+                         // nullptr for a dense GEMM
   const int* n_jobs;     // grouped: number of valid jobs (device)
   int b_stride;          // grouped: B rows per group (b_row0 = group * b_stride)
   int up_off;            // kSwiGLU: B row offset of the up half from the gate half
@@ -122,8 +123,8 @@ __device__ __forceinline__ void qkv_head_epilogue(const QkvEpilogue& e, uint32_t
 // Output tile t of a launch: A rows [a_row0, a_row0 + rows), B rows from b_row0, output
 // columns [n0, n0 + NT). Dense GEMMs walk (row tile, column tile) in groups of kGroupM row
 // tiles per column tile: the tiles the resident CTAs hold at one time cover a compact block of
-// the output, so both operands' tiles are reused through L2. Grouped GEMMs take tile
-// t = job * num_n + column tile.
+// the output, so both operands' tiles are reused through L2. Grouped GEMMs walk each group's
+// (expert's) tiles column by column, its jobs fastest (tile_of).
 struct Tile {
   int a_row0, b_row0, rows, n0;
 };
@@ -140,9 +141,20 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, int num_m, i
     r.b_row0 = 0;
     r.rows = BM;
   } else {
-    const int jb = t / num_n;
+    // An expert's tiles occupy one contiguous range of t; inside it the tiles go column by
+    // column, the expert's row tiles (jobs) fastest, so the CTAs that share a column of the
+    // expert's weights run side by side and read it from L2 once (job-major order split an
+    // expert's columns across waves of the persistent grid: 1.39x the weight bytes from DRAM).
+    int jb = t / num_n, col = t - jb * num_n;
+    const int w = p.jobs[jb].w;
+    const int je0 = w & 0xFFFFF, nje = w >> 20;
+    if (nje > 0) {
+      const int local = t - je0 * num_n;
+      col = local / nje;
+      jb = je0 + (local - col * nje);
+    }
     const int4 j = p.jobs[jb];
-    r.n0 = (t - jb * num_n) * NT;
+    r.n0 = col * NT;
     r.b_row0 = j.x * p.b_stride;
     r.a_row0 = j.y;
     r.rows = j.z;

@@ -41,7 +41,8 @@ struct MoePlan {
   int* active;     // [E] expert ids, increasing
   int* act_off;    // [E+1] offsets into pairs
   int* pairs;      // [P] pair ids t*k + j grouped by expert
-  int4* jobs;      // grouped GEMM only: {expert, first sorted row, rows <= 128, 0}
+  int4* jobs;      // grouped GEMM only: {expert, first sorted row, rows <= 128,
+                   //  the expert's first job | its job count << 20}
   int* n_jobs;     // [1]
 };
 
@@ -134,7 +135,10 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const int32_t* _
       int nj = 0;
       for (int a = 0; a < a_tot; ++a) {
         const int e = pl.active[a], o0 = pl.act_off[a], c = pl.act_off[a + 1] - o0;
-        for (int r = 0; r < c; r += 128) pl.jobs[nj++] = make_int4(e, o0 + r, min(128, c - r), 0);
+        // w: the expert's first job and its job count, for the GEMM's tile order
+        const int first = nj, n = (c + 127) / 128;
+        for (int r = 0; r < c; r += 128)
+          pl.jobs[nj++] = make_int4(e, o0 + r, min(128, c - r), first | (n << 20));
       }
       *pl.n_jobs = nj;
     }
