@@ -16,6 +16,16 @@ BF16_MAX_REL, BF16_MEAN_REL = 2e-2, 1e-3
 FP8_MAX_REL, FP8_MEAN_REL = 5e-2, 2e-3
 LOGIT_REL = 1e-5
 
+# Every comparison made in the session: (test id, what, max-abs-rel, mean-rel, stated max bar,
+# stated mean bar, kind) with kind "stated" (held to the stated bars) or "chained" (held to
+# the widened bar of chained steps). conftest.py prints a summary at the end of the run.
+LEDGER = []
+CURRENT_TEST = [""]
+
+
+def _record(what, mx, mn, lim_mx, lim_mn, kind):
+    LEDGER.append((CURRENT_TEST[0], what, float(mx), float(mn), lim_mx, lim_mn, kind))
+
 
 def np64(t):
     return t.detach().float().cpu().double().numpy()
@@ -35,6 +45,7 @@ def assert_close(a, r, what, fp8=False):
     mx, mn = max_abs_rel(a, r), mean_rel(a, r)
     lim_mx, lim_mn = (FP8_MAX_REL, FP8_MEAN_REL) if fp8 else (BF16_MAX_REL, BF16_MEAN_REL)
     print(f"{what}: max-abs-rel {mx:.3e} mean-rel {mn:.3e} (bars {lim_mx} / {lim_mn})")
+    _record(what, mx, mn, lim_mx, lim_mn, "stated")
     assert np.all(np.isfinite(a)), f"{what}: non-finite output"
     assert mx <= lim_mx and mn <= lim_mn, \
         f"{what}: max-abs-rel {mx:.3e} (<= {lim_mx}), mean-rel {mn:.3e} (<= {lim_mn})"
@@ -211,6 +222,8 @@ def assert_chained_close(got, ref, floors, fp8=False, factor=3.0, rows=None, row
         mx, mn = max_abs_rel(a, r), mean_rel(a, r)
         stated = mx <= (FP8_MAX_REL if fp8 else BF16_MAX_REL) and \
             mn <= (FP8_MEAN_REL if fp8 else BF16_MEAN_REL)
+        _record(k, mx, mn, FP8_MAX_REL if fp8 else BF16_MAX_REL,
+                FP8_MEAN_REL if fp8 else BF16_MEAN_REL, "chained")
         print(f"{k}: max-abs-rel {mx:.3e} mean-rel {mn:.3e} (stated bar "
               f"{'met' if stated else 'NOT met'}; oracle noise floor {floors[k][0]:.2e} / "
               f"{floors[k][1]:.2e})")
@@ -367,6 +380,7 @@ def compare_chained(got, ref, fp8=False, floors=None, widened=(), factor=3.0, la
         if k in widened and fl is not None:
             lim_mx, lim_mn = max(lim_mx, factor * fl[0]), max(lim_mn, factor * fl[1])
         stated_ok = mx <= lim_mx0 and mn <= lim_mn0
+        _record(f"{label}{k}", mx, mn, lim_mx0, lim_mn0, "chained" if k in widened else "stated")
         rows.append(f"{label}{k}: max-abs-rel {mx:.3e} mean-rel {mn:.3e} "
                     f"(stated bar {'met' if stated_ok else 'NOT met'}"
                     + (f"; oracle noise floor {fl[0]:.2e} / {fl[1]:.2e}" if fl else "")
