@@ -328,7 +328,9 @@ inline cudaError_t launch_gemv_mma(const uint16_t* W, int N, int K, const uint16
 // gemv_flat.cuh when its shape allows. Measured per call at one token (graph replays, 152 SMs):
 // the dense MLP's 419 MB gate/up 74.9 -> 67.2 us and 210 MB down 42.2 -> 34.7 us; the QKV
 // projection (147 MB) 22.7 -> 26.3 us and o_proj (63 MB) no better inside the layer, so only
-// the dense MLP passes true.
+// the dense MLP passes true. The mma.sync form at one token (one valid token column) timed
+// alone is faster still (dense MLP call 119.8 -> 107.5 us) but inside the step's CUDA graph
+// the 6-layer decode went from 175 to 184 us per token per layer, so it stays at 2+ tokens.
 template <int MODE>
 inline cudaError_t launch_gemv(const uint16_t* W, int N, int K, const uint16_t* X, int T,
                                float* yf, uint16_t* yb, int ldy, cudaStream_t st,
