@@ -847,11 +847,10 @@ def main():
     args = ap.parse_args()
     if args.lm_head_vocab and args.workload == "stack_prefill":
         ap.error("--lm-head-vocab is timed for decode workloads")
-    if args.experts != "bf16" and args.workload == "stack_prefill":
-        ap.error("--experts nvfp4 / fp8 are decode formats here (their kernels take up to 31 "
-                 "tokens)")
+    if args.experts == "fp8" and args.workload == "stack_prefill":
+        ap.error("--experts fp8 is a decode format here (its kernels take up to 31 tokens)")
     if args.experts != "bf16":
-        args.no_prefill = True
+        args.no_prefill = True   # the stack_decode line's prefill object stays BF16
     if args.workload == "stack_verify" and not 1 <= args.chunk <= 16:
         ap.error("stack_verify takes 1-16 new tokens per sequence (--chunk)")
     world = int(os.environ.get("WORLD_SIZE", "1"))

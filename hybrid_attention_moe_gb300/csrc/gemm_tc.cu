@@ -47,6 +47,8 @@ struct GemmParams {
   int b_stride;          // grouped: B rows per group (b_row0 = group * b_stride)
   int up_off;            // kSwiGLU: B row offset of the up half from the gate half
   const int* row_map;    // optional: C row of A row r is row_map[r]
+  const float* group_scale;   // grouped, optional: the accumulator of group g is multiplied by
+                              // group_scale[g] before the epilogue (per-matrix weight scales)
 };
 
 // The QKV epilogue for one token row and one 128-column head of the tile (kQKV mode).
@@ -126,7 +128,7 @@ __device__ __forceinline__ void qkv_head_epilogue(const QkvEpilogue& e, uint32_t
 // the output, so both operands' tiles are reused through L2. Grouped GEMMs walk each group's
 // (expert's) tiles column by column, its jobs fastest (tile_of).
 struct Tile {
-  int a_row0, b_row0, rows, n0;
+  int a_row0, b_row0, rows, n0, group;
 };
 template <int NT>
 __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, int num_m, int num_n) {
@@ -140,6 +142,7 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, int num_m, i
     r.n0 = (in_group / gsize) * NT;
     r.b_row0 = 0;
     r.rows = BM;
+    r.group = 0;
   } else {
     // An expert's tiles occupy one contiguous range of t; inside it the tiles go column by
     // column, the expert's row tiles (jobs) fastest, so the CTAs that share a column of the
@@ -156,6 +159,7 @@ __device__ __forceinline__ Tile tile_of(const GemmParams& p, int t, int num_m, i
     const int4 j = p.jobs[jb];
     r.n0 = col * NT;
     r.b_row0 = j.x * p.b_stride;
+    r.group = j.x;
     r.a_row0 = j.y;
     r.rows = j.z;
   }
@@ -311,6 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool row_ok = r < tl.rows && arow < p.M;
       const int crow = row_ok ? (p.row_map ? p.row_map[arow] : arow) : 0;
       const int n0 = tl.n0;
+      const float gsc = p.group_scale != nullptr ? p.group_scale[tl.group] : 1.f;
       const uint32_t tbase = tmem + uint32_t(ab * BN) + (uint32_t(quad * 32) << 16);
       if (MODE == kQKV) {
         // per token row: two 128-column heads of the packed projection
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               float a[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                a[e] = siluf_(__uint_as_float(v[e])) * __uint_as_float(up[e]);
+                a[e] = siluf_(__uint_as_float(v[e]) * gsc) * (__uint_as_float(up[e]) * gsc);
               if (col + 16 <= p.N && (p.ldc & 7) == 0) {
                 uint32_t q[8];
 #pragma unroll
@@ -361,6 +366,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           } else if (row_ok && col < p.N) {
+            if (p.group_scale != nullptr) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * gsc);
+            }
             if (MODE == kF32 || MODE == kF32Add) {
               float* dst = static_cast<float*>(p.C) + size_t(crow) * p.ldc + col;
               if (col + 16 <= p.N && (p.ldc & 3) == 0) {
@@ -534,7 +543,7 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
 cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
                          int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
                          int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
-                         cudaStream_t st) {
+                         cudaStream_t st, const float* group_scale) {
   if (M <= 0 || N <= 0 || max_jobs <= 0) return cudaSuccess;
   if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
   if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
@@ -542,7 +551,7 @@ cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, con
   const int bbox = mode == kSwiGLU ? BN / 2 : BN;
   if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, b_rows, ldb, bbox))
     return cudaErrorInvalidValue;
-  GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map};
+  GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map, group_scale};
   const int nt = mode == kSwiGLU ? BN / 2 : BN;
   const int tiles = ((N + nt - 1) / nt) * max_jobs;
   if (mode == kSwiGLU) return launch<kSwiGLU>(ta, tb, p, tiles, st);

@@ -57,11 +57,12 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
 // g * b_stride of B (a 2-D matrix of b_rows rows: all experts stacked). Output column count N
 // (units for kSwiGLU, whose up half starts up_off rows after the gate half). The output row
 // of A row r is row_map[r] if given. The grid covers max_jobs jobs; jobs at index >= *n_jobs
-// return at once.
+// return at once. group_scale (optional, device): group g's products are multiplied by
+// group_scale[g] in FP32 before the epilogue (kSwiGLU: both gate and up).
 cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
                          int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
                          int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
-                         cudaStream_t st);
+                         cudaStream_t st, const float* group_scale = nullptr);
 
 }  // namespace tc
 }  // namespace beam

@@ -751,6 +751,97 @@ __global__ void __launch_bounds__(256, 3) moe_down_fp4_kernel(
 }
 
 // ------------------------------------------------------------------------------------------
+// NVFP4 experts from kMoeGemmMinT tokens: the grouped BF16 tensor-core GEMMs on dequantised
+// weights. An e2m1 value times its e4m3 block scale has at most 6 significant bits and lies
+// in [2^-10, 2688], so it is exact in BF16: the selected experts' weights are expanded to BF16
+// kFp4Chunk experts at a time into workspace scratch, and the grouped GEMMs run over that
+// chunk's jobs with each expert's FP32 matrix scale applied to the FP32 accumulators (the
+// same products as the oracle's exact dequantisation; activations stay BF16).
+// ------------------------------------------------------------------------------------------
+constexpr int kFp4Chunk = 16;   // experts dequantised per pass
+
+// Chunk `chunk` of the active experts: expert a = chunk * kFp4Chunk + blockIdx.y. Each thread
+// expands 32 elements of one row (16 code bytes and their two block scales) to BF16.
+__global__ void __launch_bounds__(256) fp4_dequant_kernel(beam_nvfp4_experts W, int H, int F,
+                                                          MoePlan pl, int chunk,
+                                                          uint16_t* __restrict__ gu_bf,
+                                                          uint16_t* __restrict__ dn_bf) {
+  pdl_trigger();
+  pdl_wait();   // the previous chunk's GEMMs have finished reading the scratch
+  const int g = blockIdx.y, a = chunk * kFp4Chunk + g;
+  if (a >= *pl.n_active) return;
+  const int e = pl.active[a];
+  const size_t n_gu = size_t(2) * F * (H / 32), n_dn = size_t(H) * (F / 32);
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_gu + n_dn;
+       i += size_t(gridDim.x) * blockDim.x) {
+    const bool gu = i < n_gu;
+    const size_t j = gu ? i : i - n_gu;
+    const int K = gu ? H : F;
+    const size_t row = j / (K / 32), c32 = j - row * (K / 32);   // 32-element group in the row
+    const size_t erow = (gu ? size_t(e) * 2 * F : size_t(e) * H) + row;
+    const uint8_t* codes = (gu ? W.gate_up : W.down) + erow * (K / 2) + c32 * 16;
+    const uint8_t* scl = (gu ? W.gate_up_scale : W.down_scale) + erow * (K / 16) + c32 * 2;
+    const uint4 q = *reinterpret_cast<const uint4*>(codes);
+    uint32_t slo, shi;
+    e4m3x2_scales(*reinterpret_cast<const uint16_t*>(scl), slo, shi);
+    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t h[4];
+      e2m1x8_to_f16(qw[k], h);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t v = hmul2(h[t], k < 2 ? slo : shi);   // exact in f16
+        float lo, hi;
+        asm("{.reg .f16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b;}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(v));
+        o[4 * k + t] = pack_bf2(lo, hi);   // exact in BF16
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>((gu ? gu_bf + size_t(g) * 2 * F * H
+                                              : dn_bf + size_t(g) * H * F) +
+                                          row * K + c32 * 32);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+  }
+}
+
+// The chunk's jobs (the plan's jobs, in active-expert order, are contiguous per expert): group
+// = the expert's place in the chunk, the tile-order field recomputed for the chunk's list; and
+// the chunk's FP32 matrix scales.
+__global__ void fp4_chunk_jobs_kernel(MoePlan pl, int chunk, const float* __restrict__ gu_global,
+                                      const float* __restrict__ dn_global,
+                                      int4* __restrict__ cj, int* __restrict__ cn,
+                                      float* __restrict__ sgu, float* __restrict__ sdn) {
+  pdl_trigger();
+  pdl_wait();   // the previous chunk's GEMMs have finished reading the chunk's list
+  if (threadIdx.x != 0) return;
+  const int na = *pl.n_active, nj = *pl.n_jobs;
+  const int a0 = chunk * kFp4Chunk, a1 = min(a0 + kFp4Chunk, na);
+  int n = 0, a = -1, prev_e = -1, j_local_first = 0;
+  for (int j = 0; j < nj; ++j) {
+    const int4 jb = pl.jobs[j];
+    if (jb.x != prev_e) {   // next active expert (jobs follow the active list)
+      ++a;
+      prev_e = jb.x;
+      j_local_first = n;
+    }
+    if (a < a0) continue;
+    if (a >= a1) break;
+    const int cnt = jb.w >> 20;
+    cj[n++] = make_int4(a - a0, jb.y, jb.z, j_local_first | (cnt << 20));
+  }
+  for (int g = 0; g < a1 - a0; ++g) {
+    const int e = pl.active[a0 + g];
+    sgu[g] = gu_global[e];
+    sdn[g] = dn_global[e];
+  }
+  *cn = n;
+}
+
+// ------------------------------------------------------------------------------------------
 // FP8 (e4m3, one FP32 scale per 128 x 128 block) expert weights, decode: the NVFP4 kernels'
 // layout with one byte per element. Lane (g, c) loads, per 128-element block of each of its
 // two rows, the 32 bytes of elements [32c, 32c + 32) (two 16-byte loads); cvt.rn.f16x2.e4m3x2
@@ -1047,6 +1138,10 @@ size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
   if (grouped) {
     b += align_up(size_t(max_jobs(int(P), int(E))) * 16, 256) + 256;
     b += align_up(P * c->hidden * 2, 256);                       // gathered inputs
+    // NVFP4 experts: BF16 weights of kFp4Chunk experts, the chunk's jobs and matrix scales
+    const size_t H = c->hidden, F = c->d_ff_expert;
+    b += align_up(size_t(kFp4Chunk) * 2 * F * H * 2, 256) + align_up(size_t(kFp4Chunk) * H * F * 2, 256);
+    b += align_up(size_t(max_jobs(int(P), int(E))) * 16, 256) + 3 * 256;
   }
   // FP32 per-pair rows and the down kernel's completion counters (decode forms)
   if (grouped || P > size_t(kFusedMaxPairs) || T < kMoeGemmMinT)
@@ -1218,11 +1313,61 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
   if (!aligned16(u) || !aligned16(ws) || !aligned16(w->gate_up) || !aligned16(w->down) ||
       !aligned16(w->gate_up_scale) || !aligned16(w->down_scale))
     return BEAM_ERR_INVALID_ARG;
-  if (E > 4096 || (H & 127) || (F & 127) || T >= kMoeGemmMinT) return BEAM_ERR_UNSUPPORTED;
+  if (E > 4096 || (H & 127) || (F & 127)) return BEAM_ERR_UNSUPPORTED;
   if (T == 0) return BEAM_OK;
   const int P = T * k;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Carver cv{static_cast<char*>(ws), ws_bytes};
+  if (T >= kMoeGemmMinT) {
+    // plan -> gather -> per chunk of kFp4Chunk active experts: BF16 weights, the chunk's job
+    // list, grouped gate/up and down GEMMs (matrix scales on the accumulators) -> combine
+    if (!tc::gemm_supported(u, H, w->gate_up, H, H) || !tc::gemm_supported(u, F, w->down, F, F))
+      return BEAM_ERR_UNSUPPORTED;
+    MoePlan pl = carve_plan(cv, E, P, true);
+    uint16_t* act = cv.take<uint16_t>(size_t(P) * F);
+    uint16_t* us = cv.take<uint16_t>(size_t(P) * H);
+    float* y = cv.take<float>(size_t(P) * H);
+    const int mj = max_jobs(P, E);
+    uint16_t* gu_bf = cv.take<uint16_t>(size_t(kFp4Chunk) * 2 * F * H);
+    uint16_t* dn_bf = cv.take<uint16_t>(size_t(kFp4Chunk) * H * F);
+    int4* cj = cv.take<int4>(size_t(mj));
+    int* cn = cv.take<int>(1);
+    float* sgu = cv.take<float>(kFp4Chunk);
+    float* sdn = cv.take<float>(kFp4Chunk);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+    const size_t nv = size_t(P) * (H / 8);
+    launch_pdl(gather_rows_kernel, dim3(unsigned((nv + 255) / 256)), dim3(256), 0, st, u, H, k, pl, P, us);
+    const int max_active = P < E ? P : E;
+    const int n_chunks = (max_active + kFp4Chunk - 1) / kFp4Chunk;
+    const size_t per_expert = size_t(2) * F * (H / 32) + size_t(H) * (F / 32);
+    const size_t want = (per_expert + 255) / 256;
+    const unsigned dq_blocks = unsigned(want < 64 ? want : 64);
+    for (int c = 0; c < n_chunks; ++c) {
+      launch_pdl(fp4_dequant_kernel, dim3(dq_blocks, kFp4Chunk), dim3(256), 0, st, *w, H, F, pl,
+                 c, gu_bf, dn_bf);
+      launch_pdl(fp4_chunk_jobs_kernel, dim3(1), dim3(32), 0, st, pl, c, w->gate_up_global,
+                 w->down_global, cj, cn, sgu, sdn);
+      if (const cudaError_t err_ = tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, gu_bf, kFp4Chunk * 2 * F,
+                                                    2 * F, H, cj, cn, mj, F, F, nullptr, act, F, st, sgu);
+          err_ != cudaSuccess)
+        return cuda_status(err_);
+      if (const cudaError_t err_ = tc::gemm_grouped(tc::kF32, act, P, F, F, dn_bf, kFp4Chunk * H, H, F,
+                                                    cj, cn, mj, H, 0, pl.pairs, y, H, st, sdn);
+          err_ != cudaSuccess)
+        return cuda_status(err_);
+    }
+    if ((H & 3) == 0 && aligned16(out)) {
+      const size_t n4 = size_t(T) * (H / 4);
+      launch_pdl(moe_combine4_kernel, dim3(unsigned((n4 + 255) / 256)), dim3(256), 0, st, y,
+                 topk_w, topk_idx, T, H, k, E, out);
+    } else {
+      const size_t n1 = size_t(T) * H;
+      launch_pdl(moe_combine_kernel, dim3(unsigned((n1 + 255) / 256)), dim3(256), 0, st, y,
+                 topk_w, topk_idx, T, H, k, E, out);
+    }
+    return launch_status();
+  }
   MoePlan pl = carve_plan(cv, E, P, false);
   uint16_t* a16 = cv.take<uint16_t>(size_t(P) * F);
   float* y = cv.take<float>(size_t(P) * H);

@@ -220,12 +220,14 @@ typedef struct {
   const float* down_global;
 } beam_nvfp4_experts;
 
-/* beam_moe with NVFP4 expert weights (weight-only quantisation: activations stay BF16, the
- * products run in f16 with FP32 accumulation, every dequantised weight being exact in f16).
- * Same arguments and results as beam_moe otherwise; the caller's u is rounded to f16 (exact
- * for BF16 values of magnitude 2^-14 .. 65504). Decode sizes: 1 <= T < 32 tokens; other T,
- * or H or d_ff not a multiple of 128, return BEAM_ERR_UNSUPPORTED. The workspace is the one
- * beam_workspace_bytes gives for T. */
+/* beam_moe with NVFP4 expert weights (weight-only quantisation: activations stay BF16, FP32
+ * accumulation of products of exactly dequantised weights). Same arguments and results as beam_moe otherwise. Below 32 tokens the products run on
+ * mma.sync in f16 (the caller's u is rounded to f16: exact for BF16 values of magnitude
+ * 2^-14 .. 65504); from 32 tokens the selected experts' weights are expanded to BF16 (exact:
+ * e2m1 times its e4m3 scale has at most 6 significant bits), 16 experts at a time, and the
+ * grouped BF16 tensor-core GEMMs of beam_moe run on them with the matrix scales applied to
+ * the FP32 products. H or d_ff not a multiple of 128 returns BEAM_ERR_UNSUPPORTED. The
+ * workspace is the one beam_workspace_bytes gives for T. */
 beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16* u,
                            const int32_t* topk_idx, const float* topk_w,
                            const beam_nvfp4_experts* w, int T, beam_bf16* out, void* ws,

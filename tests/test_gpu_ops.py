@@ -434,19 +434,28 @@ def _nvfp4_experts(shape, used, seed):
     return full, experts
 
 
-# a second small shape (hidden and d_ff multiples of 256, 4 of 16 experts per token)
+# a second small shape (hidden and d_ff multiples of 256, 4 of 16 experts per token), and one
+# with 64 experts, 8 per token: from 32 tokens its active experts span several dequantisation
+# chunks of the grouped GEMM path
 NVFP4_MID = dataclasses.replace(TINY, hidden=512, d_ff_expert=256)
+NVFP4_WIDE = dataclasses.replace(TINY, hidden=512, d_ff_expert=256, n_experts=64, n_groups=8,
+                                 topk_groups=4, topk=8)
 
 
 @pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 5, None),
                                             (TINY, 13, None), (TINY, 31, 6), (NVFP4_MID, 1, None),
                                             (NVFP4_MID, 2, None), (BEAM, 1, None),
-                                            (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None)])
+                                            (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None),
+                                            (TINY, 32, None), (TINY, 300, None),
+                                            (NVFP4_MID, 64, 5), (NVFP4_WIDE, 64, None),
+                                            (NVFP4_WIDE, 130, 37), (BEAM, 48, 9)])
 def test_moe_nvfp4(shape, T, n_used):
-    """NVFP4 expert weights (e2m1 codes, e4m3 block scales, FP32 matrix scales): mma.sync f16
-    products of the dequantised weights, the selected experts only; up to 4 tokens four warps
-    split each row block's K (T=4 and T=5 sit on either side); T=31 over 6 experts gives
-    experts more than 8 pairs (several passes)."""
+    """NVFP4 expert weights (e2m1 codes, e4m3 block scales, FP32 matrix scales): below 32
+    tokens mma.sync f16 products of the dequantised weights, the selected experts only; up to 4
+    tokens four warps split each row block's K (T=4 and T=5 sit on either side); T=31 over 6
+    experts gives experts more than 8 pairs (several passes). From 32 tokens the grouped BF16
+    tensor-core GEMMs on weights dequantised chunk by chunk (NVFP4_WIDE at 130 tokens over 37
+    experts: three chunks)."""
     seed = 91 + T
     cfg = cfg_of(shape)
     idx, w = _random_routing(shape, T, seed, n_used)
