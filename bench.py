@@ -847,8 +847,6 @@ def main():
     args = ap.parse_args()
     if args.lm_head_vocab and args.workload == "stack_prefill":
         ap.error("--lm-head-vocab is timed for decode workloads")
-    if args.experts == "fp8" and args.workload == "stack_prefill":
-        ap.error("--experts fp8 is a decode format here (its kernels take up to 31 tokens)")
     if args.experts != "bf16":
         args.no_prefill = True   # the stack_decode line's prefill object stays BF16
     if args.workload == "stack_verify" and not 1 <= args.chunk <= 16:

@@ -49,6 +49,8 @@ struct GemmParams {
   const int* row_map;    // optional: C row of A row r is row_map[r]
   const float* group_scale;   // grouped, optional: the accumulator of group g is multiplied by
                               // group_scale[g] before the epilogue (per-matrix weight scales)
+  int a_k;               // A columns when the reduction runs over A twice (K = 2 a_k: B rows
+                         // hold two parts of the weights, e.g. BF16 high and low); else 0
 };
 
 // The QKV epilogue for one token row and one 128-column head of the tile (kQKV mode).
@@ -234,7 +236,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           mbar_expect_tx(full0 + 8 * s, STAGE_BYTES);
           const uint32_t sa = s_base + s * STAGE_BYTES;
-          tma_load_2d(sa, &ta, kb * BK, tl.a_row0, full0 + 8 * s);
+          tma_load_2d(sa, &ta, p.a_k > 0 && kb * BK >= p.a_k ? kb * BK - p.a_k : kb * BK,
+                      tl.a_row0, full0 + 8 * s);
           if (MODE == kSwiGLU) {
             tma_load_2d(sa + A_BYTES, &tb, kb * BK, tl.b_row0 + tl.n0, full0 + 8 * s);
             tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tb, kb * BK, tl.b_row0 + p.up_off + tl.n0,
@@ -543,15 +546,18 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
 cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
                          int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
                          int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
-                         cudaStream_t st, const float* group_scale) {
+                         cudaStream_t st, const float* group_scale, bool a_twice) {
   if (M <= 0 || N <= 0 || max_jobs <= 0) return cudaSuccess;
+  // a_twice: B rows are [part 0 | part 1] of K/2 columns each, both multiplied by A's K/2
+  const int a_k = a_twice ? K / 2 : 0;
+  if (a_twice && (K % (2 * BK)) != 0) return cudaErrorInvalidValue;
   if (!gemm_supported(A, lda, B, ldb, K)) return cudaErrorInvalidValue;
   if (!tensor_map_encoder_ready()) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const int bbox = mode == kSwiGLU ? BN / 2 : BN;
-  if (!make_map(&ta, A, K, M, lda, BM) || !make_map(&tb, B, K, b_rows, ldb, bbox))
+  if (!make_map(&ta, A, a_twice ? a_k : K, M, lda, BM) || !make_map(&tb, B, K, b_rows, ldb, bbox))
     return cudaErrorInvalidValue;
-  GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map, group_scale};
+  GemmParams p{M, N, K, C, ldc, jobs, n_jobs, b_stride, up_off, row_map, group_scale, a_k};
   const int nt = mode == kSwiGLU ? BN / 2 : BN;
   const int tiles = ((N + nt - 1) / nt) * max_jobs;
   if (mode == kSwiGLU) return launch<kSwiGLU>(ta, tb, p, tiles, st);

@@ -58,11 +58,14 @@ cudaError_t gemm_swiglu(const uint16_t* A, int M, int K, int lda, const uint16_t
 // (units for kSwiGLU, whose up half starts up_off rows after the gate half). The output row
 // of A row r is row_map[r] if given. The grid covers max_jobs jobs; jobs at index >= *n_jobs
 // return at once. group_scale (optional, device): group g's products are multiplied by
-// group_scale[g] in FP32 before the epilogue (kSwiGLU: both gate and up).
+// group_scale[g] in FP32 before the epilogue (kSwiGLU: both gate and up). a_twice: A has K/2
+// columns and every B row holds two parts of K/2 (a weight split into BF16 high and low
+// parts), each multiplied by A, so the sum runs over both (K a multiple of 128).
 cudaError_t gemm_grouped(int mode, const uint16_t* A, int M, int K, int lda, const uint16_t* B,
                          int b_rows, int b_stride, int ldb, const int4* jobs, const int* n_jobs,
                          int max_jobs, int N, int up_off, const int* row_map, void* C, int ldc,
-                         cudaStream_t st, const float* group_scale = nullptr);
+                         cudaStream_t st, const float* group_scale = nullptr,
+                         bool a_twice = false);
 
 }  // namespace tc
 }  // namespace beam

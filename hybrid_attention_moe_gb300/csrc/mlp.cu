@@ -808,10 +808,11 @@ __global__ void __launch_bounds__(256) fp4_dequant_kernel(beam_nvfp4_experts W, 
   }
 }
 
-// The chunk's jobs (the plan's jobs, in active-expert order, are contiguous per expert): group
-// = the expert's place in the chunk, the tile-order field recomputed for the chunk's list; and
-// the chunk's FP32 matrix scales.
-__global__ void fp4_chunk_jobs_kernel(MoePlan pl, int chunk, const float* __restrict__ gu_global,
+// The jobs of chunk `chunk` of `csize` active experts (the plan's jobs, in active-expert order,
+// are contiguous per expert): group = the expert's place in the chunk, the tile-order field
+// recomputed for the chunk's list; and, when given, the chunk's FP32 matrix scales.
+__global__ void moe_chunk_jobs_kernel(MoePlan pl, int chunk, int csize,
+                                      const float* __restrict__ gu_global,
                                       const float* __restrict__ dn_global,
                                       int4* __restrict__ cj, int* __restrict__ cn,
                                       float* __restrict__ sgu, float* __restrict__ sdn) {
@@ -819,7 +820,7 @@ __global__ void fp4_chunk_jobs_kernel(MoePlan pl, int chunk, const float* __rest
   pdl_wait();   // the previous chunk's GEMMs have finished reading the chunk's list
   if (threadIdx.x != 0) return;
   const int na = *pl.n_active, nj = *pl.n_jobs;
-  const int a0 = chunk * kFp4Chunk, a1 = min(a0 + kFp4Chunk, na);
+  const int a0 = chunk * csize, a1 = min(a0 + csize, na);
   int n = 0, a = -1, prev_e = -1, j_local_first = 0;
   for (int j = 0; j < nj; ++j) {
     const int4 jb = pl.jobs[j];
@@ -833,7 +834,7 @@ __global__ void fp4_chunk_jobs_kernel(MoePlan pl, int chunk, const float* __rest
     const int cnt = jb.w >> 20;
     cj[n++] = make_int4(a - a0, jb.y, jb.z, j_local_first | (cnt << 20));
   }
-  for (int g = 0; g < a1 - a0; ++g) {
+  for (int g = 0; gu_global != nullptr && g < a1 - a0; ++g) {
     const int e = pl.active[a0 + g];
     sgu[g] = gu_global[e];
     sdn[g] = dn_global[e];
@@ -1128,6 +1129,63 @@ MoePlan carve_plan(Carver& cv, int E, int P, bool grouped) {
   return pl;
 }
 
+
+// FP8 experts from kMoeGemmMinT tokens. A code times its FP32 block scale is not a BF16 number
+// in general, so each weight is stored as two BF16 parts, hi = bf16(w) and lo = bf16(w - hi)
+// (w to ~16 significant bits), side by side in a row of 2K columns, and the grouped GEMMs
+// run over K twice against the same activations (gemm_grouped's a_twice). kFp4Chunk / 2
+// experts per pass fill the same scratch as the NVFP4 path.
+constexpr int kFp8Chunk = kFp4Chunk / 2;
+
+__global__ void __launch_bounds__(256) fp8_dequant_kernel(beam_fp8_experts W, int H, int F,
+                                                          MoePlan pl, int chunk,
+                                                          uint16_t* __restrict__ gu_bf,
+                                                          uint16_t* __restrict__ dn_bf) {
+  pdl_trigger();
+  pdl_wait();   // the previous chunk's GEMMs have finished reading the scratch
+  const int g = blockIdx.y, a = chunk * kFp8Chunk + g;
+  if (a >= *pl.n_active) return;
+  const int e = pl.active[a];
+  const size_t n_gu = size_t(2) * F * (H / 16), n_dn = size_t(H) * (F / 16);
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_gu + n_dn;
+       i += size_t(gridDim.x) * blockDim.x) {
+    const bool gu = i < n_gu;
+    const size_t j = gu ? i : i - n_gu;
+    const int K = gu ? H : F, R = gu ? 2 * F : H;
+    const size_t row = j / (K / 16), c16 = j - row * (K / 16);   // 16-element group in the row
+    const uint8_t* codes = (gu ? W.gate_up : W.down) + (size_t(e) * R + row) * K + c16 * 16;
+    const float sc = (gu ? W.gate_up_scale : W.down_scale)[(size_t(e) * (R / 128) + row / 128) *
+                                                               (K / 128) + (c16 * 16) / 128];
+    const uint4 q = *reinterpret_cast<const uint4*>(codes);
+    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+      uint32_t h2[2];
+      e4m3x4_to_f16(qw[k2], h2[0], h2[1]);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float x0, x1;
+        asm("{.reg .f16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b;}"
+            : "=f"(x0), "=f"(x1)
+            : "r"(h2[t]));
+        const float w0 = x0 * sc, w1 = x1 * sc;
+        const uint32_t hh = pack_bf2(w0, w1);
+        hi[2 * k2 + t] = hh;
+        lo[2 * k2 + t] = pack_bf2(w0 - __uint_as_float(hh << 16), w1 - __uint_as_float(hh & 0xFFFF0000u));
+      }
+    }
+    uint16_t* rowp = (gu ? gu_bf + size_t(g) * 2 * F * 2 * H : dn_bf + size_t(g) * H * 2 * F) +
+                     row * 2 * K;
+    uint4* dh = reinterpret_cast<uint4*>(rowp + c16 * 16);
+    uint4* dl = reinterpret_cast<uint4*>(rowp + K + c16 * 16);
+    dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  }
+}
+
 }  // namespace
 
 size_t moe_ws_bytes(const beam_layer_cfg* c, int T) {
@@ -1346,8 +1404,8 @@ extern "C" beam_status beam_moe_nvfp4(const beam_layer_cfg* cfg, const beam_bf16
     for (int c = 0; c < n_chunks; ++c) {
       launch_pdl(fp4_dequant_kernel, dim3(dq_blocks, kFp4Chunk), dim3(256), 0, st, *w, H, F, pl,
                  c, gu_bf, dn_bf);
-      launch_pdl(fp4_chunk_jobs_kernel, dim3(1), dim3(32), 0, st, pl, c, w->gate_up_global,
-                 w->down_global, cj, cn, sgu, sdn);
+      launch_pdl(moe_chunk_jobs_kernel, dim3(1), dim3(32), 0, st, pl, c, kFp4Chunk,
+                 w->gate_up_global, w->down_global, cj, cn, sgu, sdn);
       if (const cudaError_t err_ = tc::gemm_grouped(tc::kSwiGLU, us, P, H, H, gu_bf, kFp4Chunk * 2 * F,
                                                     2 * F, H, cj, cn, mj, F, F, nullptr, act, F, st, sgu);
           err_ != cudaSuccess)
@@ -1417,11 +1475,63 @@ extern "C" beam_status beam_moe_fp8(const beam_layer_cfg* cfg, const beam_bf16* 
   if (H <= 0 || F <= 0 || E <= 0 || k <= 0) return BEAM_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(ws) || !aligned16(w->gate_up) || !aligned16(w->down))
     return BEAM_ERR_INVALID_ARG;
-  if (E > 4096 || (H & 127) || (F & 127) || T >= kMoeGemmMinT) return BEAM_ERR_UNSUPPORTED;
+  if (E > 4096 || (H & 127) || (F & 127)) return BEAM_ERR_UNSUPPORTED;
   if (T == 0) return BEAM_OK;
   const int P = T * k;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   Carver cv{static_cast<char*>(ws), ws_bytes};
+  if (T >= kMoeGemmMinT) {
+    // plan -> gather -> per chunk of kFp8Chunk active experts: BF16 high and low parts of the
+    // weights, the chunk's job list, grouped gate/up and down GEMMs over K twice -> combine
+    if (!tc::gemm_supported(u, H, w->gate_up, 2 * H, 2 * H) ||
+        !tc::gemm_supported(u, F, w->down, 2 * F, 2 * F))
+      return BEAM_ERR_UNSUPPORTED;
+    MoePlan pl = carve_plan(cv, E, P, true);
+    uint16_t* act = cv.take<uint16_t>(size_t(P) * F);
+    uint16_t* us = cv.take<uint16_t>(size_t(P) * H);
+    float* y = cv.take<float>(size_t(P) * H);
+    const int mj = max_jobs(P, E);
+    uint16_t* gu_bf = cv.take<uint16_t>(size_t(kFp4Chunk) * 2 * F * H);   // kFp8Chunk x 2 parts
+    uint16_t* dn_bf = cv.take<uint16_t>(size_t(kFp4Chunk) * H * F);
+    int4* cj = cv.take<int4>(size_t(mj));
+    int* cn = cv.take<int>(1);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    launch_pdl(moe_plan_kernel, dim3(1), dim3(kPlanThreads), 3 * E * sizeof(int), st, topk_idx, P, E, pl);
+    const size_t nv = size_t(P) * (H / 8);
+    launch_pdl(gather_rows_kernel, dim3(unsigned((nv + 255) / 256)), dim3(256), 0, st, u, H, k, pl, P, us);
+    const int max_active = P < E ? P : E;
+    const int n_chunks = (max_active + kFp8Chunk - 1) / kFp8Chunk;
+    const size_t per_expert = size_t(2) * F * (H / 16) + size_t(H) * (F / 16);
+    const size_t want = (per_expert + 255) / 256;
+    const unsigned dq_blocks = unsigned(want < 128 ? want : 128);
+    for (int c = 0; c < n_chunks; ++c) {
+      launch_pdl(fp8_dequant_kernel, dim3(dq_blocks, kFp8Chunk), dim3(256), 0, st, *w, H, F, pl,
+                 c, gu_bf, dn_bf);
+      launch_pdl(moe_chunk_jobs_kernel, dim3(1), dim3(32), 0, st, pl, c, kFp8Chunk,
+                 static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), cj, cn,
+                 static_cast<float*>(nullptr), static_cast<float*>(nullptr));
+      if (const cudaError_t err_ = tc::gemm_grouped(tc::kSwiGLU, us, P, 2 * H, H, gu_bf,
+                                                    kFp8Chunk * 2 * F, 2 * F, 2 * H, cj, cn, mj, F,
+                                                    F, nullptr, act, F, st, nullptr, true);
+          err_ != cudaSuccess)
+        return cuda_status(err_);
+      if (const cudaError_t err_ = tc::gemm_grouped(tc::kF32, act, P, 2 * F, F, dn_bf, kFp8Chunk * H,
+                                                    H, 2 * F, cj, cn, mj, H, 0, pl.pairs, y, H, st,
+                                                    nullptr, true);
+          err_ != cudaSuccess)
+        return cuda_status(err_);
+    }
+    if ((H & 3) == 0 && aligned16(out)) {
+      const size_t n4 = size_t(T) * (H / 4);
+      launch_pdl(moe_combine4_kernel, dim3(unsigned((n4 + 255) / 256)), dim3(256), 0, st, y,
+                 topk_w, topk_idx, T, H, k, E, out);
+    } else {
+      const size_t n1 = size_t(T) * H;
+      launch_pdl(moe_combine_kernel, dim3(unsigned((n1 + 255) / 256)), dim3(256), 0, st, y,
+                 topk_w, topk_idx, T, H, k, E, out);
+    }
+    return launch_status();
+  }
   MoePlan pl = carve_plan(cv, E, P, false);
   uint16_t* a16 = cv.take<uint16_t>(size_t(P) * F);
   float* y = cv.take<float>(size_t(P) * H);

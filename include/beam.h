@@ -247,12 +247,15 @@ typedef struct {
   const float* down_scale;
 } beam_fp8_experts;
 
-/* beam_moe with FP8 expert weights (weight-only: activations stay BF16; codes become f16
- * exactly in registers and the products run in f16 with FP32 accumulation, each 128-element
- * block's sum multiplied by its FP32 scale). Same arguments and results as beam_moe
- * otherwise; u is rounded to f16 (exact for BF16 values of magnitude 2^-14 .. 65504). Decode
- * sizes: 1 <= T < 32 tokens; other T, or H or d_ff not a multiple of 128, return
- * BEAM_ERR_UNSUPPORTED. The workspace is the one beam_workspace_bytes gives for T. */
+/* beam_moe with FP8 expert weights (weight-only: activations stay BF16, FP32 accumulation).
+ * Same arguments and results as beam_moe otherwise. Below 32 tokens the codes become f16
+ * exactly in registers and the products run on mma.sync in f16, each 128-element block's sum
+ * multiplied by its FP32 scale (u is rounded to f16: exact for BF16 values of magnitude
+ * 2^-14 .. 65504). From 32 tokens each selected weight code x scale is expanded to two BF16
+ * parts, hi = bf16(w) and lo = bf16(w - hi) (~16 significant bits), 8 experts at a time, and
+ * the grouped BF16 tensor-core GEMMs of beam_moe run over both parts. H or d_ff not a
+ * multiple of 128 returns BEAM_ERR_UNSUPPORTED. The workspace is the one
+ * beam_workspace_bytes gives for T. */
 beam_status beam_moe_fp8(const beam_layer_cfg* cfg, const beam_bf16* u, const int32_t* topk_idx,
                          const float* topk_w, const beam_fp8_experts* w, int T, beam_bf16* out,
                          void* ws, size_t ws_bytes, beam_stream_t stream);

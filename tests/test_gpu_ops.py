@@ -510,12 +510,15 @@ def _fp8_experts(shape, used, seed):
 @pytest.mark.parametrize("shape,T,n_used", [(TINY, 1, None), (TINY, 3, 5), (TINY, 5, None),
                                             (TINY, 13, None), (TINY, 31, 6), (BEAM, 1, None),
                                             (BEAM, 2, None), (BEAM, 4, None), (BEAM, 8, None),
-                                            (BEAM, 31, 20)])
+                                            (BEAM, 31, 20), (TINY, 32, None), (TINY, 300, None),
+                                            (NVFP4_WIDE, 130, 37), (BEAM, 48, 9)])
 def test_moe_fp8(shape, T, n_used):
     """Block-scaled FP8 expert weights (e4m3 codes, one FP32 scale per 128 x 128 block):
-    mma.sync f16 products of the exactly converted codes, each block's sum times its scale;
-    up to 4 tokens four warps split each row block's K (T=4 and T=5 sit on either side);
-    T=31 over 6 experts gives experts more than 8 pairs (several passes)."""
+    below 32 tokens mma.sync f16 products of the exactly converted codes, each block's sum
+    times its scale; up to 4 tokens four warps split each row block's K (T=4 and T=5 sit on
+    either side); T=31 over 6 experts gives experts more than 8 pairs (several passes). From
+    32 tokens the grouped tensor-core GEMMs on each weight's BF16 high and low parts (130
+    tokens over 37 experts: five chunks of 8; 48 full-width tokens over 9: two)."""
     seed = 97 + T
     cfg = cfg_of(shape)
     idx, w = _random_routing(shape, T, seed, n_used)
