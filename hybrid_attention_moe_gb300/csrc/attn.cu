@@ -816,6 +816,10 @@ size_t attn_ws_bytes(const beam_layer_cfg* c, int T, int max_pos, int window) {
   const size_t d8 = adec::ws_bytes(T, c->n_kv, window, mp, true);
   if (d16 > alt) alt = d16;
   if (d8 > alt) alt = d8;
+  if (window == 0) {   // or the grouped verification form's partials and group list
+    const size_t dv = adec::verify_ws_bytes_max(T);
+    if (dv > alt) alt = dv;
+  }
   const size_t dec = b - align_up(size_t(T) * c->n_q * c->head_dim * 2, 256);
   if (alt > dec) b += alt - dec;
   return b;
@@ -848,7 +852,16 @@ extern "C" beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q,
   cudaError_t e;
   const int G = cfg->n_q / cfg->n_kv;
   const bool dec = decode_form(T, max_q_per_seq, cfg->n_kv);
-  if (dec &&
+  if (dec && adec::verify_supported(D, G, cache->window, fp8, cache->k, cache->v,
+                                    max_keys_of(cache->window, max_pos), T, max_q_per_seq)) {
+    // several tokens of a sequence: each K/V block is read once for all of them
+    const size_t vb = adec::verify_ws_bytes(T, G, max_q_per_seq);
+    void* vw = cv.take<char>(vb);
+    if (!cv.ok) return BEAM_ERR_INVALID_ARG;
+    e = adec::verify(q, g, gate_bias, seq_id, pos, T, max_pos, max_q_per_seq, cfg->n_q,
+                     cfg->n_kv, *cache, sl2, og, vw, vb, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  } else if (dec &&
       adec::supported(D, G, cache->window, cache->capacity, fp8, cache->k, cache->v,
                       max_keys_of(cache->window, max_pos))) {
     const size_t db = adec::ws_bytes(T, cfg->n_kv, cache->window, max_pos, fp8);

@@ -331,7 +331,6 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) attn_decode_tma_kernel(
     const Params P) {
   using C = Cfg<FP8>;
   constexpr int NCT = C::NCW * 32;   // consumer threads
-  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -529,6 +528,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) attn_decode_tma_kernel(
     }
   }
   __syncthreads();
+  // dependents are released only now, not at entry: launched early, the merge and the o_proj
+  // GEMV behind it (which prefetches its weights into L2 before its wait) ran beside the key
+  // stream and cost more than the launch latency they hide (measured: the 8-token
+  // verification step 2.82 -> 2.59 ms with the grouped kernel; neutral to slightly faster
+  // with the per-token one)
+  pdl_trigger();
   if (warp == C::NCW && lane == 0) {
     // normally a no-op: every issued block was consumed; after an expired wait, let the
     // copies still in flight land before the CTA's shared memory is released
@@ -620,6 +625,506 @@ __global__ void __launch_bounds__(kMergeThreads) attn_decode_merge_kernel(const 
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Verification batches (several new tokens of one sequence, full attention, BF16 cache): the
+// tokens of a sequence share every K/V block. A group is a run of up to TG consecutive tokens
+// of the call with the same sequence id; its query rows (token-major, then the G heads of the
+// KV group) are the columns of NT n-tiles of 8, so a block loaded once serves the whole group
+// instead of being read once per token. The (group, KV head) pairs take the place of the
+// (token, KV head) pairs above: blocks of 64 keys, equal contiguous ranges per CTA, partials
+// and a merge kernel for pairs split between CTAs. Consumer warp w takes n-tile w % NT and
+// the 16-key slices w / NT, w / NT + WPT, ... of every block. Each column masks the keys past
+// its own token's position; V is masked only past the group's last position (slots there may
+// hold anything). The group list is built on the device from seq_id, so any token order is
+// computed correctly; a sequence's tokens share blocks only where they are consecutive.
+// ------------------------------------------------------------------------------------------
+constexpr int kVMaxParts = 40;   // CTAs meeting one (group, KV head) pair at most
+
+template <int NT>
+struct VCfg {
+  static constexpr int WPT = NT <= 3 ? 4 : (NT <= 6 ? 2 : 1);   // warps per n-tile
+  static constexpr int NCW = NT * WPT;                           // consumer warps
+  static constexpr int THREADS = (NCW + 1) * 32;
+  static constexpr int NCOL = NT * 8;
+  static constexpr int BK = 64;
+  static constexpr int KB = BK * 2 * D;    // K (or V) bytes of one block
+  static constexpr int STAGE = 2 * KB;
+  static constexpr int NST = 4;
+  static constexpr int OLD = D + 4;
+  static constexpr int OW = NST * STAGE;                         // [NCW][8][OLD] O partials
+  static constexpr int MLW = OW + NCW * 8 * OLD * 4;             // [NCW][8][2] (m, l)
+  static constexpr int FW = MLW + NCW * 8 * 2 * 4;               // [NCW][8] warp weights
+  static constexpr int LH = FW + NCW * 8 * 4;                    // [NCOL] sums, [NCOL] maxima
+  static constexpr int GL = LH + 2 * NCOL * 4;                   // [kVerifyMaxT + 1] group starts
+  static constexpr int MISC = GL + (kVerifyMaxT + 1) * 4;        // ints: groups, abort, issued
+  static constexpr int BAR = (MISC + 16 + 7) / 8 * 8;
+  static constexpr int BYTES = BAR + 2 * NST * 8 + 1024;         // + alignment slack
+};
+static_assert(VCfg<12>::BYTES <= 227 * 1024, "verify form exceeds shared memory");
+
+struct VParams {
+  const uint16_t* q;
+  const int32_t* seq_id;
+  const int32_t* pos;
+  const uint16_t* gpre;
+  const uint16_t* gate_bias;
+  uint16_t* og;
+  float* part_acc;   // [grid][2][NCOL][D]
+  float* part_ml;    // [grid][2][NCOL][2]
+  int* groups;       // [0] = number of groups n, [1 + i] = first token of group i, [1 + n] = T
+  int T, TG, n_q, n_kv, G, num_seqs, cap;
+  int NB;            // blocks per (group, KV head) pair: positions 1 .. max_pos
+  int grid;
+  float sl2;
+};
+
+// Blocks per CTA: an equal share of the flattened (pair, block) space, and at least enough
+// that a pair meets no more than kVMaxParts CTA ranges.
+__host__ __device__ __forceinline__ int verify_range(int total, int NB, int grid) {
+  const int a = (total + grid - 1) / grid, b = (NB + kVMaxParts - 2) / (kVMaxParts - 1);
+  const int r = a > b ? a : b;
+  return r > 1 ? r : 1;
+}
+__device__ __forceinline__ size_t vpart_slot(int q, int c, int R, int NB) {
+  const int first = int((int64_t(c) * R) / NB);
+  return size_t(2 * c + (q == first ? 0 : 1));
+}
+
+// The call's group list, built by one warp: a group starts at token t when t opens a run of
+// equal sequence ids or lies a multiple of TG tokens into its run. gl[i] = first token of
+// group i, gl[n] = T; returns n (in every lane).
+__device__ int build_groups(const VParams& P, int* gl) {
+  const int lane = threadIdx.x & 31;
+  int run = 0, last_s = 0, n = 0;
+  for (int base = 0; base < P.T; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < P.T;
+    const int s = valid ? P.seq_id[t] : 0;
+    int sp = __shfl_up_sync(0xffffffffu, s, 1);
+    if (lane == 0) sp = last_s;
+    const unsigned brk = __ballot_sync(0xffffffffu, valid && (t == 0 || s != sp));
+    const unsigned below = brk & (0xffffffffu >> (31 - lane));   // bits 0 .. lane
+    const int rs = below ? base + 31 - __clz(below) : run;        // start of t's run
+    const bool start = valid && (t - rs) % P.TG == 0;
+    const unsigned sm = __ballot_sync(0xffffffffu, start);
+    if (start) gl[n + __popc(sm & ((1u << lane) - 1u))] = t;
+    n += __popc(sm);
+    run = __shfl_sync(0xffffffffu, rs, 31);
+    last_s = __shfl_sync(0xffffffffu, s, 31);
+  }
+  if (lane == 0) gl[n] = P.T;
+  __syncwarp();
+  return n;
+}
+
+// Pair q = group * n_kv + KV head. A token takes part when 1 <= pos <= cap and its position
+// lies within the host's bound (NB blocks); pg = the last position of the group's tokens that
+// take part, nbq = the blocks covering 1 .. pg.
+struct VGroup {
+  int t0, cnt, s, hk, pg, nbq;
+  unsigned int bad;
+};
+__device__ __forceinline__ bool vtoken_ok(const VParams& P, int p) {
+  return p >= 1 && p <= P.cap && (p - 1) / VCfg<2>::BK < P.NB;
+}
+__device__ __forceinline__ VGroup group_of(const VParams& P, const int* gl, int q) {
+  VGroup r;
+  const int gi = q / P.n_kv;
+  r.hk = q - gi * P.n_kv;
+  r.t0 = gl[gi];
+  r.cnt = gl[gi + 1] - r.t0;
+  r.s = P.seq_id[r.t0];
+  r.bad = 0;
+  r.pg = 0;
+  if (r.s < 0 || r.s >= P.num_seqs) {
+    r.bad = BEAM_DEV_BAD_SEQ;
+  } else {
+    for (int i = 0; i < r.cnt; ++i) {
+      const int p = P.pos[r.t0 + i];
+      if (vtoken_ok(P, p)) r.pg = max(r.pg, p);
+      else r.bad = BEAM_DEV_BAD_POSITION;
+    }
+  }
+  r.nbq = r.pg >= 1 ? (r.pg - 1) / VCfg<2>::BK + 1 : 0;
+  return r;
+}
+
+// One warp's 16 keys of a staged block for 8 query columns of a group (BF16 cache): as
+// warp_block, with a last position per accumulator column (pc0: column 2c, pc1: column 2c+1;
+// 0 = the column attends to nothing) and V masked past the group's last position pg. Keys
+// start at position 1 (full attention), so kbase >= 1.
+__device__ __forceinline__ void warp_block_cols(uint32_t kb, uint32_t vb,
+                                                const uint32_t (&qb)[8][2],
+                                                const uint32_t (&koff)[4],
+                                                const uint32_t (&voff)[4], int kbase, int pc0,
+                                                int pc1, int pg, float sl2, float (&m)[2],
+                                                float (&l)[2], float (&acc)[8][4]) {
+  using C = Cfg<false>;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int kp0 = kbase + g;
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < 8; kk += 2) {
+    uint32_t a[4], b[4];
+    ldsm_x4(kb + (kk >> 2) * (C::KB / 2) + koff[kk & 3], a[0], a[1], a[2], a[3]);
+    ldsm_x4(kb + ((kk + 1) >> 2) * (C::KB / 2) + koff[(kk + 1) & 3], b[0], b[1], b[2], b[3]);
+    mma_bf16(sa, a, qb[kk][0], qb[kk][1]);
+    mma_bf16(sb, b, qb[kk + 1][0], qb[kk + 1][1]);
+  }
+  // S^T fragment: [0] (key g, column 2c), [1] (key g, column 2c+1), [2], [3] key g + 8
+  float x[4];
+  x[0] = kp0 <= pc0 ? (sa[0] + sb[0]) * sl2 : kNegInf;
+  x[1] = kp0 <= pc1 ? (sa[1] + sb[1]) * sl2 : kNegInf;
+  x[2] = kp0 + 8 <= pc0 ? (sa[2] + sb[2]) * sl2 : kNegInf;
+  x[3] = kp0 + 8 <= pc1 ? (sa[3] + sb[3]) * sl2 : kNegInf;
+  float mh[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mh[0] = fmaxf(mh[0], __shfl_xor_sync(0xffffffffu, mh[0], o));
+    mh[1] = fmaxf(mh[1], __shfl_xor_sync(0xffffffffu, mh[1], o));
+  }
+  if (__any_sync(0xffffffffu, mh[0] > m[0] + kRescale || mh[1] > m[1] + kRescale)) {
+    float cr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float mn = fmaxf(m[h], mh[h]);
+      cr[h] = m[h] == kNegInf ? 0.f : ex2_approx(m[h] - mn);
+      m[h] = mn;
+      l[h] *= cr[h];
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= cr[0];
+      acc[mt][1] *= cr[1];
+      acc[mt][2] *= cr[0];
+      acc[mt][3] *= cr[1];
+    }
+  }
+  const float ms0 = m[0] == kNegInf ? 0.f : m[0], ms1 = m[1] == kNegInf ? 0.f : m[1];
+  const float p0 = ex2_approx(x[0] - ms0), p1 = ex2_approx(x[1] - ms1);
+  const float p2 = ex2_approx(x[2] - ms0), p3 = ex2_approx(x[3] - ms1);
+  l[0] += p0 + p2;
+  l[1] += p1 + p3;
+  const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+  const uint32_t l01 = pack_bf16x2(p0 - bf_lo(h01), p1 - bf_hi(h01));
+  const uint32_t l23 = pack_bf16x2(p2 - bf_lo(h23), p3 - bf_hi(h23));
+  const uint32_t bh0 = movtrans(h01), bh1 = movtrans(h23);
+  const uint32_t bl0 = movtrans(l01), bl1 = movtrans(l23);
+  if (kbase + 15 <= pg) {
+    pv_block<false, false>(vb, voff, bh0, bh1, bl0, bl1, 0u, 0u, acc);
+  } else {
+    auto ok = [&](int k) { return kbase + k <= pg; };
+    const uint32_t m01 = (ok(2 * c) ? 0x0000FFFFu : 0u) | (ok(2 * c + 1) ? 0xFFFF0000u : 0u);
+    const uint32_t m89 = (ok(2 * c + 8) ? 0x0000FFFFu : 0u) | (ok(2 * c + 9) ? 0xFFFF0000u : 0u);
+    pv_block<false, true>(vb, voff, bh0, bh1, bl0, bl1, m01, m89, acc);
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(VCfg<NT>::THREADS, 1) attn_verify_tma_kernel(
+    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+    const VParams P) {
+  using C = VCfg<NT>;
+  constexpr int NCT = C::NCW * 32;   // consumer threads
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar_full = sbase + C::BAR, bar_empty = bar_full + 8 * C::NST;
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + C::MISC);   // groups, abort, issued
+  int* gl = reinterpret_cast<int*>(sm + C::GL);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::NCW);
+    }
+    misc[1] = 0;
+    misc[2] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  if (warp == C::NCW) {
+    const int n = build_groups(P, gl);
+    if (lane == 0) misc[0] = n;
+    if (blockIdx.x == 0) {   // for the merge kernel
+      for (int i = lane; i <= n; i += 32) P.groups[1 + i] = gl[i];
+      if (lane == 0) P.groups[0] = n;
+    }
+  }
+  __syncthreads();
+  const int total = misc[0] * P.n_kv * P.NB;
+  const int R = verify_range(total, P.NB, P.grid);
+  const int f_lo = int(min(int64_t(total), int64_t(blockIdx.x) * R));
+  const int f_hi = min(total, f_lo + R);
+
+  if (warp == C::NCW) {
+    // ---------------- producer: one lane issues the TMA loads of every block in range
+    if (lane == 0) {
+      int i = 0;
+      bool run = true;
+      for (int f = f_lo; f < f_hi && run;) {
+        const int q = f / P.NB, j0 = f - q * P.NB, j1 = min(P.NB, j0 + (f_hi - f));
+        f += j1 - j0;
+        const VGroup gr = group_of(P, gl, q);
+        const int jl = min(j1, gr.nbq);
+        const int z = gr.s * P.n_kv + gr.hk;
+        for (int j = j0; j < jl; ++j) {
+          const int st = i % C::NST;
+          if (misc[1] != 0 ||
+              (i >= C::NST && !mbar_wait(bar_empty + 8 * st, ((i / C::NST) - 1) & 1))) {
+            misc[1] = 1;
+            run = false;
+            break;
+          }
+          const int slot = C::BK * j;
+          const uint32_t dk = sbase + st * C::STAGE, dv = dk + C::KB, fb = bar_full + 8 * st;
+          mbar_expect_tx(fb, C::STAGE);
+          tma_load_3d(dk, &tk, 0, slot, z, fb);
+          tma_load_3d(dk + C::KB / 2, &tk, 64, slot, z, fb);
+          tma_load_3d(dv, &tv, 0, slot, z, fb);
+          tma_load_3d(dv + C::KB / 2, &tv, 64, slot, z, fb);
+          ++i;
+        }
+      }
+      misc[2] = i;
+    }
+  } else {
+    // ---------------- consumers
+    const int w = warp, g = lane >> 2, c = lane & 3;
+    const int ct = threadIdx.x;
+    const int nt = w % NT, sw = w / NT;   // n-tile, first key slice
+    // ldmatrix row addresses of key slice 0 (slice s adds 16 rows = 2048 bytes); as in the
+    // per-token kernel, 128-byte swizzle: chunk ^= row % 8
+    uint32_t koff[4], voff[4];
+    {
+      const int rk = ((lane >> 3) & 1) * 8 + (lane & 7), ck = (lane >> 4) & 1;
+      const int rv = ((lane >> 4) & 1) * 8 + (lane & 7), cv = (lane >> 3) & 1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        koff[e] = uint32_t(rk * 128 + (((2 * e + ck) ^ (lane & 7)) << 4));
+        voff[e] = uint32_t(rv * 128 + (((2 * e + cv) ^ (lane & 7)) << 4));
+      }
+    }
+    float* Ow = reinterpret_cast<float*>(sm + C::OW);
+    float* MLw = reinterpret_cast<float*>(sm + C::MLW);
+    float* FWs = reinterpret_cast<float*>(sm + C::FW);
+    float* LHs = reinterpret_cast<float*>(sm + C::LH);   // [0, NCOL) sums, [NCOL, 2 NCOL) maxima
+    const int G = P.G;
+    int i = 0;
+    for (int f = f_lo; f < f_hi;) {
+      const int q = f / P.NB, j0 = f - q * P.NB, j1 = min(P.NB, j0 + (f_hi - f));
+      f += j1 - j0;
+      const VGroup gr = group_of(P, gl, q);
+      const int jl = min(j1, gr.nbq);
+      if (gr.bad && j0 == 0 && gr.hk == 0 && ct == 0) flag(gr.bad);
+      const int ncols = gr.cnt * G;
+      const bool active = 8 * nt < ncols;   // uniform over the warp
+      // last position of a column (0: a column past the group, or a token that takes no part)
+      auto col_pos = [&](int col) -> int {
+        if (col >= ncols || gr.bad == BEAM_DEV_BAD_SEQ) return 0;
+        const int p = P.pos[gr.t0 + col / G];
+        return vtoken_ok(P, p) ? p : 0;
+      };
+      const int pc0 = col_pos(8 * nt + 2 * c), pc1 = col_pos(8 * nt + 2 * c + 1);
+      // q fragments (B operand, column 8 nt + g)
+      uint32_t qb[8][2];
+      {
+        const int col = 8 * nt + g;
+        const bool rok = col < ncols;
+        const int tq = gr.t0 + (rok ? col / G : 0), hq = gr.hk * G + (rok ? col % G : 0);
+        const uint32_t* qr = reinterpret_cast<const uint32_t*>(P.q + (size_t(tq) * P.n_q + hq) * D);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qb[kk][0] = rok ? qr[8 * kk + c] : 0u;
+          qb[kk][1] = rok ? qr[8 * kk + c + 4] : 0u;
+        }
+      }
+      float acc[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+      for (int j = j0; j < jl; ++j, ++i) {
+        const int st = i % C::NST;
+        bool ok = misc[1] == 0;
+        if (ok) ok = mbar_wait(bar_full + 8 * st, (i / C::NST) & 1);
+        if (__all_sync(0xffffffffu, ok)) {
+          if (active) {
+            const uint32_t kb = sbase + st * C::STAGE;
+#pragma unroll
+            for (int s = 0; s < 4 / C::WPT; ++s) {
+              const int sl = sw + s * C::WPT;
+              warp_block_cols(kb + sl * 2048, kb + C::KB + sl * 2048, qb, koff, voff,
+                              C::BK * j + 16 * sl + 1, pc0, pc1, gr.pg, P.sl2, m, l, acc);
+            }
+          }
+        } else if (lane == 0) {
+          misc[1] = 1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+      }
+      // ---- combine the partials of the WPT warps of each n-tile
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+      }
+      consumer_bar<NCT>();   // the previous pair's readers of the combine area are done
+      {
+        float* ow = Ow + w * 8 * C::OLD;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int da = 16 * mt + g, db = da + 8;
+          ow[(2 * c) * C::OLD + da] = acc[mt][0];
+          ow[(2 * c + 1) * C::OLD + da] = acc[mt][1];
+          ow[(2 * c) * C::OLD + db] = acc[mt][2];
+          ow[(2 * c + 1) * C::OLD + db] = acc[mt][3];
+        }
+        if (g == 0) {
+          MLw[(w * 8 + 2 * c) * 2] = m[0];
+          MLw[(w * 8 + 2 * c) * 2 + 1] = l[0];
+          MLw[(w * 8 + 2 * c + 1) * 2] = m[1];
+          MLw[(w * 8 + 2 * c + 1) * 2 + 1] = l[1];
+        }
+      }
+      consumer_bar<NCT>();
+      if (ct < C::NCOL) {
+        const int ntc = ct >> 3, h8 = ct & 7;
+        float M = kNegInf;
+#pragma unroll
+        for (int jw = 0; jw < C::WPT; ++jw) M = fmaxf(M, MLw[((ntc + NT * jw) * 8 + h8) * 2]);
+        float L = 0.f;
+#pragma unroll
+        for (int jw = 0; jw < C::WPT; ++jw) {
+          const int wi = (ntc + NT * jw) * 8 + h8;
+          const float fw = M == kNegInf ? 0.f : ex2_approx(MLw[wi * 2] - M);
+          FWs[wi] = fw;
+          L += fw * MLw[wi * 2 + 1];
+        }
+        LHs[ct] = L;
+        LHs[C::NCOL + ct] = M;
+      }
+      consumer_bar<NCT>();
+      const int c_first = int((int64_t(q) * P.NB) / R);
+      const int c_last = int((int64_t(q + 1) * P.NB - 1) / R);
+      const size_t pb = c_last > c_first ? vpart_slot(q, blockIdx.x, R, P.NB) * C::NCOL : 0;
+      for (int idx = ct; idx < ncols * D; idx += NCT) {
+        const int col = idx / D, d = idx - col * D;
+        const int ntc = col >> 3, h8 = col & 7;
+        float O = 0.f;
+#pragma unroll
+        for (int jw = 0; jw < C::WPT; ++jw) {
+          const int wi = (ntc + NT * jw) * 8 + h8;
+          O += FWs[wi] * Ow[wi * C::OLD + d];
+        }
+        if (c_last == c_first) {
+          const float L = LHs[col];
+          const float o = round_bf(O * (L > 0.f ? 1.f / L : 0.f));
+          const int hq = gr.hk * G + col % G;
+          const size_t oi = (size_t(gr.t0 + col / G) * P.n_q + hq) * D + d;
+          const float gate = sigmoidf_(bf2f(P.gpre[oi]) + bf2f(P.gate_bias[hq]));
+          P.og[oi] = f2bf(o * gate);
+        } else {
+          P.part_acc[(pb + col) * D + d] = O;
+        }
+      }
+      if (c_last > c_first && ct < ncols) {
+        P.part_ml[(pb + ct) * 2] = LHs[C::NCOL + ct];
+        P.part_ml[(pb + ct) * 2 + 1] = LHs[ct];
+      }
+    }
+  }
+  __syncthreads();
+  // dependents are released only now, not at entry: launched early, the merge and the o_proj
+  // GEMV behind it (which prefetches its weights into L2 before its wait) ran beside the key
+  // stream and cost more than the launch latency they hide (measured: the 8-token
+  // verification step 2.82 -> 2.59 ms with the grouped kernel; neutral to slightly faster
+  // with the per-token one)
+  pdl_trigger();
+  if (warp == C::NCW && lane == 0) {
+    // normally a no-op: every issued block was consumed; after an expired wait, let the
+    // copies still in flight land before the CTA's shared memory is released
+    const int n = misc[2];
+    for (int k = n > C::NST ? n - C::NST : 0; k < n; ++k)
+      mbar_wait(bar_full + 8 * (k % C::NST), (k / C::NST) & 1);
+    if (misc[1]) flag(BEAM_DEV_TIMEOUT);
+  }
+}
+
+// Finish of the (group, KV head) pairs split between CTAs: merge CTA m takes the pair whose
+// first block lies in CTA m's range and that runs on past it (at most one), combines the
+// partials of CTAs c_first .. c_last for each of the group's columns, normalises, rounds,
+// gates and rounds.
+constexpr int kVMergeThreads = 256;
+template <int NT>
+__global__ void __launch_bounds__(kVMergeThreads) attn_verify_merge_kernel(const VParams P) {
+  constexpr int NCOL = NT * 8;
+  pdl_trigger();
+  __shared__ float wsh[NCOL][kVMaxParts];   // part maxima, then their weights
+  __shared__ float lsh[NCOL][kVMaxParts];   // part sums
+  __shared__ float inv[NCOL];
+  __shared__ int sl[kVMaxParts];
+  pdl_wait();
+  const int ng = P.groups[0];
+  const int total = ng * P.n_kv * P.NB;
+  const int R = verify_range(total, P.NB, P.grid);
+  const int m = blockIdx.x;
+  if (int64_t(m) * R >= total) return;
+  const int f_last = int(min(int64_t(total), int64_t(m + 1) * R) - 1);
+  const int q = f_last / P.NB;
+  const int c_first = int((int64_t(q) * P.NB) / R);
+  const int c_last = int((int64_t(q + 1) * P.NB - 1) / R);
+  if (c_first != m || c_last == m) return;
+  const int n = c_last - c_first + 1, G = P.G;
+  const int gi = q / P.n_kv, hk = q - gi * P.n_kv;
+  const int t0 = P.groups[1 + gi], ncols = (P.groups[2 + gi] - t0) * G;
+  for (int s = threadIdx.x; s < n; s += kVMergeThreads) sl[s] = int(vpart_slot(q, m + s, R, P.NB) * NCOL);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n * ncols; i += kVMergeThreads) {
+    const int s = i / ncols, h = i - s * ncols;
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(P.part_ml + (sl[s] + h) * 2));
+    wsh[h][s] = v.x;
+    lsh[h][s] = v.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < ncols) {
+    const int h = threadIdx.x;
+    float M = kNegInf;
+    for (int s = 0; s < n; ++s) M = fmaxf(M, wsh[h][s]);
+    float L = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const float fw = M == kNegInf ? 0.f : ex2_approx(wsh[h][s] - M);
+      wsh[h][s] = fw;
+      L += fw * lsh[h][s];
+    }
+    inv[h] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  // one thread per 4 consecutive outputs of a column
+  for (int o4 = threadIdx.x; o4 < ncols * (D / 4); o4 += kVMergeThreads) {
+    const int h = o4 / (D / 4), d = 4 * (o4 - h * (D / 4));
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n; ++s) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(P.part_acc + size_t(sl[s] + h) * D + d));
+      const float fw = wsh[h][s];
+      O.x += fw * v.x;
+      O.y += fw * v.y;
+      O.z += fw * v.z;
+      O.w += fw * v.w;
+    }
+    const int hq = hk * G + h % G;
+    const size_t oi = (size_t(t0 + h / G) * P.n_q + hq) * D + d;
+    const float gb = bf2f(P.gate_bias[hq]);
+    const uint2 gv = *reinterpret_cast<const uint2*>(P.gpre + oi);
+    const float o0 = round_bf(O.x * inv[h]), o1 = round_bf(O.y * inv[h]);
+    const float o2 = round_bf(O.z * inv[h]), o3 = round_bf(O.w * inv[h]);
+    const uint32_t r0 = pack_bf16x2(o0 * sigmoidf_(bf_lo(gv.x) + gb), o1 * sigmoidf_(bf_hi(gv.x) + gb));
+    const uint32_t r1 = pack_bf16x2(o2 * sigmoidf_(bf_lo(gv.y) + gb), o3 * sigmoidf_(bf_hi(gv.y) + gb));
+    *reinterpret_cast<uint2*>(P.og + oi) = make_uint2(r0, r1);
+  }
+}
+
 struct Plan {
   int NB, R, grid, total;
 };
@@ -701,6 +1206,97 @@ cudaError_t decode(const uint16_t* q, const uint16_t* g, const uint16_t* gate_bi
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
+}
+
+
+namespace {
+
+// n-tile counts compiled for the grouped form; a group's G * TG columns take the next one up
+constexpr int kVerifyNT[] = {2, 3, 4, 6, 12};
+constexpr int kVerifyMaxNT = 12;
+
+int verify_tg(int G, int max_q_per_seq) {
+  const int cap = kVerifyMaxNT * 8 / G;
+  return max_q_per_seq < cap ? max_q_per_seq : cap;
+}
+int verify_nt(int G, int TG) {
+  const int need = (G * TG + 7) / 8;
+  for (int nt : kVerifyNT)
+    if (nt >= need) return nt;
+  return 0;
+}
+size_t verify_ws_for(int T, int nt) {
+  const size_t parts = size_t(num_sms_cached()) * 2 * nt * 8;
+  return align_up(parts * D * 4, 256) + align_up(parts * 2 * 4, 256) +
+         align_up(size_t(T + 2) * 4, 256);
+}
+
+bool encode_kv_maps(const beam_kv_cache& kc, int n_kv, bool fp8, CUtensorMap* mk, CUtensorMap* mv) {
+  const int rowb = fp8 ? D : 2 * D;
+  const uint64_t dims[3] = {uint64_t(D), uint64_t(kc.capacity), uint64_t(kc.num_seqs) * n_kv};
+  const uint64_t str[2] = {uint64_t(rowb), uint64_t(kc.capacity) * rowb};
+  const uint32_t box[3] = {uint32_t(fp8 ? 128 : 64), uint32_t(fp8 ? Cfg<true>::BK : Cfg<false>::BK), 1};
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode_tiled(mk, dt, 3, kc.k, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_tiled(mv, dt, 3, kc.v, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int NT>
+cudaError_t launch_verify(const CUtensorMap& mk, const CUtensorMap& mv, const VParams& prm,
+                          cudaStream_t st) {
+  auto kern = attn_verify_tma_kernel<NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, VCfg<NT>::BYTES);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(prm.grid), dim3(VCfg<NT>::THREADS), VCfg<NT>::BYTES, st, mk, mv, prm);
+  if (e != cudaSuccess) return e;
+  // whether a pair is split between CTAs is known only on the device (the group count)
+  return launch_pdl(attn_verify_merge_kernel<NT>, dim3(prm.grid), dim3(kVMergeThreads), 0, st, prm);
+}
+
+}  // namespace
+
+bool verify_supported(int D_, int G, int window, bool fp8, const void* k, const void* v,
+                      int max_keys, int T, int max_q_per_seq) {
+  if (D_ != D || G < 1 || G > kHeads || window != 0 || fp8 || max_keys < kMinKeys) return false;
+  if (T < 1 || T > kVerifyMaxT || max_q_per_seq < 2) return false;
+  return aligned16(k) && aligned16(v) && tensor_map_encoder_ready();
+}
+
+size_t verify_ws_bytes(int T, int G, int max_q_per_seq) {
+  if (T <= 0 || G < 1 || G > kHeads) return 0;
+  return verify_ws_for(T, verify_nt(G, verify_tg(G, max_q_per_seq)));
+}
+
+size_t verify_ws_bytes_max(int T) {
+  return T > 0 && T <= kVerifyMaxT ? verify_ws_for(T, kVerifyMaxNT) : 0;
+}
+
+cudaError_t verify(const uint16_t* q, const uint16_t* g, const uint16_t* gate_bias,
+                   const int32_t* seq_id, const int32_t* pos, int T, int max_pos,
+                   int max_q_per_seq, int n_q, int n_kv, const beam_kv_cache& kc, float sl2,
+                   uint16_t* og, void* ws, size_t ws_len, cudaStream_t st) {
+  const int G = n_q / n_kv;
+  const int TG = verify_tg(G, max_q_per_seq), nt = verify_nt(G, TG);
+  if (nt == 0 || ws_len < verify_ws_for(T, nt)) return cudaErrorInvalidValue;
+  const int grid = num_sms_cached();
+  const size_t parts = size_t(grid) * 2 * nt * 8;
+  char* w = static_cast<char*>(ws);
+  float* part_acc = reinterpret_cast<float*>(w);
+  float* part_ml = reinterpret_cast<float*>(w + align_up(parts * D * 4, 256));
+  int* groups = reinterpret_cast<int*>(w + align_up(parts * D * 4, 256) + align_up(parts * 2 * 4, 256));
+  CUtensorMap mk, mv;
+  if (!encode_kv_maps(kc, n_kv, false, &mk, &mv)) return cudaErrorInvalidValue;
+  const int NB = (max_pos + VCfg<2>::BK - 1) / VCfg<2>::BK;
+  const VParams prm{q,  seq_id, pos, g,    gate_bias,   og,          part_acc, part_ml, groups,
+                    T,  TG,     n_q, n_kv, G,           kc.num_seqs, kc.capacity, NB,   grid,
+                    sl2};
+  switch (nt) {
+    case 2: return launch_verify<2>(mk, mv, prm, st);
+    case 3: return launch_verify<3>(mk, mv, prm, st);
+    case 4: return launch_verify<4>(mk, mv, prm, st);
+    case 6: return launch_verify<6>(mk, mv, prm, st);
+    default: return launch_verify<12>(mk, mv, prm, st);
+  }
 }
 
 }  // namespace adec

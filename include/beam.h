@@ -149,10 +149,13 @@ beam_status beam_qkv_gate(const beam_layer_cfg* cfg, const beam_bf16* u,
  *  max_q_per_seq  host-side upper bound of the number of the call's tokens that belong to one
  *            sequence (1 for a decode batch). Up to 4 -- and up to 16 (the verification
  *            batches of speculative decoding) while the call holds fewer than two
- *            (sequence, KV head) pairs per SM -- every token runs split-K over its keys;
- *            otherwise tokens are taken in tiles of consecutive tokens that share K/V tiles,
- *            which expects the tokens of a sequence to be consecutive in the call (any order
- *            is still computed correctly, only more slowly).
+ *            (sequence, KV head) pairs per SM -- the keys are split across SMs: per token,
+ *            or, for a bound of 2 or more over a full-attention BF16 cache (head_dim 128, at
+ *            least 2048 keys, T <= 1024), per group of up to max_q_per_seq consecutive tokens
+ *            of one sequence that read each K/V block once; otherwise tokens are taken in
+ *            tiles of consecutive tokens that share K/V tiles. Both sharing forms expect the
+ *            tokens of a sequence to be consecutive in the call (any order is still computed
+ *            correctly, only more slowly).
  *  w_o       (device) [H][n_q*D] bf16.   out (device) [T][H] bf16. */
 beam_status beam_attn(const beam_layer_cfg* cfg, const beam_bf16* q, const beam_bf16* g,
                       const beam_bf16* gate_bias, const beam_kv_cache* cache,

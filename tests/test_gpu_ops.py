@@ -194,14 +194,17 @@ def test_attn(case, kind, fp8, form):
 
 @pytest.mark.parametrize("q_len", [2, 4, 7, 8])
 @pytest.mark.parametrize("kind", ["nope", "swa_ring128"])
-@pytest.mark.parametrize("form", ["decode", "prefill"])
+@pytest.mark.parametrize("form", ["decode", "grouped", "prefill"])
 def test_attn_verify_batches(q_len, kind, form):
     """Multi-token verification batches of speculative decoding at full width: q_len new tokens
-    per sequence (2 sequences) after 100,000 cached ones, through both forms of beam_attn --
-    split-K decode (which a bound of 1 always takes, and a true bound up to 16 takes for so
-    few sequences) and the query-tile prefill kernel (a bound above 16) -- whatever q_len is."""
+    per sequence (2 sequences) after 100,000 cached ones, through every form of beam_attn --
+    split-K decode per token (which a bound of 1 always takes), the grouped form in which a
+    sequence's tokens share each K/V block (the true bound, full attention over a BF16 cache)
+    and the query-tile prefill kernel (a bound above 16) -- whatever q_len is."""
     shape = BEAM
     nope = kind == "nope"
+    if form == "grouped" and not nope:
+        pytest.skip("a 512-key window takes the per-token decode kernels whatever the bound")
     ctxs = [100_000, 99_123]
     S = len(ctxs)
     T = S * q_len
@@ -220,13 +223,90 @@ def test_attn_verify_batches(q_len, kind, form):
     pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
     cfg = cfg_of(shape, nope)
     out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
-    mq = 1 if form == "decode" else 17   # a bound above 16 always takes the query tiles
+    # a bound above 16 always takes the query tiles
+    mq = {"decode": 1, "grouped": q_len, "prefill": 17}[form]
     B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
                 ws_for(cfg, T, max_pos), max_q_per_seq=mq)
     check_status()
     ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
                       positions, np64(W["w_o"]))
     assert_close(np64(out), ref, "attn out")
+
+
+# The grouped verification form over layouts a serving batch can take: runs of different
+# lengths (one of a single token), a sequence's tokens interleaved with other sequences' (they
+# still share blocks only where consecutive), many short groups at 8K context (pairs whole in
+# one CTA and pairs split between CTAs), 16 tokens of one sequence (96 query columns, the
+# widest group) and runs longer than the bound (split into groups of the bound). Every slot past
+# a sequence's last position holds NaN, so keys a column must not see cannot leak.
+GROUPED_CASES = {
+    # name: (tokens as (sequence, position) in call order, contexts per sequence, bound)
+    "runs": ([(0, 3001 + i) for i in range(5)] + [(1, 2501)] + [(2, 4101 + i) for i in range(9)],
+             [3000, 2500, 4100], 9),
+    "interleaved": ([(0, 2201), (1, 3301), (0, 2202), (1, 3302), (2, 2801), (0, 2203), (2, 2802)],
+                    [2200, 3300, 2800], 3),
+    "many": ([(s, 2100 + 397 * s + 1 + i) for s in range(16) for i in range(2)],
+             [2100 + 397 * s for s in range(16)], 2),
+    "q16": ([(0, 100_001 + i) for i in range(16)], [100_000], 16),
+    "split_runs": ([(s, 5000 + 77 * s + 1 + i) for s in range(2) for i in range(8)],
+                   [5000, 5077], 4),
+}
+
+
+@pytest.mark.parametrize("name", list(GROUPED_CASES))
+def test_attn_grouped_layouts(name):
+    shape = BEAM
+    tokens, ctxs, mq = GROUPED_CASES[name]
+    seqs = [s for s, _ in tokens]
+    positions = [p for _, p in tokens]
+    S, T = len(ctxs), len(tokens)
+    max_pos = max(positions)
+    cap = max_pos + 7
+    seed = 900 + T
+    c = synth.kv_cache(shape, S, cap, seed, device=DEV)
+    for s in range(S):
+        last = max(p for t, p in tokens if t == s)
+        c["k"][s, :, last:] = float("nan")
+        c["v"][s, :, last:] = float("nan")
+    kc = B.KVCache(c["k"], c["v"], 0)
+    q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, seed, ("q",), DEV)
+    g = synth.activations(T, shape.q_rows, seed, "g", DEV)
+    W = synth.attention_weights(shape, 0, seed, device=DEV)
+    seq = torch.tensor(seqs, dtype=torch.int32, device=DEV)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    cfg = cfg_of(shape, nope=True)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, seq, pos, max_pos, W["w_o"], out,
+                ws_for(cfg, T, max_pos), max_q_per_seq=mq)
+    check_status()
+    ref = O.attention(shape, np64(q), np64(g), np64(W["gate_bias"]), oracle_cache(kc), seqs,
+                      positions, np64(W["w_o"]))
+    assert_close(np64(out), ref, f"attn out ({name})")
+
+
+def test_grouped_form_flags_positions_past_max_pos():
+    """A group whose last token lies past the host's max_pos: that token is flagged and its row
+    left at zero; its group's other tokens are exact."""
+    shape = BEAM
+    cfg = cfg_of(shape, nope=True)
+    cap, max_pos = 5000, 3000
+    c = synth.kv_cache(shape, 1, cap, 5, device=DEV)
+    kc = B.KVCache(c["k"], c["v"], 0)
+    seqs, positions = [0, 0, 0], [2500, 2501, 4000]
+    T = len(seqs)
+    q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, 5, ("q",), DEV)
+    g = synth.activations(T, shape.q_rows, 5, "g", DEV)
+    W = synth.attention_weights(shape, 0, 5, device=DEV)
+    out = torch.empty((T, shape.hidden), dtype=torch.bfloat16, device=DEV)
+    B.beam_get_device_status()
+    B.beam_attn(cfg, q, g, W["gate_bias"], kc, torch.tensor(seqs, dtype=torch.int32, device=DEV),
+                torch.tensor(positions, dtype=torch.int32, device=DEV), max_pos, W["w_o"], out,
+                ws_for(cfg, T, max_pos), max_q_per_seq=3)
+    assert B.beam_get_device_status() & B.DEV_BAD_POSITION
+    ref = O.attention(shape, np64(q[:2]), np64(g[:2]), np64(W["gate_bias"]), oracle_cache(kc),
+                      seqs[:2], positions[:2], np64(W["w_o"]))
+    assert_close(np64(out[:2]), ref, "attn out, valid tokens")
+    assert not out[2].float().abs().max().item()
 
 
 # A sliding window longer than 2048 keys takes the long-context decode kernel when the ring's
