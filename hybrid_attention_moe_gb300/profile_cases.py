@@ -13,7 +13,9 @@ qkv_decode, oproj_decode (via beam_attn on a 512-key window), attn_nope_decode (
 route_decode, norm_decode, gemm_prefill (2048 x 14336 x 5120 tensor-core GEMM),
 moe_prefill (grouped tensor-core GEMMs, 2048 tokens over 32 experts), attn_nope_prefill
 (tensor-core attention: one sequence, 2048 new tokens after --ctx cached keys, NoPE, BF16 KV),
-attn_swa_prefill (the same over a 512-key sliding window, 8 sequences).
+attn_swa_prefill (the same over a 512-key sliding window, 8 sequences), attn_nope_verify
+(--tokens new tokens of one sequence after --ctx cached keys, NoPE, BF16 KV, bound = tokens:
+the grouped decode form of a verification batch).
 """
 from __future__ import annotations
 
@@ -141,6 +143,19 @@ def main():
         ws = torch.empty(B.workspace_bytes(cf, T, ctx + chunk), dtype=torch.uint8, device=dev)
         fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + chunk, W["w_o"],  # noqa: E731
                                  out, ws, max_q_per_seq=chunk)
+    elif c == "attn_nope_verify":
+        ctx, T = args.ctx, args.tokens
+        cf = B.LayerCfg.from_shape(shape, B.BEAM_ATTN_NOPE_SSMAX)
+        W = synth.attention_weights(shape, 5, 0, device=dev)
+        kv = synth.kv_cache(shape, 1, ctx + T + 8, 0, device=dev)
+        kc = B.KVCache(kv["k"], kv["v"], 0)
+        q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, 0, ("q",), dev)
+        gg = synth.activations(T, shape.q_rows, 0, "g", dev)
+        seq, pos = synth.prefill_positions([ctx], T, dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(B.workspace_bytes(cf, T, ctx + T), dtype=torch.uint8, device=dev)
+        fn = lambda: B.beam_attn(cf, q, gg, W["gate_bias"], kc, seq, pos, ctx + T, W["w_o"], out,  # noqa: E731
+                                 ws, max_q_per_seq=T)
     elif c == "route_decode":
         R = synth.router_weights(shape, 3, 0, device=dev)
         u = synth.activations(1, H, 0, "u", dev)
