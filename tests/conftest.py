@@ -55,6 +55,13 @@ def pytest_terminal_summary(terminalreporter):
         w(f"parity: {len(outside)} outside them, {len(chained)} of these chained outputs held "
           f"to the widened bar (oracle self-divergence x3); largest mean-rel {worst[3]:.2e} "
           f"({worst[1]}, {worst[0].split('::')[-1]})")
+        by_test = {}
+        for r in outside:
+            by_test.setdefault(r[0].split("::")[-1], []).append(r)
+        for name, rs in sorted(by_test.items()):
+            wr = max(rs, key=lambda r: r[3] / r[5])
+            w(f"parity:   outside in {name}: {len(rs)} outputs, largest mean-rel {wr[3]:.2e} "
+              f"max-abs-rel {wr[2]:.2e} ({wr[1]}, {wr[6]})")
     closest = sorted(within, key=lambda r: -max(r[2] / r[4], r[3] / r[5]))[:3]
     for r in closest:
         w(f"parity: closest within: {r[1]} max-abs-rel {r[2]:.2e} mean-rel {r[3]:.2e} "

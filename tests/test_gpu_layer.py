@@ -16,7 +16,8 @@ import synth
 from synth import BEAM
 from hybrid_attention_moe_gb300 import beam as B
 from hybrid_attention_moe_gb300.stack import BeamStack
-from parity import assert_chained_close, np64, oracle_cache, routing_stable
+from parity import (assert_chained_close, assert_close, assert_logits_close, np64, oracle_cache,
+                    routing_stable)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -173,6 +174,38 @@ def _layer_case(shape, layer, contexts, fp8=False, scale=(1.0, 1.0), seed=0, nvf
     got = {"L0.q": np64(gtr[0]["q"]), "L0.attn": np64(gtr[0]["attn"]),
            "L0.mlp": np64(gtr[0]["mlp"]), "h": np64(out)}
     assert_chained_close(got, ref, floors, fp8)
+
+    # every step again on the GPU's own inputs, at the stated bars: the attention (+ gate and
+    # o_proj) on the GPU's q and g over the cache holding the GPU's K/V of the new tokens, the
+    # boundary norm on the GPU's attention output, the router and the experts on the GPU's u
+    t = gtr[0]
+    for s_, p_ in zip(seqs, positions):
+        sl = oc0.slot(p_)
+        if fp8:
+            oc0.k[s_][:, sl] = kc.k[s_, :, sl].cpu().numpy()
+            oc0.v[s_][:, sl] = kc.v[s_, :, sl].cpu().numpy()
+        else:
+            oc0.k[s_][:, sl] = kc.k[s_, :, sl].float().cpu().numpy()
+            oc0.v[s_][:, sl] = kc.v[s_, :, sl].float().cpu().numpy()
+    a_o = O.attention(shape, np64(t["q"]), np64(t["g"]), Wo["gate_bias"], oc0, seqs, positions,
+                      Wo["w_o"])
+    assert_close(np64(t["attn"]), a_o, "L0.attn (step)", fp8)
+    hm_o, um_o = O.boundary_norm(np64(t["attn"]), ho, Wo["attn_post"], Wo["mlp_pre"],
+                                 2 * layer + 2, shape.eps)
+    assert_close(np64(t["h_mid"]), hm_o, "L0.h_mid (step)")
+    assert_close(np64(t["mlp_in"]), um_o, "L0.mlp_in (step)")
+    u_g = np64(t["mlp_in"])
+    lg_g, idx_g, w_g = (x.cpu().numpy() for x in t["route"])
+    lg_o, idx_o, _ = O.route(shape, u_g, R["router"], R["corr_bias"])
+    assert_logits_close(lg_g.astype(np.float64), lg_o)
+    assert np.array_equal(np.sort(idx_g, 1), np.sort(idx_o, 1)), "step: routing differs"
+    if nvfp4:
+        m_o = O.moe_nvfp4(shape, u_g, idx_g, w_g.astype(np.float64), Wo["nvfp4_experts"])
+    elif fp8_experts:
+        m_o = O.moe_fp8(shape, u_g, idx_g, w_g.astype(np.float64), Wo["fp8_experts"])
+    else:
+        m_o = O.moe(shape, u_g, idx_g, w_g.astype(np.float64), Wo["w_gate_up"], Wo["w_down"])
+    assert_close(np64(t["mlp"]), m_o, "L0.mlp (step)")
 
 
 def test_full_width_swa_moe_layer_decode_ctx4096():
