@@ -56,6 +56,7 @@ struct Job {
 
 // Shared memory (offsets from a 1024-aligned base). A 64-column half of a 128-row bf16 tile is
 // 128 rows x 128 B = 16 KB (128-byte swizzle atoms of 8 rows).
+
 template <int D>
 struct Smem {
   static constexpr int NH = D / 64;
@@ -404,36 +405,30 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
     // path is kept short: descriptors are stepped in their low word (the address field) only.
     const uint32_t dq0_hi = uint32_t(dq0 >> 32), dk0_hi = uint32_t(dk0 >> 32);
     auto qk = [&](int u, int ks) {
-      if (lane == 0) {
-        const uint32_t qlo = uint32_t(dq0) + uint32_t((u * S::NH * S::HALF) >> 4);
-        const uint32_t klo = uint32_t(dk0) + uint32_t((ks * S::TILE) >> 4);
+      const uint32_t qlo = uint32_t(dq0) + uint32_t((u * S::NH * S::HALF) >> 4);
+      const uint32_t klo = uint32_t(dk0) + uint32_t((ks * S::TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk & 3) * 32) >> 4;
-          umma_ss_w(tmem + 128 * u, qlo + ((kk >> 2) * S::HALF >> 4) + off, dq0_hi,
-                    klo + ((kk >> 2) * KT * 128 >> 4) + off, dk0_hi, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full + 8 * u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk & 3) * 32) >> 4;
+        umma_ss_e(tmem + 128 * u, qlo + ((kk >> 2) * S::HALF >> 4) + off, dq0_hi,
+                  klo + ((kk >> 2) * KT * 128 >> 4) + off, dk0_hi, IDESC_QK, kk > 0 ? 1u : 0u);
       }
-      __syncwarp();
+      umma_commit_e(s_full + 8 * u);
     };
     const uint32_t dv0_hi = uint32_t(dv0 >> 32);
     auto pv = [&](int u, int vs, bool first) {
-      if (lane == 0) {
-        const uint32_t blo = uint32_t(dv0) + uint32_t((vs * S::TILE) >> 4);
-        const uint32_t ts = tmem + 128 * u, to = tmem + 256 + 128 * u;
-        umma_ts_w(to, ts, blo, dv0_hi, IDESC_PV, first ? 0u : 1u);
-        umma_ts_w(to, ts + 16, blo, dv0_hi, IDESC_PV, 1u);
+      const uint32_t blo = uint32_t(dv0) + uint32_t((vs * S::TILE) >> 4);
+      const uint32_t ts = tmem + 128 * u, to = tmem + 256 + 128 * u;
+      umma_ts_e(to, ts, blo, dv0_hi, IDESC_PV, first ? 0u : 1u);
+      umma_ts_e(to, ts + 16, blo, dv0_hi, IDESC_PV, 1u);
 #pragma unroll
-        for (int kk = 1; kk < KT / 16; ++kk) {
-          const uint32_t b = blo + uint32_t((kk * 16 * 128) >> 4);
-          const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
-          umma_ts_acc(to, a_hi, b, dv0_hi, IDESC_PV);
-          umma_ts_acc(to, a_hi + 16, b, dv0_hi, IDESC_PV);
-        }
-        umma_commit(s_free + 8 * u);
+      for (int kk = 1; kk < KT / 16; ++kk) {
+        const uint32_t b = blo + uint32_t((kk * 16 * 128) >> 4);
+        const uint32_t a_hi = ts + 32 * (kk >> 1) + 8 * (kk & 1);
+        umma_ts_e(to, a_hi, b, dv0_hi, IDESC_PV, 1u);
+        umma_ts_e(to, a_hi + 16, b, dv0_hi, IDESC_PV, 1u);
       }
-      __syncwarp();
+      umma_commit_e(s_free + 8 * u);
     };
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item) {
       const int hk = w / njobs;
@@ -446,12 +441,9 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         const uint32_t oph = (ostart & 1) ^ 1;
         if (!all(mbar_wait(o_empty, oph) && mbar_wait(o_empty + 8, oph))) { ok = false; break; }
         ++ostart;
-        if (lane == 0) {
-          umma_commit(q_empty);
-          umma_commit(o_full);
-          umma_commit(o_full + 8);
-        }
-        __syncwarp();
+        umma_commit_e(q_empty);
+        umma_commit_e(o_full);
+        umma_commit_e(o_full + 8);
         continue;
       }
       int ks = int(kc % KSTAGES);
@@ -459,11 +451,8 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
       tc_fence_after();
       qk(0, ks);
       qk(1, ks);
-      if (lane == 0) {
-        umma_commit(k_empty + 8 * ks);
-        if (wk.n == 1) umma_commit(q_empty);
-      }
-      __syncwarp();
+      umma_commit_e(k_empty + 8 * ks);
+      if (wk.n == 1) umma_commit_e(q_empty);
       ++kc;
       uint32_t gt_i = 0;   // key tiles of this item done
       for (int i = 0; i < wk.n; ++i) {
@@ -505,8 +494,7 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         }
         tc_fence_after();
         pv(0, vs, fresh);
-        if (lane == 0 && !more) umma_commit(o_full);
-        __syncwarp();
+        if (!more) umma_commit_e(o_full);
         const bool r_pb = mbar_test(p_full + 8, (pt + gt_i) & 1);   // answered while QK_A issues
         if (more) qk(0, ks);
         // ---- query tile B
@@ -516,19 +504,13 @@ __global__ void __maxnreg__(96) attn_prefill_tc_kernel(
         if (fresh) ++ostart;
         tc_fence_after();
         pv(1, vs, fresh);
-        if (lane == 0) {
-          umma_commit(v_empty + 8 * vs);
-          if (!more) umma_commit(o_full + 8);
-        }
-        __syncwarp();
+        umma_commit_e(v_empty + 8 * vs);
+        if (!more) umma_commit_e(o_full + 8);
         ++vc;
         if (more) {
           qk(1, ks);
-          if (lane == 0) {
-            umma_commit(k_empty + 8 * ks);
-            if (i + 1 == wk.n - 1) umma_commit(q_empty);
-          }
-          __syncwarp();
+          umma_commit_e(k_empty + 8 * ks);
+          if (i + 1 == wk.n - 1) umma_commit_e(q_empty);
           ++kc;
         }
         ++gt_i;

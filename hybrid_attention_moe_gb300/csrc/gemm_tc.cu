@@ -253,7 +253,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
+      // the whole warp runs the issue loop on warp-uniform values and elect.sync picks the
+      // lane that issues each MMA and commit (lane 0: the warp stays converged)
       // descriptor of the ring's first byte: A and B tiles of every stage differ from it only
       // in the start address field (shared-memory offsets >> 4 stay below 2^14)
       const uint64_t d0 = smem_desc(s_base);
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++i) {
         const int ab = i & 1;
         // the epilogue has drained this accumulator (tile i - 2)
-        if (!mbar_wait(acce0 + 8 * ab, ((i >> 1) & 1) ^ 1)) {
-          *abort_flag = 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(acce0 + 8 * ab, ((i >> 1) & 1) ^ 1))) {
+          if (lane == 0) *abort_flag = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -275,29 +277,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(full0 + 8 * s, ph)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, ph))) {
             ok = false;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t alo = d_lo0 + uint32_t((s * STAGE_BYTES) >> 4);
           const uint32_t blo = alo + uint32_t(A_BYTES >> 4);
-          umma_ss_w(acc, alo, d_hi, blo, d_hi, kIdesc, kb != 0 ? 1u : 0u);
+          umma_ss_e(acc, alo, d_hi, blo, d_hi, kIdesc, kb != 0 ? 1u : 0u);
 #pragma unroll
           for (int k = 1; k < BK / 16; ++k)
-            umma_ss_w(acc, alo + uint32_t((32 * k) >> 4), d_hi, blo + uint32_t((32 * k) >> 4), d_hi,
+            umma_ss_e(acc, alo + uint32_t((32 * k) >> 4), d_hi, blo + uint32_t((32 * k) >> 4), d_hi,
                       kIdesc, 1u);
-          umma_commit(empty0 + 8 * s);
+          umma_commit_e(empty0 + 8 * s);
         }
-        umma_commit(accf0 + 8 * ab);   // arrives once every MMA issued above has completed
+        umma_commit_e(accf0 + 8 * ab);   // arrives once every MMA issued above has completed
         if (!ok) {
-          *abort_flag = 1;
+          if (lane == 0) *abort_flag = 1;
           break;
         }
       }
       // every MMA of this CTA has completed before TMEM is released (after an early exit the
       // epilogue may not have waited for them)
-      umma_commit(mma_done);
+      umma_commit_e(mma_done);
       mbar_wait(mma_done, 0);
     }
   } else {
