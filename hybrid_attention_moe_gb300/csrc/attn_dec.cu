@@ -820,6 +820,102 @@ __device__ __forceinline__ void warp_block_cols(uint32_t kb, uint32_t vb,
   }
 }
 
+// Two 16-key slices of a staged block for the same 8 columns (kb0/vb0: the first slice, kbase0
+// its first position; kb1/vb1/kbase1 the second): both S tiles first, one max and rescale over
+// the 32 keys, then both P.V products. The same arithmetic as two warp_block_cols calls up to
+// the point at which the running max is updated; the two slices' MMA chains interleave.
+__device__ __forceinline__ void warp_block_cols2(uint32_t kb0, uint32_t vb0, uint32_t kb1,
+                                                 uint32_t vb1, const uint32_t (&qb)[8][2],
+                                                 const uint32_t (&koff)[4],
+                                                 const uint32_t (&voff)[4], int kbase0, int kbase1,
+                                                 int pc0, int pc1, int pg, float sl2,
+                                                 float (&m)[2], float (&l)[2], float (&acc)[8][4]) {
+  using C = Cfg<false>;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  float s0a[4] = {0.f, 0.f, 0.f, 0.f}, s0b[4] = {0.f, 0.f, 0.f, 0.f};
+  float s1a[4] = {0.f, 0.f, 0.f, 0.f}, s1b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < 8; kk += 2) {
+    uint32_t a0[4], b0[4], a1[4], b1[4];
+    const uint32_t o0 = (kk >> 2) * (C::KB / 2) + koff[kk & 3];
+    const uint32_t o1 = ((kk + 1) >> 2) * (C::KB / 2) + koff[(kk + 1) & 3];
+    ldsm_x4(kb0 + o0, a0[0], a0[1], a0[2], a0[3]);
+    ldsm_x4(kb1 + o0, a1[0], a1[1], a1[2], a1[3]);
+    ldsm_x4(kb0 + o1, b0[0], b0[1], b0[2], b0[3]);
+    ldsm_x4(kb1 + o1, b1[0], b1[1], b1[2], b1[3]);
+    mma_bf16(s0a, a0, qb[kk][0], qb[kk][1]);
+    mma_bf16(s1a, a1, qb[kk][0], qb[kk][1]);
+    mma_bf16(s0b, b0, qb[kk + 1][0], qb[kk + 1][1]);
+    mma_bf16(s1b, b1, qb[kk + 1][0], qb[kk + 1][1]);
+  }
+  const int k0 = kbase0 + g, k1 = kbase1 + g;
+  float x[8];
+  x[0] = k0 <= pc0 ? (s0a[0] + s0b[0]) * sl2 : kNegInf;
+  x[1] = k0 <= pc1 ? (s0a[1] + s0b[1]) * sl2 : kNegInf;
+  x[2] = k0 + 8 <= pc0 ? (s0a[2] + s0b[2]) * sl2 : kNegInf;
+  x[3] = k0 + 8 <= pc1 ? (s0a[3] + s0b[3]) * sl2 : kNegInf;
+  x[4] = k1 <= pc0 ? (s1a[0] + s1b[0]) * sl2 : kNegInf;
+  x[5] = k1 <= pc1 ? (s1a[1] + s1b[1]) * sl2 : kNegInf;
+  x[6] = k1 + 8 <= pc0 ? (s1a[2] + s1b[2]) * sl2 : kNegInf;
+  x[7] = k1 + 8 <= pc1 ? (s1a[3] + s1b[3]) * sl2 : kNegInf;
+  float mh[2] = {fmaxf(fmaxf(x[0], x[2]), fmaxf(x[4], x[6])),
+                 fmaxf(fmaxf(x[1], x[3]), fmaxf(x[5], x[7]))};
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mh[0] = fmaxf(mh[0], __shfl_xor_sync(0xffffffffu, mh[0], o));
+    mh[1] = fmaxf(mh[1], __shfl_xor_sync(0xffffffffu, mh[1], o));
+  }
+  if (__any_sync(0xffffffffu, mh[0] > m[0] + kRescale || mh[1] > m[1] + kRescale)) {
+    float cr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float mn = fmaxf(m[h], mh[h]);
+      cr[h] = m[h] == kNegInf ? 0.f : ex2_approx(m[h] - mn);
+      m[h] = mn;
+      l[h] *= cr[h];
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acc[mt][0] *= cr[0];
+      acc[mt][1] *= cr[1];
+      acc[mt][2] *= cr[0];
+      acc[mt][3] *= cr[1];
+    }
+  }
+  const float ms0 = m[0] == kNegInf ? 0.f : m[0], ms1 = m[1] == kNegInf ? 0.f : m[1];
+  float p[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) p[e] = ex2_approx(x[e] - ((e & 1) ? ms1 : ms0));
+  l[0] += (p[0] + p[2]) + (p[4] + p[6]);
+  l[1] += (p[1] + p[3]) + (p[5] + p[7]);
+  uint32_t bh[4], bl[4];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const uint32_t h01 = pack_bf16x2(p[4 * s], p[4 * s + 1]);
+    const uint32_t h23 = pack_bf16x2(p[4 * s + 2], p[4 * s + 3]);
+    const uint32_t l01 = pack_bf16x2(p[4 * s] - bf_lo(h01), p[4 * s + 1] - bf_hi(h01));
+    const uint32_t l23 = pack_bf16x2(p[4 * s + 2] - bf_lo(h23), p[4 * s + 3] - bf_hi(h23));
+    bh[2 * s] = movtrans(h01);
+    bh[2 * s + 1] = movtrans(h23);
+    bl[2 * s] = movtrans(l01);
+    bl[2 * s + 1] = movtrans(l23);
+  }
+  auto pv = [&](uint32_t vb, int kbase, int s) {
+    if (kbase + 15 <= pg) {
+      pv_block<false, false>(vb, voff, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1], 0u,
+                             0u, acc);
+    } else {
+      auto ok = [&](int k) { return kbase + k <= pg; };
+      const uint32_t m01 = (ok(2 * c) ? 0x0000FFFFu : 0u) | (ok(2 * c + 1) ? 0xFFFF0000u : 0u);
+      const uint32_t m89 = (ok(2 * c + 8) ? 0x0000FFFFu : 0u) | (ok(2 * c + 9) ? 0xFFFF0000u : 0u);
+      pv_block<false, true>(vb, voff, bh[2 * s], bh[2 * s + 1], bl[2 * s], bl[2 * s + 1], m01,
+                            m89, acc);
+    }
+  };
+  pv(vb0, kbase0, 0);
+  pv(vb1, kbase1, 1);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(VCfg<NT>::THREADS, 1) attn_verify_tma_kernel(
     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -951,11 +1047,21 @@ __global__ void __launch_bounds__(VCfg<NT>::THREADS, 1) attn_verify_tma_kernel(
         if (__all_sync(0xffffffffu, ok)) {
           if (active) {
             const uint32_t kb = sbase + st * C::STAGE;
+            if constexpr (C::WPT == 2) {
+              // this warp's two slices together (their MMA chains interleave)
+              const int s0 = sw, s1 = sw + 2;
+              warp_block_cols2(kb + s0 * 2048, kb + C::KB + s0 * 2048, kb + s1 * 2048,
+                               kb + C::KB + s1 * 2048, qb, koff, voff, C::BK * j + 16 * s0 + 1,
+                               C::BK * j + 16 * s1 + 1, pc0, pc1, gr.pg, P.sl2, m, l, acc);
+            } else {
+              // one slice (WPT 4), or four one after the other (WPT 1: the paired form
+              // would spill at this warp count's register budget)
 #pragma unroll
-            for (int s = 0; s < 4 / C::WPT; ++s) {
-              const int sl = sw + s * C::WPT;
-              warp_block_cols(kb + sl * 2048, kb + C::KB + sl * 2048, qb, koff, voff,
-                              C::BK * j + 16 * sl + 1, pc0, pc1, gr.pg, P.sl2, m, l, acc);
+              for (int s = 0; s < 4 / C::WPT; ++s) {
+                const int sl = sw + s * C::WPT;
+                warp_block_cols(kb + sl * 2048, kb + C::KB + sl * 2048, qb, koff, voff,
+                                C::BK * j + 16 * sl + 1, pc0, pc1, gr.pg, P.sl2, m, l, acc);
+              }
             }
           }
         } else if (lane == 0) {

@@ -284,15 +284,20 @@ def test_attn_grouped_layouts(name):
     assert_close(np64(out), ref, f"attn out ({name})")
 
 
-def test_grouped_form_flags_positions_past_max_pos():
-    """A group whose last token lies past the host's max_pos: that token is flagged and its row
-    left at zero; its group's other tokens are exact."""
+@pytest.mark.parametrize("bad", ["position", "sequence"])
+def test_grouped_form_flags_bad_tokens(bad):
+    """Grouped form: a token whose position lies past the host's max_pos (its group's other
+    tokens still exact), or a group whose sequence id is out of range: the status word says so
+    and the bad rows are left at zero; the other tokens are exact."""
     shape = BEAM
     cfg = cfg_of(shape, nope=True)
     cap, max_pos = 5000, 3000
     c = synth.kv_cache(shape, 1, cap, 5, device=DEV)
     kc = B.KVCache(c["k"], c["v"], 0)
-    seqs, positions = [0, 0, 0], [2500, 2501, 4000]
+    if bad == "position":
+        seqs, positions = [0, 0, 0], [2500, 2501, 4000]
+    else:
+        seqs, positions = [0, 0, 3], [2500, 2501, 2900]
     T = len(seqs)
     q = synth.normal((T, shape.n_q, shape.head_dim), 1.0, 0.0, 5, ("q",), DEV)
     g = synth.activations(T, shape.q_rows, 5, "g", DEV)
@@ -302,7 +307,8 @@ def test_grouped_form_flags_positions_past_max_pos():
     B.beam_attn(cfg, q, g, W["gate_bias"], kc, torch.tensor(seqs, dtype=torch.int32, device=DEV),
                 torch.tensor(positions, dtype=torch.int32, device=DEV), max_pos, W["w_o"], out,
                 ws_for(cfg, T, max_pos), max_q_per_seq=3)
-    assert B.beam_get_device_status() & B.DEV_BAD_POSITION
+    assert B.beam_get_device_status() & (B.DEV_BAD_POSITION if bad == "position"
+                                         else B.DEV_BAD_SEQ)
     ref = O.attention(shape, np64(q[:2]), np64(g[:2]), np64(W["gate_bias"]), oracle_cache(kc),
                       seqs[:2], positions[:2], np64(W["w_o"]))
     assert_close(np64(out[:2]), ref, "attn out, valid tokens")
