@@ -33,6 +33,22 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   f[4] = bflo(v.z); f[5] = bfhi(v.z); f[6] = bflo(v.w); f[7] = bfhi(v.w);
 }
 
+// acc + w.lo * x.lo, then + w.hi * x.hi, for two bf16 pairs packed in 32-bit words. Each step
+// is one mixed-precision FMA (fma.rn.f32.bf16: the bf16 operands widen exactly, the product
+// and the sum are rounded once to FP32), so the result equals
+// fmaf(bfhi(w), bfhi(x), fmaf(bflo(w), bflo(x), acc)) without the two unpacking instructions
+// per element that the FP32 form spends.
+__device__ __forceinline__ float fma_bf16x2(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
 // Streaming 16-byte load that does not allocate in L1 (weights are read once per call).
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;

@@ -14,7 +14,13 @@ namespace beam {
 
 // acc[r][t] = sum_k W_r[k] * X_t[k] for rows w[0..NR) and activations x[0..NT), length K
 // (a multiple of 8). Activations t >= nt are skipped. Result is complete in every lane.
-template <int NR, int NT, int U>
+// MIXED: the products run as mixed-precision bf16 FMAs (fma_bf16x2) instead of FP32 FMAs on
+// unpacked operands -- the same sums bit for bit, about half the instructions, but the compiler
+// then keeps every requested chunk in registers (the one-token expert kernels went from 72 to
+// 148 registers and lost two thirds of their occupancy), so only the one-token plain GEMV takes
+// it (measured inside the 6-layer decode step: the attention call with its o_proj GEMV
+// 29.1 -> 26.0 us, the QKV projection unchanged).
+template <int NR, int NT, int U, bool MIXED = false>
 __device__ __forceinline__ void warp_dot(const uint16_t* const (&w)[NR],
                                          const uint16_t* const (&x)[NT], int nt, int K,
                                          float (&acc)[NR][NT]) {
@@ -33,6 +39,22 @@ __device__ __forceinline__ void warp_dot(const uint16_t* const (&w)[NR],
       for (int r = 0; r < NR; ++r) wv[u][r] = ld_stream(w[r] + size_t(c + 32 * u) * 8);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      if (MIXED) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t < nt) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x[t] + size_t(c + 32 * u) * 8));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+              acc[r][t] = fma_bf16x2(wv[u][r].x, xv.x, acc[r][t]);
+              acc[r][t] = fma_bf16x2(wv[u][r].y, xv.y, acc[r][t]);
+              acc[r][t] = fma_bf16x2(wv[u][r].z, xv.z, acc[r][t]);
+              acc[r][t] = fma_bf16x2(wv[u][r].w, xv.w, acc[r][t]);
+            }
+          }
+        }
+        continue;
+      }
       float wf[NR][8];
 #pragma unroll
       for (int r = 0; r < NR; ++r) unpack8(wv[u][r], wf[r]);
@@ -50,6 +72,25 @@ __device__ __forceinline__ void warp_dot(const uint16_t* const (&w)[NR],
     }
   }
   for (; c < nchunk; c += 32) {
+    if (MIXED) {
+      uint4 wv[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) wv[r] = ld_stream(w[r] + size_t(c) * 8);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (t < nt) {
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x[t] + size_t(c) * 8));
+#pragma unroll
+          for (int r = 0; r < NR; ++r) {
+            acc[r][t] = fma_bf16x2(wv[r].x, xv.x, acc[r][t]);
+            acc[r][t] = fma_bf16x2(wv[r].y, xv.y, acc[r][t]);
+            acc[r][t] = fma_bf16x2(wv[r].z, xv.z, acc[r][t]);
+            acc[r][t] = fma_bf16x2(wv[r].w, xv.w, acc[r][t]);
+          }
+        }
+      }
+      continue;
+    }
     float wf[NR][8];
 #pragma unroll
     for (int r = 0; r < NR; ++r) unpack8(ld_stream(w[r] + size_t(c) * 8), wf[r]);
@@ -119,7 +160,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
 #pragma unroll
   for (int t = 0; t < NT; ++t) x[t] = X + size_t(t0 + min(t, nt - 1)) * K;
   float acc[ROWS][NT];
-  warp_dot<ROWS, NT, U>(w, x, nt, K, acc);
+  warp_dot<ROWS, NT, U, NT == 1>(w, x, nt, K, acc);
   // lanes write distinct (r, t) outputs
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
