@@ -27,13 +27,17 @@ constexpr int kFusedMaxPairs = 1024;  // down+combine in shared memory up to thi
 
 constexpr int kMoeGemmMinT = 32;   // from here the experts run as grouped tensor-core GEMMs
 // Weight chunks in flight per lane in the single-token gate/up and down kernels. The down kernel
-// takes 4 rows of 2560 per warp, 5 chunks each (20 KB per warp in two full round trips):
-// measured 8-10 us faster than 2 rows x 8 chunks (a third, ragged round trip per warp). The
-// gate/up kernel takes 2 (gate, up) row pairs of 5120 per warp, 5 chunks each: 5 us faster than
-// one pair with 4 chunks.
-constexpr int kDecodeGateUpU = 5;
+// takes 4 rows of 2560 per warp, the gate/up kernel 2 (gate, up) row pairs of 5120 (with the
+// FP32 products: 4 rows x 5 chunks measured 8-10 us faster than 2 rows x 8 chunks for the
+// down kernel, 2 pairs x 5 chunks 5 us faster than one pair x 4 for gate/up). Both multiply
+// with mixed-precision bf16 FMAs (warp_dot's MIXED form); that form keeps every requested chunk
+// in registers, so they run 3 chunks per row at three CTAs per SM (80 registers, no spills):
+// measured in the 6-layer decode step 164.3 -> 162.9 us per token per layer, against 5 chunks
+// with the FP32 products (72 registers) and 5 chunks with the mixed form capped at three CTAs
+// (80 registers and spills, 163.1).
+constexpr int kDecodeGateUpU = 3;
 constexpr int kDecodeGateUpFPW = 2;   // gate/up row pairs per warp in the one-token kernel
-constexpr int kDecodeDownU = 5;
+constexpr int kDecodeDownU = 3;
 constexpr int kDecodeDownNR = 4;   // rows per warp in the one-token down kernel
 
 struct MoePlan {
@@ -172,7 +176,7 @@ __device__ __forceinline__ int pair_at(const MoePlan& pl, const int32_t* direct,
 // row F+f, dotted with up to NT of the expert's pairs per weight pass. CTA (0, 0) also clears
 // the n_cnt completion counters of the down kernel that follows.
 template <int U, int NT, int FPW>
-__global__ void __launch_bounds__(256) moe_gate_up_kernel(
+__global__ void __launch_bounds__(256, NT == 1 ? 3 : 1) moe_gate_up_kernel(
     const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_gu, int H, int F, int k,
     MoePlan pl, const int32_t* __restrict__ direct, int E, int* __restrict__ cnt, int n_cnt,
     uint16_t* __restrict__ a) {
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(256) moe_gate_up_kernel(
       x[i] = u + size_t(pid[i] / k) * H;
     }
     float acc[2 * FPW][NT];
-    warp_dot<2 * FPW, NT, U>(w, x, nt, H, acc);
+    warp_dot<2 * FPW, NT, U, NT == 1>(w, x, nt, H, acc);
 #pragma unroll
     for (int j = 0; j < FPW; ++j)
 #pragma unroll
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(256) moe_down_combine_kernel(
 // slots in order, skipping slots whose expert index is out of range. Without counters a
 // separate combine pass follows.
 template <int U, int NT, int NR>
-__global__ void __launch_bounds__(256) moe_down_kernel(
+__global__ void __launch_bounds__(256, NT == 1 ? 3 : 1) moe_down_kernel(
     const uint16_t* __restrict__ a, const uint16_t* __restrict__ w_dn, int H, int F, MoePlan pl,
     const int32_t* __restrict__ direct, const int32_t* __restrict__ topk_idx,
     const float* __restrict__ topk_w, int T, int k, int E, int* __restrict__ cnt,
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(256) moe_down_kernel(
         x[i] = a + size_t(pid[i]) * F;
       }
       float acc[NR][NT];
-      warp_dot<NR, NT, U>(w, x, nt, F, acc);
+      warp_dot<NR, NT, U, NT == 1>(w, x, nt, F, acc);
 #pragma unroll
       for (int r = 0; r < NR; ++r)
 #pragma unroll
