@@ -17,9 +17,10 @@ namespace beam {
 // MIXED: the products run as mixed-precision bf16 FMAs (fma_bf16x2) instead of FP32 FMAs on
 // unpacked operands -- the same sums bit for bit, about half the instructions, but the compiler
 // then keeps every requested chunk in registers (the one-token expert kernels went from 72 to
-// 148 registers and lost two thirds of their occupancy), so only the one-token plain GEMV takes
-// it (measured inside the 6-layer decode step: the attention call with its o_proj GEMV
-// 29.1 -> 26.0 us, the QKV projection unchanged).
+// 148 registers at 5 chunks per row), so each caller sizes its chunks for its occupancy: the
+// one-token plain GEMV as before (measured inside the 6-layer decode step: the attention call
+// with its o_proj GEMV 29.1 -> 26.0 us, the QKV projection unchanged), the one-token expert
+// kernels at 3 chunks per row and three CTAs per SM (mlp.cu).
 template <int NR, int NT, int U, bool MIXED = false>
 __device__ __forceinline__ void warp_dot(const uint16_t* const (&w)[NR],
                                          const uint16_t* const (&x)[NT], int nt, int K,
